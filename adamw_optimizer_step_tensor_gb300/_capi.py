@@ -1,0 +1,164 @@
+"""ctypes binding of libadamw (include/adamw.h): argument marshalling only.
+
+Every function here has the name and argument order of the C entry point it
+wraps; pointers are passed as Python ints (``tensor.data_ptr()``) and the
+stream as an int handle (``torch.cuda.current_stream().cuda_stream``).  A
+non-OK status raises ``AdamWError`` carrying the library's message.  All
+device work happens inside the library's kernels; nothing here computes.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "_build", "libadamw.so")
+
+OK, EINVAL, EALIGN, EDTYPE, ENOMEM, ECUDA, EUNSUPPORTED = range(7)
+STATUS_NAMES = ["OK", "EINVAL", "EALIGN", "EDTYPE", "ENOMEM", "ECUDA", "EUNSUPPORTED"]
+F32, F16, BF16 = 0, 1, 2
+MODE_FP32, MODE_BF16_REM, MODE_Q8 = 0, 1, 2
+Q8_BLOCK = 256
+
+_vp = ctypes.c_void_p
+
+
+class AdamWError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        name = STATUS_NAMES[status] if 0 <= status < len(STATUS_NAMES) else str(status)
+        super().__init__(f"ADAMW_{name}: {message}")
+        self.status = status
+
+
+class adamw_tensor(ctypes.Structure):
+    _fields_ = [
+        ("param", _vp),
+        ("param_rem", _vp),
+        ("grad", _vp),
+        ("exp_avg", _vp),
+        ("exp_avg_sq", _vp),
+        ("absmax_m", _vp),
+        ("absmax_v", _vp),
+        ("numel", ctypes.c_int64),
+        ("weight_decay", ctypes.c_float),
+    ]
+
+
+_SIGNATURES = {
+    "adamw_plan_create": (ctypes.c_int, [ctypes.POINTER(adamw_tensor), ctypes.c_int32, ctypes.c_int,
+                                         ctypes.c_int, ctypes.POINTER(_vp)]),
+    "adamw_plan_destroy": (ctypes.c_int, [_vp]),
+    "adamw_plan_info": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int64),
+                                       ctypes.POINTER(ctypes.c_int64),
+                                       ctypes.POINTER(ctypes.c_int32),
+                                       ctypes.POINTER(ctypes.c_int32)]),
+    "adamw_check_nonfinite": (ctypes.c_int, [_vp, _vp, _vp]),
+    "adamw_step": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                  _vp, _vp, _vp]),
+    "adamw_bf16rem_split": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int64, _vp]),
+    "adamw_bf16rem_join": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int64, _vp]),
+    "adamw_q8_default_maps": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float),
+                                             ctypes.POINTER(ctypes.c_float)]),
+    "adamw_q8_set_maps": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_float),
+                                         ctypes.POINTER(ctypes.c_float)]),
+    "adamw_q8_dequant": (ctypes.c_int, [_vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int64, _vp]),
+    "adamw_q8_quant": (ctypes.c_int, [_vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int64, _vp]),
+    "adamw_last_error": (ctypes.c_char_p, []),
+    "adamw_abi_version": (ctypes.c_int32, []),
+}
+
+_lib = None
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load the library once; fails loudly when it has not been built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise ImportError(
+            f"libadamw.so not found at {path}; build it first with "
+            "`python -m adamw_optimizer_step_tensor_gb300.build` (needs nvcc)")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def _check(status: int) -> None:
+    if status != OK:
+        raise AdamWError(status, load().adamw_last_error().decode())
+
+
+def adamw_last_error() -> str:
+    return load().adamw_last_error().decode()
+
+
+def adamw_abi_version() -> int:
+    return int(load().adamw_abi_version())
+
+
+def adamw_plan_create(tensors: list[adamw_tensor], mode: int, grad_dtype: int) -> int:
+    arr = (adamw_tensor * max(1, len(tensors)))(*tensors)
+    out = _vp()
+    _check(load().adamw_plan_create(arr, len(tensors), mode, grad_dtype, ctypes.byref(out)))
+    return out.value
+
+
+def adamw_plan_destroy(plan: int) -> None:
+    _check(load().adamw_plan_destroy(plan))
+
+
+def adamw_plan_info(plan: int) -> dict:
+    n, c = ctypes.c_int64(), ctypes.c_int64()
+    g, b = ctypes.c_int32(), ctypes.c_int32()
+    _check(load().adamw_plan_info(plan, ctypes.byref(n), ctypes.byref(c), ctypes.byref(g),
+                                  ctypes.byref(b)))
+    return {"total_numel": n.value, "n_chunks": c.value, "grid_blocks": g.value,
+            "block_threads": b.value}
+
+
+def adamw_check_nonfinite(plan: int, found_inf_dev: int, stream: int | None) -> None:
+    _check(load().adamw_check_nonfinite(plan, found_inf_dev, stream))
+
+
+def adamw_step(plan: int, lr_dev: int, step_dev: int, beta1: float, beta2: float, eps: float,
+               grad_scale_dev: int | None, found_inf_dev: int | None, stream: int | None) -> None:
+    _check(load().adamw_step(plan, lr_dev, step_dev, beta1, beta2, eps, grad_scale_dev,
+                             found_inf_dev, stream))
+
+
+def adamw_bf16rem_split(master: int, bf16: int, rem: int, n: int, stream: int | None) -> None:
+    _check(load().adamw_bf16rem_split(master, bf16, rem, n, stream))
+
+
+def adamw_bf16rem_join(bf16: int, rem: int, master: int, n: int, stream: int | None) -> None:
+    _check(load().adamw_bf16rem_join(bf16, rem, master, n, stream))
+
+
+def adamw_q8_default_maps():
+    """Host call: returns (signed_map, unsigned_map) as two lists of 256 floats."""
+    s, u = (ctypes.c_float * 256)(), (ctypes.c_float * 256)()
+    _check(load().adamw_q8_default_maps(s, u))
+    return list(s), list(u)
+
+
+def adamw_q8_set_maps(plan: int, signed_map, unsigned_map) -> None:
+    s = (ctypes.c_float * 256)(*[float(x) for x in signed_map])
+    u = (ctypes.c_float * 256)(*[float(x) for x in unsigned_map])
+    _check(load().adamw_q8_set_maps(plan, s, u))
+
+
+def adamw_q8_dequant(plan: int, which: int, codes: int, absmax: int, out: int, n: int,
+                     stream: int | None) -> None:
+    _check(load().adamw_q8_dequant(plan, which, codes, absmax, out, n, stream))
+
+
+def adamw_q8_quant(plan: int, which: int, x: int, codes: int, absmax: int, n: int,
+                   stream: int | None) -> None:
+    _check(load().adamw_q8_quant(plan, which, x, codes, absmax, n, stream))

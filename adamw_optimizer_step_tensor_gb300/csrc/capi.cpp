@@ -1,0 +1,350 @@
+// capi.cpp -- the extern "C" entry points of libadamw: argument validation,
+// the multi-tensor plan (chunk and tensor tables on the device), and launches.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <memory>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+
+namespace adamw {
+void default_maps(float smap[256], float umap[256]);
+int build_qmap(const float value[256], QMapDev* out);
+int zero_code_of(const float value[256]);
+}  // namespace adamw
+
+using namespace adamw;
+
+struct adamw_plan {
+  int device = -1;
+  adamw_mode mode = ADAMW_MODE_FP32;
+  adamw_dtype gdt = ADAMW_F32;
+  int32_t n_tensors = 0;
+  int64_t total_numel = 0;
+  int64_t n_chunks = 0;
+  int grid = 1;
+  int grid_check = 1;
+  TensorDesc* d_tensors = nullptr;
+  Chunk* d_chunks = nullptr;
+  uint32_t* d_ticket = nullptr;
+  QTables* d_qt = nullptr;
+};
+
+namespace {
+
+thread_local std::string g_err;
+
+adamw_status fail(adamw_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  std::vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return st;
+}
+
+adamw_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(ADAMW_ECUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t dtype_size(adamw_dtype d) { return d == ADAMW_F32 ? 4 : 2; }
+
+bool valid_dtype(int d) { return d == ADAMW_F32 || d == ADAMW_F16 || d == ADAMW_BF16; }
+bool valid_mode(int m) {
+  return m == ADAMW_MODE_FP32 || m == ADAMW_MODE_BF16_REM || m == ADAMW_MODE_Q8;
+}
+
+void free_plan(adamw_plan* p) {
+  if (!p) return;
+  cudaFree(p->d_tensors);
+  cudaFree(p->d_chunks);
+  cudaFree(p->d_ticket);
+  cudaFree(p->d_qt);
+  delete p;
+}
+
+adamw_status check_device(const adamw_plan* p) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev != p->device)
+    return fail(ADAMW_EINVAL, "plan was created on device %d but device %d is current",
+                p->device, dev);
+  return ADAMW_OK;
+}
+
+adamw_status build_qtables(const float smap[256], const float umap[256], QTables* qt) {
+  std::memset(qt, 0, sizeof(QTables));
+  const int r0 = build_qmap(smap, &qt->map[0]);
+  const int r1 = build_qmap(umap, &qt->map[1]);
+  if (r0 < 0 || r1 < 0)
+    return fail(ADAMW_EINVAL, "code maps must hold 256 strictly ascending finite floats "
+                              "whose neighbour sums are exact in float64");
+  qt->zero_code[0] = zero_code_of(smap);
+  qt->zero_code[1] = zero_code_of(umap);
+  if (qt->zero_code[0] < 0 || qt->zero_code[1] < 0)
+    return fail(ADAMW_EINVAL, "code maps must contain 0.0");
+  const int r = r0 > r1 ? r0 : r1;
+  if (r > kMaxRefine)
+    return fail(ADAMW_EUNSUPPORTED,
+                "code maps too dense for the bucketed search (%d thresholds share a bucket, "
+                "at most %d supported)", r, kMaxRefine);
+  qt->refine = r < 1 ? 1 : r;
+  return ADAMW_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* adamw_last_error(void) { return g_err.c_str(); }
+
+int32_t adamw_abi_version(void) { return ADAMW_ABI_VERSION; }
+
+adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, adamw_mode mode,
+                               adamw_dtype grad_dtype, adamw_plan** out) {
+  if (!out) return fail(ADAMW_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (n_tensors < 0) return fail(ADAMW_EINVAL, "n_tensors < 0");
+  if (n_tensors > 0 && !tensors) return fail(ADAMW_EINVAL, "tensors is NULL");
+  if (!valid_mode(mode)) return fail(ADAMW_EDTYPE, "unknown mode %d", (int)mode);
+  if (!valid_dtype(grad_dtype)) return fail(ADAMW_EDTYPE, "unknown grad dtype %d", (int)grad_dtype);
+
+  const size_t psz = mode == ADAMW_MODE_BF16_REM ? 2 : 4;
+  const size_t ssz = mode == ADAMW_MODE_Q8 ? 1 : 4;
+  const size_t gsz = dtype_size(grad_dtype);
+  const size_t svec = mode == ADAMW_MODE_Q8 ? 8 : 16;
+
+  std::vector<TensorDesc> td(static_cast<size_t>(n_tensors));
+  std::vector<Chunk> chunks;
+  int64_t total = 0;
+  for (int32_t i = 0; i < n_tensors; ++i) {
+    const adamw_tensor& t = tensors[i];
+    if (t.numel < 0) return fail(ADAMW_EINVAL, "tensor %d: numel < 0", i);
+    if (!std::isfinite(t.weight_decay))
+      return fail(ADAMW_EINVAL, "tensor %d: weight_decay is not finite", i);
+    TensorDesc& d = td[i];
+    d.p = t.param;
+    d.rem = t.param_rem;
+    d.g = t.grad;
+    d.m = t.exp_avg;
+    d.v = t.exp_avg_sq;
+    d.am = t.absmax_m;
+    d.av = t.absmax_v;
+    d.numel = t.numel;
+    d.wd = t.weight_decay;
+    if (t.numel == 0) continue;
+    if (!t.param || !t.grad || !t.exp_avg || !t.exp_avg_sq)
+      return fail(ADAMW_EINVAL, "tensor %d: param, grad, exp_avg and exp_avg_sq must be set", i);
+    if ((mode == ADAMW_MODE_BF16_REM) != (t.param_rem != nullptr))
+      return fail(ADAMW_EINVAL, "tensor %d: param_rem must be set exactly in BF16_REM mode", i);
+    if ((mode == ADAMW_MODE_Q8) != (t.absmax_m != nullptr && t.absmax_v != nullptr) ||
+        (mode != ADAMW_MODE_Q8 && (t.absmax_m || t.absmax_v)))
+      return fail(ADAMW_EINVAL, "tensor %d: absmax_m/absmax_v must be set exactly in Q8 mode", i);
+    if (!aligned(t.param, psz) || !aligned(t.grad, gsz) || !aligned(t.exp_avg, ssz) ||
+        !aligned(t.exp_avg_sq, ssz) || (t.param_rem && !aligned(t.param_rem, 2)) ||
+        (t.absmax_m && !aligned(t.absmax_m, 4)) || (t.absmax_v && !aligned(t.absmax_v, 4)))
+      return fail(ADAMW_EALIGN, "tensor %d: a pointer is not aligned to its element size", i);
+    d.vec_ok = aligned(t.param, 16) && aligned(t.grad, 16) && aligned(t.exp_avg, svec) &&
+               aligned(t.exp_avg_sq, svec) && (!t.param_rem || aligned(t.param_rem, 16));
+    for (int64_t s = 0; s < t.numel; s += kChunk) {
+      const int64_t len = t.numel - s < kChunk ? t.numel - s : kChunk;
+      chunks.push_back(Chunk{s, i, static_cast<int32_t>(len)});
+    }
+    total += t.numel;
+  }
+
+  std::unique_ptr<adamw_plan, void (*)(adamw_plan*)> p(new adamw_plan, free_plan);
+  p->mode = mode;
+  p->gdt = grad_dtype;
+  p->n_tensors = n_tensors;
+  p->total_numel = total;
+  p->n_chunks = static_cast<int64_t>(chunks.size());
+
+  cudaError_t e = cudaGetDevice(&p->device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  int sms = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  int bps = 0, smem = 0;
+  e = step_occupancy(mode, grad_dtype, &bps, &smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  if (bps < 1) bps = 1;
+  const int64_t resident = static_cast<int64_t>(bps) * sms;
+  p->grid = static_cast<int>(p->n_chunks < resident ? (p->n_chunks > 0 ? p->n_chunks : 1) : resident);
+  const int64_t check_res = 8LL * sms;
+  p->grid_check = static_cast<int>(p->n_chunks < check_res ? (p->n_chunks > 0 ? p->n_chunks : 1) : check_res);
+
+  const size_t tb = td.size() * sizeof(TensorDesc), cb = chunks.size() * sizeof(Chunk);
+  if (tb && (e = cudaMalloc(&p->d_tensors, tb)) != cudaSuccess)
+    return fail(ADAMW_ENOMEM, "cudaMalloc(tensor table): %s", cudaGetErrorString(e));
+  if (cb && (e = cudaMalloc(&p->d_chunks, cb)) != cudaSuccess)
+    return fail(ADAMW_ENOMEM, "cudaMalloc(chunk table): %s", cudaGetErrorString(e));
+  if ((e = cudaMalloc(&p->d_ticket, sizeof(uint32_t))) != cudaSuccess)
+    return fail(ADAMW_ENOMEM, "cudaMalloc(ticket): %s", cudaGetErrorString(e));
+  if (tb && (e = cudaMemcpy(p->d_tensors, td.data(), tb, cudaMemcpyHostToDevice)) != cudaSuccess)
+    return cuda_fail(e, "upload tensor table");
+  if (cb && (e = cudaMemcpy(p->d_chunks, chunks.data(), cb, cudaMemcpyHostToDevice)) != cudaSuccess)
+    return cuda_fail(e, "upload chunk table");
+  if ((e = cudaMemset(p->d_ticket, 0, sizeof(uint32_t))) != cudaSuccess)
+    return cuda_fail(e, "clear ticket");
+  if (mode == ADAMW_MODE_Q8) {
+    std::unique_ptr<QTables> qt(new QTables);
+    float smap[256], umap[256];
+    default_maps(smap, umap);
+    adamw_status st = build_qtables(smap, umap, qt.get());
+    if (st != ADAMW_OK) return st;
+    if ((e = cudaMalloc(&p->d_qt, sizeof(QTables))) != cudaSuccess)
+      return fail(ADAMW_ENOMEM, "cudaMalloc(code maps): %s", cudaGetErrorString(e));
+    if ((e = cudaMemcpy(p->d_qt, qt.get(), sizeof(QTables), cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e, "upload code maps");
+  }
+  *out = p.release();
+  return ADAMW_OK;
+}
+
+adamw_status adamw_plan_destroy(adamw_plan* plan) {
+  if (!plan) return ADAMW_OK;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  cudaSetDevice(plan->device);
+  cudaDeviceSynchronize();
+  free_plan(plan);
+  if (prev >= 0) cudaSetDevice(prev);
+  return ADAMW_OK;
+}
+
+adamw_status adamw_plan_info(const adamw_plan* plan, int64_t* total_numel, int64_t* n_chunks,
+                             int32_t* grid_blocks, int32_t* block_threads) {
+  if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
+  if (total_numel) *total_numel = plan->total_numel;
+  if (n_chunks) *n_chunks = plan->n_chunks;
+  if (grid_blocks) *grid_blocks = plan->grid;
+  if (block_threads) *block_threads = kThreads;
+  return ADAMW_OK;
+}
+
+adamw_status adamw_check_nonfinite(const adamw_plan* plan, float* found_inf_dev, void* stream) {
+  if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
+  if (!found_inf_dev) return fail(ADAMW_EINVAL, "found_inf_dev is NULL");
+  if (!aligned(found_inf_dev, 4)) return fail(ADAMW_EALIGN, "found_inf_dev is not 4-byte aligned");
+  adamw_status st = check_device(plan);
+  if (st != ADAMW_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(found_inf_dev, 0, sizeof(float), s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(found_inf)");
+  if (plan->n_chunks == 0) return ADAMW_OK;
+  e = launch_nonfinite(plan->gdt, plan->d_tensors, plan->d_chunks, plan->n_chunks, found_inf_dev,
+                       plan->grid_check, s);
+  if (e != cudaSuccess) return cuda_fail(e, "launch nonfinite check");
+  return ADAMW_OK;
+}
+
+adamw_status adamw_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev, float beta1,
+                        float beta2, float eps, const float* grad_scale_dev,
+                        const float* found_inf_dev, void* stream) {
+  if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
+  if (!lr_dev || !step_dev) return fail(ADAMW_EINVAL, "lr_dev and step_dev must be set");
+  if (!aligned(lr_dev, 4) || !aligned(step_dev, 4) || !aligned(grad_scale_dev, 4) ||
+      !aligned(found_inf_dev, 4))
+    return fail(ADAMW_EALIGN, "a scalar pointer is not 4-byte aligned");
+  if (!(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f))
+    return fail(ADAMW_EINVAL, "betas must lie in [0, 1)");
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(ADAMW_EINVAL, "eps must be finite and >= 0");
+  adamw_status st = check_device(plan);
+  if (st != ADAMW_OK) return st;
+  StepArgs a;
+  a.tensors = plan->d_tensors;
+  a.chunks = plan->d_chunks;
+  a.n_chunks = plan->n_chunks;
+  a.lr = lr_dev;
+  a.step = step_dev;
+  a.grad_scale = grad_scale_dev;
+  a.found_inf = found_inf_dev;
+  a.beta1 = beta1;
+  a.beta2 = beta2;
+  a.eps = eps;
+  a.ticket = plan->d_ticket;
+  a.qt = plan->d_qt;
+  cudaError_t e = launch_step(plan->mode, plan->gdt, a, plan->grid, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "launch adamw step");
+  return ADAMW_OK;
+}
+
+adamw_status adamw_bf16rem_split(const float* master, uint16_t* bf16, int16_t* rem, int64_t n,
+                                 void* stream) {
+  if (n < 0) return fail(ADAMW_EINVAL, "n < 0");
+  if (n == 0) return ADAMW_OK;
+  if (!master || !bf16 || !rem) return fail(ADAMW_EINVAL, "NULL pointer");
+  if (!aligned(master, 4) || !aligned(bf16, 2) || !aligned(rem, 2))
+    return fail(ADAMW_EALIGN, "pointer not aligned to its element size");
+  cudaError_t e = launch_split(master, bf16, rem, n, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ADAMW_OK : cuda_fail(e, "launch split");
+}
+
+adamw_status adamw_bf16rem_join(const uint16_t* bf16, const int16_t* rem, float* master, int64_t n,
+                                void* stream) {
+  if (n < 0) return fail(ADAMW_EINVAL, "n < 0");
+  if (n == 0) return ADAMW_OK;
+  if (!master || !bf16 || !rem) return fail(ADAMW_EINVAL, "NULL pointer");
+  if (!aligned(master, 4) || !aligned(bf16, 2) || !aligned(rem, 2))
+    return fail(ADAMW_EALIGN, "pointer not aligned to its element size");
+  cudaError_t e = launch_join(bf16, rem, master, n, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ADAMW_OK : cuda_fail(e, "launch join");
+}
+
+adamw_status adamw_q8_default_maps(float signed_map[256], float unsigned_map[256]) {
+  if (!signed_map || !unsigned_map) return fail(ADAMW_EINVAL, "NULL map");
+  default_maps(signed_map, unsigned_map);
+  return ADAMW_OK;
+}
+
+adamw_status adamw_q8_set_maps(adamw_plan* plan, const float signed_map[256],
+                               const float unsigned_map[256]) {
+  if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
+  if (plan->mode != ADAMW_MODE_Q8 || !plan->d_qt) return fail(ADAMW_EINVAL, "plan is not in Q8 mode");
+  if (!signed_map || !unsigned_map) return fail(ADAMW_EINVAL, "NULL map");
+  std::unique_ptr<QTables> qt(new QTables);
+  adamw_status st = build_qtables(signed_map, unsigned_map, qt.get());
+  if (st != ADAMW_OK) return st;
+  cudaError_t e = cudaMemcpy(plan->d_qt, qt.get(), sizeof(QTables), cudaMemcpyHostToDevice);
+  return e == cudaSuccess ? ADAMW_OK : cuda_fail(e, "upload code maps");
+}
+
+static adamw_status q8_io_check(const adamw_plan* plan, int32_t which, const void* a,
+                                const void* b, const void* c, int64_t n) {
+  if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
+  if (plan->mode != ADAMW_MODE_Q8 || !plan->d_qt) return fail(ADAMW_EINVAL, "plan is not in Q8 mode");
+  if (which != 0 && which != 1) return fail(ADAMW_EINVAL, "which must be 0 (m) or 1 (v)");
+  if (n < 0) return fail(ADAMW_EINVAL, "n < 0");
+  if (n > 0 && (!a || !b || !c)) return fail(ADAMW_EINVAL, "NULL pointer");
+  return check_device(plan);
+}
+
+adamw_status adamw_q8_dequant(const adamw_plan* plan, int32_t which, const uint8_t* codes,
+                              const float* absmax, float* out, int64_t n, void* stream) {
+  adamw_status st = q8_io_check(plan, which, codes, absmax, out, n);
+  if (st != ADAMW_OK || n == 0) return st;
+  if (!aligned(absmax, 4) || !aligned(out, 4)) return fail(ADAMW_EALIGN, "misaligned float pointer");
+  cudaError_t e = launch_q8_dequant(plan->d_qt, which, codes, absmax, out, n,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ADAMW_OK : cuda_fail(e, "launch q8 dequant");
+}
+
+adamw_status adamw_q8_quant(const adamw_plan* plan, int32_t which, const float* x, uint8_t* codes,
+                            float* absmax, int64_t n, void* stream) {
+  adamw_status st = q8_io_check(plan, which, x, codes, absmax, n);
+  if (st != ADAMW_OK || n == 0) return st;
+  if (!aligned(absmax, 4) || !aligned(x, 4)) return fail(ADAMW_EALIGN, "misaligned float pointer");
+  cudaError_t e = launch_q8_quant(plan->d_qt, which, x, codes, absmax, n,
+                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ADAMW_OK : cuda_fail(e, "launch q8 quant");
+}
+
+}  // extern "C"

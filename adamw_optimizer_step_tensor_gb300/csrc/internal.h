@@ -1,0 +1,98 @@
+// internal.h -- device tables, launch arguments and the per-element update
+// shared by the host plan code and the sm_103a kernels of libadamw.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "adamw.h"
+
+namespace adamw {
+
+// One CTA is 256 threads; every thread owns 8 consecutive elements per pass,
+// so a warp covers exactly one 256-element Q8 block per pass.
+constexpr int kThreads = 256;
+constexpr int kVec = 8;
+constexpr int kPass = kThreads * kVec;       // 2048 elements per CTA pass
+constexpr int kChunk = 4 * kPass;            // 8192 elements per chunk
+constexpr int kQBlock = ADAMW_Q8_BLOCK;      // 256
+static_assert(kChunk % kQBlock == 0, "chunks must hold whole Q8 blocks");
+static_assert(32 * kVec == kQBlock, "one warp pass covers exactly one Q8 block");
+
+// Q8 nearest-code search tables (see qmap.cpp for how they are built).
+constexpr int kBuckets = 1 + 25 * 128;       // |x| in [0, 2^-24) plus 25 binades x 128
+constexpr int kMaxRefine = 4;                // thresholds compared per lookup, at most
+
+struct TensorDesc {
+  void* p;            // fp32 or bf16 param
+  int16_t* rem;       // remainders (BF16_REM)
+  const void* g;      // grads
+  void* m;            // fp32 or uint8 codes
+  void* v;            // fp32 or uint8 codes
+  float* am;          // Q8 absmax of m per 256 block
+  float* av;          // Q8 absmax of v per 256 block
+  int64_t numel;
+  float wd;
+  int32_t vec_ok;     // all pointers 16-byte aligned
+};
+
+struct Chunk {
+  int64_t start;      // first element, a multiple of kChunk
+  int32_t tensor;     // index into the tensor table
+  int32_t len;        // elements, 1..kChunk
+};
+
+struct QMapDev {                       // one code map and its search tables
+  float value[256];                    // ascending map values (dequantisation)
+  float thr[256 + kMaxRefine];         // thr[k]: smallest float nearer to value[k+1]; +inf padding
+  uint8_t lo_pos[kBuckets];            // lowest code of any x >= 0 in the bucket of |x|
+  uint8_t lo_neg[kBuckets];            // lowest code of any x <= 0 in the bucket of |x|
+};
+
+struct alignas(16) QTables {
+  QMapDev map[2];                      // 0: signed (m), 1: unsigned (v)
+  int32_t zero_code[2];
+  int32_t refine;                      // thresholds to compare per lookup (1..kMaxRefine)
+};
+static_assert(sizeof(QTables) % 16 == 0, "QTables is copied to shared memory in 16-byte words");
+
+struct StepArgs {
+  const TensorDesc* tensors;
+  const Chunk* chunks;
+  int64_t n_chunks;
+  const float* lr;
+  int32_t* step;
+  const float* grad_scale;    // may be null
+  const float* found_inf;     // may be null
+  float beta1, beta2, eps;
+  uint32_t* ticket;           // plan-owned counter, zero between launches
+  const QTables* qt;          // Q8 only
+};
+
+// Host-side bucket index of a non-negative float bit pattern (no NaN).
+__host__ __device__ __forceinline__ int bucket_of(uint32_t mag) {
+  uint32_t e = mag >> 23;
+  if (e < 103u) return 0;
+  if (e > 127u) return kBuckets - 1;
+  return 1 + static_cast<int>((e - 103u) * 128u + ((mag >> 16) & 127u));
+}
+
+}  // namespace adamw
+
+// Launchers implemented in the kernel translation units.
+namespace adamw {
+cudaError_t launch_step(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int grid,
+                        cudaStream_t s);
+cudaError_t step_occupancy(adamw_mode mode, adamw_dtype gdt, int* blocks_per_sm,
+                           int* smem_bytes);
+cudaError_t launch_nonfinite(adamw_dtype gdt, const TensorDesc* tensors, const Chunk* chunks,
+                             int64_t n_chunks, float* found_inf, int grid, cudaStream_t s);
+cudaError_t launch_split(const float* master, uint16_t* hi, int16_t* rem, int64_t n,
+                         cudaStream_t s);
+cudaError_t launch_join(const uint16_t* hi, const int16_t* rem, float* master, int64_t n,
+                        cudaStream_t s);
+cudaError_t launch_q8_dequant(const QTables* qt, int which, const uint8_t* codes,
+                              const float* absmax, float* out, int64_t n, cudaStream_t s);
+cudaError_t launch_q8_quant(const QTables* qt, int which, const float* x, uint8_t* codes,
+                            float* absmax, int64_t n, cudaStream_t s);
+}  // namespace adamw

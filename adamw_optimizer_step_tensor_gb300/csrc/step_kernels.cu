@@ -1,0 +1,432 @@
+// step_kernels.cu -- the fused AdamW step kernels for sm_103a.
+//
+// One persistent launch covers every tensor of a plan: CTAs stride over the
+// plan's chunk table (8192 contiguous elements of one tensor per chunk), and
+// each thread moves 8 consecutive elements per pass with 128-bit streaming
+// loads and stores.  The step is a pure HBM stream (28 B per element in fp32
+// mode, 26 in bf16+remainder mode, 14.06 in 8-bit mode), so there is no
+// tensor-core work; the kernel's job is to keep enough bytes in flight.
+//
+// The element update is the decoupled-decay AdamW of "Fix decoupled weight
+// decay ordering in the CUDA Adam/AdEMAMix kernels" (bitsandbytes PR #2040):
+// decay and update both read the previous p.  Every operation is an explicit
+// round-to-nearest intrinsic, so the compiler cannot contract a multiply and
+// an add into an FMA and the result is the float32 sequence the header
+// documents, bit for bit.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace adamw {
+namespace {
+
+struct Scal {
+  float b1, b2, omb1, omb2, eps, lr, step_size, sqrt_bc2, inv_scale;
+  int scaled;
+};
+
+// b^t by float64 square-and-multiply; every product is one IEEE rounding.
+__device__ double pow_binary(double b, int t) {
+  double r = 1.0, x = b;
+  while (t) {
+    if (t & 1) r = __dmul_rn(r, x);
+    x = __dmul_rn(x, x);
+    t >>= 1;
+  }
+  return r;
+}
+
+// Thread 0 of every CTA: read the run-time scalars, decide skip, and take a
+// ticket; the last CTA to take one stores the new step count.  Every CTA has
+// read *step before its ticket (the fence orders it), so no CTA can see the
+// new value.  Nothing waits on anything.
+__device__ bool prologue(const StepArgs& a, Scal& s) {
+  const bool skip = a.found_inf != nullptr && *a.found_inf != 0.0f;
+  if (skip) return true;
+  const int t = *a.step + 1;
+  const float lr = *a.lr;
+  s.b1 = a.beta1;
+  s.b2 = a.beta2;
+  s.omb1 = __fsub_rn(1.0f, a.beta1);
+  s.omb2 = __fsub_rn(1.0f, a.beta2);
+  s.eps = a.eps;
+  s.lr = lr;
+  const float bc1 = __double2float_rn(__dsub_rn(1.0, pow_binary((double)a.beta1, t)));
+  s.sqrt_bc2 = __double2float_rn(__dsqrt_rn(__dsub_rn(1.0, pow_binary((double)a.beta2, t))));
+  s.step_size = __fdiv_rn(lr, bc1);
+  s.scaled = a.grad_scale != nullptr;
+  s.inv_scale = s.scaled ? __fdiv_rn(1.0f, *a.grad_scale) : 1.0f;
+  __threadfence();
+  const unsigned tk = atomicAdd(a.ticket, 1u);
+  if (tk == gridDim.x - 1) {
+    *a.step = t;
+    atomicExch(a.ticket, 0u);
+  }
+  return false;
+}
+
+__device__ __forceinline__ void update(float& p, float g, float& m, float& v, const Scal& s,
+                                       float decay) {
+  if (s.scaled) g = __fmul_rn(g, s.inv_scale);
+  m = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
+  v = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, __fmul_rn(g, g)));
+  const float h = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), s.sqrt_bc2), s.eps);
+  const float u = __fdiv_rn(m, h);
+  p = __fsub_rn(__fmul_rn(p, decay), __fmul_rn(s.step_size, u));
+}
+
+// ---------------------------------------------------------------- loads/stores
+__device__ __forceinline__ void ld8f(const float* q, float (&x)[8]) {
+  const float4 a = __ldcs(reinterpret_cast<const float4*>(q));
+  const float4 b = __ldcs(reinterpret_cast<const float4*>(q) + 1);
+  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
+__device__ __forceinline__ void st8f(float* q, const float (&x)[8]) {
+  __stcs(reinterpret_cast<float4*>(q), make_float4(x[0], x[1], x[2], x[3]));
+  __stcs(reinterpret_cast<float4*>(q) + 1, make_float4(x[4], x[5], x[6], x[7]));
+}
+__device__ __forceinline__ void ld8u16(const void* q, uint32_t (&w)[4]) {
+  const uint4 a = __ldcs(reinterpret_cast<const uint4*>(q));
+  w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+}
+__device__ __forceinline__ void st8u16(void* q, const uint32_t (&w)[4]) {
+  __stcs(reinterpret_cast<uint4*>(q), make_uint4(w[0], w[1], w[2], w[3]));
+}
+
+__device__ __forceinline__ float bf16_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
+__device__ __forceinline__ float f16_to_f32(uint32_t h) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
+}
+
+template <typename GT> struct Grad;
+template <> struct Grad<float> {
+  static __device__ __forceinline__ void load8(const void* g, int64_t e, float (&x)[8]) {
+    ld8f(static_cast<const float*>(g) + e, x);
+  }
+  static __device__ __forceinline__ float load1(const void* g, int64_t e) {
+    return static_cast<const float*>(g)[e];
+  }
+};
+template <> struct Grad<__half> {
+  static __device__ __forceinline__ void load8(const void* g, int64_t e, float (&x)[8]) {
+    uint32_t w[4];
+    ld8u16(static_cast<const uint16_t*>(g) + e, w);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = f16_to_f32(w[i] & 0xFFFFu);
+      x[2 * i + 1] = f16_to_f32(w[i] >> 16);
+    }
+  }
+  static __device__ __forceinline__ float load1(const void* g, int64_t e) {
+    return f16_to_f32(static_cast<const uint16_t*>(g)[e]);
+  }
+};
+template <> struct Grad<__nv_bfloat16> {
+  static __device__ __forceinline__ void load8(const void* g, int64_t e, float (&x)[8]) {
+    uint32_t w[4];
+    ld8u16(static_cast<const uint16_t*>(g) + e, w);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x[2 * i] = bf16_to_f32(w[i] & 0xFFFFu);
+      x[2 * i + 1] = bf16_to_f32(w[i] >> 16);
+    }
+  }
+  static __device__ __forceinline__ float load1(const void* g, int64_t e) {
+    return bf16_to_f32(static_cast<const uint16_t*>(g)[e]);
+  }
+};
+
+// Remainder join / split on one element (integer only; see adamw.h).
+__device__ __forceinline__ float rem_join(uint32_t hi, uint32_t rem16) {
+  const uint32_t top = (hi - (rem16 >> 15)) & 0xFFFFu;
+  return __uint_as_float((top << 16) | (rem16 & 0xFFFFu));
+}
+__device__ __forceinline__ void rem_split(float x, uint32_t& hi, uint32_t& rem16) {
+  const uint32_t b = __float_as_uint(x);
+  const uint32_t lo = b & 0xFFFFu;
+  hi = ((b >> 16) + (lo >> 15)) & 0xFFFFu;
+  rem16 = lo;
+}
+
+// ---------------------------------------------------------------- fp32 / bf16+rem
+template <adamw_mode MODE, typename GT>
+__global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
+  __shared__ Scal s_sc;
+  __shared__ int s_skip;
+  if (threadIdx.x == 0) s_skip = prologue(a, s_sc);
+  __syncthreads();
+  if (s_skip) return;
+  const Scal s = s_sc;
+
+  for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
+    const Chunk ch = a.chunks[c];
+    const TensorDesc& td = a.tensors[ch.tensor];
+    const float decay = __fsub_rn(1.0f, __fmul_rn(s.lr, td.wd));
+    const bool vec = td.vec_ok != 0;
+    float* const pf = static_cast<float*>(td.p);
+    uint16_t* const ph = static_cast<uint16_t*>(td.p);
+    int16_t* const pr = td.rem;
+    float* const mf = static_cast<float*>(td.m);
+    float* const vf = static_cast<float*>(td.v);
+    const void* const g = td.g;
+
+    for (int off = threadIdx.x * kVec; off < ch.len; off += kPass) {
+      const int64_t e = ch.start + off;
+      if (vec && off + kVec <= ch.len) {
+        float p[8], gr[8], m[8], v[8];
+        uint32_t hw[4], rw[4];
+        if (MODE == ADAMW_MODE_FP32) {
+          ld8f(pf + e, p);
+        } else {
+          ld8u16(ph + e, hw);
+          ld8u16(pr + e, rw);
+        }
+        Grad<GT>::load8(g, e, gr);
+        ld8f(mf + e, m);
+        ld8f(vf + e, v);
+        if (MODE == ADAMW_MODE_BF16_REM) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            p[2 * i] = rem_join(hw[i] & 0xFFFFu, rw[i] & 0xFFFFu);
+            p[2 * i + 1] = rem_join(hw[i] >> 16, rw[i] >> 16);
+          }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) update(p[i], gr[i], m[i], v[i], s, decay);
+        if (MODE == ADAMW_MODE_FP32) {
+          st8f(pf + e, p);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            uint32_t h0, r0, h1, r1;
+            rem_split(p[2 * i], h0, r0);
+            rem_split(p[2 * i + 1], h1, r1);
+            hw[i] = h0 | (h1 << 16);
+            rw[i] = r0 | (r1 << 16);
+          }
+          st8u16(ph + e, hw);
+          st8u16(pr + e, rw);
+        }
+        st8f(mf + e, m);
+        st8f(vf + e, v);
+      } else {
+        const int n = min(kVec, ch.len - off);
+        for (int i = 0; i < n; ++i) {
+          const int64_t k = e + i;
+          float p = MODE == ADAMW_MODE_FP32
+                        ? pf[k]
+                        : rem_join(ph[k], static_cast<uint16_t>(pr[k]));
+          float m = mf[k], v = vf[k];
+          update(p, Grad<GT>::load1(g, k), m, v, s, decay);
+          if (MODE == ADAMW_MODE_FP32) {
+            pf[k] = p;
+          } else {
+            uint32_t h, r;
+            rem_split(p, h, r);
+            ph[k] = static_cast<uint16_t>(h);
+            pr[k] = static_cast<int16_t>(static_cast<uint16_t>(r));
+          }
+          mf[k] = m;
+          vf[k] = v;
+        }
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- 8-bit states
+// Nearest code of x in one map: the bucket of |x| gives the lowest code any x
+// of that bucket can have; at most `refine` thresholds lie inside a bucket,
+// and code = lo + #{r : thr[lo + r] <= x} because thr is ascending.
+__device__ __forceinline__ uint32_t nearest_code(float x, const QMapDev& t, int refine) {
+  const uint32_t b = __float_as_uint(x);
+  const uint32_t mag = b & 0x7FFFFFFFu;
+  if (mag > 0x7F800000u) return 0u;  // NaN
+  const int k = bucket_of(mag);
+  const uint32_t lo = (b >> 31) ? t.lo_neg[k] : t.lo_pos[k];
+  uint32_t c = lo;
+#pragma unroll
+  for (int r = 0; r < kMaxRefine; ++r)
+    if (r < refine) c += (t.thr[lo + r] <= x) ? 1u : 0u;
+  return c;
+}
+
+__device__ __forceinline__ uint32_t quant(float x, uint32_t amax_bits, float amax,
+                                          const QMapDev& t, int zero_code, int refine) {
+  if (amax_bits == 0u) return static_cast<uint32_t>(zero_code);
+  return nearest_code(__fdiv_rn(x, amax), t, refine);
+}
+
+template <typename GT>
+__global__ void __launch_bounds__(kThreads) step_q8_kernel(const StepArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  QTables& qt = *reinterpret_cast<QTables*>(smem_raw);
+  __shared__ Scal s_sc;
+  __shared__ int s_skip;
+  if (threadIdx.x == 0) s_skip = prologue(a, s_sc);
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(a.qt);
+    uint4* dst = reinterpret_cast<uint4*>(smem_raw);
+    for (int i = threadIdx.x; i < static_cast<int>(sizeof(QTables) / 16); i += kThreads)
+      dst[i] = src[i];
+  }
+  __syncthreads();
+  if (s_skip) return;
+  const Scal s = s_sc;
+  const int refine = qt.refine;
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+
+  for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
+    const Chunk ch = a.chunks[c];
+    const TensorDesc& td = a.tensors[ch.tensor];
+    const float decay = __fsub_rn(1.0f, __fmul_rn(s.lr, td.wd));
+    const bool vec = td.vec_ok != 0;
+    float* const pf = static_cast<float*>(td.p);
+    uint8_t* const cm = static_cast<uint8_t*>(td.m);
+    uint8_t* const cv = static_cast<uint8_t*>(td.v);
+    const void* const g = td.g;
+
+    // warp w owns the 256-element block starting at `wb` of every pass
+    for (int wb = warp * kQBlock; wb < ch.len; wb += kPass) {
+      const int64_t e0 = ch.start + wb;            // block-aligned within the tensor
+      const int64_t blk = e0 / kQBlock;
+      const int off = wb + lane * kVec;
+      const int n = max(0, min(kVec, ch.len - off));
+      const int64_t e = ch.start + off;
+      const float am = td.am[blk], av = td.av[blk];
+
+      float p[8], gr[8], m[8], v[8];
+      if (vec && n == kVec) {
+        ld8f(pf + e, p);
+        Grad<GT>::load8(g, e, gr);
+        const uint2 qm = __ldcs(reinterpret_cast<const uint2*>(cm + e));
+        const uint2 qv = __ldcs(reinterpret_cast<const uint2*>(cv + e));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t wm = i < 4 ? qm.x : qm.y, wv = i < 4 ? qv.x : qv.y;
+          const int sh = (i & 3) * 8;
+          m[i] = __fmul_rn(qt.map[0].value[(wm >> sh) & 0xFFu], am);
+          v[i] = __fmul_rn(qt.map[1].value[(wv >> sh) & 0xFFu], av);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (i < n) {
+            p[i] = pf[e + i];
+            gr[i] = Grad<GT>::load1(g, e + i);
+            m[i] = __fmul_rn(qt.map[0].value[cm[e + i]], am);
+            v[i] = __fmul_rn(qt.map[1].value[cv[e + i]], av);
+          } else {
+            p[i] = gr[i] = m[i] = v[i] = 0.0f;
+          }
+        }
+      }
+      uint32_t mx_m = 0u, mx_v = 0u;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        if (i < n) {
+          update(p[i], gr[i], m[i], v[i], s, decay);
+          mx_m = max(mx_m, __float_as_uint(m[i]) & 0x7FFFFFFFu);
+          mx_v = max(mx_v, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+        }
+      }
+      mx_m = __reduce_max_sync(0xFFFFFFFFu, mx_m);
+      mx_v = __reduce_max_sync(0xFFFFFFFFu, mx_v);
+      const float Am = __uint_as_float(mx_m), Av = __uint_as_float(mx_v);
+      uint32_t q_m[8], q_v[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        q_m[i] = quant(m[i], mx_m, Am, qt.map[0], qt.zero_code[0], refine);
+        q_v[i] = quant(v[i], mx_v, Av, qt.map[1], qt.zero_code[1], refine);
+      }
+      if (vec && n == kVec) {
+        st8f(pf + e, p);
+        __stcs(reinterpret_cast<uint2*>(cm + e),
+               make_uint2(q_m[0] | q_m[1] << 8 | q_m[2] << 16 | q_m[3] << 24,
+                          q_m[4] | q_m[5] << 8 | q_m[6] << 16 | q_m[7] << 24));
+        __stcs(reinterpret_cast<uint2*>(cv + e),
+               make_uint2(q_v[0] | q_v[1] << 8 | q_v[2] << 16 | q_v[3] << 24,
+                          q_v[4] | q_v[5] << 8 | q_v[6] << 16 | q_v[7] << 24));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          if (i < n) {
+            pf[e + i] = p[i];
+            cm[e + i] = static_cast<uint8_t>(q_m[i]);
+            cv[e + i] = static_cast<uint8_t>(q_v[i]);
+          }
+        }
+      }
+      if (lane == 0) {
+        td.am[blk] = Am;
+        td.av[blk] = Av;
+      }
+    }
+  }
+}
+
+template <typename K>
+cudaError_t occ(K kernel, int smem, int* bps) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, kernel, kThreads, smem);
+}
+
+template <typename GT>
+cudaError_t launch_mode(adamw_mode mode, const StepArgs& a, int grid, cudaStream_t st) {
+  switch (mode) {
+    case ADAMW_MODE_FP32:
+      step_kernel<ADAMW_MODE_FP32, GT><<<grid, kThreads, 0, st>>>(a);
+      break;
+    case ADAMW_MODE_BF16_REM:
+      step_kernel<ADAMW_MODE_BF16_REM, GT><<<grid, kThreads, 0, st>>>(a);
+      break;
+    case ADAMW_MODE_Q8:
+      step_q8_kernel<GT><<<grid, kThreads, sizeof(QTables), st>>>(a);
+      break;
+    default:
+      return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+template <typename GT>
+cudaError_t occupancy_mode(adamw_mode mode, int* bps, int* smem) {
+  switch (mode) {
+    case ADAMW_MODE_FP32:
+      *smem = 0;
+      return occ(step_kernel<ADAMW_MODE_FP32, GT>, 0, bps);
+    case ADAMW_MODE_BF16_REM:
+      *smem = 0;
+      return occ(step_kernel<ADAMW_MODE_BF16_REM, GT>, 0, bps);
+    case ADAMW_MODE_Q8:
+      *smem = static_cast<int>(sizeof(QTables));
+      return occ(step_q8_kernel<GT>, *smem, bps);
+    default:
+      return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_step(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int grid,
+                        cudaStream_t s) {
+  switch (gdt) {
+    case ADAMW_F32: return launch_mode<float>(mode, a, grid, s);
+    case ADAMW_F16: return launch_mode<__half>(mode, a, grid, s);
+    case ADAMW_BF16: return launch_mode<__nv_bfloat16>(mode, a, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t step_occupancy(adamw_mode mode, adamw_dtype gdt, int* bps, int* smem) {
+  switch (gdt) {
+    case ADAMW_F32: return occupancy_mode<float>(mode, bps, smem);
+    case ADAMW_F16: return occupancy_mode<__half>(mode, bps, smem);
+    case ADAMW_BF16: return occupancy_mode<__nv_bfloat16>(mode, bps, smem);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace adamw

@@ -1,0 +1,652 @@
+#!/usr/bin/env python3
+"""Throughput of the fused AdamW step on GB300 (params/s and achieved HBM GB/s).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload gpt2_small|single|amp|q8|llama3_8b]
+
+One "step" is one AdamW update of every tensor of the workload (one launch of
+the library's step kernel; plus the non-finite check in the AMP workload).
+The default workload is the GPT-2-small fp32 parameter list (148 tensors,
+124,439,808 elements) with a device learning rate on a cosine schedule.  Its
+inputs (3.48 GB moved per step) are larger than L2, so no flush is needed
+between steps; the L2-resident single-tensor workloads flush L2 between timed
+launches.  Inputs are synthetic and seeded (``synth``), resident in HBM before
+timing.  Under torchrun every rank runs its own copy of the workload on its own
+GPU (weak scaling; the update is element-wise and needs no exchange).
+
+``--impl reference`` times the CPU oracle (numpy, float64 definition) on a
+bounded sample of the same workload on the host cores instead.
+One JSON line is printed by rank 0.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "optimizer-step params/sec and achieved HBM GB/s (% of GB300 peak)"
+UNIT = "params/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gpt2_small",
+                    choices=["gpt2_small", "single", "amp", "q8", "llama3_8b"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured (MEASURED_PEAKS.json hbm_gbs, burst copy)"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    d = os.path.join(ROOT, "adamw_optimizer_step_tensor_gb300", "csrc")
+    for name in ("step_kernels.cu", "internal.h"):
+        with open(os.path.join(d, name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it still matches the source."""
+    path = os.path.join(ROOT, "profiles", f"step_kernel_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", txt)
+    tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not sha or not tr or sha.group(1) != kernel_source_sha():
+        return None
+    return float(tr.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms in the background."""
+
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t_begin: float, t_end: float):
+        import datetime
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+                except ValueError:
+                    continue
+        os.unlink(self.path)
+        sel = [r for r in rows if t_begin <= r[0] <= t_end]
+        note = None
+        if len(sel) < 3:
+            sel = rows
+            note = (f"timed region {(t_end - t_begin) * 1e3:.0f} ms holds fewer than 3 of the 200 ms "
+                    "samples; median over the whole run (warm-up and timed steps)")
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in sel for i in range(4) if r[3][i].lower() == "active"})
+        out = {"sm_mhz": statistics.median(r[1] for r in sel),
+               "sm_max_mhz": max(r[2] for r in sel), "reasons": reasons, "samples": len(sel)}
+        if note:
+            out["note"] = note
+        return out
+
+
+def dist_setup(gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+
+# ----------------------------------------------------------------------------- CPU samples
+def cpu_sample_fp32(n, amp=False, lr=1e-3, wd=0.1):
+    """One float64-oracle step over n elements per call (fp32-state workloads)."""
+    import numpy as np
+    from oracle import adamw as OA
+    rng = np.random.default_rng(0)
+    scale = 65536.0 if amp else None
+    g = rng.normal(0, 1e-3, n) * (scale or 1.0)
+    x = OA.Tensor(p=rng.normal(0, 0.02, n), g=g, m=np.zeros(n), v=np.zeros(n), wd=wd)
+    state = {"t": 0}
+
+    def run():
+        state["t"] += 1
+        OA.step_fp64([x], lr=lr, beta1=0.9, beta2=0.999, eps=1e-8, t=state["t"], grad_scale=scale)
+    return run, f"{n} elements per step, float64 oracle (oracle.adamw.step_fp64)"
+
+
+def cpu_sample_q8(n):
+    import numpy as np
+    from oracle import q8 as OQ
+    n = max(256, n // 256 * 256)
+    rng = np.random.default_rng(0)
+    p = rng.normal(0, 0.02, n).astype(np.float32)
+    g = rng.normal(0, 1e-3, n).astype(np.float32)
+    cm, cv = np.zeros(n, np.uint8), np.zeros(n, np.uint8)
+    am, av = np.zeros(n // 256, np.float32), np.zeros(n // 256, np.float32)
+    maps = OQ.Maps()
+    state = {"t": 0}
+
+    def run():
+        state["t"] += 1
+        OQ.step_f32(p, g, cm, cv, am, av, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.01,
+                    t=state["t"], maps=maps)
+    return run, f"{n} elements per step, strict-fp32 8-bit-state oracle (oracle.q8.step_f32)"
+
+
+def cpu_sample_bf16rem(n):
+    import numpy as np
+    from oracle import adamw as OA, remainder as OR
+    rng = np.random.default_rng(0)
+    hi = (rng.normal(0, 0.02, n).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    rem = rng.integers(0, 1 << 15, n).astype(np.int16)
+    g = rng.normal(0, 1e-4, n).astype(np.float32)
+    m, v = np.zeros(n, np.float32), np.zeros(n, np.float32)
+    state = {"t": 0, "hi": hi, "rem": rem}
+
+    def run():
+        state["t"] += 1
+        x = OA.Tensor(p=OR.join(state["hi"], state["rem"]), g=g, m=m, v=v, wd=0.1)
+        OA.step_f32([x], lr=3e-4, beta1=0.9, beta2=0.999, eps=1e-8, t=state["t"])
+        state["hi"], state["rem"] = OR.split(x.p)
+    return run, f"{n} elements per step, strict-fp32 oracle with remainder join/split"
+
+
+CPU_SAMPLES = {
+    "gpt2_small": lambda n: cpu_sample_fp32(n),
+    "single": lambda n: cpu_sample_fp32(n, lr=0.1),
+    "amp": lambda n: cpu_sample_fp32(n, amp=True, lr=0.1),
+    "q8": cpu_sample_q8,
+    "llama3_8b": cpu_sample_bf16rem,
+}
+
+# ----------------------------------------------------------------------------- workloads
+def _flat_views(specs, dtype, device, fill=None, align=64):
+    """One contiguous buffer holding every tensor, each starting 256-byte aligned."""
+    import torch
+    offs, o = [], 0
+    for s in specs:
+        offs.append(o)
+        o += (s.numel + align - 1) // align * align
+    buf = torch.zeros(o, dtype=dtype, device=device)
+    views = [buf[a:a + s.numel] for a, s in zip(offs, specs)]
+    return buf, views
+
+
+class Workload:
+    name = ""
+    bytes_per_param = 0.0
+    n_params = 0
+    launches_per_step = 1
+    flush_l2 = False
+    dtype = "f32"
+
+    def step(self, i):  # one optimizer step on the current stream
+        raise NotImplementedError
+
+    def e2e_step(self, i):
+        raise NotImplementedError
+
+
+
+class Gpt2Small(Workload):
+    name = "gpt2_small_fp32_cosine_lr"
+    bytes_per_param = 28.0
+
+    def __init__(self, seed=0):
+        import torch
+        import synth
+        from adamw_optimizer_step_tensor_gb300 import FusedAdamW, _capi
+        dev = torch.device("cuda")
+        self.C = _capi
+        self.specs = synth.gpt2_small()
+        self.n_params = synth.total_numel(self.specs)
+        self.p_buf, ps = _flat_views(self.specs, torch.float32, dev)
+        self.g_buf, gs = _flat_views(self.specs, torch.float32, dev)
+        self.m_buf, ms = _flat_views(self.specs, torch.float32, dev)
+        self.v_buf, vs = _flat_views(self.specs, torch.float32, dev)
+        for i, (p, g) in enumerate(zip(ps, gs)):
+            p.copy_(synth.normal(p.numel(), 0.02, seed + i, dev))
+            g.copy_(synth.normal(g.numel(), 1e-3, synth.grad_seed(seed, 0, i), dev))
+        self.opt = FusedAdamW(ps, gs, ms, vs, [s.wd for s in self.specs])
+        self.lr_table = torch.tensor([synth.cosine_lr(s) for s in range(100)], dtype=torch.float32,
+                                     device=dev)
+        self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.lr_ptrs = [self.lr_table.data_ptr() + 4 * s for s in range(100)]
+        self.stream = torch.cuda.current_stream().cuda_stream
+        self.config = {"workload": "gpt2_small fp32 param list, cosine lr from a device table",
+                       "tensors": len(self.specs), "numel": self.n_params,
+                       "bytes_per_param": self.bytes_per_param,
+                       "grad_dtype": "f32", "state_dtype": "f32",
+                       "l2": "no flush: 3.48 GB moved per step, larger than the 126 MB L2",
+                       "lr_schedule": "cosine 1e-3 -> 1e-4 over 100 steps, lr_dev points into it"}
+        self._host = None
+
+    def step(self, i):
+        self.C.adamw_step(self.opt.plan, self.lr_ptrs[i % 100], self.step_dev.data_ptr(), 0.9, 0.999,
+                          1e-8, None, None, self.stream)
+
+    def e2e_setup(self):
+        import torch
+        self._host_g = torch.empty_like(self.g_buf, device="cpu").pin_memory()
+        self._host_g.copy_(self.g_buf)
+        self._host_p = torch.empty_like(self.p_buf, device="cpu").pin_memory()
+        return self._host_g.numel() * 4, self._host_p.numel() * 4
+
+    def e2e_step(self, i):
+        self.g_buf.copy_(self._host_g, non_blocking=True)
+        self.step(i)
+        self._host_p.copy_(self.p_buf, non_blocking=True)
+
+
+
+class Single(Workload):
+    name = "single_fp32_1M_l2flush"
+    bytes_per_param = 28.0
+    flush_l2 = True
+
+    def __init__(self, amp=False, seed=1):
+        import torch
+        import synth
+        from adamw_optimizer_step_tensor_gb300 import FusedAdamW, _capi
+        dev = torch.device("cuda")
+        self.C = _capi
+        self.amp = amp
+        n = self.n_params = 1 << 20
+        self.p = synth.normal(n, 0.02, seed, dev)
+        gd = torch.float16 if amp else torch.float32
+        self.g = (synth.normal(n, 1e-3, seed + 1, dev) * (65536.0 if amp else 1.0)).to(gd)
+        self.m = torch.zeros(n, device=dev)
+        self.v = torch.zeros(n, device=dev)
+        self.opt = FusedAdamW([self.p], [self.g], [self.m], [self.v], [0.1])
+        self.lr = torch.tensor([0.1], dtype=torch.float32, device=dev)
+        self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.scale = torch.tensor([65536.0], device=dev)
+        self.found = torch.zeros(1, device=dev)
+        self.stream = torch.cuda.current_stream().cuda_stream
+        self.launches_per_step = 2 if amp else 1
+        if amp:
+            self.name = "amp_fp16_grads_1M_l2flush"
+            self.bytes_per_param = 28.0
+            self.inject = synth.amp_injection(10 ** 6, n, seed=3)
+        self.config = {"workload": ("AMP fp16 grads x65536, fused unscale + found_inf skip, 1 tensor"
+                                    if amp else "single fp32 tensor"),
+                       "tensors": 1, "numel": n, "bytes_per_param": self.bytes_per_param,
+                       "l2": f"L2 flushed ({L2_FLUSH_BYTES >> 20} MB write) before every timed launch; "
+                             "launch times summed"}
+
+    def step(self, i):
+        if self.amp:
+            self.C.adamw_check_nonfinite(self.opt.plan, self.found.data_ptr(), self.stream)
+            self.C.adamw_step(self.opt.plan, self.lr.data_ptr(), self.step_dev.data_ptr(), 0.9, 0.999,
+                              1e-8, self.scale.data_ptr(), self.found.data_ptr(), self.stream)
+        else:
+            self.C.adamw_step(self.opt.plan, self.lr.data_ptr(), self.step_dev.data_ptr(), 0.9, 0.999,
+                              1e-8, None, None, self.stream)
+
+    def e2e_setup(self):
+        import torch
+        self._host_g = torch.empty_like(self.g, device="cpu").pin_memory()
+        self._host_g.copy_(self.g)
+        self._host_p = torch.empty_like(self.p, device="cpu").pin_memory()
+        return self._host_g.numel() * self._host_g.element_size(), self._host_p.numel() * 4
+
+    def e2e_step(self, i):
+        self.g.copy_(self._host_g, non_blocking=True)
+        self.step(i)
+        self._host_p.copy_(self.p, non_blocking=True)
+
+
+
+class Q8(Workload):
+    name = "q8_blockwise_1G"
+    bytes_per_param = 14.0625
+
+    def __init__(self, seed=4):
+        import torch
+        import synth
+        from adamw_optimizer_step_tensor_gb300 import FusedAdamW, _capi
+        dev = torch.device("cuda")
+        self.C = _capi
+        n = self.n_params = 1 << 30
+        self.p = synth.normal(n, 0.02, seed, dev)
+        self.g = synth.normal(n, 1e-3, seed + 1, dev, dtype=torch.bfloat16)
+        self.cm = torch.zeros(n, dtype=torch.uint8, device=dev)
+        self.cv = torch.zeros(n, dtype=torch.uint8, device=dev)
+        nb = n // 256
+        self.am = torch.zeros(nb, device=dev)
+        self.av = torch.zeros(nb, device=dev)
+        self.opt = FusedAdamW([self.p], [self.g], [self.cm], [self.cv], [0.01], mode="q8",
+                              absmax_m=[self.am], absmax_v=[self.av])
+        self.lr = torch.tensor([1e-3], dtype=torch.float32, device=dev)
+        self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream().cuda_stream
+        self.dtype = "f32 (u8 states)"
+        self.config = {"workload": "8-bit blockwise m,v; one flat fp32 param of 2^30, bf16 grads",
+                       "tensors": 1, "numel": n, "bytes_per_param": self.bytes_per_param,
+                       "l2": "no flush: 15.1 GB moved per step"}
+
+    def step(self, i):
+        self.C.adamw_step(self.opt.plan, self.lr.data_ptr(), self.step_dev.data_ptr(), 0.9, 0.999,
+                          1e-8, None, None, self.stream)
+
+    def e2e_setup(self):
+        import torch
+        self._host_g = torch.empty_like(self.g, device="cpu").pin_memory()
+        self._host_g.copy_(self.g)
+        self._host_p = torch.empty_like(self.p, device="cpu").pin_memory()
+        return self._host_g.numel() * 2, self._host_p.numel() * 4
+
+    def e2e_step(self, i):
+        self.g.copy_(self._host_g, non_blocking=True)
+        self.step(i)
+        self._host_p.copy_(self.p, non_blocking=True)
+
+
+
+class Llama3(Workload):
+    name = "llama3_8b_bf16_rem"
+    bytes_per_param = 26.0
+
+    def __init__(self, seed=5):
+        import torch
+        import synth
+        from adamw_optimizer_step_tensor_gb300 import FusedAdamW, _capi
+        dev = torch.device("cuda")
+        self.C = _capi
+        self.specs = synth.llama3_8b()
+        self.n_params = synth.total_numel(self.specs)
+        _, hs = _flat_views(self.specs, torch.bfloat16, dev)
+        _, rs = _flat_views(self.specs, torch.int16, dev)
+        _, gs = _flat_views(self.specs, torch.bfloat16, dev)
+        _, ms = _flat_views(self.specs, torch.float32, dev)
+        _, vs = _flat_views(self.specs, torch.float32, dev)
+        for i, (h, r, g, s) in enumerate(zip(hs, rs, gs, self.specs)):
+            if "norm" in s.name:
+                h.fill_(1.0)
+            else:
+                hi, rem = synth.bf16_params_with_remainders(s.numel, 0.02, seed + i, dev)
+                h.copy_(hi)
+                r.copy_(rem)
+                del hi, rem
+            g.copy_(synth.normal(s.numel, 1e-4, synth.grad_seed(seed, 0, i), dev, torch.bfloat16))
+        self.opt = FusedAdamW(hs, gs, ms, vs, [s.wd for s in self.specs], mode="bf16_rem",
+                              param_rems=rs)
+        self._views = (hs, rs, gs, ms, vs)
+        self.lr = torch.tensor([3e-4], dtype=torch.float32, device=dev)
+        self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream().cuda_stream
+        self.dtype = "f32 (bf16+int16 params)"
+        self.config = {"workload": "Llama-3-8B param list, bf16 params + int16 remainders",
+                       "tensors": len(self.specs), "numel": self.n_params,
+                       "bytes_per_param": self.bytes_per_param,
+                       "l2": "no flush: 209 GB moved per step"}
+
+    def step(self, i):
+        self.C.adamw_step(self.opt.plan, self.lr.data_ptr(), self.step_dev.data_ptr(), 0.9, 0.999,
+                          1e-8, None, None, self.stream)
+
+    def e2e_setup(self):
+        return None
+
+
+
+def make_workload(name):
+    return {"gpt2_small": Gpt2Small, "single": Single, "amp": lambda: Single(amp=True),
+            "q8": Q8, "llama3_8b": Llama3}[name]()
+
+
+# ----------------------------------------------------------------------------- CPU timing
+def time_cpu(run, n, budget_s, min_calls=1):
+    run()  # warm the caches / allocator
+    t0 = time.perf_counter()
+    calls = 0
+    while calls < min_calls or time.perf_counter() - t0 < budget_s:
+        run()
+        calls += 1
+    dt = time.perf_counter() - t0
+    return n * calls / dt, calls, dt
+
+
+def cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+# ----------------------------------------------------------------------------- main
+def run_reference(args, rank, world):
+    """The oracle as it stands, on the host cores, on a bounded sample of the workload."""
+    if rank != 0:
+        return 0
+    make = CPU_SAMPLES[args.workload]
+    run, _ = make(1 << 16)                     # calibrate: seconds per element
+    t0 = time.perf_counter()
+    run()
+    per_elem = (time.perf_counter() - t0) / (1 << 16)
+    budget = 120.0                             # whole --steps/--warmup run within ~2 minutes
+    n = int(budget / max(1, args.steps + args.warmup) / max(per_elem, 1e-12))
+    n = max(4096, min(1 << 24, n // 256 * 256))
+    run, desc = make(n)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = time.perf_counter() - t0
+    value = n * args.steps / dt
+    sample = f"{desc}; numpy, single-threaded ({cpu_threads()} host cores present)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": args.workload, "sample_elements_per_step": n},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+
+    import torch
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    w = make_workload(args.workload)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda") if w.flush_l2 else None
+
+    for i in range(max(3, args.warmup)):
+        w.step(i)
+    torch.cuda.synchronize()
+
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    region0 = torch.cuda.Event(enable_timing=True)
+    region1 = torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_begin = time.time()
+    region0.record(stream)
+    for i in range(K):
+        if flush is not None:
+            flush.zero_()
+        starts[i].record(stream)
+        w.step(args.warmup + i)
+        ends[i].record(stream)
+    region1.record(stream)
+    torch.cuda.synchronize()
+    t_end = time.time()
+    barrier(world)
+    time.sleep(0.3)
+    clocks.stop()
+    clk = clocks.summary(t_begin, t_end)
+
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    region_ms = region0.elapsed_time(region1)
+    step_ms = sum(launch_ms) / K if flush is not None else region_ms / K
+    step_ms = max_over_ranks(step_ms, world)
+    value = w.n_params * world / (step_ms * 1e-3)
+    kernel_ms = statistics.mean(launch_ms)
+    alg_bytes = w.bytes_per_param * w.n_params
+    achieved = alg_bytes / (kernel_ms * 1e-3) / 1e9
+    peak, peak_src = measured_peak()
+
+    # ---- end to end through the C ABI with pinned host buffers
+    e2e = None
+    setup = w.e2e_setup() if hasattr(w, "e2e_setup") else None
+    if setup is not None and args.e2e_steps > 0:
+        h2d, d2h = setup
+        for i in range(3):
+            w.e2e_step(i)
+        torch.cuda.synchronize()
+        barrier(world)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.e2e_steps):
+            w.e2e_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world)
+        e2e = {"value": w.n_params * world / (e2e_ms * 1e-3), "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+               "ms_per_step": e2e_ms,
+               "what": "pinned-host grads -> device, adamw_step, updated params -> pinned host"}
+    else:
+        e2e = {"value": None, "unit": UNIT, "h2d_bytes_per_step": None, "d2h_bytes_per_step": None,
+               "note": "no pinned-host copy of this workload's buffers fits beside it"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = 1 << 22
+        run, desc = CPU_SAMPLES[args.workload](n)
+        v, calls, dt = time_cpu(run, n, args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"{desc}; {calls} steps in {dt:.1f} s, numpy single-threaded "
+                         f"({cpu_threads()} host cores present)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": step_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": dict(w.config, parallelism=f"replicas x{world}" if world > 1 else "1 GPU"),
+            "achieved_hbm_gbs": achieved,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": ncu_traffic(args.workload),
+                         "peak_source": peak_src, "kernel_ms": kernel_ms,
+                         "algorithmic_bytes_per_launch": alg_bytes},
+            "e2e": e2e,
+            "gpu_launches": K * w.launches_per_step,
+            "clocks": clk,
+            "cpu_baseline": cpu,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,199 @@
+/*
+ * adamw.h -- C ABI of libadamw: a fused AdamW optimizer step for sm_103a (GB300).
+ *
+ * The step follows "Fix decoupled weight decay ordering in the CUDA
+ * Adam/AdEMAMix kernels" (bitsandbytes PR #2040), PR description: weight decay
+ * and the gradient-based update are both taken from the previous parameter,
+ *     p <- p * (1 - lr*wd) - (lr / bc1) * m / (sqrt(v) / sqrt(bc2) + eps),
+ * with m <- b1*m + (1-b1)*g, v <- b2*v + (1-b2)*g*g, bc1 = 1 - b1^t,
+ * bc2 = 1 - b2^t, and eps added after the bias correction of sqrt(v) as in the
+ * AdamW branch of the AdamWMini listing on "Adam-mini <> DTensor".
+ *
+ * Arithmetic contract.  Every element is updated in float32 with exactly one
+ * IEEE round-to-nearest-even rounding per operation, no fused multiply-add,
+ * in this order:
+ *     g  = g_raw [* inv_scale]        inv_scale = 1 / *grad_scale_dev
+ *     m' = b1*m + (1-b1)*g
+ *     v' = b2*v + (1-b2)*(g*g)
+ *     u  = m' / (sqrt(v') / sqrt_bc2 + eps)
+ *     p' = p*(1 - lr*wd) - (lr/bc1)*u
+ * where b^t is float64 square-and-multiply, and bc1 = 1 - b1^t and
+ * sqrt_bc2 = sqrt(1 - b2^t) are float64 values rounded once to float32.
+ * Results are therefore reproducible bit for bit by any IEEE float32
+ * implementation of the same sequence.
+ *
+ * Conventions shared by all entry points
+ *   - Every tensor, scalar and stream is owned by the caller.  Pointers named
+ *     *_dev and all tensor pointers are device pointers on the device that
+ *     was current when the plan was created.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Device work is asynchronous on it; no entry point that takes
+ *     a stream synchronises the host or allocates memory.
+ *   - Arguments are validated before any launch; a non-OK status means
+ *     nothing was enqueued.  adamw_last_error() returns a message for the
+ *     last non-OK status of the calling thread.  Nothing is thrown across
+ *     the ABI.
+ *   - A plan must not be used by two steps that may run concurrently (it
+ *     holds a small device counter used to advance the step count).
+ */
+#ifndef ADAMW_GB300_H
+#define ADAMW_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ADAMW_ABI_VERSION 1
+#define ADAMW_Q8_BLOCK 256
+
+typedef enum {
+  ADAMW_OK = 0,
+  ADAMW_EINVAL = 1,       /* null/negative/inconsistent argument */
+  ADAMW_EALIGN = 2,       /* a pointer is not aligned to its element size */
+  ADAMW_EDTYPE = 3,       /* unknown dtype or mode value */
+  ADAMW_ENOMEM = 4,       /* plan allocation failed */
+  ADAMW_ECUDA = 5,        /* a CUDA runtime call or launch failed */
+  ADAMW_EUNSUPPORTED = 6  /* a valid but unsupported combination */
+} adamw_status;
+
+typedef enum { ADAMW_F32 = 0, ADAMW_F16 = 1, ADAMW_BF16 = 2 } adamw_dtype;
+
+/* Parameter / state storage of every tensor in a plan. */
+typedef enum {
+  /* fp32 param, fp32 m and v. */
+  ADAMW_MODE_FP32 = 0,
+  /* bf16 model param plus an int16 remainder per element that together hold
+   * the fp32 master exactly ("Support store_param_remainders feature from
+   * Apex in TE Fused Adam #1408", Description); fp32 m and v.  The pair is
+   * joined to the fp32 master, updated, and split again in registers; the
+   * split is adamw_bf16rem_split's. */
+  ADAMW_MODE_BF16_REM = 1,
+  /* fp32 param; m and v stored as uint8 codes into a signed (m) and an
+   * unsigned (v) 256-entry code map with one fp32 absmax per 256-element
+   * block of each tensor (the 8-bit blockwise 2-state step named in the
+   * bitsandbytes PR above).  Per block: dequantise, update with the
+   * unquantised m', v', then absmax = max|m'| and code = nearest map entry
+   * to m'/absmax (exact tie -> lower code; all-zero block -> absmax 0 and
+   * the code of 0.0). */
+  ADAMW_MODE_Q8 = 2
+} adamw_mode;
+
+/* One parameter tensor, flat and contiguous (numel elements). */
+typedef struct {
+  void* param;          /* fp32 [numel]; bf16 [numel] in BF16_REM mode       */
+  int16_t* param_rem;   /* BF16_REM: int16 [numel]; otherwise must be NULL    */
+  const void* grad;     /* grad_dtype [numel], possibly loss-scaled           */
+  void* exp_avg;        /* m: fp32 [numel]; uint8 codes [numel] in Q8 mode    */
+  void* exp_avg_sq;     /* v: fp32 [numel]; uint8 codes [numel] in Q8 mode    */
+  float* absmax_m;      /* Q8: fp32 [ceil(numel/256)]; otherwise NULL         */
+  float* absmax_v;      /* Q8: fp32 [ceil(numel/256)]; otherwise NULL         */
+  int64_t numel;        /* >= 0; tensors with numel 0 are ignored             */
+  float weight_decay;   /* per tensor (e.g. 0 for norms and biases)           */
+} adamw_tensor;
+
+typedef struct adamw_plan adamw_plan;
+
+/*
+ * Build a plan for a fixed tensor list: validates every tensor, splits the
+ * list into chunks of contiguous elements, and uploads the chunk and tensor
+ * tables (and, in Q8 mode, the default code maps) to the current device.
+ * The multi-tensor chunk list plays the role of the multi_tensor_adam lists
+ * on the TransformerEngine page: one launch covers every tensor.
+ * Pointers must be aligned to their element size (EALIGN otherwise); tensors
+ * whose pointers are all 16-byte aligned take the 128-bit vector path, the
+ * rest a scalar path.  Synchronous (allocates device memory and copies).
+ * On success *out owns the device tables until adamw_plan_destroy.
+ */
+adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors,
+                               adamw_mode mode, adamw_dtype grad_dtype,
+                               adamw_plan** out);
+
+/* Free a plan (NULL is allowed).  Synchronises with the device first. */
+adamw_status adamw_plan_destroy(adamw_plan* plan);
+
+/* Plan facts for logging: element count, chunk count, launch grid. Any
+ * output pointer may be NULL. */
+adamw_status adamw_plan_info(const adamw_plan* plan, int64_t* total_numel,
+                             int64_t* n_chunks, int32_t* grid_blocks,
+                             int32_t* block_threads);
+
+/*
+ * found_inf: "FusedAdam & PyTorch Lightning AMP" -- a fused step does the
+ * grad unscale itself and needs to know whether any grad is non-finite.
+ * Writes 0.0f to *found_inf_dev, then 1.0f if any raw grad element of the
+ * plan is +-inf or NaN.  Two stream-ordered operations (a 4-byte memset and
+ * one launch); the caller may instead supply its own flag to adamw_step.
+ */
+adamw_status adamw_check_nonfinite(const adamw_plan* plan, float* found_inf_dev,
+                                   void* stream);
+
+/*
+ * One AdamW step over every tensor of the plan, in one launch.
+ *   lr_dev         device fp32 learning rate, read by the kernel at run time,
+ *                  so a per-step schedule only rewrites 4 bytes (or points at
+ *                  another entry of a device schedule table) and nothing is
+ *                  rebuilt ("4 bit Adam should support non constant lr").
+ *   step_dev       device int32 count of completed steps; this step uses
+ *                  t = *step_dev + 1 and stores t there unless skipped.
+ *   beta1, beta2   in [0, 1); eps > 0 (float32).
+ *   grad_scale_dev NULL, or device fp32 loss scale: grads are multiplied by
+ *                  1 / *grad_scale_dev before use.
+ *   found_inf_dev  NULL, or device fp32 flag: when non-zero at run time the
+ *                  whole step is skipped -- params, states, absmax and
+ *                  *step_dev are left untouched.
+ */
+adamw_status adamw_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev,
+                        float beta1, float beta2, float eps,
+                        const float* grad_scale_dev, const float* found_inf_dev,
+                        void* stream);
+
+/*
+ * Remainder split / join (the rule used by ADAMW_MODE_BF16_REM).
+ *   split: lo = bits & 0xFFFF; bf16 = (bits >> 16) + (lo >= 0x8000) (mod 2^16);
+ *          rem = (int16)lo.  bf16 is the nearest bf16, ties away from zero.
+ *   join:  bits = ((bf16 - (rem < 0)) mod 2^16) << 16 | (uint16)rem.
+ * join(split(x)) == x for all 2^32 bit patterns.  n >= 0 elements; device
+ * pointers, each aligned to its element size.
+ */
+adamw_status adamw_bf16rem_split(const float* master, uint16_t* bf16, int16_t* rem,
+                                 int64_t n, void* stream);
+adamw_status adamw_bf16rem_join(const uint16_t* bf16, const int16_t* rem, float* master,
+                                int64_t n, void* stream);
+
+/*
+ * The default code maps (host arrays of 256 floats, ascending): dynamic
+ * exponent maps after Dettmers et al., arXiv:2110.02861 -- after the sign, E
+ * zero bits give 10^-E, a one bit, then F fraction bits splitting [0.1, 1]
+ * into 2^F equal bins (values at bin centres); signed: E = 0..6, F = 6-E,
+ * both signs; unsigned: F = 7-E; each plus exact 0 and +1.0.  Host only.
+ */
+adamw_status adamw_q8_default_maps(float signed_map[256], float unsigned_map[256]);
+
+/* Replace a Q8 plan's maps (host arrays, 256 strictly ascending finite
+ * floats each).  Synchronous.  EUNSUPPORTED if the maps are too dense for the
+ * kernel's bucketed nearest-code search. */
+adamw_status adamw_q8_set_maps(adamw_plan* plan, const float signed_map[256],
+                               const float unsigned_map[256]);
+
+/* Q8 state export / import with a plan's maps, blockwise over n elements
+ * (blocks of 256 from element 0).  which: 0 = m (signed map), 1 = v
+ * (unsigned map).  dequant: out = map[code] * absmax[block].  quant: absmax
+ * and nearest codes as in the step. */
+adamw_status adamw_q8_dequant(const adamw_plan* plan, int32_t which, const uint8_t* codes,
+                              const float* absmax, float* out, int64_t n, void* stream);
+adamw_status adamw_q8_quant(const adamw_plan* plan, int32_t which, const float* x,
+                            uint8_t* codes, float* absmax, int64_t n, void* stream);
+
+/* Message for the calling thread's last non-OK status ("" if none). */
+const char* adamw_last_error(void);
+
+/* ADAMW_ABI_VERSION of the loaded library. */
+int32_t adamw_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ADAMW_GB300_H */
