@@ -153,12 +153,24 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
       return fail(ADAMW_EALIGN, "tensor %d: a pointer is not aligned to its element size", i);
     d.vec_ok = aligned(t.param, 16) && aligned(t.grad, 16) && aligned(t.exp_avg, svec) &&
                aligned(t.exp_avg_sq, svec) && (!t.param_rem || aligned(t.param_rem, 16));
-    for (int64_t s = 0; s < t.numel; s += kChunk) {
-      const int64_t len = t.numel - s < kChunk ? t.numel - s : kChunk;
-      chunks.push_back(Chunk{s, i, static_cast<int32_t>(len)});
-    }
     total += t.numel;
   }
+
+  // Every argument is valid; only now touch the device.
+  int device = -1, sms = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  // Chunk size: the largest of 16384, 8192, 4096, 2048 elements that still gives
+  // every SM several chunks, so that small plans spread over the whole GPU.
+  int64_t chunk = kChunkMax;
+  while (chunk > kPass && total / chunk < 8LL * sms) chunk /= 2;
+  for (int32_t i = 0; i < n_tensors; ++i)
+    for (int64_t s = 0; s < td[i].numel; s += chunk) {
+      const int64_t len = td[i].numel - s < chunk ? td[i].numel - s : chunk;
+      chunks.push_back(Chunk{s, i, static_cast<int32_t>(len)});
+    }
 
   std::unique_ptr<adamw_plan, void (*)(adamw_plan*)> p(new adamw_plan, free_plan);
   p->mode = mode;
@@ -167,11 +179,7 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
   p->total_numel = total;
   p->n_chunks = static_cast<int64_t>(chunks.size());
 
-  cudaError_t e = cudaGetDevice(&p->device);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-  int sms = 0;
-  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, p->device);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+  p->device = device;
   int bps = 0, smem = 0;
   e = step_occupancy(mode, grad_dtype, &bps, &smem);
   if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");

@@ -1,9 +1,9 @@
 // step_kernels.cu -- the fused AdamW step kernels for sm_103a.
 //
 // One persistent launch covers every tensor of a plan: CTAs stride over the
-// plan's chunk table (8192 contiguous elements of one tensor per chunk), and
-// each thread moves 8 consecutive elements per pass with 128-bit streaming
-// loads and stores.  The step is a pure HBM stream (28 B per element in fp32
+// plan's chunk table (2048-16384 contiguous elements of one tensor per chunk),
+// and each thread moves 8 consecutive elements per pass with 128-bit
+// streaming loads and stores.  The step is a pure HBM stream (28 B per element in fp32
 // mode, 26 in bf16+remainder mode, 14.06 in 8-bit mode), so there is no
 // tensor-core work; the kernel's job is to keep enough bytes in flight.
 //
@@ -151,8 +151,84 @@ __device__ __forceinline__ void rem_split(float x, uint32_t& hi, uint32_t& rem16
 }
 
 // ---------------------------------------------------------------- fp32 / bf16+rem
+// The 8 consecutive elements one thread owns in one pass, in registers.
+struct Group {
+  float p[8], g[8], m[8], v[8];
+};
+
 template <adamw_mode MODE, typename GT>
-__global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
+__device__ __forceinline__ void load_group(const TensorDesc& td, int64_t e, Group& x) {
+  if (MODE == ADAMW_MODE_FP32) {
+    ld8f(static_cast<const float*>(td.p) + e, x.p);
+  } else {
+    uint32_t hw[4], rw[4];
+    ld8u16(static_cast<const uint16_t*>(td.p) + e, hw);
+    ld8u16(td.rem + e, rw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      x.p[2 * i] = rem_join(hw[i] & 0xFFFFu, rw[i] & 0xFFFFu);
+      x.p[2 * i + 1] = rem_join(hw[i] >> 16, rw[i] >> 16);
+    }
+  }
+  Grad<GT>::load8(td.g, e, x.g);
+  ld8f(static_cast<const float*>(td.m) + e, x.m);
+  ld8f(static_cast<const float*>(td.v) + e, x.v);
+}
+
+template <adamw_mode MODE>
+__device__ __forceinline__ void update_store_group(const TensorDesc& td, int64_t e, Group& x,
+                                                   const Scal& s, float decay) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) update(x.p[i], x.g[i], x.m[i], x.v[i], s, decay);
+  if (MODE == ADAMW_MODE_FP32) {
+    st8f(static_cast<float*>(td.p) + e, x.p);
+  } else {
+    uint32_t hw[4], rw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t h0, r0, h1, r1;
+      rem_split(x.p[2 * i], h0, r0);
+      rem_split(x.p[2 * i + 1], h1, r1);
+      hw[i] = h0 | (h1 << 16);
+      rw[i] = r0 | (r1 << 16);
+    }
+    st8u16(static_cast<uint16_t*>(td.p) + e, hw);
+    st8u16(td.rem + e, rw);
+  }
+  st8f(static_cast<float*>(td.m) + e, x.m);
+  st8f(static_cast<float*>(td.v) + e, x.v);
+}
+
+// Elements [e, e + n) one at a time: ragged tails and tensors whose pointers
+// are not all 16-byte aligned.
+template <adamw_mode MODE, typename GT>
+__device__ void update_scalar(const TensorDesc& td, int64_t e, int n, const Scal& s,
+                              float decay) {
+  float* const pf = static_cast<float*>(td.p);
+  uint16_t* const ph = static_cast<uint16_t*>(td.p);
+  float* const mf = static_cast<float*>(td.m);
+  float* const vf = static_cast<float*>(td.v);
+  for (int i = 0; i < n; ++i) {
+    const int64_t k = e + i;
+    float p = MODE == ADAMW_MODE_FP32 ? pf[k] : rem_join(ph[k], static_cast<uint16_t>(td.rem[k]));
+    float m = mf[k], v = vf[k];
+    update(p, Grad<GT>::load1(td.g, k), m, v, s, decay);
+    if (MODE == ADAMW_MODE_FP32) {
+      pf[k] = p;
+    } else {
+      uint32_t h, r;
+      rem_split(p, h, r);
+      ph[k] = static_cast<uint16_t>(h);
+      td.rem[k] = static_cast<int16_t>(static_cast<uint16_t>(r));
+    }
+    mf[k] = m;
+    vf[k] = v;
+  }
+}
+
+template <adamw_mode MODE, typename GT>
+__global__ void __launch_bounds__(kThreads, Tune<MODE>::min_blocks) step_kernel(const StepArgs a) {
+  constexpr int kUnroll = Tune<MODE>::unroll;
   __shared__ Scal s_sc;
   __shared__ int s_skip;
   if (threadIdx.x == 0) s_skip = prologue(a, s_sc);
@@ -162,75 +238,24 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const StepArgs a) {
 
   for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
     const Chunk ch = a.chunks[c];
-    const TensorDesc& td = a.tensors[ch.tensor];
+    const TensorDesc td = a.tensors[ch.tensor];
     const float decay = __fsub_rn(1.0f, __fmul_rn(s.lr, td.wd));
     const bool vec = td.vec_ok != 0;
-    float* const pf = static_cast<float*>(td.p);
-    uint16_t* const ph = static_cast<uint16_t*>(td.p);
-    int16_t* const pr = td.rem;
-    float* const mf = static_cast<float*>(td.m);
-    float* const vf = static_cast<float*>(td.v);
-    const void* const g = td.g;
-
-    for (int off = threadIdx.x * kVec; off < ch.len; off += kPass) {
-      const int64_t e = ch.start + off;
-      if (vec && off + kVec <= ch.len) {
-        float p[8], gr[8], m[8], v[8];
-        uint32_t hw[4], rw[4];
-        if (MODE == ADAMW_MODE_FP32) {
-          ld8f(pf + e, p);
-        } else {
-          ld8u16(ph + e, hw);
-          ld8u16(pr + e, rw);
-        }
-        Grad<GT>::load8(g, e, gr);
-        ld8f(mf + e, m);
-        ld8f(vf + e, v);
-        if (MODE == ADAMW_MODE_BF16_REM) {
+    // kUnroll passes per trip: all their loads are issued before any update
+    for (int base = threadIdx.x * kVec; base < ch.len; base += kPass * kUnroll) {
+      Group x[kUnroll];
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            p[2 * i] = rem_join(hw[i] & 0xFFFFu, rw[i] & 0xFFFFu);
-            p[2 * i + 1] = rem_join(hw[i] >> 16, rw[i] >> 16);
-          }
-        }
+      for (int u = 0; u < kUnroll; ++u) {
+        const int off = base + u * kPass;
+        if (vec && off + kVec <= ch.len) load_group<MODE, GT>(td, ch.start + off, x[u]);
+      }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) update(p[i], gr[i], m[i], v[i], s, decay);
-        if (MODE == ADAMW_MODE_FP32) {
-          st8f(pf + e, p);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            uint32_t h0, r0, h1, r1;
-            rem_split(p[2 * i], h0, r0);
-            rem_split(p[2 * i + 1], h1, r1);
-            hw[i] = h0 | (h1 << 16);
-            rw[i] = r0 | (r1 << 16);
-          }
-          st8u16(ph + e, hw);
-          st8u16(pr + e, rw);
-        }
-        st8f(mf + e, m);
-        st8f(vf + e, v);
-      } else {
-        const int n = min(kVec, ch.len - off);
-        for (int i = 0; i < n; ++i) {
-          const int64_t k = e + i;
-          float p = MODE == ADAMW_MODE_FP32
-                        ? pf[k]
-                        : rem_join(ph[k], static_cast<uint16_t>(pr[k]));
-          float m = mf[k], v = vf[k];
-          update(p, Grad<GT>::load1(g, k), m, v, s, decay);
-          if (MODE == ADAMW_MODE_FP32) {
-            pf[k] = p;
-          } else {
-            uint32_t h, r;
-            rem_split(p, h, r);
-            ph[k] = static_cast<uint16_t>(h);
-            pr[k] = static_cast<int16_t>(static_cast<uint16_t>(r));
-          }
-          mf[k] = m;
-          vf[k] = v;
-        }
+      for (int u = 0; u < kUnroll; ++u) {
+        const int off = base + u * kPass;
+        if (vec && off + kVec <= ch.len)
+          update_store_group<MODE>(td, ch.start + off, x[u], s, decay);
+        else if (off < ch.len)
+          update_scalar<MODE, GT>(td, ch.start + off, min(kVec, ch.len - off), s, decay);
       }
     }
   }
@@ -260,7 +285,7 @@ __device__ __forceinline__ uint32_t quant(float x, uint32_t amax_bits, float ama
 }
 
 template <typename GT>
-__global__ void __launch_bounds__(kThreads) step_q8_kernel(const StepArgs a) {
+__global__ void __launch_bounds__(kThreads, Tune<ADAMW_MODE_Q8>::min_blocks) step_q8_kernel(const StepArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   QTables& qt = *reinterpret_cast<QTables*>(smem_raw);
   __shared__ Scal s_sc;
