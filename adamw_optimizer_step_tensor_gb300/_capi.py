@@ -56,6 +56,9 @@ _SIGNATURES = {
     "adamw_check_nonfinite": (ctypes.c_int, [_vp, _vp, _vp]),
     "adamw_step": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                   _vp, _vp, _vp]),
+    "adamw_step_noalloc": (ctypes.c_int, [ctypes.POINTER(adamw_tensor), ctypes.c_int32, ctypes.c_int,
+                                          ctypes.c_int, _vp, _vp, ctypes.c_float, ctypes.c_float,
+                                          ctypes.c_float, _vp, _vp, _vp]),
     "adamw_bf16rem_split": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int64, _vp]),
     "adamw_bf16rem_join": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int64, _vp]),
     "adamw_q8_default_maps": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float),
@@ -131,6 +134,17 @@ def adamw_step(plan: int, lr_dev: int, step_dev: int, beta1: float, beta2: float
                grad_scale_dev: int | None, found_inf_dev: int | None, stream: int | None) -> None:
     _check(load().adamw_step(plan, lr_dev, step_dev, beta1, beta2, eps, grad_scale_dev,
                              found_inf_dev, stream))
+
+
+def adamw_step_noalloc(tensors: list[adamw_tensor], mode: int, grad_dtype: int, lr_dev: int,
+                       step_dev: int, beta1: float, beta2: float, eps: float,
+                       grad_scale_dev: int | None, found_inf_dev: int | None,
+                       stream: int | None) -> None:
+    """One step without allocating: for callers that cannot call cudaMalloc
+    and so cannot build a plan (see include/adamw.h for limits and rules)."""
+    arr = (adamw_tensor * max(1, len(tensors)))(*tensors)
+    _check(load().adamw_step_noalloc(arr, len(tensors), mode, grad_dtype, lr_dev, step_dev, beta1,
+                                     beta2, eps, grad_scale_dev, found_inf_dev, stream))
 
 
 def adamw_bf16rem_split(master: int, bf16: int, rem: int, n: int, stream: int | None) -> None:

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libadamw.so")
-SOURCES = ["capi.cpp", "qmap.cpp", "step_kernels.cu", "aux_kernels.cu"]
+SOURCES = ["capi.cpp", "qmap.cpp", "step_kernels.cu", "aux_kernels.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -101,6 +101,8 @@ adamw_status build_qtables(const float smap[256], const float umap[256], QTables
 
 }  // namespace
 
+void adamw::set_last_error(const char* msg) { g_err = msg; }
+
 extern "C" {
 
 const char* adamw_last_error(void) { return g_err.c_str(); }

@@ -87,6 +87,7 @@ __host__ __device__ __forceinline__ int bucket_of(uint32_t mag) {
 
 // Launchers implemented in the kernel translation units.
 namespace adamw {
+void set_last_error(const char* msg);  // message returned by adamw_last_error()
 cudaError_t launch_step(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int grid,
                         cudaStream_t s);
 cudaError_t step_occupancy(adamw_mode mode, adamw_dtype gdt, int* blocks_per_sm,

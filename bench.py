@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--numel", type=int, default=0,
+                    help="element count override for the single/amp/q8 workloads (profiling)")
     return ap.parse_args()
 
 
@@ -332,14 +334,14 @@ class Single(Workload):
     bytes_per_param = 28.0
     flush_l2 = True
 
-    def __init__(self, amp=False, seed=1):
+    def __init__(self, amp=False, seed=1, numel=0):
         import torch
         import synth
         from adamw_optimizer_step_tensor_gb300 import FusedAdamW, _capi
         dev = torch.device("cuda")
         self.C = _capi
         self.amp = amp
-        n = self.n_params = 1 << 20
+        n = self.n_params = numel or (1 << 20)
         self.p = synth.normal(n, 0.02, seed, dev)
         gd = torch.float16 if amp else torch.float32
         self.g = (synth.normal(n, 1e-3, seed + 1, dev) * (65536.0 if amp else 1.0)).to(gd)
@@ -389,18 +391,18 @@ class Q8(Workload):
     name = "q8_blockwise_1G"
     bytes_per_param = 14.0625
 
-    def __init__(self, seed=4):
+    def __init__(self, seed=4, numel=0):
         import torch
         import synth
         from adamw_optimizer_step_tensor_gb300 import FusedAdamW, _capi
         dev = torch.device("cuda")
         self.C = _capi
-        n = self.n_params = 1 << 30
+        n = self.n_params = numel or (1 << 30)
         self.p = synth.normal(n, 0.02, seed, dev)
         self.g = synth.normal(n, 1e-3, seed + 1, dev, dtype=torch.bfloat16)
         self.cm = torch.zeros(n, dtype=torch.uint8, device=dev)
         self.cv = torch.zeros(n, dtype=torch.uint8, device=dev)
-        nb = n // 256
+        nb = (n + 255) // 256
         self.am = torch.zeros(nb, device=dev)
         self.av = torch.zeros(nb, device=dev)
         self.opt = FusedAdamW([self.p], [self.g], [self.cm], [self.cv], [0.01], mode="q8",
@@ -478,9 +480,10 @@ class Llama3(Workload):
 
 
 
-def make_workload(name):
-    return {"gpt2_small": Gpt2Small, "single": Single, "amp": lambda: Single(amp=True),
-            "q8": Q8, "llama3_8b": Llama3}[name]()
+def make_workload(name, numel=0):
+    return {"gpt2_small": lambda: Gpt2Small(), "single": lambda: Single(numel=numel),
+            "amp": lambda: Single(amp=True, numel=numel), "q8": lambda: Q8(numel=numel),
+            "llama3_8b": lambda: Llama3()}[name]()
 
 
 # ----------------------------------------------------------------------------- CPU timing
@@ -547,7 +550,7 @@ def main():
         print(json.dumps({"error": "no CUDA device"}))
         return 1
     torch.cuda.set_device(local)
-    w = make_workload(args.workload)
+    w = make_workload(args.workload, args.numel)
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda") if w.flush_l2 else None
 

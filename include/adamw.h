@@ -150,6 +150,40 @@ adamw_status adamw_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev
                         void* stream);
 
 /*
+ * adamw_step_noalloc -- one AdamW step over a tensor list without any memory
+ * allocation.  The pages have no counterpart: this entry point exists for
+ * callers that cannot call cudaMalloc (a caching allocator already owns the
+ * free device memory, an allocation inside the training or serving loop is
+ * not allowed because it can synchronise or fail late, or an embedding
+ * application permits no allocation outside its own pool), and therefore
+ * cannot build a plan.
+ *
+ * Arguments are those of adamw_plan_create followed by those of adamw_step,
+ * with the same meaning, validation and arithmetic; the result of a call is
+ * bit-identical to adamw_plan_create + adamw_step on the same inputs.  Modes
+ * ADAMW_MODE_FP32 and ADAMW_MODE_BF16_REM only (EUNSUPPORTED otherwise).
+ *
+ * Instead of plan memory the call uses one static device array built into the
+ * library (about 1.1 MB on every GPU that loads it, held until the process
+ * exits).  Limits: at most 1024 tensors and 65536 chunks per call (chunks are
+ * 2048-16384 elements, about 1.07e9 elements in all); larger lists are rejected
+ * with ADAMW_EINVAL before anything is enqueued.  Each call copies the tensor
+ * and chunk tables from a static host buffer into the array (a pageable
+ * host-to-device copy, which may make the host wait for the stream) and clears
+ * the array's step counter, then launches the step kernel.
+ * The first call on each device looks up the array's device address with that
+ * device current; make that first call before any stream capture.  All calls
+ * share the one array: calls whose work may overlap on the GPU (different
+ * streams without ordering between them) race and must not be issued.
+ */
+adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t n_tensors,
+                                adamw_mode mode, adamw_dtype grad_dtype,
+                                const float* lr_dev, int32_t* step_dev,
+                                float beta1, float beta2, float eps,
+                                const float* grad_scale_dev, const float* found_inf_dev,
+                                void* stream);
+
+/*
  * Remainder split / join (the rule used by ADAMW_MODE_BF16_REM).
  *   split: lo = bits & 0xFFFF; bf16 = (bits >> 16) + (lo >= 0x8000) (mod 2^16);
  *          rem = (int16)lo.  bf16 is the nearest bf16, ties away from zero.
