@@ -113,6 +113,8 @@ __global__ void q8_quant_kernel(const QTables* __restrict__ qt, int which,
     }
     mx = __reduce_max_sync(0xFFFFFFFFu, mx);
     const float A = __uint_as_float(mx);
+    const float scale = A < kTinyAbsmax ? kTinyScale : 1.0f;
+    const float inv = __frcp_rn(__fmul_rn(A, scale));
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
       const int64_t e = b * kQBlock + lane * 8 + i;
@@ -121,7 +123,7 @@ __global__ void q8_quant_kernel(const QTables* __restrict__ qt, int which,
       if (mx == 0u) {
         c = static_cast<uint32_t>(qt->zero_code[which]);
       } else {
-        const float q = __fdiv_rn(v[i], A);
+        const float q = __fmul_rn(__fmul_rn(v[i], scale), inv);
         const uint32_t bits = __float_as_uint(q);
         const uint32_t mag = bits & 0x7FFFFFFFu;
         if (mag > 0x7F800000u) {

@@ -31,6 +31,7 @@ struct adamw_plan {
   Chunk* d_chunks = nullptr;
   uint32_t* d_ticket = nullptr;
   QTables* d_qt = nullptr;
+  int refine = 1;              // Q8: thresholds per bucket lookup of the current maps
 };
 
 namespace {
@@ -210,6 +211,7 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
     default_maps(smap, umap);
     adamw_status st = build_qtables(smap, umap, qt.get());
     if (st != ADAMW_OK) return st;
+    p->refine = qt->refine;
     if ((e = cudaMalloc(&p->d_qt, sizeof(QTables))) != cudaSuccess)
       return fail(ADAMW_ENOMEM, "cudaMalloc(code maps): %s", cudaGetErrorString(e));
     if ((e = cudaMemcpy(p->d_qt, qt.get(), sizeof(QTables), cudaMemcpyHostToDevice)) != cudaSuccess)
@@ -282,6 +284,7 @@ adamw_status adamw_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev
   a.eps = eps;
   a.ticket = plan->d_ticket;
   a.qt = plan->d_qt;
+  a.refine = plan->refine;
   cudaError_t e = launch_step(plan->mode, plan->gdt, a, plan->grid, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "launch adamw step");
   return ADAMW_OK;
@@ -324,7 +327,9 @@ adamw_status adamw_q8_set_maps(adamw_plan* plan, const float signed_map[256],
   adamw_status st = build_qtables(signed_map, unsigned_map, qt.get());
   if (st != ADAMW_OK) return st;
   cudaError_t e = cudaMemcpy(plan->d_qt, qt.get(), sizeof(QTables), cudaMemcpyHostToDevice);
-  return e == cudaSuccess ? ADAMW_OK : cuda_fail(e, "upload code maps");
+  if (e != cudaSuccess) return cuda_fail(e, "upload code maps");
+  plan->refine = qt->refine;
+  return ADAMW_OK;
 }
 
 static adamw_status q8_io_check(const adamw_plan* plan, int32_t which, const void* a,

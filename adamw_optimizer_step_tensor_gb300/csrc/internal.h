@@ -73,15 +73,23 @@ struct StepArgs {
   float beta1, beta2, eps;
   uint32_t* ticket;           // plan-owned counter, zero between launches
   const QTables* qt;          // Q8 only
+  int refine;                 // Q8 only: thresholds per lookup (1, 2 or 4)
 };
 
-// Host-side bucket index of a non-negative float bit pattern (no NaN).
+// Bucket of a non-negative float bit pattern: 0 for |x| < 2^-24, then 128
+// buckets per binade (exponent and the top 7 mantissa bits) up to [1, 2),
+// everything larger in the last bucket.  (mag >> 16) is exponent * 128 plus
+// those 7 bits, so the bucket is one subtraction and a clamp.
 __host__ __device__ __forceinline__ int bucket_of(uint32_t mag) {
-  uint32_t e = mag >> 23;
-  if (e < 103u) return 0;
-  if (e > 127u) return kBuckets - 1;
-  return 1 + static_cast<int>((e - 103u) * 128u + ((mag >> 16) & 127u));
+  const int k = static_cast<int>(mag >> 16) - (103 * 128 - 1);
+  return k < 0 ? 0 : (k > kBuckets - 1 ? kBuckets - 1 : k);
 }
+
+// Normalisation of a block by its absmax A (both sides of the 8-bit path):
+// x * fl(1/A); below 2^-64 both are scaled by 2^64 first (exact) so that the
+// reciprocal cannot overflow.
+constexpr float kTinyAbsmax = 5.42101086242752217e-20f;   // 2^-64
+constexpr float kTinyScale = 1.84467440737095516e19f;     // 2^64
 
 }  // namespace adamw
 

@@ -185,6 +185,7 @@ extern "C" adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t 
   a.eps = eps;
   a.ticket = d_ticket;
   a.qt = nullptr;
+  a.refine = 1;
   const int64_t resident = static_cast<int64_t>(bps) * ds.sms;
   const int grid = static_cast<int>(n_chunks < 1 ? 1 : (n_chunks < resident ? n_chunks : resident));
   e = launch_step(mode, grad_dtype, a, grid, st);

@@ -263,29 +263,46 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::min_blocks) step_kernel(
 
 // ---------------------------------------------------------------- 8-bit states
 // Nearest code of x in one map: the bucket of |x| gives the lowest code any x
-// of that bucket can have; at most `refine` thresholds lie inside a bucket,
-// and code = lo + #{r : thr[lo + r] <= x} because thr is ascending.
-__device__ __forceinline__ uint32_t nearest_code(float x, const QMapDev& t, int refine) {
+// of that bucket can have; at most R thresholds lie inside a bucket, and
+// code = lo + #{r < R : thr[lo + r] <= x} because thr is ascending.
+template <int R>
+__device__ __forceinline__ uint32_t nearest_code(float x, const QMapDev& t) {
   const uint32_t b = __float_as_uint(x);
   const uint32_t mag = b & 0x7FFFFFFFu;
-  if (mag > 0x7F800000u) return 0u;  // NaN
   const int k = bucket_of(mag);
   const uint32_t lo = (b >> 31) ? t.lo_neg[k] : t.lo_pos[k];
   uint32_t c = lo;
 #pragma unroll
-  for (int r = 0; r < kMaxRefine; ++r)
-    if (r < refine) c += (t.thr[lo + r] <= x) ? 1u : 0u;
-  return c;
+  for (int r = 0; r < R; ++r) c += (t.thr[lo + r] <= x) ? 1u : 0u;
+  return mag > 0x7F800000u ? 0u : c;  // NaN -> code 0
 }
 
-__device__ __forceinline__ uint32_t quant(float x, uint32_t amax_bits, float amax,
-                                          const QMapDev& t, int zero_code, int refine) {
-  if (amax_bits == 0u) return static_cast<uint32_t>(zero_code);
-  return nearest_code(__fdiv_rn(x, amax), t, refine);
+// Per-warp block constants for re-quantisation: the absmax bits, the scale
+// (1, or 2^64 below 2^-64) and the reciprocal fl(1/(A*scale)).
+struct BlockNorm {
+  uint32_t bits;
+  float scale, inv;
+};
+
+__device__ __forceinline__ BlockNorm block_norm(uint32_t amax_bits) {
+  const float A = __uint_as_float(amax_bits);
+  BlockNorm n;
+  n.bits = amax_bits;
+  n.scale = A < kTinyAbsmax ? kTinyScale : 1.0f;
+  n.inv = __frcp_rn(__fmul_rn(A, n.scale));
+  return n;
 }
 
-template <typename GT>
-__global__ void __launch_bounds__(kThreads, Tune<ADAMW_MODE_Q8>::min_blocks) step_q8_kernel(const StepArgs a) {
+template <int R>
+__device__ __forceinline__ uint32_t quant(float x, const BlockNorm& n, const QMapDev& t,
+                                          int zero_code) {
+  if (n.bits == 0u) return static_cast<uint32_t>(zero_code);
+  return nearest_code<R>(__fmul_rn(__fmul_rn(x, n.scale), n.inv), t);
+}
+
+template <typename GT, int R>
+__global__ void __launch_bounds__(kThreads, Tune<ADAMW_MODE_Q8>::min_blocks)
+step_q8_kernel(const StepArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   QTables& qt = *reinterpret_cast<QTables*>(smem_raw);
   __shared__ Scal s_sc;
@@ -300,9 +317,9 @@ __global__ void __launch_bounds__(kThreads, Tune<ADAMW_MODE_Q8>::min_blocks) ste
   __syncthreads();
   if (s_skip) return;
   const Scal s = s_sc;
-  const int refine = qt.refine;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
+  const int zc_m = qt.zero_code[0], zc_v = qt.zero_code[1];
 
   for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
     const Chunk ch = a.chunks[c];
@@ -358,14 +375,13 @@ __global__ void __launch_bounds__(kThreads, Tune<ADAMW_MODE_Q8>::min_blocks) ste
           mx_v = max(mx_v, __float_as_uint(v[i]) & 0x7FFFFFFFu);
         }
       }
-      mx_m = __reduce_max_sync(0xFFFFFFFFu, mx_m);
-      mx_v = __reduce_max_sync(0xFFFFFFFFu, mx_v);
-      const float Am = __uint_as_float(mx_m), Av = __uint_as_float(mx_v);
+      const BlockNorm nm = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_m));
+      const BlockNorm nv = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_v));
       uint32_t q_m[8], q_v[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        q_m[i] = quant(m[i], mx_m, Am, qt.map[0], qt.zero_code[0], refine);
-        q_v[i] = quant(v[i], mx_v, Av, qt.map[1], qt.zero_code[1], refine);
+        q_m[i] = quant<R>(m[i], nm, qt.map[0], zc_m);
+        q_v[i] = quant<R>(v[i], nv, qt.map[1], zc_v);
       }
       if (vec && n == kVec) {
         st8f(pf + e, p);
@@ -386,8 +402,8 @@ __global__ void __launch_bounds__(kThreads, Tune<ADAMW_MODE_Q8>::min_blocks) ste
         }
       }
       if (lane == 0) {
-        td.am[blk] = Am;
-        td.av[blk] = Av;
+        td.am[blk] = __uint_as_float(nm.bits);
+        td.av[blk] = __uint_as_float(nv.bits);
       }
     }
   }
@@ -408,7 +424,12 @@ cudaError_t launch_mode(adamw_mode mode, const StepArgs& a, int grid, cudaStream
       step_kernel<ADAMW_MODE_BF16_REM, GT><<<grid, kThreads, 0, st>>>(a);
       break;
     case ADAMW_MODE_Q8:
-      step_q8_kernel<GT><<<grid, kThreads, sizeof(QTables), st>>>(a);
+      if (a.refine <= 1)
+        step_q8_kernel<GT, 1><<<grid, kThreads, sizeof(QTables), st>>>(a);
+      else if (a.refine <= 2)
+        step_q8_kernel<GT, 2><<<grid, kThreads, sizeof(QTables), st>>>(a);
+      else
+        step_q8_kernel<GT, kMaxRefine><<<grid, kThreads, sizeof(QTables), st>>>(a);
       break;
     default:
       return cudaErrorInvalidValue;
@@ -427,7 +448,7 @@ cudaError_t occupancy_mode(adamw_mode mode, int* bps, int* smem) {
       return occ(step_kernel<ADAMW_MODE_BF16_REM, GT>, 0, bps);
     case ADAMW_MODE_Q8:
       *smem = static_cast<int>(sizeof(QTables));
-      return occ(step_q8_kernel<GT>, *smem, bps);
+      return occ(step_q8_kernel<GT, kMaxRefine>, *smem, bps);
     default:
       return cudaErrorInvalidValue;
   }

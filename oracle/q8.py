@@ -18,12 +18,17 @@ tensor may be partial), in the order written:
   absmax       Am' = max |m'|,  Av' = max |v'|   (max of the float32 bit
                patterns with the sign cleared: exact and order-free; equals
                the float maximum for non-NaN data)
-  requantise   x = m' / Am' (0 when Am' == 0), cm' = nearest code of x in smap
-               y = v' / Av' (0 when Av' == 0), cv' = nearest code of y in umap
+  requantise   x = m' * fl(1/Am')   (Am' == 0: the zero code), cm' = nearest code of x
+               y = v' * fl(1/Av')   likewise with the unsigned map
+               -- the ratio is formed with the block's reciprocal rounded once
+               and one multiply per element; when the absmax is below 2**-64
+               both factors are first scaled by 2**64 (exact), so that the
+               reciprocal cannot overflow
 
 Readings (the pages are silent): an all-zero block stores absmax 0 and the
 zero code; nearest-code ties go to the lower code; v uses its own absmax
-``max v'`` with the unsigned map.
+``max v'`` with the unsigned map; the normalised value is ``m' * fl(1/absmax)``
+(one reciprocal per block), not a per-element division.
 """
 
 from __future__ import annotations
@@ -54,6 +59,17 @@ def dequantize(codes: np.ndarray, absmax: np.ndarray, table: np.ndarray,
     return (table[codes] * np.asarray(absmax, dtype=F32)[idx]).astype(F32)
 
 
+SMALL = F32(2.0 ** -64)
+SCALE = F32(2.0 ** 64)
+
+
+def normalise(xb: np.ndarray, a: np.float32) -> np.ndarray:
+    """x * fl(1/a), with x and a first scaled by 2**64 when a < 2**-64 (exact scalings)."""
+    s = SCALE if a < SMALL else F32(1.0)
+    y = F32(1.0) / F32(a * s)
+    return (np.asarray(xb, dtype=F32) * s) * y
+
+
 def quantize_blockwise(x: np.ndarray, table: np.ndarray, thr: np.ndarray,
                        block: int = BLOCK) -> tuple[np.ndarray, np.ndarray]:
     """float32 state -> (uint8 codes, float32 absmax per block)."""
@@ -69,7 +85,7 @@ def quantize_blockwise(x: np.ndarray, table: np.ndarray, thr: np.ndarray,
         if a == 0:
             codes[b * block:(b + 1) * block] = z
         else:
-            codes[b * block:(b + 1) * block] = qm.quantize(xb / a, table, thr)
+            codes[b * block:(b + 1) * block] = qm.quantize(normalise(xb, a), table, thr)
     return codes, amax
 
 

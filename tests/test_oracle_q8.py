@@ -197,3 +197,19 @@ def test_q8_skip(maps, bad):
     assert ok is False
     for a, b in zip((p, cm, cv, am, av), before):
         assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("scale", [1e-3, 1.0, 1e30, 3e-20, 1e-30, 1e-39])
+def test_normalise_is_ratio_within_one_ulp(scale):
+    """x * fl(1/A) (with the 2**64 pre-scaling below 2**-64) stays within about
+    one ulp of the exact ratio x / A, also for tiny and subnormal absmax."""
+    rng = np.random.default_rng(17)
+    xb = (rng.uniform(-1, 1, 256) * scale).astype(F32)
+    a = q8.absmax_bits(xb)
+    got = q8.normalise(xb, a).astype(np.float64)
+    exact = xb.astype(np.float64) / np.float64(a)
+    assert np.all(np.abs(got) <= 1.0)
+    assert np.all(np.abs(got - exact) <= 2.5 * 2.0 ** -24 * np.maximum(np.abs(exact), 2.0 ** -126))
+    # the element holding the absmax maps to exactly +-1 whenever 1/A is exact
+    if a == F32(2.0) ** int(np.log2(a)):
+        assert np.max(np.abs(got)) == 1.0
