@@ -298,6 +298,7 @@ class Gpt2Small(Workload):
             p.copy_(synth.normal(p.numel(), 0.02, seed + i, dev))
             g.copy_(synth.normal(g.numel(), 1e-3, synth.grad_seed(seed, 0, i), dev))
         self.opt = FusedAdamW(ps, gs, ms, vs, [s.wd for s in self.specs])
+        self.ps, self.gs, self.ms, self.vs = ps, gs, ms, vs
         self.lr_table = torch.tensor([synth.cosine_lr(s) for s in range(100)], dtype=torch.float32,
                                      device=dev)
         self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)

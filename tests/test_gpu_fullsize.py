@@ -1,0 +1,158 @@
+"""GPU parity at the workloads' full sizes, in the launch configuration bench.py times.
+
+The workloads are built by bench.py's own classes (same plans, same layout,
+same grids).  Each step gets new seeded device grads; a fixed sample of
+elements -- the first and last elements of every tensor plus random windows
+(whole 256-element blocks on the 8-bit path) -- is followed through every step
+by the strict-fp32 oracle, from inputs copied off the device before the library
+touches them.  Sampled outputs must match bit for bit, and the fp32 params must
+stay within the float64 definition's tolerance.
+"""
+
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import bench
+import synth
+from oracle import adamw as OA
+from oracle import q8 as OQ
+from oracle import remainder as OR
+
+pytestmark = pytest.mark.gpu
+
+
+def _free_gib():
+    free, _ = torch.cuda.mem_get_info()
+    return free / 2 ** 30
+
+
+def _windows(numels, rng, edge=64, n_rand=24, width=256, align=1):
+    """Per tensor: sorted element indices (edges + random windows)."""
+    out = []
+    for n in numels:
+        idx = set(range(min(edge, n))) | set(range(max(0, n - edge), n))
+        for _ in range(n_rand if n > 4 * width else 0):
+            s = int(rng.integers(0, n - width)) // align * align
+            idx |= set(range(s, s + width))
+        out.append(np.array(sorted(idx), dtype=np.int64))
+    return out
+
+
+def _take(t, idx):
+    return t.view(-1)[torch.from_numpy(idx).to(t.device)]
+
+
+def _cleanup():
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+def test_gpt2_small_full_size_cosine_lr_sampled():
+    """148 tensors, 124,439,808 elements, lr from the device cosine table, 100 steps."""
+    w = bench.Gpt2Small()
+    try:
+        rng = np.random.default_rng(21)
+        idx = _windows([p.numel() for p in w.ps], rng)
+        orc = [OA.Tensor(p=_take(p, i).cpu().numpy(), g=None, m=_take(m, i).cpu().numpy(),
+                         v=_take(v, i).cpu().numpy(), wd=s.wd)
+               for p, m, v, i, s in zip(w.ps, w.ms, w.vs, idx, w.specs)]
+        ref = [OA.Tensor(p=o.p.astype(np.float64), g=None, m=o.m.astype(np.float64),
+                         v=o.v.astype(np.float64), wd=o.wd) for o in orc]
+        for s in range(100):
+            for k, g in enumerate(w.gs):
+                g.copy_(synth.normal(g.numel(), 1e-3, synth.grad_seed(7, s, k), "cuda"))
+            for o, r, g, i in zip(orc, ref, w.gs, idx):
+                o.g = _take(g, i).cpu().numpy()
+                r.g = o.g.astype(np.float64)
+            w.step(s)
+            lr = float(w.lr_table[s % 100].item())
+            OA.step_f32(orc, lr=lr, beta1=OA.f32(0.9), beta2=OA.f32(0.999), eps=OA.f32(1e-8), t=s + 1)
+            OA.step_fp64(ref, lr=lr, beta1=OA.f32(0.9), beta2=OA.f32(0.999), eps=OA.f32(1e-8), t=s + 1)
+            if s in (0, 1, 50, 99):
+                torch.cuda.synchronize()
+                for k, (p, m, v, i, o) in enumerate(zip(w.ps, w.ms, w.vs, idx, orc)):
+                    assert np.array_equal(_take(p, i).cpu().numpy().view(np.uint32), o.p.view(np.uint32)), (s, k)
+                    assert np.array_equal(_take(m, i).cpu().numpy().view(np.uint32), o.m.view(np.uint32)), (s, k)
+                    assert np.array_equal(_take(v, i).cpu().numpy().view(np.uint32), o.v.view(np.uint32)), (s, k)
+        assert int(w.step_dev.item()) == 100
+        worst = max(np.max(np.abs(o.p.astype(np.float64) - r.p)) for o, r in zip(orc, ref))
+        assert worst <= 5e-5
+    finally:
+        del w
+        _cleanup()
+
+
+def test_q8_full_size_2e30_sampled_blocks():
+    """One 2^30 fp32 tensor, 8-bit m and v, bf16 grads, lr 1e-3, wd 0.01, 20 steps."""
+    if _free_gib() < 12:
+        pytest.skip("needs ~9 GiB of free device memory")
+    w = bench.Q8()
+    try:
+        rng = np.random.default_rng(22)
+        n = w.n_params
+        blocks = np.unique(np.concatenate([[0, 1, n // 256 - 1],
+                                           rng.integers(0, n // 256, 64)]))
+        idx = (blocks[:, None] * 256 + np.arange(256)[None, :]).ravel()
+        bidx = torch.from_numpy(blocks).cuda()
+        p = _take(w.p, idx).cpu().numpy()
+        cm = _take(w.cm, idx).cpu().numpy()
+        cv = _take(w.cv, idx).cpu().numpy()
+        am = w.am[bidx].cpu().numpy()
+        av = w.av[bidx].cpu().numpy()
+        maps = OQ.Maps()
+        for s in range(20):
+            w.g.copy_(synth.normal(n, 1e-3, synth.grad_seed(8, s), "cuda", torch.bfloat16))
+            g = _take(w.g, idx).float().cpu().numpy()
+            w.step(s)
+            OQ.step_f32(p, g, cm, cv, am, av, lr=OA.f32(1e-3), beta1=OA.f32(0.9), beta2=OA.f32(0.999),
+                        eps=OA.f32(1e-8), wd=OA.f32(0.01), t=s + 1, maps=maps)
+        torch.cuda.synchronize()
+        assert np.array_equal(_take(w.p, idx).cpu().numpy().view(np.uint32), p.view(np.uint32))
+        assert np.array_equal(_take(w.cm, idx).cpu().numpy(), cm)
+        assert np.array_equal(_take(w.cv, idx).cpu().numpy(), cv)
+        assert np.array_equal(w.am[bidx].cpu().numpy().view(np.uint32), am.view(np.uint32))
+        assert np.array_equal(w.av[bidx].cpu().numpy().view(np.uint32), av.view(np.uint32))
+        assert int(w.step_dev.item()) == 20
+    finally:
+        del w
+        _cleanup()
+
+
+def test_llama3_8b_bf16_remainders_full_size_sampled():
+    """291 tensors, 8,030,261,248 elements as bf16 + int16 remainders, 5 steps."""
+    if _free_gib() < 120:
+        pytest.skip("needs ~115 GiB of free device memory")
+    w = bench.Llama3()
+    try:
+        hs, rs, gs, ms, vs = w._views
+        rng = np.random.default_rng(23)
+        idx = _windows([h.numel() for h in hs], rng, n_rand=4)
+        orc = []
+        for h, r, m, v, i, spec in zip(hs, rs, ms, vs, idx, w.specs):
+            hi = _take(h.view(torch.int16), i).cpu().numpy().view(np.uint16)
+            rem = _take(r, i).cpu().numpy()
+            orc.append(OA.Tensor(p=OR.join(hi, rem), g=None, m=_take(m, i).cpu().numpy(),
+                                 v=_take(v, i).cpu().numpy(), wd=spec.wd))
+        for s in range(5):
+            for k, g in enumerate(gs):
+                g.copy_(synth.normal(g.numel(), 1e-4, synth.grad_seed(9, s, k), "cuda", torch.bfloat16))
+            for o, g, i in zip(orc, gs, idx):
+                o.g = _take(g, i).float().cpu().numpy()
+            w.step(s)
+            OA.step_f32(orc, lr=OA.f32(3e-4), beta1=OA.f32(0.9), beta2=OA.f32(0.999), eps=OA.f32(1e-8),
+                        t=s + 1)
+        torch.cuda.synchronize()
+        for k, (h, r, m, v, i, o) in enumerate(zip(hs, rs, ms, vs, idx, orc)):
+            ohi, orem = OR.split(o.p)
+            assert np.array_equal(_take(h.view(torch.int16), i).cpu().numpy().view(np.uint16), ohi), k
+            assert np.array_equal(_take(r, i).cpu().numpy(), orem), k
+            assert np.array_equal(_take(m, i).cpu().numpy().view(np.uint32), o.m.view(np.uint32)), k
+            assert np.array_equal(_take(v, i).cpu().numpy().view(np.uint32), o.v.view(np.uint32)), k
+        assert int(w.step_dev.item()) == 5
+    finally:
+        del w
+        _cleanup()
