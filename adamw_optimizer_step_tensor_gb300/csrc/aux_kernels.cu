@@ -123,17 +123,13 @@ __global__ void q8_quant_kernel(const QTables* __restrict__ qt, int which,
       if (mx == 0u) {
         c = static_cast<uint32_t>(qt->zero_code[which]);
       } else {
+        // |q| <= 1 or NaN; NaN falls in the last bucket, which yields code 0
         const float q = __fmul_rn(__fmul_rn(v[i], scale), inv);
         const uint32_t bits = __float_as_uint(q);
-        const uint32_t mag = bits & 0x7FFFFFFFu;
-        if (mag > 0x7F800000u) {
-          c = 0u;
-        } else {
-          const int k = bucket_of(mag);
-          const uint32_t lo = (bits >> 31) ? t.lo_neg[k] : t.lo_pos[k];
-          c = lo;
-          for (int r = 0; r < refine; ++r) c += (t.thr[lo + r] <= q) ? 1u : 0u;
-        }
+        const int k = bucket_of(bits & 0x7FFFFFFFu);
+        const uint32_t lo = (bits >> 31) ? t.lo_neg[k] : t.lo_pos[k];
+        c = lo;
+        for (int r = 0; r < refine; ++r) c += (t.thr[lo + r] <= q) ? 1u : 0u;
       }
       codes[e] = static_cast<uint8_t>(c);
     }

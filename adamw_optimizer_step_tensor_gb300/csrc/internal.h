@@ -17,10 +17,11 @@ constexpr int kPass = kThreads * kVec;       // 2048 elements per CTA pass
 // Passes whose loads a thread issues together, and the resident CTAs per SM
 // the register budget targets, per storage mode (measured on GB300: fp32
 // states 2 x 2 -> 92% of copy bandwidth vs 88% for 1 x 3; bf16+remainder
-// 1 x 3 -> 94%; the instruction-bound 8-bit path gains from 4 CTAs/SM).
+// 1 x 3 -> 94%; the instruction-bound 8-bit path: 3 CTAs/SM, 80 registers,
+// beat 4 CTAs/SM, whose 64-register budget spills).
 template <int MODE> struct Tune { static constexpr int unroll = 1, min_blocks = 3; };
 template <> struct Tune<ADAMW_MODE_FP32> { static constexpr int unroll = 2, min_blocks = 2; };
-template <> struct Tune<ADAMW_MODE_Q8> { static constexpr int unroll = 1, min_blocks = 4; };
+template <> struct Tune<ADAMW_MODE_Q8> { static constexpr int unroll = 1, min_blocks = 3; };
 constexpr int kChunkMax = 8 * kPass;         // chunks hold 2048..16384 elements (chosen per plan)
 constexpr int kQBlock = ADAMW_Q8_BLOCK;      // 256
 static_assert(kPass % kQBlock == 0, "chunks must hold whole Q8 blocks");

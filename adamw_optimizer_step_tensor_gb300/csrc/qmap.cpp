@@ -92,8 +92,16 @@ int build_qmap(const float value[256], QMapDev* out) {
     out->thr[k] = c;
   }
   for (int k = 255; k < 256 + kMaxRefine; ++k) out->thr[k] = INFINITY;
+  // Normalised values satisfy |x| <= 1, so the last bucket (|x| >= 1.9921875)
+  // is reached only by NaN: its lowest code is 0 and, since no threshold
+  // compares true against NaN, NaN quantises to code 0.
   int refine = 0;
   for (int k = 0; k < kBuckets; ++k) {
+    if (k == kBuckets - 1) {
+      out->lo_pos[k] = 0;
+      out->lo_neg[k] = 0;
+      continue;
+    }
     uint32_t lo_bits, hi_bits;
     if (k == 0) {
       lo_bits = 0u;
@@ -102,7 +110,7 @@ int build_qmap(const float value[256], QMapDev* out) {
       const uint32_t e = 103u + static_cast<uint32_t>(k - 1) / 128u;
       const uint32_t mt = static_cast<uint32_t>(k - 1) % 128u;
       lo_bits = (e << 23) | (mt << 16);
-      hi_bits = (k == kBuckets - 1) ? 0x7F800000u : (lo_bits | 0xFFFFu);
+      hi_bits = lo_bits | 0xFFFFu;
     }
     const float lo = bits_to_float(lo_bits), hi = bits_to_float(hi_bits);
     const int pos_lo = count_le(out->thr, lo), pos_hi = count_le(out->thr, hi);

@@ -22,7 +22,7 @@ namespace adamw {
 namespace {
 
 struct Scal {
-  float b1, b2, omb1, omb2, eps, lr, step_size, sqrt_bc2, inv_scale;
+  float b1, b2, omb1, omb2, eps, lr, step_size, inv_sqrt_bc2, inv_scale;
   int scaled;
 };
 
@@ -53,7 +53,8 @@ __device__ bool prologue(const StepArgs& a, Scal& s) {
   s.eps = a.eps;
   s.lr = lr;
   const float bc1 = __double2float_rn(__dsub_rn(1.0, pow_binary((double)a.beta1, t)));
-  s.sqrt_bc2 = __double2float_rn(__dsqrt_rn(__dsub_rn(1.0, pow_binary((double)a.beta2, t))));
+  s.inv_sqrt_bc2 = __double2float_rn(
+      __ddiv_rn(1.0, __dsqrt_rn(__dsub_rn(1.0, pow_binary((double)a.beta2, t)))));
   s.step_size = __fdiv_rn(lr, bc1);
   s.scaled = a.grad_scale != nullptr;
   s.inv_scale = s.scaled ? __fdiv_rn(1.0f, *a.grad_scale) : 1.0f;
@@ -71,7 +72,7 @@ __device__ __forceinline__ void update(float& p, float g, float& m, float& v, co
   if (s.scaled) g = __fmul_rn(g, s.inv_scale);
   m = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
   v = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, __fmul_rn(g, g)));
-  const float h = __fadd_rn(__fdiv_rn(__fsqrt_rn(v), s.sqrt_bc2), s.eps);
+  const float h = __fadd_rn(__fmul_rn(__fsqrt_rn(v), s.inv_sqrt_bc2), s.eps);
   const float u = __fdiv_rn(m, h);
   p = __fsub_rn(__fmul_rn(p, decay), __fmul_rn(s.step_size, u));
 }
@@ -262,19 +263,20 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::min_blocks) step_kernel(
 }
 
 // ---------------------------------------------------------------- 8-bit states
-// Nearest code of x in one map: the bucket of |x| gives the lowest code any x
-// of that bucket can have; at most R thresholds lie inside a bucket, and
-// code = lo + #{r < R : thr[lo + r] <= x} because thr is ascending.
+// Nearest code of a normalised x (|x| <= 1, or NaN) in one map: the bucket of
+// |x| gives the lowest code any x of that bucket can have; at most R
+// thresholds lie inside a bucket, and code = lo + #{r < R : thr[lo + r] <= x}
+// because thr is ascending.  NaN lands in the last bucket, whose lowest code
+// is 0 and whose thresholds never compare true: code 0.
 template <int R>
 __device__ __forceinline__ uint32_t nearest_code(float x, const QMapDev& t) {
   const uint32_t b = __float_as_uint(x);
-  const uint32_t mag = b & 0x7FFFFFFFu;
-  const int k = bucket_of(mag);
+  const int k = bucket_of(b & 0x7FFFFFFFu);
   const uint32_t lo = (b >> 31) ? t.lo_neg[k] : t.lo_pos[k];
   uint32_t c = lo;
 #pragma unroll
   for (int r = 0; r < R; ++r) c += (t.thr[lo + r] <= x) ? 1u : 0u;
-  return mag > 0x7F800000u ? 0u : c;  // NaN -> code 0
+  return c;
 }
 
 // Per-warp block constants for re-quantisation: the absmax bits, the scale
@@ -293,11 +295,28 @@ __device__ __forceinline__ BlockNorm block_norm(uint32_t amax_bits) {
   return n;
 }
 
+// Codes of the 8 values one lane owns.  All branches are warp-uniform (the
+// block constants are the same in every lane); x * 1 is exact, so the
+// scaled multiply is skipped when the scale is 1.
 template <int R>
-__device__ __forceinline__ uint32_t quant(float x, const BlockNorm& n, const QMapDev& t,
-                                          int zero_code) {
-  if (n.bits == 0u) return static_cast<uint32_t>(zero_code);
-  return nearest_code<R>(__fmul_rn(__fmul_rn(x, n.scale), n.inv), t);
+__device__ __forceinline__ void quant8(const float (&x)[8], const BlockNorm& n,
+                                       const QMapDev& t, uint32_t zero_code, uint32_t (&q)[8]) {
+  if (n.bits == 0u) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = zero_code;
+  } else if (n.scale == 1.0f) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = nearest_code<R>(__fmul_rn(x[i], n.inv), t);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      q[i] = nearest_code<R>(__fmul_rn(__fmul_rn(x[i], n.scale), n.inv), t);
+  }
+}
+
+__device__ __forceinline__ uint2 pack8(const uint32_t (&q)[8]) {
+  return make_uint2(q[0] | q[1] << 8 | q[2] << 16 | q[3] << 24,
+                    q[4] | q[5] << 8 | q[6] << 16 | q[7] << 24);
 }
 
 template <typename GT, int R>
@@ -319,79 +338,74 @@ step_q8_kernel(const StepArgs a) {
   const Scal s = s_sc;
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const int zc_m = qt.zero_code[0], zc_v = qt.zero_code[1];
+  const uint32_t zc_m = qt.zero_code[0], zc_v = qt.zero_code[1];
 
   for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
     const Chunk ch = a.chunks[c];
-    const TensorDesc& td = a.tensors[ch.tensor];
+    const TensorDesc td = a.tensors[ch.tensor];
     const float decay = __fsub_rn(1.0f, __fmul_rn(s.lr, td.wd));
     const bool vec = td.vec_ok != 0;
     float* const pf = static_cast<float*>(td.p);
     uint8_t* const cm = static_cast<uint8_t*>(td.m);
     uint8_t* const cv = static_cast<uint8_t*>(td.v);
-    const void* const g = td.g;
 
     // warp w owns the 256-element block starting at `wb` of every pass
     for (int wb = warp * kQBlock; wb < ch.len; wb += kPass) {
-      const int64_t e0 = ch.start + wb;            // block-aligned within the tensor
-      const int64_t blk = e0 / kQBlock;
+      const int64_t blk = (ch.start + wb) / kQBlock;   // block-aligned within the tensor
       const int off = wb + lane * kVec;
-      const int n = max(0, min(kVec, ch.len - off));
       const int64_t e = ch.start + off;
       const float am = td.am[blk], av = td.av[blk];
-
       float p[8], gr[8], m[8], v[8];
-      if (vec && n == kVec) {
+      uint32_t q_m[8], q_v[8];
+      // a whole block on the 128-bit path: no per-element predicates
+      if (vec && wb + kQBlock <= ch.len) {
         ld8f(pf + e, p);
-        Grad<GT>::load8(g, e, gr);
+        Grad<GT>::load8(td.g, e, gr);
         const uint2 qm = __ldcs(reinterpret_cast<const uint2*>(cm + e));
         const uint2 qv = __ldcs(reinterpret_cast<const uint2*>(cv + e));
+        uint32_t mx_m = 0u, mx_v = 0u;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           const uint32_t wm = i < 4 ? qm.x : qm.y, wv = i < 4 ? qv.x : qv.y;
           const int sh = (i & 3) * 8;
           m[i] = __fmul_rn(qt.map[0].value[(wm >> sh) & 0xFFu], am);
           v[i] = __fmul_rn(qt.map[1].value[(wv >> sh) & 0xFFu], av);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          if (i < n) {
-            p[i] = pf[e + i];
-            gr[i] = Grad<GT>::load1(g, e + i);
-            m[i] = __fmul_rn(qt.map[0].value[cm[e + i]], am);
-            v[i] = __fmul_rn(qt.map[1].value[cv[e + i]], av);
-          } else {
-            p[i] = gr[i] = m[i] = v[i] = 0.0f;
-          }
-        }
-      }
-      uint32_t mx_m = 0u, mx_v = 0u;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        if (i < n) {
           update(p[i], gr[i], m[i], v[i], s, decay);
           mx_m = max(mx_m, __float_as_uint(m[i]) & 0x7FFFFFFFu);
           mx_v = max(mx_v, __float_as_uint(v[i]) & 0x7FFFFFFFu);
         }
-      }
-      const BlockNorm nm = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_m));
-      const BlockNorm nv = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_v));
-      uint32_t q_m[8], q_v[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        q_m[i] = quant<R>(m[i], nm, qt.map[0], zc_m);
-        q_v[i] = quant<R>(v[i], nv, qt.map[1], zc_v);
-      }
-      if (vec && n == kVec) {
+        const BlockNorm nm = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_m));
+        const BlockNorm nv = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_v));
+        quant8<R>(m, nm, qt.map[0], zc_m, q_m);
+        quant8<R>(v, nv, qt.map[1], zc_v, q_v);
         st8f(pf + e, p);
-        __stcs(reinterpret_cast<uint2*>(cm + e),
-               make_uint2(q_m[0] | q_m[1] << 8 | q_m[2] << 16 | q_m[3] << 24,
-                          q_m[4] | q_m[5] << 8 | q_m[6] << 16 | q_m[7] << 24));
-        __stcs(reinterpret_cast<uint2*>(cv + e),
-               make_uint2(q_v[0] | q_v[1] << 8 | q_v[2] << 16 | q_v[3] << 24,
-                          q_v[4] | q_v[5] << 8 | q_v[6] << 16 | q_v[7] << 24));
+        __stcs(reinterpret_cast<uint2*>(cm + e), pack8(q_m));
+        __stcs(reinterpret_cast<uint2*>(cv + e), pack8(q_v));
+        if (lane == 0) {
+          td.am[blk] = __uint_as_float(nm.bits);
+          td.av[blk] = __uint_as_float(nv.bits);
+        }
       } else {
+        // the last (partial) block of a tensor, or a misaligned tensor
+        const int n = max(0, min(kVec, ch.len - off));
+        uint32_t mx_m = 0u, mx_v = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          p[i] = gr[i] = m[i] = v[i] = 0.0f;
+          if (i < n) {
+            p[i] = pf[e + i];
+            gr[i] = Grad<GT>::load1(td.g, e + i);
+            m[i] = __fmul_rn(qt.map[0].value[cm[e + i]], am);
+            v[i] = __fmul_rn(qt.map[1].value[cv[e + i]], av);
+            update(p[i], gr[i], m[i], v[i], s, decay);
+            mx_m = max(mx_m, __float_as_uint(m[i]) & 0x7FFFFFFFu);
+            mx_v = max(mx_v, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+          }
+        }
+        const BlockNorm nm = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_m));
+        const BlockNorm nv = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_v));
+        quant8<R>(m, nm, qt.map[0], zc_m, q_m);
+        quant8<R>(v, nv, qt.map[1], zc_v, q_v);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           if (i < n) {
@@ -400,10 +414,10 @@ step_q8_kernel(const StepArgs a) {
             cv[e + i] = static_cast<uint8_t>(q_v[i]);
           }
         }
-      }
-      if (lane == 0) {
-        td.am[blk] = __uint_as_float(nm.bits);
-        td.av[blk] = __uint_as_float(nv.bits);
+        if (lane == 0) {
+          td.am[blk] = __uint_as_float(nm.bits);
+          td.av[blk] = __uint_as_float(nv.bits);
+        }
       }
     }
   }

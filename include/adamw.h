@@ -15,10 +15,12 @@
  *     g  = g_raw [* inv_scale]        inv_scale = 1 / *grad_scale_dev
  *     m' = b1*m + (1-b1)*g
  *     v' = b2*v + (1-b2)*(g*g)
- *     u  = m' / (sqrt(v') / sqrt_bc2 + eps)
+ *     u  = m' / (sqrt(v') * inv_sqrt_bc2 + eps)
  *     p' = p*(1 - lr*wd) - (lr/bc1)*u
  * where b^t is float64 square-and-multiply, and bc1 = 1 - b1^t and
- * sqrt_bc2 = sqrt(1 - b2^t) are float64 values rounded once to float32.
+ * inv_sqrt_bc2 = 1 / sqrt(1 - b2^t) are float64 values rounded once to
+ * float32 (the bias correction of sqrt(v) is a multiplication by its
+ * reciprocal rather than a per-element division).
  * Results are therefore reproducible bit for bit by any IEEE float32
  * implementation of the same sequence.
  *

@@ -33,9 +33,11 @@ Two modes
                no fused multiply-add, in exactly the order written below.  The
                bias corrections are the one exception: ``b**t`` is taken by
                float64 binary exponentiation (``pow_binary``), ``1 - b**t``
-               and ``sqrt(1 - b2**t)`` in float64, each rounded to float32
-               once.  Discrete outputs (remainders, 8-bit codes) are defined
-               against this mode.
+               and ``1 / sqrt(1 - b2**t)`` in float64, each rounded to
+               float32 once; the correction of ``sqrt(v)`` is applied as a
+               multiplication by that reciprocal (the pages write a division
+               and fix no rounding).  Discrete outputs (remainders, 8-bit
+               codes) are defined against this mode.
 
 Hyper-parameters are the float32 values the GPU entry point receives
 (``lr`` read from a float32 device scalar; ``beta1``, ``beta2``, ``eps``,
@@ -158,7 +160,7 @@ class F32Scalars:
     eps: np.float32
     lr: np.float32
     step_size: np.float32  # fl(lr / bc1)
-    sqrt_bc2: np.float32   # fl32(sqrt(1 - b2**t) in float64)
+    inv_sqrt_bc2: np.float32   # fl32(1 / sqrt(1 - b2**t), both in float64)
     inv_scale: np.float32 | None  # fl(1 / grad_scale), None = no unscale
 
 
@@ -170,7 +172,7 @@ def f32_scalars(*, lr, beta1, beta2, eps, t, grad_scale=None) -> F32Scalars:
     return F32Scalars(
         b1=b1, b2=b2, omb1=F32(F32(1.0) - b1), omb2=F32(F32(1.0) - b2),
         eps=F32(eps), lr=lr32, step_size=F32(lr32 / bc1_32),
-        sqrt_bc2=F32(sqrt_bc2),
+        inv_sqrt_bc2=F32(1.0 / sqrt_bc2),
         inv_scale=None if grad_scale is None else F32(F32(1.0) / F32(grad_scale)),
     )
 
@@ -188,7 +190,7 @@ def elementwise_f32(p, g_raw, m, v, s: F32Scalars, decay: np.float32):
         g   = g * inv_scale                (only when a grad scale is given)
         m'  = b1*m + omb1*g
         v'  = b2*v + omb2*(g*g)
-        h   = sqrt(v') / sqrt_bc2 + eps
+        h   = sqrt(v') * inv_sqrt_bc2 + eps
         u   = m' / h
         p'  = p*decay - step_size*u
     """
@@ -197,7 +199,7 @@ def elementwise_f32(p, g_raw, m, v, s: F32Scalars, decay: np.float32):
         g = g * s.inv_scale
     m1 = s.b1 * m + s.omb1 * g
     v1 = s.b2 * v + s.omb2 * (g * g)
-    h = np.sqrt(v1) / s.sqrt_bc2 + s.eps
+    h = np.sqrt(v1) * s.inv_sqrt_bc2 + s.eps
     u = m1 / h
     p1 = p * decay - s.step_size * u
     return p1.astype(F32), m1.astype(F32), v1.astype(F32)
