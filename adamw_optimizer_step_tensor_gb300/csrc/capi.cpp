@@ -29,7 +29,7 @@ struct adamw_plan {
   int grid_check = 1;
   TensorDesc* d_tensors = nullptr;
   Chunk* d_chunks = nullptr;
-  uint32_t* d_ticket = nullptr;
+  StepScratch* d_scratch = nullptr;
   QTables* d_qt = nullptr;
   int refine = 1;              // Q8: thresholds per bucket lookup of the current maps
 };
@@ -65,7 +65,7 @@ void free_plan(adamw_plan* p) {
   if (!p) return;
   cudaFree(p->d_tensors);
   cudaFree(p->d_chunks);
-  cudaFree(p->d_ticket);
+  cudaFree(p->d_scratch);
   cudaFree(p->d_qt);
   delete p;
 }
@@ -165,10 +165,11 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  // Chunk size: the largest of 16384, 8192, 4096, 2048 elements that still gives
-  // every SM several chunks, so that small plans spread over the whole GPU.
-  int64_t chunk = kChunkMax;
-  while (chunk > kPass && total / chunk < 8LL * sms) chunk /= 2;
+  int bps = 0, smem = 0;
+  e = step_occupancy(mode, grad_dtype, &bps, &smem);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  if (bps < 1) bps = 1;
+  const int64_t chunk = choose_chunk(total, sms, bps);
   for (int32_t i = 0; i < n_tensors; ++i)
     for (int64_t s = 0; s < td[i].numel; s += chunk) {
       const int64_t len = td[i].numel - s < chunk ? td[i].numel - s : chunk;
@@ -183,10 +184,6 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
   p->n_chunks = static_cast<int64_t>(chunks.size());
 
   p->device = device;
-  int bps = 0, smem = 0;
-  e = step_occupancy(mode, grad_dtype, &bps, &smem);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
-  if (bps < 1) bps = 1;
   const int64_t resident = static_cast<int64_t>(bps) * sms;
   p->grid = static_cast<int>(p->n_chunks < resident ? (p->n_chunks > 0 ? p->n_chunks : 1) : resident);
   const int64_t check_res = 8LL * sms;
@@ -197,14 +194,14 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
     return fail(ADAMW_ENOMEM, "cudaMalloc(tensor table): %s", cudaGetErrorString(e));
   if (cb && (e = cudaMalloc(&p->d_chunks, cb)) != cudaSuccess)
     return fail(ADAMW_ENOMEM, "cudaMalloc(chunk table): %s", cudaGetErrorString(e));
-  if ((e = cudaMalloc(&p->d_ticket, sizeof(uint32_t))) != cudaSuccess)
-    return fail(ADAMW_ENOMEM, "cudaMalloc(ticket): %s", cudaGetErrorString(e));
+  if ((e = cudaMalloc(&p->d_scratch, sizeof(StepScratch))) != cudaSuccess)
+    return fail(ADAMW_ENOMEM, "cudaMalloc(step scratch): %s", cudaGetErrorString(e));
   if (tb && (e = cudaMemcpy(p->d_tensors, td.data(), tb, cudaMemcpyHostToDevice)) != cudaSuccess)
     return cuda_fail(e, "upload tensor table");
   if (cb && (e = cudaMemcpy(p->d_chunks, chunks.data(), cb, cudaMemcpyHostToDevice)) != cudaSuccess)
     return cuda_fail(e, "upload chunk table");
-  if ((e = cudaMemset(p->d_ticket, 0, sizeof(uint32_t))) != cudaSuccess)
-    return cuda_fail(e, "clear ticket");
+  if ((e = cudaMemset(p->d_scratch, 0, sizeof(StepScratch))) != cudaSuccess)
+    return cuda_fail(e, "clear step scratch");
   if (mode == ADAMW_MODE_Q8) {
     std::unique_ptr<QTables> qt(new QTables);
     float smap[256], umap[256];
@@ -282,7 +279,7 @@ adamw_status adamw_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev
   a.beta1 = beta1;
   a.beta2 = beta2;
   a.eps = eps;
-  a.ticket = plan->d_ticket;
+  a.scratch = plan->d_scratch;
   a.qt = plan->d_qt;
   a.refine = plan->refine;
   cudaError_t e = launch_step(plan->mode, plan->gdt, a, plan->grid, static_cast<cudaStream_t>(stream));

@@ -27,6 +27,17 @@ constexpr int kQBlock = ADAMW_Q8_BLOCK;      // 256
 static_assert(kPass % kQBlock == 0, "chunks must hold whole Q8 blocks");
 static_assert(32 * kVec == kQBlock, "one warp pass covers exactly one Q8 block");
 
+// Chunk size of a plan: the whole list spread over the resident CTAs
+// (sms x blocks per SM), rounded up to whole 256-element blocks and capped at
+// kChunkMax.  Small plans then run as one balanced wave (one chunk per CTA);
+// large ones get 16384-element chunks that CTAs stride over.
+inline int64_t choose_chunk(int64_t total, int sms, int blocks_per_sm) {
+  const int64_t resident = static_cast<int64_t>(sms) * (blocks_per_sm > 0 ? blocks_per_sm : 1);
+  int64_t chunk = (total + resident - 1) / resident;
+  chunk = (chunk + kQBlock - 1) / kQBlock * kQBlock;
+  return chunk < kQBlock ? kQBlock : (chunk > kChunkMax ? kChunkMax : chunk);
+}
+
 // Q8 nearest-code search tables (see qmap.cpp for how they are built).
 constexpr int kBuckets = 1 + 25 * 128;       // |x| in [0, 2^-24) plus 25 binades x 128
 constexpr int kMaxRefine = 4;                // thresholds compared per lookup, at most
@@ -64,6 +75,17 @@ struct alignas(16) QTables {
 };
 static_assert(sizeof(QTables) % 16 == 0, "QTables is copied to shared memory in 16-byte words");
 
+// Plan-owned device words the step kernel keeps between launches.
+struct StepScratch {
+  uint32_t ticket;             // CTAs of the running launch that took a ticket; 0 between launches
+  int32_t memo_t;              // step index whose bias corrections are memoised (0: none)
+  uint32_t memo_b1, memo_b2;   // bit patterns of the betas they were computed for
+  float memo_bc1;              // fl32(1 - b1^t)
+  float memo_inv_sqrt_bc2;     // fl32(1 / sqrt(1 - b2^t))
+  uint32_t pad[2];
+};
+static_assert(sizeof(StepScratch) == 32, "StepScratch layout");
+
 struct StepArgs {
   const TensorDesc* tensors;
   const Chunk* chunks;
@@ -73,7 +95,7 @@ struct StepArgs {
   const float* grad_scale;    // may be null
   const float* found_inf;     // may be null
   float beta1, beta2, eps;
-  uint32_t* ticket;           // plan-owned counter, zero between launches
+  StepScratch* scratch;       // plan-owned; ticket zero between launches
   const QTables* qt;          // Q8 only
   int refine;                 // Q8 only: thresholds per lookup (1, 2 or 4)
 };

@@ -11,7 +11,7 @@
 // and runs the unchanged step kernel on it.
 //
 // Limits: at most kNoAllocMaxTensors tensors and kNoAllocMaxChunks chunks per
-// call (chunks are 2048..16384 elements, so up to about 1.07e9 elements);
+// call (chunks are at most 16384 elements, so up to about 1.07e9 elements);
 // the array is about 1.1 MB and every GPU that loads the library holds it
 // until the process exits.  fp32 and bf16+remainder modes only.
 #include <cstdio>
@@ -31,7 +31,7 @@ constexpr size_t kScratchBytes = kTicketOffset + 256;
 static_assert(kTensorBytes % 256 == 0 && kChunkBytes % 256 == 0, "keep the parts 256-byte aligned");
 constexpr int kMaxDevices = 64;
 
-// The scratch: tensor table, chunk table, ticket counter.  Host code must
+// The scratch: tensor table, chunk table, step scratch (ticket and memo).  Host code must
 // never use this symbol as an address; it goes through cudaGetSymbolAddress.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
 
@@ -129,8 +129,7 @@ extern "C" adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t 
   }
 
   // Same chunking rule as a plan: the largest chunk that gives every SM work.
-  int64_t chunk = kChunkMax;
-  while (chunk > kPass && total / chunk < 8LL * ds.sms) chunk /= 2;
+  const int64_t chunk = choose_chunk(total, ds.sms, bps);
   int64_t n_chunks = 0;
   for (int32_t i = 0; i < n_tensors; ++i) {
     const adamw_tensor& t = tensors[i];
@@ -158,9 +157,9 @@ extern "C" adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   TensorDesc* d_tensors = reinterpret_cast<TensorDesc*>(ds.scratch);
   Chunk* d_chunks = reinterpret_cast<Chunk*>(ds.scratch + kTensorBytes);
-  uint32_t* d_ticket = reinterpret_cast<uint32_t*>(ds.scratch + kTicketOffset);
+  StepScratch* d_step = reinterpret_cast<StepScratch*>(ds.scratch + kTicketOffset);
   // The array keeps whatever the previous call left: refresh both tables and
-  // zero the ticket (the step kernel expects it to start at 0).
+  // zero the step scratch (the ticket must start at 0; a zero memo is empty).
   if (n_tensors > 0 &&
       (e = cudaMemcpyAsync(d_tensors, g_host_tensors, sizeof(TensorDesc) * n_tensors,
                            cudaMemcpyHostToDevice, st)) != cudaSuccess)
@@ -169,8 +168,8 @@ extern "C" adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t 
       (e = cudaMemcpyAsync(d_chunks, g_host_chunks, sizeof(Chunk) * n_chunks,
                            cudaMemcpyHostToDevice, st)) != cudaSuccess)
     return fail_cuda(e, "upload chunk table");
-  if ((e = cudaMemsetAsync(d_ticket, 0, sizeof(uint32_t), st)) != cudaSuccess)
-    return fail_cuda(e, "clear ticket");
+  if ((e = cudaMemsetAsync(d_step, 0, sizeof(StepScratch), st)) != cudaSuccess)
+    return fail_cuda(e, "clear step scratch");
 
   StepArgs a;
   a.tensors = d_tensors;
@@ -183,7 +182,7 @@ extern "C" adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t 
   a.beta1 = beta1;
   a.beta2 = beta2;
   a.eps = eps;
-  a.ticket = d_ticket;
+  a.scratch = d_step;
   a.qt = nullptr;
   a.refine = 1;
   const int64_t resident = static_cast<int64_t>(bps) * ds.sms;

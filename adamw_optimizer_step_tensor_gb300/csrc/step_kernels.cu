@@ -37,34 +37,67 @@ __device__ double pow_binary(double b, int t) {
   return r;
 }
 
-// Thread 0 of every CTA: read the run-time scalars, decide skip, and take a
-// ticket; the last CTA to take one stores the new step count.  Every CTA has
-// read *step before its ticket (the fence orders it), so no CTA can see the
-// new value.  Nothing waits on anything.
-__device__ bool prologue(const StepArgs& a, Scal& s) {
-  const bool skip = a.found_inf != nullptr && *a.found_inf != 0.0f;
-  if (skip) return true;
-  const int t = *a.step + 1;
+struct BiasCorr {
+  float bc1, inv_sqrt_bc2;
+};
+
+// fl32(1 - b1^t) and fl32(1 / sqrt(1 - b2^t)), every step in float64.
+__device__ BiasCorr bias_corrections(float beta1, float beta2, int t) {
+  BiasCorr r;
+  r.bc1 = __double2float_rn(__dsub_rn(1.0, pow_binary((double)beta1, t)));
+  r.inv_sqrt_bc2 = __double2float_rn(
+      __ddiv_rn(1.0, __dsqrt_rn(__dsub_rn(1.0, pow_binary((double)beta2, t)))));
+  return r;
+}
+
+// Thread 0 of every CTA, before the CTA's barrier: read the run-time scalars
+// (all loads issued together) and decide skip.  The float64 bias corrections
+// are taken from the plan's memo when the previous launch left them for this
+// step index and these betas, otherwise computed here.
+__device__ bool prologue(const StepArgs& a, Scal& s, int& t_out) {
+  const float found = a.found_inf != nullptr ? *a.found_inf : 0.0f;
+  const int step = *a.step;
   const float lr = *a.lr;
+  const float gscale = a.grad_scale != nullptr ? *a.grad_scale : 1.0f;
+  const StepScratch memo = *a.scratch;
+  if (found != 0.0f) return true;
+  const int t = step + 1;
+  const BiasCorr bc = (memo.memo_t == t && memo.memo_b1 == __float_as_uint(a.beta1) &&
+                       memo.memo_b2 == __float_as_uint(a.beta2))
+                          ? BiasCorr{memo.memo_bc1, memo.memo_inv_sqrt_bc2}
+                          : bias_corrections(a.beta1, a.beta2, t);
   s.b1 = a.beta1;
   s.b2 = a.beta2;
   s.omb1 = __fsub_rn(1.0f, a.beta1);
   s.omb2 = __fsub_rn(1.0f, a.beta2);
   s.eps = a.eps;
   s.lr = lr;
-  const float bc1 = __double2float_rn(__dsub_rn(1.0, pow_binary((double)a.beta1, t)));
-  s.inv_sqrt_bc2 = __double2float_rn(
-      __ddiv_rn(1.0, __dsqrt_rn(__dsub_rn(1.0, pow_binary((double)a.beta2, t)))));
-  s.step_size = __fdiv_rn(lr, bc1);
+  s.inv_sqrt_bc2 = bc.inv_sqrt_bc2;
+  s.step_size = __fdiv_rn(lr, bc.bc1);
   s.scaled = a.grad_scale != nullptr;
-  s.inv_scale = s.scaled ? __fdiv_rn(1.0f, *a.grad_scale) : 1.0f;
+  s.inv_scale = s.scaled ? __fdiv_rn(1.0f, gscale) : 1.0f;
+  t_out = t;
+  return false;
+}
+
+// Thread 0 of every CTA that runs the step, after the barrier: take a ticket.
+// Every CTA read *step (and the memo) before its ticket -- the fence orders
+// it -- so the last CTA to take one can store t and the memo for step t + 1
+// without any CTA of this launch seeing either.  Nothing waits on anything.
+__device__ void take_ticket(const StepArgs& a, int t) {
   __threadfence();
-  const unsigned tk = atomicAdd(a.ticket, 1u);
+  const unsigned tk = atomicAdd(&a.scratch->ticket, 1u);
   if (tk == gridDim.x - 1) {
     *a.step = t;
-    atomicExch(a.ticket, 0u);
+    const BiasCorr nx = bias_corrections(a.beta1, a.beta2, t + 1);
+    StepScratch* m = a.scratch;
+    m->memo_bc1 = nx.bc1;
+    m->memo_inv_sqrt_bc2 = nx.inv_sqrt_bc2;
+    m->memo_b1 = __float_as_uint(a.beta1);
+    m->memo_b2 = __float_as_uint(a.beta2);
+    m->memo_t = t + 1;
+    atomicExch(&m->ticket, 0u);
   }
-  return false;
 }
 
 __device__ __forceinline__ void update(float& p, float g, float& m, float& v, const Scal& s,
@@ -227,38 +260,78 @@ __device__ void update_scalar(const TensorDesc& td, int64_t e, int n, const Scal
   }
 }
 
+// A thread's position in its sequence of trips: chunk c (strided by the
+// grid), element offset `base` inside it (strided by kPass * unroll).
+struct Cursor {
+  int64_t c;
+  int base;
+  Chunk ch;
+};
+
+// Move k to the next (chunk, offset) that holds work for this thread.
+__device__ __forceinline__ bool seek(const StepArgs& a, Cursor& k) {
+  while (k.c < a.n_chunks) {
+    k.ch = a.chunks[k.c];
+    if (k.base < k.ch.len) return true;
+    k.c += gridDim.x;
+    k.base = threadIdx.x * kVec;
+  }
+  return false;
+}
+
+template <adamw_mode MODE, typename GT, int U>
+__device__ __forceinline__ void load_trip(const TensorDesc& td, const Cursor& k, bool vec,
+                                          Group (&x)[U]) {
+#pragma unroll
+  for (int u = 0; u < U; ++u) {
+    const int off = k.base + u * kPass;
+    if (vec && off + kVec <= k.ch.len) load_group<MODE, GT>(td, k.ch.start + off, x[u]);
+  }
+}
+
 template <adamw_mode MODE, typename GT>
 __global__ void __launch_bounds__(kThreads, Tune<MODE>::min_blocks) step_kernel(const StepArgs a) {
   constexpr int kUnroll = Tune<MODE>::unroll;
   __shared__ Scal s_sc;
   __shared__ int s_skip;
-  if (threadIdx.x == 0) s_skip = prologue(a, s_sc);
+  // The first trip's loads are issued before the run-time scalars are known,
+  // so thread 0's float64 bias corrections overlap their DRAM latency.  Loads
+  // are harmless if the step turns out to be skipped: nothing is stored.
+  Cursor k{static_cast<int64_t>(blockIdx.x), static_cast<int>(threadIdx.x) * kVec, Chunk{}};
+  bool have = seek(a, k);
+  TensorDesc td{};
+  Group x[kUnroll];
+  if (have) {
+    td = a.tensors[k.ch.tensor];
+    load_trip<MODE, GT, kUnroll>(td, k, td.vec_ok != 0, x);
+  }
+  int t = 0;
+  if (threadIdx.x == 0) s_skip = prologue(a, s_sc, t);
   __syncthreads();
   if (s_skip) return;
   const Scal s = s_sc;
+  if (threadIdx.x == 0) take_ticket(a, t);
 
-  for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
-    const Chunk ch = a.chunks[c];
-    const TensorDesc td = a.tensors[ch.tensor];
+  while (have) {
     const float decay = __fsub_rn(1.0f, __fmul_rn(s.lr, td.wd));
     const bool vec = td.vec_ok != 0;
-    // kUnroll passes per trip: all their loads are issued before any update
-    for (int base = threadIdx.x * kVec; base < ch.len; base += kPass * kUnroll) {
-      Group x[kUnroll];
 #pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int off = base + u * kPass;
-        if (vec && off + kVec <= ch.len) load_group<MODE, GT>(td, ch.start + off, x[u]);
-      }
-#pragma unroll
-      for (int u = 0; u < kUnroll; ++u) {
-        const int off = base + u * kPass;
-        if (vec && off + kVec <= ch.len)
-          update_store_group<MODE>(td, ch.start + off, x[u], s, decay);
-        else if (off < ch.len)
-          update_scalar<MODE, GT>(td, ch.start + off, min(kVec, ch.len - off), s, decay);
-      }
+    for (int u = 0; u < kUnroll; ++u) {
+      const int off = k.base + u * kPass;
+      if (vec && off + kVec <= k.ch.len)
+        update_store_group<MODE>(td, k.ch.start + off, x[u], s, decay);
+      else if (off < k.ch.len)
+        update_scalar<MODE, GT>(td, k.ch.start + off, min(kVec, k.ch.len - off), s, decay);
     }
+    k.base += kPass * kUnroll;
+    if (k.base >= k.ch.len) {
+      const int32_t prev = k.ch.tensor;
+      k.c += gridDim.x;
+      k.base = threadIdx.x * kVec;
+      have = seek(a, k);
+      if (have && k.ch.tensor != prev) td = a.tensors[k.ch.tensor];
+    }
+    if (have) load_trip<MODE, GT, kUnroll>(td, k, td.vec_ok != 0, x);
   }
 }
 
@@ -326,7 +399,8 @@ step_q8_kernel(const StepArgs a) {
   QTables& qt = *reinterpret_cast<QTables*>(smem_raw);
   __shared__ Scal s_sc;
   __shared__ int s_skip;
-  if (threadIdx.x == 0) s_skip = prologue(a, s_sc);
+  int t = 0;
+  if (threadIdx.x == 0) s_skip = prologue(a, s_sc, t);
   {
     const uint4* src = reinterpret_cast<const uint4*>(a.qt);
     uint4* dst = reinterpret_cast<uint4*>(smem_raw);
@@ -336,6 +410,7 @@ step_q8_kernel(const StepArgs a) {
   __syncthreads();
   if (s_skip) return;
   const Scal s = s_sc;
+  if (threadIdx.x == 0) take_ticket(a, t);
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const uint32_t zc_m = qt.zero_code[0], zc_v = qt.zero_code[1];
