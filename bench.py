@@ -49,7 +49,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gpt2_small",
-                    choices=["gpt2_small", "single", "amp", "q8", "llama3_8b"])
+                    choices=["gpt2_small", "single", "amp", "q8", "llama3_8b", "bf16rem"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -247,6 +247,7 @@ CPU_SAMPLES = {
     "amp": lambda n: cpu_sample_fp32(n, amp=True, lr=0.1),
     "q8": cpu_sample_q8,
     "llama3_8b": cpu_sample_bf16rem,
+    "bf16rem": cpu_sample_bf16rem,
 }
 
 # ----------------------------------------------------------------------------- workloads
@@ -481,10 +482,41 @@ class Llama3(Workload):
 
 
 
+class Bf16Rem(Workload):
+    """One flat bf16+remainder tensor: a small stand-in for the Llama-3-8B list (profiling)."""
+    name = "bf16rem_flat"
+    bytes_per_param = 26.0
+
+    def __init__(self, seed=6, numel=0):
+        import torch
+        import synth
+        from adamw_optimizer_step_tensor_gb300 import FusedAdamW, _capi
+        dev = torch.device("cuda")
+        self.C = _capi
+        n = self.n_params = numel or (1 << 26)
+        self.h, self.r = synth.bf16_params_with_remainders(n, 0.02, seed, dev)
+        self.g = synth.normal(n, 1e-4, seed + 1, dev, torch.bfloat16)
+        self.m = torch.zeros(n, device=dev)
+        self.v = torch.zeros(n, device=dev)
+        self.opt = FusedAdamW([self.h], [self.g], [self.m], [self.v], [0.1], mode="bf16_rem",
+                              param_rems=[self.r])
+        self.lr = torch.tensor([3e-4], dtype=torch.float32, device=dev)
+        self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream().cuda_stream
+        self.dtype = "f32 (bf16+int16 params)"
+        self.config = {"workload": "one flat bf16+remainder tensor, bf16 grads", "tensors": 1,
+                       "numel": n, "bytes_per_param": self.bytes_per_param,
+                       "l2": "no flush: inputs larger than L2"}
+
+    def step(self, i):
+        self.C.adamw_step(self.opt.plan, self.lr.data_ptr(), self.step_dev.data_ptr(), 0.9, 0.999,
+                          1e-8, None, None, self.stream)
+
+
 def make_workload(name, numel=0):
     return {"gpt2_small": lambda: Gpt2Small(), "single": lambda: Single(numel=numel),
             "amp": lambda: Single(amp=True, numel=numel), "q8": lambda: Q8(numel=numel),
-            "llama3_8b": lambda: Llama3()}[name]()
+            "llama3_8b": lambda: Llama3(), "bf16rem": lambda: Bf16Rem(numel=numel)}[name]()
 
 
 # ----------------------------------------------------------------------------- CPU timing
