@@ -14,8 +14,8 @@ from . import _capi
 from ._capi import (  # noqa: F401
     AdamWError, adamw_abi_version, adamw_bf16rem_join, adamw_bf16rem_split,
     adamw_check_nonfinite, adamw_last_error, adamw_plan_create, adamw_plan_destroy,
-    adamw_plan_info, adamw_q8_default_maps, adamw_q8_dequant, adamw_q8_quant,
-    adamw_q8_set_maps, adamw_step,
+    adamw_plan_info, adamw_plan_status, adamw_q8_default_maps, adamw_q8_dequant, adamw_q8_quant,
+    adamw_q8_set_maps, adamw_step, adamw_step_noalloc, adamw_wait_selftest,
 )
 
 MODES = {"fp32": _capi.MODE_FP32, "bf16_rem": _capi.MODE_BF16_REM, "q8": _capi.MODE_Q8}
@@ -94,6 +94,10 @@ class FusedAdamW:
 
     def info(self) -> dict:
         return adamw_plan_info(self.plan)
+
+    def status(self) -> int:
+        """Device-side fault bits (0 = healthy); raises AdamWError if a bounded wait gave up."""
+        return adamw_plan_status(self.plan)
 
     def check_nonfinite(self, found_inf, stream=None) -> None:
         adamw_check_nonfinite(self.plan, _ptr(found_inf), _stream(stream))

@@ -15,8 +15,8 @@ import os
 HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "_build", "libadamw.so")
 
-OK, EINVAL, EALIGN, EDTYPE, ENOMEM, ECUDA, EUNSUPPORTED = range(7)
-STATUS_NAMES = ["OK", "EINVAL", "EALIGN", "EDTYPE", "ENOMEM", "ECUDA", "EUNSUPPORTED"]
+OK, EINVAL, EALIGN, EDTYPE, ENOMEM, ECUDA, EUNSUPPORTED, ETIMEOUT = range(8)
+STATUS_NAMES = ["OK", "EINVAL", "EALIGN", "EDTYPE", "ENOMEM", "ECUDA", "EUNSUPPORTED", "ETIMEOUT"]
 F32, F16, BF16 = 0, 1, 2
 MODE_FP32, MODE_BF16_REM, MODE_Q8 = 0, 1, 2
 Q8_BLOCK = 256
@@ -53,6 +53,8 @@ _SIGNATURES = {
                                        ctypes.POINTER(ctypes.c_int64),
                                        ctypes.POINTER(ctypes.c_int32),
                                        ctypes.POINTER(ctypes.c_int32)]),
+    "adamw_plan_status": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_uint32)]),
+    "adamw_wait_selftest": (ctypes.c_int, [ctypes.c_int32, ctypes.POINTER(ctypes.c_double), _vp]),
     "adamw_check_nonfinite": (ctypes.c_int, [_vp, _vp, _vp]),
     "adamw_step": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                   _vp, _vp, _vp]),
@@ -75,11 +77,12 @@ _lib = None
 
 
 def load(path: str | None = None) -> ctypes.CDLL:
-    """Load the library once; fails loudly when it has not been built."""
+    """Load the library once (``path``, else $ADAMW_LIB, else the in-tree build);
+    fails loudly when it has not been built."""
     global _lib
     if _lib is not None:
         return _lib
-    path = path or LIB_PATH
+    path = path or os.environ.get("ADAMW_LIB") or LIB_PATH
     if not os.path.exists(path):
         raise ImportError(
             f"libadamw.so not found at {path}; build it first with "
@@ -124,6 +127,22 @@ def adamw_plan_info(plan: int) -> dict:
                                   ctypes.byref(b)))
     return {"total_numel": n.value, "n_chunks": c.value, "grid_blocks": g.value,
             "block_threads": b.value}
+
+
+def adamw_plan_status(plan: int) -> int:
+    """Fault bits of the plan's device-side pipeline; raises AdamWError (ETIMEOUT) if set."""
+    bits = ctypes.c_uint32()
+    _check(load().adamw_plan_status(plan, ctypes.byref(bits)))
+    return bits.value
+
+
+def adamw_wait_selftest(limit_us: int, stream: int | None) -> tuple[int, float]:
+    """(status, ms waited) of the bounded-wait self-test; ETIMEOUT is its normal status."""
+    ms = ctypes.c_double()
+    st = load().adamw_wait_selftest(limit_us, ctypes.byref(ms), stream)
+    if st not in (OK, ETIMEOUT):
+        _check(st)
+    return st, ms.value
 
 
 def adamw_check_nonfinite(plan: int, found_inf_dev: int, stream: int | None) -> None:

@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libadamw.so")
-SOURCES = ["capi.cpp", "qmap.cpp", "step_kernels.cu", "aux_kernels.cu", "noalloc.cu"]
+SOURCES = ["capi.cpp", "qmap.cpp", "step_kernels.cu", "bulk_kernels.cu", "aux_kernels.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -32,7 +32,7 @@ def nvcc() -> str:
 
 def _deps() -> list[str]:
     files = [os.path.join(CSRC, s) for s in SOURCES]
-    files += [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".h")]
+    files += [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     files += [os.path.join(INCLUDE, f) for f in os.listdir(INCLUDE) if f.endswith(".h")]
     return files
 

@@ -1,0 +1,345 @@
+// bulk_kernels.cu -- the fp32 and bf16+remainder step with bulk-async staging.
+//
+// One CTA per SM: a producer warp streams each 2048-element tile of every
+// input (p [+ remainder], g, m, v) into a ring of shared-memory stages with
+// cp.async.bulk (the TMA engine, completion counted on an mbarrier per stage),
+// and eight consumer warps update the tile from shared memory and store the
+// results straight to global memory.  Many tiles are in flight per SM without
+// holding them in registers, which is what an HBM-bound stream needs.
+//
+// Every wait on an mbarrier is bounded: after kWaitLimitNs (2 s of
+// %globaltimer) the waiting thread records a fault code in the plan's scratch
+// word and leaves; a producer that gives up first waits, again bounded, for
+// the copies it already issued so none lands in freed shared memory.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+#include "step_common.cuh"
+
+namespace adamw {
+namespace {
+
+constexpr int kConsumers = 2 * kThreads;        // consumer threads (16 warps)
+constexpr int kBulkThreads = kConsumers + 32;   // + 1 producer warp
+constexpr int kTile = kConsumers * 4;           // elements per stage: 4 per consumer thread
+static_assert(kTile % kVec == 0, "bulk copies move whole 8-element groups");
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+// Bounded wait: false if the phase did not complete within limit_ns.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (global_ns() - t0 > limit_ns) return false;
+  return true;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Byte layout of one stage: p, rem (bf16 mode), g, m, v -- each kTile elements.
+template <adamw_mode MODE, typename GT>
+struct Stage {
+  static constexpr int kP = MODE == ADAMW_MODE_FP32 ? 4 : 2;
+  static constexpr int kG = sizeof(GT);
+  static constexpr int oP = 0;
+  static constexpr int oR = oP + kTile * kP;
+  static constexpr int oG = oR + (MODE == ADAMW_MODE_BF16_REM ? kTile * 2 : 0);
+  static constexpr int oM = oG + kTile * kG;
+  static constexpr int oV = oM + kTile * 4;
+  static constexpr int kBytes = oV + kTile * 4;
+  static_assert(kBytes % 128 == 0, "stages stay 128-byte aligned");
+};
+
+// Measured on GB300 (GPT-2 list, fp32 states): 16 consumer warps with 3
+// stages moved 98% of the copy bandwidth; 8 warps x 6 stages 91%, 16 x 4-5
+// stages 97%, 24-30 warps 96-97%.
+template <int MODE> struct BulkTune { static constexpr int stages = 3; };
+
+template <adamw_mode MODE, typename GT>
+constexpr int bulk_smem_bytes() {
+  return BulkTune<MODE>::stages * Stage<MODE, GT>::kBytes + 2 * BulkTune<MODE>::stages * 8;
+}
+
+__device__ __forceinline__ void fault(const StepArgs& a, uint32_t code) {
+  atomicOr(&a.scratch->fault, code);
+}
+
+// The producer: one thread issues the bulk copies of every tile of this CTA.
+template <adamw_mode MODE, typename GT>
+__device__ void produce(const StepArgs& a, unsigned char* ring, uint64_t* full, uint64_t* empty) {
+  using L = Stage<MODE, GT>;
+  constexpr int S = BulkTune<MODE>::stages;
+  uint32_t i = 0;
+  bool ok = true;
+  for (int64_t c = blockIdx.x; ok && c < a.n_chunks; c += gridDim.x) {
+    const Chunk ch = a.chunks[c];
+    const TensorDesc td = a.tensors[ch.tensor];
+    for (int k = 0; k * kTile < ch.len; ++k, ++i) {
+      const uint32_t s = i % S;
+      if (!mbar_wait(&empty[s], ((i / S) & 1u) ^ 1u)) {
+        fault(a, 1u);
+        ok = false;
+        break;
+      }
+      const int len = min(kTile, ch.len - k * kTile);
+      const int nb = td.vec_ok ? (len & ~(kVec - 1)) : 0;  // elements moved in bulk
+      const int64_t e = ch.start + static_cast<int64_t>(k) * kTile;
+      unsigned char* st = ring + static_cast<size_t>(s) * L::kBytes;
+      const uint32_t bytes = nb * (L::kP + L::kG + 8 + (MODE == ADAMW_MODE_BF16_REM ? 2 : 0));
+      mbar_expect_tx(&full[s], bytes);
+      if (nb > 0) {
+        bulk_g2s(st + L::oP, static_cast<const unsigned char*>(td.p) + e * L::kP, nb * L::kP, &full[s]);
+        if (MODE == ADAMW_MODE_BF16_REM)
+          bulk_g2s(st + L::oR, td.rem + e, nb * 2, &full[s]);
+        bulk_g2s(st + L::oG, static_cast<const unsigned char*>(td.g) + e * L::kG, nb * L::kG, &full[s]);
+        bulk_g2s(st + L::oM, static_cast<const float*>(td.m) + e, nb * 4, &full[s]);
+        bulk_g2s(st + L::oV, static_cast<const float*>(td.v) + e, nb * 4, &full[s]);
+      }
+    }
+  }
+  if (!ok) {
+    // drain: every stage issued in the last S tiles completes on its own
+    for (uint32_t j = (i > S ? i - S : 0); j < i; ++j)
+      if (!mbar_wait(&full[j % S], (j / S) & 1u)) fault(a, 4u);
+  }
+}
+
+template <typename GT>
+__device__ __forceinline__ float grad_from_smem(const unsigned char* base, int idx) {
+  if constexpr (sizeof(GT) == 4) {
+    return reinterpret_cast<const float*>(base)[idx];
+  } else {
+    const uint32_t h = reinterpret_cast<const uint16_t*>(base)[idx];
+    if constexpr (std::is_same<GT, __half>::value) return f16_to_f32(h);
+    return bf16_to_f32(h);
+  }
+}
+
+// Four consecutive elements [j, j+4) of a tile from shared memory.
+template <adamw_mode MODE, typename GT>
+__device__ __forceinline__ void load4_smem(const unsigned char* st, int j, float (&p)[4],
+                                           float (&g)[4], float (&m)[4], float (&v)[4]) {
+  using L = Stage<MODE, GT>;
+  if (MODE == ADAMW_MODE_FP32) {
+    const float4 x = *reinterpret_cast<const float4*>(st + L::oP + j * 4);
+    p[0] = x.x; p[1] = x.y; p[2] = x.z; p[3] = x.w;
+  } else {
+    const uint2 h = *reinterpret_cast<const uint2*>(st + L::oP + j * 2);
+    const uint2 r = *reinterpret_cast<const uint2*>(st + L::oR + j * 2);
+    p[0] = rem_join(h.x & 0xFFFFu, r.x & 0xFFFFu);
+    p[1] = rem_join(h.x >> 16, r.x >> 16);
+    p[2] = rem_join(h.y & 0xFFFFu, r.y & 0xFFFFu);
+    p[3] = rem_join(h.y >> 16, r.y >> 16);
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) g[q] = grad_from_smem<GT>(st + L::oG, j + q);
+  const float4 mm = *reinterpret_cast<const float4*>(st + L::oM + j * 4);
+  const float4 vv = *reinterpret_cast<const float4*>(st + L::oV + j * 4);
+  m[0] = mm.x; m[1] = mm.y; m[2] = mm.z; m[3] = mm.w;
+  v[0] = vv.x; v[1] = vv.y; v[2] = vv.z; v[3] = vv.w;
+}
+
+template <adamw_mode MODE>
+__device__ __forceinline__ void store4(const TensorDesc& td, int64_t e, const float (&p)[4],
+                                       const float (&m)[4], const float (&v)[4]) {
+  if (MODE == ADAMW_MODE_FP32) {
+    __stcs(reinterpret_cast<float4*>(static_cast<float*>(td.p) + e), make_float4(p[0], p[1], p[2], p[3]));
+  } else {
+    uint32_t h0, r0, h1, r1, h2, r2, h3, r3;
+    rem_split(p[0], h0, r0);
+    rem_split(p[1], h1, r1);
+    rem_split(p[2], h2, r2);
+    rem_split(p[3], h3, r3);
+    __stcs(reinterpret_cast<uint2*>(static_cast<uint16_t*>(td.p) + e),
+           make_uint2(h0 | (h1 << 16), h2 | (h3 << 16)));
+    __stcs(reinterpret_cast<uint2*>(td.rem + e), make_uint2(r0 | (r1 << 16), r2 | (r3 << 16)));
+  }
+  __stcs(reinterpret_cast<float4*>(static_cast<float*>(td.m) + e), make_float4(m[0], m[1], m[2], m[3]));
+  __stcs(reinterpret_cast<float4*>(static_cast<float*>(td.v) + e), make_float4(v[0], v[1], v[2], v[3]));
+}
+
+template <adamw_mode MODE, typename GT>
+__global__ void __launch_bounds__(kBulkThreads, 1) step_bulk_kernel(const StepArgs a) {
+  using L = Stage<MODE, GT>;
+  constexpr int S = BulkTune<MODE>::stages;
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  unsigned char* ring = smem_raw;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + S * L::kBytes);
+  uint64_t* empty = full + S;
+  __shared__ Scal s_sc;
+  __shared__ int s_skip;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);                     // the producer's arrive.expect_tx
+      mbar_init(&empty[s], kConsumers / 32);      // one arrive per consumer warp
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  __syncthreads();
+
+  if (threadIdx.x >= kConsumers) {
+    // producer warp: one lane issues; the skip flag is read here too, so that
+    // no copy is issued for a skipped step
+    if (threadIdx.x == kConsumers) {
+      const bool skip = a.found_inf != nullptr && *a.found_inf != 0.0f;
+      if (!skip) produce<MODE, GT>(a, ring, full, empty);
+    }
+    return;
+  }
+
+  int t = 0;
+  if (threadIdx.x == 0) s_skip = prologue(a, s_sc, t);
+  asm volatile("bar.sync 1, %0;" ::"n"(kConsumers) : "memory");   // consumers only
+  if (s_skip) return;
+  const Scal s = s_sc;
+  if (threadIdx.x == 0) take_ticket(a, t);
+  const int lane = threadIdx.x & 31;
+
+  uint32_t i = 0;
+  for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
+    const Chunk ch = a.chunks[c];
+    const TensorDesc td = a.tensors[ch.tensor];
+    const float decay = __fsub_rn(1.0f, __fmul_rn(s.lr, td.wd));
+    for (int k = 0; k * kTile < ch.len; ++k, ++i) {
+      const uint32_t st_i = i % S;
+      if (!mbar_wait(&full[st_i], (i / S) & 1u)) {
+        fault(a, 2u);
+        return;
+      }
+      const int len = min(kTile, ch.len - k * kTile);
+      const int nb = td.vec_ok ? (len & ~(kVec - 1)) : 0;
+      const int64_t e0 = ch.start + static_cast<int64_t>(k) * kTile;
+      const unsigned char* st = ring + static_cast<size_t>(st_i) * L::kBytes;
+      // thread t owns elements [4t, 4t+4) of the tile: conflict-free 16-byte smem reads
+      {
+        const int j = threadIdx.x * 4;
+        if (j + 4 <= nb) {
+          float p[4], g[4], m[4], v[4];
+          load4_smem<MODE, GT>(st, j, p, g, m, v);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) update(p[q], g[q], m[q], v[q], s, decay);
+          store4<MODE>(td, e0 + j, p, m, v);
+        } else if (j < len) {
+          update_scalar<MODE, GT>(td, e0 + j, min(4, len - j), s, decay);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st_i]);
+    }
+  }
+}
+
+template <typename GT>
+cudaError_t launch_bulk_mode(adamw_mode mode, const StepArgs& a, int grid, cudaStream_t st) {
+  if (mode == ADAMW_MODE_FP32) {
+    step_bulk_kernel<ADAMW_MODE_FP32, GT>
+        <<<grid, kBulkThreads, bulk_smem_bytes<ADAMW_MODE_FP32, GT>(), st>>>(a);
+  } else {
+    step_bulk_kernel<ADAMW_MODE_BF16_REM, GT>
+        <<<grid, kBulkThreads, bulk_smem_bytes<ADAMW_MODE_BF16_REM, GT>(), st>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+template <typename GT>
+cudaError_t prepare_bulk_mode(adamw_mode mode) {
+  if (mode == ADAMW_MODE_FP32)
+    return cudaFuncSetAttribute(step_bulk_kernel<ADAMW_MODE_FP32, GT>,
+                                cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                bulk_smem_bytes<ADAMW_MODE_FP32, GT>());
+  return cudaFuncSetAttribute(step_bulk_kernel<ADAMW_MODE_BF16_REM, GT>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              bulk_smem_bytes<ADAMW_MODE_BF16_REM, GT>());
+}
+
+// Self-test of the bounded wait: one thread waits on an mbarrier phase that
+// nothing completes; the wait must give up after limit_ns and report it.
+__device__ uint32_t g_selftest_fault;
+__device__ unsigned long long g_selftest_ns;
+
+__global__ void wait_selftest_kernel(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  const uint64_t t0 = global_ns();
+  const bool done = mbar_wait(&bar, 0u, limit_ns);   // phase 0 never completes
+  g_selftest_ns = global_ns() - t0;
+  g_selftest_fault = done ? 0u : 1u;
+}
+
+}  // namespace
+
+cudaError_t run_wait_selftest(int limit_us, cudaStream_t s, uint32_t* fault_bits,
+                              double* waited_ms) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(static_cast<uint64_t>(limit_us) * 1000ull);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return e;
+  unsigned long long ns = 0;
+  if ((e = cudaMemcpyFromSymbol(fault_bits, g_selftest_fault, sizeof(uint32_t))) != cudaSuccess)
+    return e;
+  if ((e = cudaMemcpyFromSymbol(&ns, g_selftest_ns, sizeof(ns))) != cudaSuccess) return e;
+  *waited_ms = static_cast<double>(ns) * 1e-6;
+  return cudaSuccess;
+}
+
+cudaError_t launch_step_bulk(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int grid,
+                             cudaStream_t s) {
+  switch (gdt) {
+    case ADAMW_F32: return launch_bulk_mode<float>(mode, a, grid, s);
+    case ADAMW_F16: return launch_bulk_mode<__half>(mode, a, grid, s);
+    case ADAMW_BF16: return launch_bulk_mode<__nv_bfloat16>(mode, a, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t prepare_step_bulk(adamw_mode mode, adamw_dtype gdt) {
+  switch (gdt) {
+    case ADAMW_F32: return prepare_bulk_mode<float>(mode);
+    case ADAMW_F16: return prepare_bulk_mode<__half>(mode);
+    case ADAMW_BF16: return prepare_bulk_mode<__nv_bfloat16>(mode);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace adamw

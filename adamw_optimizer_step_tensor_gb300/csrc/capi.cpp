@@ -32,6 +32,7 @@ struct adamw_plan {
   StepScratch* d_scratch = nullptr;
   QTables* d_qt = nullptr;
   int refine = 1;              // Q8: thresholds per bucket lookup of the current maps
+  bool bulk = false;           // launch the bulk-staged step kernel
 };
 
 namespace {
@@ -166,8 +167,15 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
   int bps = 0, smem = 0;
-  e = step_occupancy(mode, grad_dtype, &bps, &smem);
-  if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  const bool bulk = kUseBulk && mode != ADAMW_MODE_Q8;
+  if (bulk) {
+    e = prepare_step_bulk(mode, grad_dtype);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bulk step)");
+    bps = 1;
+  } else {
+    e = step_occupancy(mode, grad_dtype, &bps, &smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
+  }
   if (bps < 1) bps = 1;
   const int64_t chunk = choose_chunk(total, sms, bps);
   for (int32_t i = 0; i < n_tensors; ++i)
@@ -184,6 +192,7 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
   p->n_chunks = static_cast<int64_t>(chunks.size());
 
   p->device = device;
+  p->bulk = bulk;
   const int64_t resident = static_cast<int64_t>(bps) * sms;
   p->grid = static_cast<int>(p->n_chunks < resident ? (p->n_chunks > 0 ? p->n_chunks : 1) : resident);
   const int64_t check_res = 8LL * sms;
@@ -239,6 +248,32 @@ adamw_status adamw_plan_info(const adamw_plan* plan, int64_t* total_numel, int64
   return ADAMW_OK;
 }
 
+adamw_status adamw_plan_status(const adamw_plan* plan, uint32_t* fault_bits) {
+  if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
+  adamw_status st = check_device(plan);
+  if (st != ADAMW_OK) return st;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  uint32_t bits = 0;
+  e = cudaMemcpy(&bits, &plan->d_scratch->fault, sizeof(bits), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read fault word");
+  if (fault_bits) *fault_bits = bits;
+  if (bits != 0)
+    return fail(ADAMW_ETIMEOUT, "a bounded wait in the step pipeline gave up (fault bits 0x%x)", bits);
+  return ADAMW_OK;
+}
+
+adamw_status adamw_wait_selftest(int32_t limit_us, double* waited_ms, void* stream) {
+  if (limit_us < 0 || limit_us > 5000000) return fail(ADAMW_EINVAL, "limit_us must lie in [0, 5e6]");
+  uint32_t bits = 0;
+  double ms = 0.0;
+  cudaError_t e = run_wait_selftest(limit_us, static_cast<cudaStream_t>(stream), &bits, &ms);
+  if (e != cudaSuccess) return cuda_fail(e, "wait self-test");
+  if (waited_ms) *waited_ms = ms;
+  if (bits != 0) return fail(ADAMW_ETIMEOUT, "the self-test wait gave up after %.3f ms", ms);
+  return ADAMW_OK;
+}
+
 adamw_status adamw_check_nonfinite(const adamw_plan* plan, float* found_inf_dev, void* stream) {
   if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
   if (!found_inf_dev) return fail(ADAMW_EINVAL, "found_inf_dev is NULL");
@@ -282,7 +317,10 @@ adamw_status adamw_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev
   a.scratch = plan->d_scratch;
   a.qt = plan->d_qt;
   a.refine = plan->refine;
-  cudaError_t e = launch_step(plan->mode, plan->gdt, a, plan->grid, static_cast<cudaStream_t>(stream));
+  cudaError_t e = plan->bulk ? launch_step_bulk(plan->mode, plan->gdt, a, plan->grid,
+                                                static_cast<cudaStream_t>(stream))
+                             : launch_step(plan->mode, plan->gdt, a, plan->grid,
+                                           static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "launch adamw step");
   return ADAMW_OK;
 }

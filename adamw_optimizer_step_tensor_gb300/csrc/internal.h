@@ -22,7 +22,10 @@ constexpr int kPass = kThreads * kVec;       // 2048 elements per CTA pass
 template <int MODE> struct Tune { static constexpr int unroll = 1, min_blocks = 3; };
 template <> struct Tune<ADAMW_MODE_FP32> { static constexpr int unroll = 2, min_blocks = 2; };
 template <> struct Tune<ADAMW_MODE_Q8> { static constexpr int unroll = 1, min_blocks = 3; };
-constexpr int kChunkMax = 8 * kPass;         // chunks hold 2048..16384 elements (chosen per plan)
+constexpr int kChunkMax = 8 * kPass;         // chunks hold up to 16384 elements (chosen per plan)
+// fp32 and bf16+remainder steps: stage tiles through shared memory with bulk
+// async copies (bulk_kernels.cu) instead of 128-bit register loads.
+constexpr bool kUseBulk = true;
 constexpr int kQBlock = ADAMW_Q8_BLOCK;      // 256
 static_assert(kPass % kQBlock == 0, "chunks must hold whole Q8 blocks");
 static_assert(32 * kVec == kQBlock, "one warp pass covers exactly one Q8 block");
@@ -82,7 +85,8 @@ struct StepScratch {
   uint32_t memo_b1, memo_b2;   // bit patterns of the betas they were computed for
   float memo_bc1;              // fl32(1 - b1^t)
   float memo_inv_sqrt_bc2;     // fl32(1 / sqrt(1 - b2^t))
-  uint32_t pad[2];
+  uint32_t fault;              // nonzero: a bounded wait in a kernel gave up (bit per site)
+  uint32_t pad;
 };
 static_assert(sizeof(StepScratch) == 32, "StepScratch layout");
 
@@ -124,6 +128,11 @@ cudaError_t launch_step(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int
                         cudaStream_t s);
 cudaError_t step_occupancy(adamw_mode mode, adamw_dtype gdt, int* blocks_per_sm,
                            int* smem_bytes);
+cudaError_t launch_step_bulk(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int grid,
+                             cudaStream_t s);
+cudaError_t prepare_step_bulk(adamw_mode mode, adamw_dtype gdt);
+cudaError_t run_wait_selftest(int limit_us, cudaStream_t s, uint32_t* fault_bits,
+                              double* waited_ms);
 cudaError_t launch_nonfinite(adamw_dtype gdt, const TensorDesc* tensors, const Chunk* chunks,
                              int64_t n_chunks, float* found_inf, int grid, cudaStream_t s);
 cudaError_t launch_split(const float* master, uint16_t* hi, int16_t* rem, int64_t n,

@@ -17,172 +17,10 @@
 #include <cuda_fp16.h>
 
 #include "internal.h"
+#include "step_common.cuh"
 
 namespace adamw {
 namespace {
-
-struct Scal {
-  float b1, b2, omb1, omb2, eps, lr, step_size, inv_sqrt_bc2, inv_scale;
-  int scaled;
-};
-
-// b^t by float64 square-and-multiply; every product is one IEEE rounding.
-__device__ double pow_binary(double b, int t) {
-  double r = 1.0, x = b;
-  while (t) {
-    if (t & 1) r = __dmul_rn(r, x);
-    x = __dmul_rn(x, x);
-    t >>= 1;
-  }
-  return r;
-}
-
-struct BiasCorr {
-  float bc1, inv_sqrt_bc2;
-};
-
-// fl32(1 - b1^t) and fl32(1 / sqrt(1 - b2^t)), every step in float64.
-__device__ BiasCorr bias_corrections(float beta1, float beta2, int t) {
-  BiasCorr r;
-  r.bc1 = __double2float_rn(__dsub_rn(1.0, pow_binary((double)beta1, t)));
-  r.inv_sqrt_bc2 = __double2float_rn(
-      __ddiv_rn(1.0, __dsqrt_rn(__dsub_rn(1.0, pow_binary((double)beta2, t)))));
-  return r;
-}
-
-// Thread 0 of every CTA, before the CTA's barrier: read the run-time scalars
-// (all loads issued together) and decide skip.  The float64 bias corrections
-// are taken from the plan's memo when the previous launch left them for this
-// step index and these betas, otherwise computed here.
-__device__ bool prologue(const StepArgs& a, Scal& s, int& t_out) {
-  const float found = a.found_inf != nullptr ? *a.found_inf : 0.0f;
-  const int step = *a.step;
-  const float lr = *a.lr;
-  const float gscale = a.grad_scale != nullptr ? *a.grad_scale : 1.0f;
-  const StepScratch memo = *a.scratch;
-  if (found != 0.0f) return true;
-  const int t = step + 1;
-  const BiasCorr bc = (memo.memo_t == t && memo.memo_b1 == __float_as_uint(a.beta1) &&
-                       memo.memo_b2 == __float_as_uint(a.beta2))
-                          ? BiasCorr{memo.memo_bc1, memo.memo_inv_sqrt_bc2}
-                          : bias_corrections(a.beta1, a.beta2, t);
-  s.b1 = a.beta1;
-  s.b2 = a.beta2;
-  s.omb1 = __fsub_rn(1.0f, a.beta1);
-  s.omb2 = __fsub_rn(1.0f, a.beta2);
-  s.eps = a.eps;
-  s.lr = lr;
-  s.inv_sqrt_bc2 = bc.inv_sqrt_bc2;
-  s.step_size = __fdiv_rn(lr, bc.bc1);
-  s.scaled = a.grad_scale != nullptr;
-  s.inv_scale = s.scaled ? __fdiv_rn(1.0f, gscale) : 1.0f;
-  t_out = t;
-  return false;
-}
-
-// Thread 0 of every CTA that runs the step, after the barrier: take a ticket.
-// Every CTA read *step (and the memo) before its ticket -- the fence orders
-// it -- so the last CTA to take one can store t and the memo for step t + 1
-// without any CTA of this launch seeing either.  Nothing waits on anything.
-__device__ void take_ticket(const StepArgs& a, int t) {
-  __threadfence();
-  const unsigned tk = atomicAdd(&a.scratch->ticket, 1u);
-  if (tk == gridDim.x - 1) {
-    *a.step = t;
-    const BiasCorr nx = bias_corrections(a.beta1, a.beta2, t + 1);
-    StepScratch* m = a.scratch;
-    m->memo_bc1 = nx.bc1;
-    m->memo_inv_sqrt_bc2 = nx.inv_sqrt_bc2;
-    m->memo_b1 = __float_as_uint(a.beta1);
-    m->memo_b2 = __float_as_uint(a.beta2);
-    m->memo_t = t + 1;
-    atomicExch(&m->ticket, 0u);
-  }
-}
-
-__device__ __forceinline__ void update(float& p, float g, float& m, float& v, const Scal& s,
-                                       float decay) {
-  if (s.scaled) g = __fmul_rn(g, s.inv_scale);
-  m = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
-  v = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, __fmul_rn(g, g)));
-  const float h = __fadd_rn(__fmul_rn(__fsqrt_rn(v), s.inv_sqrt_bc2), s.eps);
-  const float u = __fdiv_rn(m, h);
-  p = __fsub_rn(__fmul_rn(p, decay), __fmul_rn(s.step_size, u));
-}
-
-// ---------------------------------------------------------------- loads/stores
-__device__ __forceinline__ void ld8f(const float* q, float (&x)[8]) {
-  const float4 a = __ldcs(reinterpret_cast<const float4*>(q));
-  const float4 b = __ldcs(reinterpret_cast<const float4*>(q) + 1);
-  x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-  x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
-__device__ __forceinline__ void st8f(float* q, const float (&x)[8]) {
-  __stcs(reinterpret_cast<float4*>(q), make_float4(x[0], x[1], x[2], x[3]));
-  __stcs(reinterpret_cast<float4*>(q) + 1, make_float4(x[4], x[5], x[6], x[7]));
-}
-__device__ __forceinline__ void ld8u16(const void* q, uint32_t (&w)[4]) {
-  const uint4 a = __ldcs(reinterpret_cast<const uint4*>(q));
-  w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-}
-__device__ __forceinline__ void st8u16(void* q, const uint32_t (&w)[4]) {
-  __stcs(reinterpret_cast<uint4*>(q), make_uint4(w[0], w[1], w[2], w[3]));
-}
-
-__device__ __forceinline__ float bf16_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
-__device__ __forceinline__ float f16_to_f32(uint32_t h) {
-  return __half2float(__ushort_as_half(static_cast<unsigned short>(h)));
-}
-
-template <typename GT> struct Grad;
-template <> struct Grad<float> {
-  static __device__ __forceinline__ void load8(const void* g, int64_t e, float (&x)[8]) {
-    ld8f(static_cast<const float*>(g) + e, x);
-  }
-  static __device__ __forceinline__ float load1(const void* g, int64_t e) {
-    return static_cast<const float*>(g)[e];
-  }
-};
-template <> struct Grad<__half> {
-  static __device__ __forceinline__ void load8(const void* g, int64_t e, float (&x)[8]) {
-    uint32_t w[4];
-    ld8u16(static_cast<const uint16_t*>(g) + e, w);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x[2 * i] = f16_to_f32(w[i] & 0xFFFFu);
-      x[2 * i + 1] = f16_to_f32(w[i] >> 16);
-    }
-  }
-  static __device__ __forceinline__ float load1(const void* g, int64_t e) {
-    return f16_to_f32(static_cast<const uint16_t*>(g)[e]);
-  }
-};
-template <> struct Grad<__nv_bfloat16> {
-  static __device__ __forceinline__ void load8(const void* g, int64_t e, float (&x)[8]) {
-    uint32_t w[4];
-    ld8u16(static_cast<const uint16_t*>(g) + e, w);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      x[2 * i] = bf16_to_f32(w[i] & 0xFFFFu);
-      x[2 * i + 1] = bf16_to_f32(w[i] >> 16);
-    }
-  }
-  static __device__ __forceinline__ float load1(const void* g, int64_t e) {
-    return bf16_to_f32(static_cast<const uint16_t*>(g)[e]);
-  }
-};
-
-// Remainder join / split on one element (integer only; see adamw.h).
-__device__ __forceinline__ float rem_join(uint32_t hi, uint32_t rem16) {
-  const uint32_t top = (hi - (rem16 >> 15)) & 0xFFFFu;
-  return __uint_as_float((top << 16) | (rem16 & 0xFFFFu));
-}
-__device__ __forceinline__ void rem_split(float x, uint32_t& hi, uint32_t& rem16) {
-  const uint32_t b = __float_as_uint(x);
-  const uint32_t lo = b & 0xFFFFu;
-  hi = ((b >> 16) + (lo >> 15)) & 0xFFFFu;
-  rem16 = lo;
-}
 
 // ---------------------------------------------------------------- fp32 / bf16+rem
 // The 8 consecutive elements one thread owns in one pass, in registers.
@@ -231,33 +69,6 @@ __device__ __forceinline__ void update_store_group(const TensorDesc& td, int64_t
   }
   st8f(static_cast<float*>(td.m) + e, x.m);
   st8f(static_cast<float*>(td.v) + e, x.v);
-}
-
-// Elements [e, e + n) one at a time: ragged tails and tensors whose pointers
-// are not all 16-byte aligned.
-template <adamw_mode MODE, typename GT>
-__device__ void update_scalar(const TensorDesc& td, int64_t e, int n, const Scal& s,
-                              float decay) {
-  float* const pf = static_cast<float*>(td.p);
-  uint16_t* const ph = static_cast<uint16_t*>(td.p);
-  float* const mf = static_cast<float*>(td.m);
-  float* const vf = static_cast<float*>(td.v);
-  for (int i = 0; i < n; ++i) {
-    const int64_t k = e + i;
-    float p = MODE == ADAMW_MODE_FP32 ? pf[k] : rem_join(ph[k], static_cast<uint16_t>(td.rem[k]));
-    float m = mf[k], v = vf[k];
-    update(p, Grad<GT>::load1(td.g, k), m, v, s, decay);
-    if (MODE == ADAMW_MODE_FP32) {
-      pf[k] = p;
-    } else {
-      uint32_t h, r;
-      rem_split(p, h, r);
-      ph[k] = static_cast<uint16_t>(h);
-      td.rem[k] = static_cast<int16_t>(static_cast<uint16_t>(r));
-    }
-    mf[k] = m;
-    vf[k] = v;
-  }
 }
 
 // A thread's position in its sequence of trips: chunk c (strided by the

@@ -57,7 +57,8 @@ typedef enum {
   ADAMW_EDTYPE = 3,       /* unknown dtype or mode value */
   ADAMW_ENOMEM = 4,       /* plan allocation failed */
   ADAMW_ECUDA = 5,        /* a CUDA runtime call or launch failed */
-  ADAMW_EUNSUPPORTED = 6  /* a valid but unsupported combination */
+  ADAMW_EUNSUPPORTED = 6, /* a valid but unsupported combination */
+  ADAMW_ETIMEOUT = 7      /* a bounded device-side wait gave up (see adamw_plan_status) */
 } adamw_status;
 
 typedef enum { ADAMW_F32 = 0, ADAMW_F16 = 1, ADAMW_BF16 = 2 } adamw_dtype;
@@ -120,6 +121,26 @@ adamw_status adamw_plan_destroy(adamw_plan* plan);
 adamw_status adamw_plan_info(const adamw_plan* plan, int64_t* total_numel,
                              int64_t* n_chunks, int32_t* grid_blocks,
                              int32_t* block_threads);
+
+/*
+ * Device-side health of a plan.  The fp32 and bf16+remainder steps stage
+ * tiles through shared memory with asynchronous bulk copies; every wait of
+ * that pipeline is bounded (2 s), and a wait that gives up records a bit in
+ * the plan's fault word and ends its CTA without touching further data.
+ * Waits for all work on the device, then copies the word to *fault_bits
+ * (may be NULL): ADAMW_OK if it is 0, ADAMW_ETIMEOUT otherwise.  The word
+ * stays set until the plan is destroyed.
+ */
+adamw_status adamw_plan_status(const adamw_plan* plan, uint32_t* fault_bits);
+
+/*
+ * Self-test of the bounded wait used by the pipeline: one thread waits on an
+ * mbarrier phase that nothing completes, for limit_us microseconds.  Returns
+ * ADAMW_ETIMEOUT when the wait gave up as it must (the normal result) and
+ * writes the time waited to *waited_ms; the CUDA context stays usable.
+ * Synchronous on `stream`.
+ */
+adamw_status adamw_wait_selftest(int32_t limit_us, double* waited_ms, void* stream);
 
 /*
  * found_inf: "FusedAdam & PyTorch Lightning AMP" -- a fused step does the

@@ -79,6 +79,7 @@ def test_gpt2_small_full_size_cosine_lr_sampled():
                     assert np.array_equal(_take(m, i).cpu().numpy().view(np.uint32), o.m.view(np.uint32)), (s, k)
                     assert np.array_equal(_take(v, i).cpu().numpy().view(np.uint32), o.v.view(np.uint32)), (s, k)
         assert int(w.step_dev.item()) == 100
+        assert w.opt.status() == 0
         worst = max(np.max(np.abs(o.p.astype(np.float64) - r.p)) for o, r in zip(orc, ref))
         assert worst <= 5e-5
     finally:
@@ -153,6 +154,7 @@ def test_llama3_8b_bf16_remainders_full_size_sampled():
             assert np.array_equal(_take(m, i).cpu().numpy().view(np.uint32), o.m.view(np.uint32)), k
             assert np.array_equal(_take(v, i).cpu().numpy().view(np.uint32), o.v.view(np.uint32)), k
         assert int(w.step_dev.item()) == 5
+        assert w.opt.status() == 0
     finally:
         del w
         _cleanup()
