@@ -72,7 +72,7 @@ def measured_peak():
 def kernel_source_sha() -> str:
     h = hashlib.sha256()
     d = os.path.join(ROOT, "adamw_optimizer_step_tensor_gb300", "csrc")
-    for name in ("step_kernels.cu", "internal.h"):
+    for name in ("step_kernels.cu", "bulk_kernels.cu", "step_common.cuh", "internal.h"):
         with open(os.path.join(d, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
