@@ -147,62 +147,6 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::min_blocks) step_kernel(
 }
 
 // ---------------------------------------------------------------- 8-bit states
-// Nearest code of a normalised x (|x| <= 1, or NaN) in one map: the bucket of
-// |x| gives the lowest code any x of that bucket can have; at most R
-// thresholds lie inside a bucket, and code = lo + #{r < R : thr[lo + r] <= x}
-// because thr is ascending.  NaN lands in the last bucket, whose lowest code
-// is 0 and whose thresholds never compare true: code 0.
-template <int R>
-__device__ __forceinline__ uint32_t nearest_code(float x, const QMapDev& t) {
-  const uint32_t b = __float_as_uint(x);
-  const int k = bucket_of(b & 0x7FFFFFFFu);
-  const uint32_t lo = (b >> 31) ? t.lo_neg[k] : t.lo_pos[k];
-  uint32_t c = lo;
-#pragma unroll
-  for (int r = 0; r < R; ++r) c += (t.thr[lo + r] <= x) ? 1u : 0u;
-  return c;
-}
-
-// Per-warp block constants for re-quantisation: the absmax bits, the scale
-// (1, or 2^64 below 2^-64) and the reciprocal fl(1/(A*scale)).
-struct BlockNorm {
-  uint32_t bits;
-  float scale, inv;
-};
-
-__device__ __forceinline__ BlockNorm block_norm(uint32_t amax_bits) {
-  const float A = __uint_as_float(amax_bits);
-  BlockNorm n;
-  n.bits = amax_bits;
-  n.scale = A < kTinyAbsmax ? kTinyScale : 1.0f;
-  n.inv = __frcp_rn(__fmul_rn(A, n.scale));
-  return n;
-}
-
-// Codes of the 8 values one lane owns.  All branches are warp-uniform (the
-// block constants are the same in every lane); x * 1 is exact, so the
-// scaled multiply is skipped when the scale is 1.
-template <int R>
-__device__ __forceinline__ void quant8(const float (&x)[8], const BlockNorm& n,
-                                       const QMapDev& t, uint32_t zero_code, uint32_t (&q)[8]) {
-  if (n.bits == 0u) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = zero_code;
-  } else if (n.scale == 1.0f) {
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = nearest_code<R>(__fmul_rn(x[i], n.inv), t);
-  } else {
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-      q[i] = nearest_code<R>(__fmul_rn(__fmul_rn(x[i], n.scale), n.inv), t);
-  }
-}
-
-__device__ __forceinline__ uint2 pack8(const uint32_t (&q)[8]) {
-  return make_uint2(q[0] | q[1] << 8 | q[2] << 16 | q[3] << 24,
-                    q[4] | q[5] << 8 | q[6] << 16 | q[7] << 24);
-}
-
 template <typename GT, int R>
 __global__ void __launch_bounds__(kThreads, Tune<ADAMW_MODE_Q8>::min_blocks)
 step_q8_kernel(const StepArgs a) {
