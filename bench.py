@@ -282,6 +282,8 @@ class Workload:
 class Gpt2Small(Workload):
     name = "gpt2_small_fp32_cosine_lr"
     bytes_per_param = 28.0
+    e2e_what = ("pinned-host grads -> device, adamw_step, updated params -> pinned host; the list "
+                "in 8 groups (one plan each) so copies in, steps and copies out overlap on 3 streams")
 
     def __init__(self, seed=0):
         import torch
@@ -317,18 +319,64 @@ class Gpt2Small(Workload):
         self.C.adamw_step(self.opt.plan, self.lr_ptrs[i % 100], self.step_dev.data_ptr(), 0.9, 0.999,
                           1e-8, None, None, self.stream)
 
-    def e2e_setup(self):
+    def e2e_setup(self, groups=8):
+        """Host-offload step: grads arrive from pinned host memory, params go back.
+
+        The list is split into `groups` contiguous runs of tensors with about
+        equal element counts, one plan (and step counter) each, so that the
+        host-to-device copy of one group, the step of the previous one and the
+        device-to-host copy of the one before overlap on three streams.
+        """
         import torch
+        from adamw_optimizer_step_tensor_gb300 import FusedAdamW
         self._host_g = torch.empty_like(self.g_buf, device="cpu").pin_memory()
         self._host_g.copy_(self.g_buf)
         self._host_p = torch.empty_like(self.p_buf, device="cpu").pin_memory()
+        base = self.p_buf.data_ptr()
+        offs = [(p.data_ptr() - base) // 4 for p in self.ps]
+        target = self.n_params / groups
+        self._groups, start, acc = [], 0, 0
+        for k, p in enumerate(self.ps):
+            acc += p.numel()
+            if acc >= target * (len(self._groups) + 1) or k == len(self.ps) - 1:
+                idx = list(range(start, k + 1))
+                lo, hi = offs[start], offs[k] + self.ps[k].numel()
+                opt = FusedAdamW([self.ps[j] for j in idx], [self.gs[j] for j in idx],
+                                 [self.ms[j] for j in idx], [self.vs[j] for j in idx],
+                                 [self.specs[j].wd for j in idx])
+                self._groups.append((lo, hi, opt, torch.zeros(1, dtype=torch.int32, device="cuda")))
+                start = k + 1
+        self._s = [torch.cuda.Stream() for _ in range(3)]          # in, step, out
+        n = len(self._groups)
+        self._ev = [[torch.cuda.Event() for _ in range(n)] for _ in range(3)]
         return self._host_g.numel() * 4, self._host_p.numel() * 4
 
-    def e2e_step(self, i):
-        self.g_buf.copy_(self._host_g, non_blocking=True)
-        self.step(i)
-        self._host_p.copy_(self.p_buf, non_blocking=True)
+    def e2e_begin(self, stream):
+        for s in self._s:
+            s.wait_stream(stream)
 
+    def e2e_end(self, stream):
+        for s in self._s:
+            stream.wait_stream(s)
+
+    def e2e_step(self, i):
+        import torch
+        s_in, s_cmp, s_out = self._s
+        ev_in, ev_cmp, ev_out = self._ev
+        for k, (lo, hi, opt, step_dev) in enumerate(self._groups):
+            s_in.wait_event(ev_cmp[k])            # the previous step has consumed these grads
+            with torch.cuda.stream(s_in):
+                self.g_buf[lo:hi].copy_(self._host_g[lo:hi], non_blocking=True)
+            ev_in[k].record(s_in)
+            s_cmp.wait_event(ev_in[k])
+            s_cmp.wait_event(ev_out[k])           # the previous copy-out has read these params
+            self.C.adamw_step(opt.plan, self.lr_ptrs[i % 100], step_dev.data_ptr(), 0.9, 0.999,
+                              1e-8, None, None, s_cmp.cuda_stream)
+            ev_cmp[k].record(s_cmp)
+            s_out.wait_event(ev_cmp[k])
+            with torch.cuda.stream(s_out):
+                self._host_p[lo:hi].copy_(self.p_buf[lo:hi], non_blocking=True)
+            ev_out[k].record(s_out)
 
 
 class Single(Workload):
@@ -632,22 +680,33 @@ def main():
     setup = w.e2e_setup() if hasattr(w, "e2e_setup") else None
     if setup is not None and args.e2e_steps > 0:
         h2d, d2h = setup
+        begin = getattr(w, "e2e_begin", None)
+        end = getattr(w, "e2e_end", None)
+        if begin:
+            begin(stream)
         for i in range(3):
             w.e2e_step(i)
+        if end:
+            end(stream)
         torch.cuda.synchronize()
         barrier(world)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        if begin:
+            begin(stream)
         for i in range(args.e2e_steps):
             w.e2e_step(i)
+        if end:
+            end(stream)
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world)
         e2e = {"value": w.n_params * world / (e2e_ms * 1e-3), "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                "ms_per_step": e2e_ms,
-               "what": "pinned-host grads -> device, adamw_step, updated params -> pinned host"}
+               "what": getattr(w, "e2e_what",
+                               "pinned-host grads -> device, adamw_step, updated params -> pinned host")}
     else:
         e2e = {"value": None, "unit": UNIT, "h2d_bytes_per_step": None, "d2h_bytes_per_step": None,
                "note": "no pinned-host copy of this workload's buffers fits beside it"}
