@@ -13,7 +13,8 @@ from __future__ import annotations
 from . import _capi
 from ._capi import (  # noqa: F401
     AdamWError, adamw_abi_version, adamw_bf16rem_join, adamw_bf16rem_split,
-    adamw_check_nonfinite, adamw_last_error, adamw_plan_create, adamw_plan_destroy,
+    adamw_check_nonfinite, adamw_last_error, adamw_lr_from_table, adamw_plan_create,
+    adamw_plan_destroy,
     adamw_plan_info, adamw_plan_status, adamw_q8_default_maps, adamw_q8_dequant, adamw_q8_quant,
     adamw_q8_set_maps, adamw_step, adamw_step_noalloc, adamw_wait_selftest,
 )

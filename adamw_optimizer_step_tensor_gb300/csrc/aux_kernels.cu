@@ -137,6 +137,14 @@ __global__ void q8_quant_kernel(const QTables* __restrict__ qt, int which,
   }
 }
 
+// lr = table[clamp(completed steps, 0, n - 1)]: one thread, stream-ordered.
+__global__ void lr_from_table_kernel(const float* __restrict__ table, int32_t n,
+                                     const int32_t* __restrict__ step, float* __restrict__ lr) {
+  int32_t s = *step;
+  s = s < 0 ? 0 : (s > n - 1 ? n - 1 : s);
+  *lr = table[s];
+}
+
 int grid_for(int64_t n, int per_block) {
   int64_t g = (n + per_block - 1) / per_block;
   if (g < 1) g = 1;
@@ -161,6 +169,12 @@ cudaError_t launch_nonfinite(adamw_dtype gdt, const TensorDesc* tensors, const C
     default:
       return cudaErrorInvalidValue;
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_lr_from_table(const float* table, int32_t n, const int32_t* step, float* lr,
+                                 cudaStream_t s) {
+  lr_from_table_kernel<<<1, 1, 0, s>>>(table, n, step, lr);
   return cudaGetLastError();
 }
 

@@ -325,6 +325,16 @@ adamw_status adamw_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev
   return ADAMW_OK;
 }
 
+adamw_status adamw_lr_from_table(const float* table, int32_t n, const int32_t* step_dev,
+                                 float* lr_dev, void* stream) {
+  if (n < 1) return fail(ADAMW_EINVAL, "the schedule table needs at least one entry");
+  if (!table || !step_dev || !lr_dev) return fail(ADAMW_EINVAL, "NULL pointer");
+  if (!aligned(table, 4) || !aligned(step_dev, 4) || !aligned(lr_dev, 4))
+    return fail(ADAMW_EALIGN, "pointers must be 4-byte aligned");
+  cudaError_t e = launch_lr_from_table(table, n, step_dev, lr_dev, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ADAMW_OK : cuda_fail(e, "launch lr lookup");
+}
+
 adamw_status adamw_bf16rem_split(const float* master, uint16_t* bf16, int16_t* rem, int64_t n,
                                  void* stream) {
   if (n < 0) return fail(ADAMW_EINVAL, "n < 0");

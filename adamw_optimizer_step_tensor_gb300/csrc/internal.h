@@ -15,13 +15,13 @@ constexpr int kThreads = 256;
 constexpr int kVec = 8;
 constexpr int kPass = kThreads * kVec;       // 2048 elements per CTA pass
 // Passes whose loads a thread issues together, and the resident CTAs per SM
-// the register budget targets, per storage mode (measured on GB300: fp32
-// states 2 x 2 -> 92% of copy bandwidth vs 88% for 1 x 3; bf16+remainder
-// 1 x 3 -> 94%; the instruction-bound 8-bit path: 3 CTAs/SM, 80 registers,
-// beat 4 CTAs/SM, whose 64-register budget spills).
+// the register budget targets, per storage mode.  Measured on GB300: the
+// register-load fp32 kernel (now only behind adamw_step_noalloc) 2 x 2 -> 92%
+// of copy bandwidth vs 88% for 1 x 3; the instruction-bound 8-bit kernel runs
+// best at 4 CTAs/SM (64 registers: 3.37 ms for 2^30 elements vs 3.63 ms at 3).
 template <int MODE> struct Tune { static constexpr int unroll = 1, min_blocks = 3; };
 template <> struct Tune<ADAMW_MODE_FP32> { static constexpr int unroll = 2, min_blocks = 2; };
-template <> struct Tune<ADAMW_MODE_Q8> { static constexpr int unroll = 1, min_blocks = 3; };
+template <> struct Tune<ADAMW_MODE_Q8> { static constexpr int unroll = 1, min_blocks = 4; };
 constexpr int kChunkMax = 8 * kPass;         // chunks hold up to 16384 elements (chosen per plan)
 // fp32 and bf16+remainder steps stage tiles through shared memory with bulk
 // async copies (bulk_kernels.cu) instead of 128-bit register loads.  The
@@ -139,6 +139,8 @@ cudaError_t launch_nonfinite(adamw_dtype gdt, const TensorDesc* tensors, const C
                              int64_t n_chunks, float* found_inf, int grid, cudaStream_t s);
 cudaError_t launch_split(const float* master, uint16_t* hi, int16_t* rem, int64_t n,
                          cudaStream_t s);
+cudaError_t launch_lr_from_table(const float* table, int32_t n, const int32_t* step, float* lr,
+                                 cudaStream_t s);
 cudaError_t launch_join(const uint16_t* hi, const int16_t* rem, float* master, int64_t n,
                         cudaStream_t s);
 cudaError_t launch_q8_dequant(const QTables* qt, int which, const uint8_t* codes,

@@ -204,12 +204,14 @@ step_q8_kernel(const StepArgs a) {
           mx_m = max(mx_m, __float_as_uint(m[i]) & 0x7FFFFFFFu);
           mx_v = max(mx_v, __float_as_uint(v[i]) & 0x7FFFFFFFu);
         }
-        const BlockNorm nm = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_m));
-        const BlockNorm nv = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_v));
-        quant8<R>(m, nm, qt.map[0], zc_m, q_m);
-        quant8<R>(v, nv, qt.map[1], zc_v, q_v);
+        // store each result as soon as it is final: short live ranges keep the
+        // kernel within the register budget of 3 CTAs per SM
         st8f(pf + e, p);
+        const BlockNorm nm = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_m));
+        quant8<R>(m, nm, qt.map[0], zc_m, q_m);
         __stcs(reinterpret_cast<uint2*>(cm + e), pack8(q_m));
+        const BlockNorm nv = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_v));
+        quant8<R>(v, nv, qt.map[1], zc_v, q_v);
         __stcs(reinterpret_cast<uint2*>(cv + e), pack8(q_v));
         if (lane == 0) {
           td.am[blk] = __uint_as_float(nm.bits);

@@ -207,6 +207,18 @@ adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t n_tensors,
                                 void* stream);
 
 /*
+ * On-device learning-rate schedule: *lr_dev = table[clamp(*step_dev, 0, n-1)],
+ * one single-thread launch on `stream`.  Issued before adamw_step on the same
+ * stream with the step's own counter, it feeds the step the schedule entry of
+ * the step about to run (entry s for the step after s completed steps), so a
+ * captured CUDA graph of lookup + step walks a schedule (e.g. the cosine decay
+ * of "4 bit Adam should support non constant lr") with no host work per step.
+ * table: device fp32 [n], n >= 1; all pointers device, 4-byte aligned.
+ */
+adamw_status adamw_lr_from_table(const float* table, int32_t n, const int32_t* step_dev,
+                                 float* lr_dev, void* stream);
+
+/*
  * Remainder split / join (the rule used by ADAMW_MODE_BF16_REM).
  *   split: lo = bits & 0xFFFF; bf16 = (bits >> 16) + (lo >= 0x8000) (mod 2^16);
  *          rem = (int16)lo.  bf16 is the nearest bf16, ties away from zero.

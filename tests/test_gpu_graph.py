@@ -87,3 +87,42 @@ def test_graph_replay_matches_eager(mode):
                     b = d_g[k].view(torch.int16 if d_g[k].element_size() == 2 else torch.int32)
                     assert torch.equal(a, b), (it, k)
     assert int(scalars["graph"]["step"].item()) == 10
+
+
+def test_graph_walks_a_device_lr_schedule():
+    """lookup(table[step]) + step captured once; each replay takes the next cosine entry."""
+    import synth
+    from adamw_optimizer_step_tensor_gb300 import _capi as C
+    from oracle import adamw as OA
+
+    n = 20000
+    rng = np.random.default_rng(9)
+    p0 = rng.normal(0, 0.02, n).astype(np.float32)
+    grads = [rng.normal(0, 1e-3, n).astype(np.float32) for _ in range(7)]
+    table = torch.tensor([OA.f32(synth.cosine_lr(s, total=7)) for s in range(7)], device="cuda")
+    p = torch.from_numpy(p0.copy()).cuda()
+    g = torch.zeros(n, device="cuda")
+    m, v = torch.zeros(n, device="cuda"), torch.zeros(n, device="cuda")
+    opt = FusedAdamW([p], [g], [m], [v], [0.1])
+    lr = torch.zeros(1, device="cuda")
+    step = torch.zeros(1, dtype=torch.int32, device="cuda")
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        s = torch.cuda.current_stream().cuda_stream
+        C.adamw_lr_from_table(table.data_ptr(), 7, step.data_ptr(), lr.data_ptr(), s)
+        opt.step(lr, step)
+    torch.cuda.synchronize()
+    ref = OA.Tensor(p=p0.copy(), g=None, m=np.zeros(n, np.float32), v=np.zeros(n, np.float32),
+                    wd=OA.f32(0.1))
+    for t in range(1, 8):
+        g.copy_(torch.from_numpy(grads[t - 1]))
+        graph.replay()
+        ref.g = grads[t - 1]
+        OA.step_f32([ref], lr=OA.f32(synth.cosine_lr(t - 1, total=7)), beta1=OA.f32(0.9),
+                    beta2=OA.f32(0.999), eps=OA.f32(1e-8), t=t)
+        torch.cuda.synchronize()
+        assert float(lr.item()) == OA.f32(synth.cosine_lr(t - 1, total=7))
+        assert np.array_equal(p.cpu().numpy().view(np.uint32), ref.p.view(np.uint32)), t
+    assert int(step.item()) == 7
