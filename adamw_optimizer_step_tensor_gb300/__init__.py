@@ -16,7 +16,7 @@ from ._capi import (  # noqa: F401
     adamw_check_nonfinite, adamw_last_error, adamw_lr_from_table, adamw_plan_create,
     adamw_plan_destroy,
     adamw_plan_info, adamw_plan_status, adamw_q8_default_maps, adamw_q8_dequant, adamw_q8_quant,
-    adamw_q8_set_maps, adamw_step, adamw_step_noalloc, adamw_wait_selftest,
+    adamw_q8_set_maps, adamw_step, adamw_step_amp, adamw_step_noalloc, adamw_wait_selftest,
 )
 
 MODES = {"fp32": _capi.MODE_FP32, "bf16_rem": _capi.MODE_BF16_REM, "q8": _capi.MODE_Q8}
@@ -108,6 +108,12 @@ class FusedAdamW:
         """lr: float32 CUDA scalar tensor; step: int32 CUDA scalar (completed steps)."""
         adamw_step(self.plan, _ptr(lr), _ptr(step), float(betas[0]), float(betas[1]), float(eps),
                    _ptr(grad_scale), _ptr(found_inf), _stream(stream))
+
+    def step_amp(self, lr, step, found_inf, *, betas=(0.9, 0.999), eps=1e-8, grad_scale=None,
+                 stream=None) -> None:
+        """Check + step in one launch; found_inf (float32 CUDA scalar) is written, not read."""
+        adamw_step_amp(self.plan, _ptr(lr), _ptr(step), float(betas[0]), float(betas[1]),
+                       float(eps), _ptr(grad_scale), _ptr(found_inf), _stream(stream))
 
     def set_maps(self, signed_map, unsigned_map) -> None:
         adamw_q8_set_maps(self.plan, signed_map, unsigned_map)

@@ -62,6 +62,8 @@ _SIGNATURES = {
                                           ctypes.c_int, _vp, _vp, ctypes.c_float, ctypes.c_float,
                                           ctypes.c_float, _vp, _vp, _vp]),
     "adamw_lr_from_table": (ctypes.c_int, [_vp, ctypes.c_int32, _vp, _vp, _vp]),
+    "adamw_step_amp": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                      _vp, _vp, _vp]),
     "adamw_bf16rem_split": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int64, _vp]),
     "adamw_bf16rem_join": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int64, _vp]),
     "adamw_q8_default_maps": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float),
@@ -165,6 +167,12 @@ def adamw_step_noalloc(tensors: list[adamw_tensor], mode: int, grad_dtype: int, 
     arr = (adamw_tensor * max(1, len(tensors)))(*tensors)
     _check(load().adamw_step_noalloc(arr, len(tensors), mode, grad_dtype, lr_dev, step_dev, beta1,
                                      beta2, eps, grad_scale_dev, found_inf_dev, stream))
+
+
+def adamw_step_amp(plan: int, lr_dev: int, step_dev: int, beta1: float, beta2: float, eps: float,
+                   grad_scale_dev: int | None, found_inf_dev: int, stream: int | None) -> None:
+    _check(load().adamw_step_amp(plan, lr_dev, step_dev, beta1, beta2, eps, grad_scale_dev,
+                                 found_inf_dev, stream))
 
 
 def adamw_lr_from_table(table: int, n: int, step_dev: int, lr_dev: int, stream: int | None) -> None:

@@ -33,6 +33,11 @@ struct adamw_plan {
   QTables* d_qt = nullptr;
   int refine = 1;              // Q8: thresholds per bucket lookup of the current maps
   bool bulk = false;           // launch the bulk-staged step kernel
+  // fused check + step (adamw_step_amp): its own chunk table, sized for its own
+  // co-resident grid (fp32 and bf16+remainder plans only)
+  Chunk* d_chunks_fused = nullptr;
+  int64_t n_chunks_fused = 0;
+  int grid_fused = 0;
 };
 
 namespace {
@@ -66,6 +71,7 @@ void free_plan(adamw_plan* p) {
   if (!p) return;
   cudaFree(p->d_tensors);
   cudaFree(p->d_chunks);
+  cudaFree(p->d_chunks_fused);
   cudaFree(p->d_scratch);
   cudaFree(p->d_qt);
   delete p;
@@ -211,6 +217,28 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
     return cuda_fail(e, "upload chunk table");
   if ((e = cudaMemset(p->d_scratch, 0, sizeof(StepScratch))) != cudaSuccess)
     return cuda_fail(e, "clear step scratch");
+  if (mode != ADAMW_MODE_Q8) {
+    int bpf = 0;
+    if ((e = fused_occupancy(mode, grad_dtype, &bpf)) != cudaSuccess)
+      return cuda_fail(e, "occupancy of the fused step");
+    if (bpf < 1) bpf = 1;
+    const int64_t fchunk = choose_chunk(total, sms, bpf);
+    std::vector<Chunk> fchunks;
+    for (int32_t i = 0; i < n_tensors; ++i)
+      for (int64_t s0 = 0; s0 < td[i].numel; s0 += fchunk) {
+        const int64_t len = td[i].numel - s0 < fchunk ? td[i].numel - s0 : fchunk;
+        fchunks.push_back(Chunk{s0, i, static_cast<int32_t>(len)});
+      }
+    p->n_chunks_fused = static_cast<int64_t>(fchunks.size());
+    const int64_t fres = static_cast<int64_t>(bpf) * sms;
+    p->grid_fused = static_cast<int>(p->n_chunks_fused < 1 ? 1
+                                     : (p->n_chunks_fused < fres ? p->n_chunks_fused : fres));
+    const size_t fb = fchunks.size() * sizeof(Chunk);
+    if (fb && (e = cudaMalloc(&p->d_chunks_fused, fb)) != cudaSuccess)
+      return fail(ADAMW_ENOMEM, "cudaMalloc(fused chunk table): %s", cudaGetErrorString(e));
+    if (fb && (e = cudaMemcpy(p->d_chunks_fused, fchunks.data(), fb, cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e, "upload fused chunk table");
+  }
   if (mode == ADAMW_MODE_Q8) {
     std::unique_ptr<QTables> qt(new QTables);
     float smap[256], umap[256];
@@ -333,6 +361,43 @@ adamw_status adamw_lr_from_table(const float* table, int32_t n, const int32_t* s
     return fail(ADAMW_EALIGN, "pointers must be 4-byte aligned");
   cudaError_t e = launch_lr_from_table(table, n, step_dev, lr_dev, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ADAMW_OK : cuda_fail(e, "launch lr lookup");
+}
+
+adamw_status adamw_step_amp(adamw_plan* plan, const float* lr_dev, int32_t* step_dev, float beta1,
+                            float beta2, float eps, const float* grad_scale_dev, float* found_inf_dev,
+                            void* stream) {
+  if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
+  if (!lr_dev || !step_dev || !found_inf_dev)
+    return fail(ADAMW_EINVAL, "lr_dev, step_dev and found_inf_dev must be set");
+  if (!aligned(lr_dev, 4) || !aligned(step_dev, 4) || !aligned(grad_scale_dev, 4) ||
+      !aligned(found_inf_dev, 4))
+    return fail(ADAMW_EALIGN, "a scalar pointer is not 4-byte aligned");
+  if (!(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f))
+    return fail(ADAMW_EINVAL, "betas must lie in [0, 1)");
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(ADAMW_EINVAL, "eps must be finite and >= 0");
+  if (plan->mode == ADAMW_MODE_Q8)
+    return fail(ADAMW_EUNSUPPORTED, "the fused check + step covers the fp32 and bf16+remainder modes");
+  adamw_status st = check_device(plan);
+  if (st != ADAMW_OK) return st;
+  // every CTA of the cooperative launch is resident at once (grid sized at plan creation)
+  StepArgs a;
+  a.tensors = plan->d_tensors;
+  a.chunks = plan->d_chunks_fused;
+  a.n_chunks = plan->n_chunks_fused;
+  a.lr = lr_dev;
+  a.step = step_dev;
+  a.grad_scale = grad_scale_dev;
+  a.found_inf = nullptr;      // decided inside the launch
+  a.beta1 = beta1;
+  a.beta2 = beta2;
+  a.eps = eps;
+  a.scratch = plan->d_scratch;
+  a.qt = nullptr;
+  a.refine = 1;
+  cudaError_t e = launch_step_fused_amp(plan->mode, plan->gdt, a, plan->grid_fused, found_inf_dev,
+                                        static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cooperative launch of the fused step");
+  return ADAMW_OK;
 }
 
 adamw_status adamw_bf16rem_split(const float* master, uint16_t* bf16, int16_t* rem, int64_t n,

@@ -89,8 +89,14 @@ struct StepScratch {
   float memo_inv_sqrt_bc2;     // fl32(1 / sqrt(1 - b2^t))
   uint32_t fault;              // nonzero: a bounded wait in a kernel gave up (bit per site)
   uint32_t pad;
+  // fused AMP step (grid barrier between the scan and the update); all three
+  // only ever grow, so nothing is reset between launches
+  unsigned long long amp_enter;   // CTAs that entered; / grid = launch index
+  unsigned long long amp_arrive;  // CTAs that published their scan result
+  unsigned long long amp_inf;     // 1 + index of the last launch that saw a non-finite grad
+  unsigned long long pad2;
 };
-static_assert(sizeof(StepScratch) == 32, "StepScratch layout");
+static_assert(sizeof(StepScratch) == 64, "StepScratch layout");
 
 struct StepArgs {
   const TensorDesc* tensors;
@@ -139,6 +145,9 @@ cudaError_t launch_nonfinite(adamw_dtype gdt, const TensorDesc* tensors, const C
                              int64_t n_chunks, float* found_inf, int grid, cudaStream_t s);
 cudaError_t launch_split(const float* master, uint16_t* hi, int16_t* rem, int64_t n,
                          cudaStream_t s);
+cudaError_t fused_occupancy(adamw_mode mode, adamw_dtype gdt, int* blocks_per_sm);
+cudaError_t launch_step_fused_amp(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int grid,
+                                  float* found_inf_out, cudaStream_t s);
 cudaError_t launch_lr_from_table(const float* table, int32_t n, const int32_t* step, float* lr,
                                  cudaStream_t s);
 cudaError_t launch_join(const uint16_t* hi, const int16_t* rem, float* master, int64_t n,

@@ -146,6 +146,132 @@ __global__ void __launch_bounds__(kThreads, Tune<MODE>::min_blocks) step_kernel(
   }
 }
 
+// ---------------------------------------------------------------- fused AMP step
+// Non-finite check and update in one cooperative launch: every CTA scans the
+// grads of the chunks it will update, publishes whether it saw +-inf or NaN,
+// and waits (bounded, 2 s) at a grid barrier; then all CTAs skip or update
+// together.  For plans whose grads stay in L2 between the two passes.
+__device__ __forceinline__ uint64_t fused_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+template <typename GT>
+__device__ __forceinline__ bool nonfinite1(const void* g, int64_t k) {
+  if (sizeof(GT) == 4)
+    return (static_cast<const uint32_t*>(g)[k] & 0x7F800000u) == 0x7F800000u;
+  const uint32_t e = std::is_same<GT, __half>::value ? 0x7C00u : 0x7F80u;
+  return (static_cast<const uint16_t*>(g)[k] & e) == e;
+}
+
+template <typename GT>
+__device__ __forceinline__ bool nonfinite8(const void* g, int64_t e) {
+  float x[8];
+  Grad<GT>::load8(g, e, x);
+  bool bad = false;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) bad |= (__float_as_uint(x[i]) & 0x7F800000u) == 0x7F800000u;
+  return bad;
+}
+
+template <adamw_mode MODE, typename GT>
+__global__ void __launch_bounds__(kThreads, Tune<MODE>::min_blocks)
+step_fused_amp_kernel(const StepArgs a, float* found_inf_out) {
+  constexpr int kUnroll = Tune<MODE>::unroll;
+  __shared__ Scal s_sc;
+  __shared__ int s_skip;
+  StepScratch* const sc = a.scratch;
+
+  // 1. scan this CTA's grads (the same elements it updates below)
+  bool bad = false;
+  for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
+    const Chunk ch = a.chunks[c];
+    const TensorDesc& td = a.tensors[ch.tensor];
+    for (int off = threadIdx.x * kVec; off < ch.len; off += kPass) {
+      if (td.vec_ok && off + kVec <= ch.len) {
+        bad |= nonfinite8<GT>(td.g, ch.start + off);
+      } else {
+        const int n = min(kVec, ch.len - off);
+        for (int i = 0; i < n; ++i) bad |= nonfinite1<GT>(td.g, ch.start + off + i);
+      }
+    }
+  }
+  bad = __syncthreads_or(bad);
+
+  // 2. grid barrier: publish, then wait until every CTA of this launch has
+  if (threadIdx.x == 0) {
+    const unsigned long long g = gridDim.x;
+    const unsigned long long launch = atomicAdd(&sc->amp_enter, 1ull) / g;
+    if (bad) atomicMax(&sc->amp_inf, launch + 1);
+    __threadfence();
+    atomicAdd(&sc->amp_arrive, 1ull);
+    const unsigned long long target = (launch + 1) * g;
+    const uint64_t t0 = fused_ns();
+    int ok = 1;
+    while (atomicAdd(&sc->amp_arrive, 0ull) < target) {
+      __nanosleep(32);
+      if (fused_ns() - t0 > 2000000000ull) {
+        atomicOr(&sc->fault, 8u);
+        ok = 0;
+        break;
+      }
+    }
+    __threadfence();
+    const bool skip = atomicAdd(&sc->amp_inf, 0ull) == launch + 1;
+    if (blockIdx.x == 0 && ok) *found_inf_out = skip ? 1.0f : 0.0f;
+    s_skip = ok ? (skip ? 1 : 0) : 2;
+  }
+  __syncthreads();
+  if (s_skip) return;
+
+  // 3. the step itself (the register-load path of step_kernel)
+  int t = 0;
+  if (threadIdx.x == 0) s_skip = prologue(a, s_sc, t);
+  __syncthreads();
+  const Scal s = s_sc;
+  if (threadIdx.x == 0) take_ticket(a, t);
+  Cursor k{static_cast<int64_t>(blockIdx.x), static_cast<int>(threadIdx.x) * kVec, Chunk{}};
+  bool have = seek(a, k);
+  while (have) {
+    const TensorDesc td = a.tensors[k.ch.tensor];
+    const float decay = __fsub_rn(1.0f, __fmul_rn(s.lr, td.wd));
+    const bool vec = td.vec_ok != 0;
+    Group x[kUnroll];
+    load_trip<MODE, GT, kUnroll>(td, k, vec, x);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int off = k.base + u * kPass;
+      if (vec && off + kVec <= k.ch.len)
+        update_store_group<MODE>(td, k.ch.start + off, x[u], s, decay);
+      else if (off < k.ch.len)
+        update_scalar<MODE, GT>(td, k.ch.start + off, min(kVec, k.ch.len - off), s, decay);
+    }
+    k.base += kPass * kUnroll;
+    if (k.base >= k.ch.len) {
+      k.c += gridDim.x;
+      k.base = threadIdx.x * kVec;
+      have = seek(a, k);
+    }
+  }
+}
+
+template <typename GT>
+cudaError_t launch_fused_mode(adamw_mode mode, const StepArgs& a, int grid, float* out,
+                              cudaStream_t st) {
+  StepArgs args = a;
+  void* params[] = {&args, &out};
+  if (mode == ADAMW_MODE_FP32)
+    return cudaLaunchCooperativeKernel(
+        reinterpret_cast<const void*>(step_fused_amp_kernel<ADAMW_MODE_FP32, GT>), dim3(grid),
+        dim3(kThreads), params, 0, st);
+  if (mode == ADAMW_MODE_BF16_REM)
+    return cudaLaunchCooperativeKernel(
+        reinterpret_cast<const void*>(step_fused_amp_kernel<ADAMW_MODE_BF16_REM, GT>), dim3(grid),
+        dim3(kThreads), params, 0, st);
+  return cudaErrorInvalidValue;
+}
+
 // ---------------------------------------------------------------- 8-bit states
 template <typename GT, int R>
 __global__ void __launch_bounds__(kThreads, Tune<ADAMW_MODE_Q8>::min_blocks)
@@ -301,6 +427,34 @@ cudaError_t occupancy_mode(adamw_mode mode, int* bps, int* smem) {
 }
 
 }  // namespace
+
+template <typename GT>
+cudaError_t fused_occ_mode(adamw_mode mode, int* bps) {
+  if (mode == ADAMW_MODE_FP32)
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+        bps, step_fused_amp_kernel<ADAMW_MODE_FP32, GT>, kThreads, 0);
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+      bps, step_fused_amp_kernel<ADAMW_MODE_BF16_REM, GT>, kThreads, 0);
+}
+
+cudaError_t fused_occupancy(adamw_mode mode, adamw_dtype gdt, int* bps) {
+  switch (gdt) {
+    case ADAMW_F32: return fused_occ_mode<float>(mode, bps);
+    case ADAMW_F16: return fused_occ_mode<__half>(mode, bps);
+    case ADAMW_BF16: return fused_occ_mode<__nv_bfloat16>(mode, bps);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_step_fused_amp(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int grid,
+                                  float* found_inf_out, cudaStream_t s) {
+  switch (gdt) {
+    case ADAMW_F32: return launch_fused_mode<float>(mode, a, grid, found_inf_out, s);
+    case ADAMW_F16: return launch_fused_mode<__half>(mode, a, grid, found_inf_out, s);
+    case ADAMW_BF16: return launch_fused_mode<__nv_bfloat16>(mode, a, grid, found_inf_out, s);
+  }
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_step(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int grid,
                         cudaStream_t s) {

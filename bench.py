@@ -49,7 +49,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gpt2_small",
-                    choices=["gpt2_small", "single", "amp", "q8", "llama3_8b", "bf16rem"])
+                    choices=["gpt2_small", "single", "amp", "amp_fused", "q8", "llama3_8b", "bf16rem"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -245,6 +245,7 @@ CPU_SAMPLES = {
     "gpt2_small": lambda n: cpu_sample_fp32(n),
     "single": lambda n: cpu_sample_fp32(n, lr=0.1),
     "amp": lambda n: cpu_sample_fp32(n, amp=True, lr=0.1),
+    "amp_fused": lambda n: cpu_sample_fp32(n, amp=True, lr=0.1),
     "q8": cpu_sample_q8,
     "llama3_8b": cpu_sample_bf16rem,
     "bf16rem": cpu_sample_bf16rem,
@@ -384,7 +385,7 @@ class Single(Workload):
     bytes_per_param = 28.0
     flush_l2 = True
 
-    def __init__(self, amp=False, seed=1, numel=0):
+    def __init__(self, amp=False, seed=1, numel=0, fused=False):
         import torch
         import synth
         from adamw_optimizer_step_tensor_gb300 import FusedAdamW, _capi
@@ -403,19 +404,26 @@ class Single(Workload):
         self.scale = torch.tensor([65536.0], device=dev)
         self.found = torch.zeros(1, device=dev)
         self.stream = torch.cuda.current_stream().cuda_stream
-        self.launches_per_step = 2 if amp else 1
+        self.fused = fused
+        self.launches_per_step = 2 if amp and not fused else 1
         if amp:
             self.name = "amp_fp16_grads_1M_l2flush"
             self.bytes_per_param = 28.0
             self.inject = synth.amp_injection(10 ** 6, n, seed=3)
-        self.config = {"workload": ("AMP fp16 grads x65536, fused unscale + found_inf skip, 1 tensor"
+        self.config = {"workload": ("AMP fp16 grads x65536, unscale + found_inf skip, 1 tensor, "
+                                    + ("check and step in one cooperative launch" if fused
+                                       else "check and step as two launches")
                                     if amp else "single fp32 tensor"),
                        "tensors": 1, "numel": n, "bytes_per_param": self.bytes_per_param,
                        "l2": f"L2 flushed ({L2_FLUSH_BYTES >> 20} MB write) before every timed launch; "
                              "launch times summed"}
 
     def step(self, i):
-        if self.amp:
+        if self.amp and self.fused:
+            self.C.adamw_step_amp(self.opt.plan, self.lr.data_ptr(), self.step_dev.data_ptr(), 0.9,
+                                  0.999, 1e-8, self.scale.data_ptr(), self.found.data_ptr(),
+                                  self.stream)
+        elif self.amp:
             self.C.adamw_check_nonfinite(self.opt.plan, self.found.data_ptr(), self.stream)
             self.C.adamw_step(self.opt.plan, self.lr.data_ptr(), self.step_dev.data_ptr(), 0.9, 0.999,
                               1e-8, self.scale.data_ptr(), self.found.data_ptr(), self.stream)
@@ -564,6 +572,7 @@ class Bf16Rem(Workload):
 def make_workload(name, numel=0):
     return {"gpt2_small": lambda: Gpt2Small(), "single": lambda: Single(numel=numel),
             "amp": lambda: Single(amp=True, numel=numel), "q8": lambda: Q8(numel=numel),
+            "amp_fused": lambda: Single(amp=True, numel=numel, fused=True),
             "llama3_8b": lambda: Llama3(), "bf16rem": lambda: Bf16Rem(numel=numel)}[name]()
 
 

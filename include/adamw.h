@@ -207,6 +207,22 @@ adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t n_tensors,
                                 void* stream);
 
 /*
+ * The AMP step in one launch ("FusedAdam & PyTorch Lightning AMP": the fused
+ * step does the unscale and decides the skip itself): every CTA first scans
+ * the raw grads of the elements it owns for +-inf / NaN, the CTAs meet at a
+ * grid barrier (a cooperative launch, so all are resident; the wait is bounded
+ * at 2 s and reported through adamw_plan_status), and then either all skip --
+ * params, states and *step_dev untouched -- or all update, exactly as
+ * adamw_check_nonfinite + adamw_step would.  *found_inf_dev (output) receives
+ * 1.0f or 0.0f for the caller's loss-scale logic.  Meant for plans whose grads
+ * stay in L2 between the scan and the update (the scan then costs one read of
+ * the grads); other arguments as adamw_step.  fp32 and bf16+remainder modes.
+ */
+adamw_status adamw_step_amp(adamw_plan* plan, const float* lr_dev, int32_t* step_dev,
+                            float beta1, float beta2, float eps,
+                            const float* grad_scale_dev, float* found_inf_dev, void* stream);
+
+/*
  * On-device learning-rate schedule: *lr_dev = table[clamp(*step_dev, 0, n-1)],
  * one single-thread launch on `stream`.  Issued before adamw_step on the same
  * stream with the step's own counter, it feeds the step the schedule entry of
