@@ -12,7 +12,7 @@ from __future__ import annotations
 
 from . import _capi
 from ._capi import (  # noqa: F401
-    AdamWError, adamw_abi_version, adamw_bf16rem_join, adamw_bf16rem_split,
+    AdamWError, adamw_abi_version, adamw_ademamix_step, adamw_bf16rem_join, adamw_bf16rem_split,
     adamw_check_nonfinite, adamw_last_error, adamw_lr_from_table, adamw_plan_create,
     adamw_plan_destroy,
     adamw_plan_info, adamw_plan_status, adamw_q8_default_maps, adamw_q8_dequant, adamw_q8_quant,
@@ -53,7 +53,7 @@ class FusedAdamW:
     """
 
     def __init__(self, params, grads, exp_avgs, exp_avg_sqs, weight_decays, *, mode="fp32",
-                 param_rems=None, absmax_m=None, absmax_v=None):
+                 param_rems=None, absmax_m=None, absmax_v=None, exp_avg_slows=None):
         import torch
         if mode not in MODES:
             raise ValueError(f"mode must be one of {sorted(MODES)}")
@@ -65,6 +65,7 @@ class FusedAdamW:
         rems = param_rems if param_rems is not None else [None] * n
         ams = absmax_m if absmax_m is not None else [None] * n
         avs = absmax_v if absmax_v is not None else [None] * n
+        slows = exp_avg_slows if exp_avg_slows is not None else [None] * n
         pdt = torch.bfloat16 if mode == "bf16_rem" else torch.float32
         sdt = torch.uint8 if mode == "q8" else torch.float32
         gdt = grads[0].dtype if n else torch.float32
@@ -87,10 +88,14 @@ class FusedAdamW:
                 for name, a in (("absmax_m", ams[i]), ("absmax_v", avs[i])):
                     if a is None or a.dtype != torch.float32 or a.numel() < nb:
                         raise TypeError(f"tensor {i}: q8 mode needs {name} float32 [{nb}]")
+            if slows[i] is not None and (slows[i].dtype != torch.float32
+                                         or slows[i].numel() != p.numel()):
+                raise TypeError(f"tensor {i}: exp_avg_slow must be float32 with one entry per element")
             recs.append(_capi.adamw_tensor(
                 _ptr(p), _ptr(rems[i]), _ptr(g), _ptr(m), _ptr(v), _ptr(ams[i]), _ptr(avs[i]),
-                int(p.numel()), float(weight_decays[i])))
-        self._keep = (list(params), list(grads), list(exp_avgs), list(exp_avg_sqs), rems, ams, avs)
+                int(p.numel()), float(weight_decays[i]), _ptr(slows[i])))
+        self._keep = (list(params), list(grads), list(exp_avgs), list(exp_avg_sqs), rems, ams, avs,
+                      slows)
         self.plan = adamw_plan_create(recs, MODES[mode], _grad_dtype(gdt))
 
     def info(self) -> dict:
@@ -108,6 +113,13 @@ class FusedAdamW:
         """lr: float32 CUDA scalar tensor; step: int32 CUDA scalar (completed steps)."""
         adamw_step(self.plan, _ptr(lr), _ptr(step), float(betas[0]), float(betas[1]), float(eps),
                    _ptr(grad_scale), _ptr(found_inf), _stream(stream))
+
+    def step_ademamix(self, lr, step, *, betas=(0.9, 0.999, 0.9999), alpha=5.0, eps=1e-8,
+                      grad_scale=None, found_inf=None, stream=None) -> None:
+        """AdEMAMix step (the plan needs exp_avg_slows); betas = (b1, b2, b3)."""
+        adamw_ademamix_step(self.plan, _ptr(lr), _ptr(step), float(betas[0]), float(betas[1]),
+                            float(betas[2]), float(alpha), float(eps), _ptr(grad_scale),
+                            _ptr(found_inf), _stream(stream))
 
     def step_amp(self, lr, step, found_inf, *, betas=(0.9, 0.999), eps=1e-8, grad_scale=None,
                  stream=None) -> None:

@@ -42,6 +42,7 @@ class adamw_tensor(ctypes.Structure):
         ("absmax_v", _vp),
         ("numel", ctypes.c_int64),
         ("weight_decay", ctypes.c_float),
+        ("exp_avg_slow", _vp),
     ]
 
 
@@ -62,6 +63,9 @@ _SIGNATURES = {
                                           ctypes.c_int, _vp, _vp, ctypes.c_float, ctypes.c_float,
                                           ctypes.c_float, _vp, _vp, _vp]),
     "adamw_lr_from_table": (ctypes.c_int, [_vp, ctypes.c_int32, _vp, _vp, _vp]),
+    "adamw_ademamix_step": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_float, ctypes.c_float,
+                                           ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                           _vp, _vp, _vp]),
     "adamw_step_amp": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                       _vp, _vp, _vp]),
     "adamw_bf16rem_split": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int64, _vp]),
@@ -167,6 +171,13 @@ def adamw_step_noalloc(tensors: list[adamw_tensor], mode: int, grad_dtype: int, 
     arr = (adamw_tensor * max(1, len(tensors)))(*tensors)
     _check(load().adamw_step_noalloc(arr, len(tensors), mode, grad_dtype, lr_dev, step_dev, beta1,
                                      beta2, eps, grad_scale_dev, found_inf_dev, stream))
+
+
+def adamw_ademamix_step(plan: int, lr_dev: int, step_dev: int, beta1: float, beta2: float,
+                        beta3: float, alpha: float, eps: float, grad_scale_dev: int | None,
+                        found_inf_dev: int | None, stream: int | None) -> None:
+    _check(load().adamw_ademamix_step(plan, lr_dev, step_dev, beta1, beta2, beta3, alpha, eps,
+                                      grad_scale_dev, found_inf_dev, stream))
 
 
 def adamw_step_amp(plan: int, lr_dev: int, step_dev: int, beta1: float, beta2: float, eps: float,

@@ -1,4 +1,5 @@
-// bulk_kernels.cu -- the fp32 and bf16+remainder step with bulk-async staging.
+// bulk_kernels.cu -- the fp32 and bf16+remainder steps (AdamW, AdEMAMix) with
+// bulk-async staging.
 //
 // One CTA per SM: a producer warp streams each 2048-element tile of every
 // input (p [+ remainder], g, m, v) into a ring of shared-memory stages with
@@ -73,8 +74,9 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
-// Byte layout of one stage: p, rem (bf16 mode), g, m, v -- each kTile elements.
-template <adamw_mode MODE, typename GT>
+// Byte layout of one stage: p, rem (bf16 mode), g, m, v, m2 (AdEMAMix) --
+// each kTile elements.
+template <adamw_mode MODE, typename GT, bool ADX>
 struct Stage {
   static constexpr int kP = MODE == ADAMW_MODE_FP32 ? 4 : 2;
   static constexpr int kG = sizeof(GT);
@@ -83,7 +85,10 @@ struct Stage {
   static constexpr int oG = oR + (MODE == ADAMW_MODE_BF16_REM ? kTile * 2 : 0);
   static constexpr int oM = oG + kTile * kG;
   static constexpr int oV = oM + kTile * 4;
-  static constexpr int kBytes = oV + kTile * 4;
+  static constexpr int oM2 = oV + kTile * 4;
+  static constexpr int kBytes = oM2 + (ADX ? kTile * 4 : 0);
+  // bytes moved per element in bulk
+  static constexpr int kPerElem = kP + (MODE == ADAMW_MODE_BF16_REM ? 2 : 0) + kG + 8 + (ADX ? 4 : 0);
   static_assert(kBytes % 128 == 0, "stages stay 128-byte aligned");
 };
 
@@ -92,9 +97,9 @@ struct Stage {
 // stages 97%, 24-30 warps 96-97%.
 template <int MODE> struct BulkTune { static constexpr int stages = 3; };
 
-template <adamw_mode MODE, typename GT>
+template <adamw_mode MODE, typename GT, bool ADX>
 constexpr int bulk_smem_bytes() {
-  return BulkTune<MODE>::stages * Stage<MODE, GT>::kBytes + 2 * BulkTune<MODE>::stages * 8;
+  return BulkTune<MODE>::stages * Stage<MODE, GT, ADX>::kBytes + 2 * BulkTune<MODE>::stages * 8;
 }
 
 __device__ __forceinline__ void fault(const StepArgs& a, uint32_t code) {
@@ -102,9 +107,9 @@ __device__ __forceinline__ void fault(const StepArgs& a, uint32_t code) {
 }
 
 // The producer: one thread issues the bulk copies of every tile of this CTA.
-template <adamw_mode MODE, typename GT>
+template <adamw_mode MODE, typename GT, bool ADX>
 __device__ void produce(const StepArgs& a, unsigned char* ring, uint64_t* full, uint64_t* empty) {
-  using L = Stage<MODE, GT>;
+  using L = Stage<MODE, GT, ADX>;
   constexpr int S = BulkTune<MODE>::stages;
   uint32_t i = 0;
   bool ok = true;
@@ -122,7 +127,7 @@ __device__ void produce(const StepArgs& a, unsigned char* ring, uint64_t* full, 
       const int nb = td.vec_ok ? (len & ~(kVec - 1)) : 0;  // elements moved in bulk
       const int64_t e = ch.start + static_cast<int64_t>(k) * kTile;
       unsigned char* st = ring + static_cast<size_t>(s) * L::kBytes;
-      const uint32_t bytes = nb * (L::kP + L::kG + 8 + (MODE == ADAMW_MODE_BF16_REM ? 2 : 0));
+      const uint32_t bytes = nb * L::kPerElem;
       mbar_expect_tx(&full[s], bytes);
       if (nb > 0) {
         bulk_g2s(st + L::oP, static_cast<const unsigned char*>(td.p) + e * L::kP, nb * L::kP, &full[s]);
@@ -131,6 +136,7 @@ __device__ void produce(const StepArgs& a, unsigned char* ring, uint64_t* full, 
         bulk_g2s(st + L::oG, static_cast<const unsigned char*>(td.g) + e * L::kG, nb * L::kG, &full[s]);
         bulk_g2s(st + L::oM, static_cast<const float*>(td.m) + e, nb * 4, &full[s]);
         bulk_g2s(st + L::oV, static_cast<const float*>(td.v) + e, nb * 4, &full[s]);
+        if (ADX) bulk_g2s(st + L::oM2, static_cast<const float*>(td.m2) + e, nb * 4, &full[s]);
       }
     }
   }
@@ -153,10 +159,10 @@ __device__ __forceinline__ float grad_from_smem(const unsigned char* base, int i
 }
 
 // Four consecutive elements [j, j+4) of a tile from shared memory.
-template <adamw_mode MODE, typename GT>
+template <adamw_mode MODE, typename GT, bool ADX>
 __device__ __forceinline__ void load4_smem(const unsigned char* st, int j, float (&p)[4],
                                            float (&g)[4], float (&m)[4], float (&v)[4]) {
-  using L = Stage<MODE, GT>;
+  using L = Stage<MODE, GT, ADX>;
   if (MODE == ADAMW_MODE_FP32) {
     const float4 x = *reinterpret_cast<const float4*>(st + L::oP + j * 4);
     p[0] = x.x; p[1] = x.y; p[2] = x.z; p[3] = x.w;
@@ -195,9 +201,9 @@ __device__ __forceinline__ void store4(const TensorDesc& td, int64_t e, const fl
   __stcs(reinterpret_cast<float4*>(static_cast<float*>(td.v) + e), make_float4(v[0], v[1], v[2], v[3]));
 }
 
-template <adamw_mode MODE, typename GT>
+template <adamw_mode MODE, typename GT, bool ADX>
 __global__ void __launch_bounds__(kBulkThreads, 1) step_bulk_kernel(const StepArgs a) {
-  using L = Stage<MODE, GT>;
+  using L = Stage<MODE, GT, ADX>;
   constexpr int S = BulkTune<MODE>::stages;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* ring = smem_raw;
@@ -221,7 +227,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) step_bulk_kernel(const StepAr
     // no copy is issued for a skipped step
     if (threadIdx.x == kConsumers) {
       const bool skip = a.found_inf != nullptr && *a.found_inf != 0.0f;
-      if (!skip) produce<MODE, GT>(a, ring, full, empty);
+      if (!skip) produce<MODE, GT, ADX>(a, ring, full, empty);
     }
     return;
   }
@@ -254,12 +260,21 @@ __global__ void __launch_bounds__(kBulkThreads, 1) step_bulk_kernel(const StepAr
         const int j = threadIdx.x * 4;
         if (j + 4 <= nb) {
           float p[4], g[4], m[4], v[4];
-          load4_smem<MODE, GT>(st, j, p, g, m, v);
+          load4_smem<MODE, GT, ADX>(st, j, p, g, m, v);
+          if (ADX) {
+            const float4 w = *reinterpret_cast<const float4*>(st + L::oM2 + j * 4);
+            float m2[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-          for (int q = 0; q < 4; ++q) update(p[q], g[q], m[q], v[q], s, decay);
+            for (int q = 0; q < 4; ++q) update_ademamix(p[q], g[q], m[q], m2[q], v[q], s, decay);
+            __stcs(reinterpret_cast<float4*>(static_cast<float*>(td.m2) + e0 + j),
+                   make_float4(m2[0], m2[1], m2[2], m2[3]));
+          } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) update(p[q], g[q], m[q], v[q], s, decay);
+          }
           store4<MODE>(td, e0 + j, p, m, v);
         } else if (j < len) {
-          update_scalar<MODE, GT>(td, e0 + j, min(4, len - j), s, decay);
+          update_scalar<MODE, GT, ADX>(td, e0 + j, min(4, len - j), s, decay);
         }
       }
       __syncwarp();
@@ -268,27 +283,35 @@ __global__ void __launch_bounds__(kBulkThreads, 1) step_bulk_kernel(const StepAr
   }
 }
 
-template <typename GT>
-cudaError_t launch_bulk_mode(adamw_mode mode, const StepArgs& a, int grid, cudaStream_t st) {
-  if (mode == ADAMW_MODE_FP32) {
-    step_bulk_kernel<ADAMW_MODE_FP32, GT>
-        <<<grid, kBulkThreads, bulk_smem_bytes<ADAMW_MODE_FP32, GT>(), st>>>(a);
-  } else {
-    step_bulk_kernel<ADAMW_MODE_BF16_REM, GT>
-        <<<grid, kBulkThreads, bulk_smem_bytes<ADAMW_MODE_BF16_REM, GT>(), st>>>(a);
-  }
+template <adamw_mode MODE, typename GT, bool ADX>
+cudaError_t launch_one(const StepArgs& a, int grid, cudaStream_t st) {
+  step_bulk_kernel<MODE, GT, ADX><<<grid, kBulkThreads, bulk_smem_bytes<MODE, GT, ADX>(), st>>>(a);
   return cudaGetLastError();
 }
 
-template <typename GT>
-cudaError_t prepare_bulk_mode(adamw_mode mode) {
-  if (mode == ADAMW_MODE_FP32)
-    return cudaFuncSetAttribute(step_bulk_kernel<ADAMW_MODE_FP32, GT>,
-                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                bulk_smem_bytes<ADAMW_MODE_FP32, GT>());
-  return cudaFuncSetAttribute(step_bulk_kernel<ADAMW_MODE_BF16_REM, GT>,
+template <adamw_mode MODE, typename GT, bool ADX>
+cudaError_t prepare_one() {
+  return cudaFuncSetAttribute(step_bulk_kernel<MODE, GT, ADX>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              bulk_smem_bytes<ADAMW_MODE_BF16_REM, GT>());
+                              bulk_smem_bytes<MODE, GT, ADX>());
+}
+
+template <typename GT>
+cudaError_t launch_bulk_mode(adamw_mode mode, const StepArgs& a, int grid, cudaStream_t st,
+                             bool adx) {
+  if (mode == ADAMW_MODE_FP32)
+    return adx ? launch_one<ADAMW_MODE_FP32, GT, true>(a, grid, st)
+               : launch_one<ADAMW_MODE_FP32, GT, false>(a, grid, st);
+  return adx ? launch_one<ADAMW_MODE_BF16_REM, GT, true>(a, grid, st)
+             : launch_one<ADAMW_MODE_BF16_REM, GT, false>(a, grid, st);
+}
+
+template <typename GT>
+cudaError_t prepare_bulk_mode(adamw_mode mode, bool adx) {
+  if (mode == ADAMW_MODE_FP32)
+    return adx ? prepare_one<ADAMW_MODE_FP32, GT, true>() : prepare_one<ADAMW_MODE_FP32, GT, false>();
+  return adx ? prepare_one<ADAMW_MODE_BF16_REM, GT, true>()
+             : prepare_one<ADAMW_MODE_BF16_REM, GT, false>();
 }
 
 // Self-test of the bounded wait: one thread waits on an mbarrier phase that
@@ -324,20 +347,20 @@ cudaError_t run_wait_selftest(int limit_us, cudaStream_t s, uint32_t* fault_bits
 }
 
 cudaError_t launch_step_bulk(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int grid,
-                             cudaStream_t s) {
+                             cudaStream_t s, bool ademamix) {
   switch (gdt) {
-    case ADAMW_F32: return launch_bulk_mode<float>(mode, a, grid, s);
-    case ADAMW_F16: return launch_bulk_mode<__half>(mode, a, grid, s);
-    case ADAMW_BF16: return launch_bulk_mode<__nv_bfloat16>(mode, a, grid, s);
+    case ADAMW_F32: return launch_bulk_mode<float>(mode, a, grid, s, ademamix);
+    case ADAMW_F16: return launch_bulk_mode<__half>(mode, a, grid, s, ademamix);
+    case ADAMW_BF16: return launch_bulk_mode<__nv_bfloat16>(mode, a, grid, s, ademamix);
   }
   return cudaErrorInvalidValue;
 }
 
-cudaError_t prepare_step_bulk(adamw_mode mode, adamw_dtype gdt) {
+cudaError_t prepare_step_bulk(adamw_mode mode, adamw_dtype gdt, bool ademamix) {
   switch (gdt) {
-    case ADAMW_F32: return prepare_bulk_mode<float>(mode);
-    case ADAMW_F16: return prepare_bulk_mode<__half>(mode);
-    case ADAMW_BF16: return prepare_bulk_mode<__nv_bfloat16>(mode);
+    case ADAMW_F32: return prepare_bulk_mode<float>(mode, ademamix);
+    case ADAMW_F16: return prepare_bulk_mode<__half>(mode, ademamix);
+    case ADAMW_BF16: return prepare_bulk_mode<__nv_bfloat16>(mode, ademamix);
   }
   return cudaErrorInvalidValue;
 }

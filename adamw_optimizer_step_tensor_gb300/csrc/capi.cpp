@@ -38,6 +38,7 @@ struct adamw_plan {
   Chunk* d_chunks_fused = nullptr;
   int64_t n_chunks_fused = 0;
   int grid_fused = 0;
+  bool has_slow = false;       // every tensor carries an AdEMAMix slow EMA
 };
 
 namespace {
@@ -134,6 +135,7 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
   std::vector<TensorDesc> td(static_cast<size_t>(n_tensors));
   std::vector<Chunk> chunks;
   int64_t total = 0;
+  int with_slow = 0, sized = 0;
   for (int32_t i = 0; i < n_tensors; ++i) {
     const adamw_tensor& t = tensors[i];
     if (t.numel < 0) return fail(ADAMW_EINVAL, "tensor %d: numel < 0", i);
@@ -147,9 +149,16 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
     d.v = t.exp_avg_sq;
     d.am = t.absmax_m;
     d.av = t.absmax_v;
+    d.m2 = t.exp_avg_slow;
     d.numel = t.numel;
     d.wd = t.weight_decay;
     if (t.numel == 0) continue;
+    ++sized;
+    if (t.exp_avg_slow) {
+      ++with_slow;
+      if (!aligned(t.exp_avg_slow, 4))
+        return fail(ADAMW_EALIGN, "tensor %d: exp_avg_slow is not 4-byte aligned", i);
+    }
     if (!t.param || !t.grad || !t.exp_avg || !t.exp_avg_sq)
       return fail(ADAMW_EINVAL, "tensor %d: param, grad, exp_avg and exp_avg_sq must be set", i);
     if ((mode == ADAMW_MODE_BF16_REM) != (t.param_rem != nullptr))
@@ -162,9 +171,15 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
         (t.absmax_m && !aligned(t.absmax_m, 4)) || (t.absmax_v && !aligned(t.absmax_v, 4)))
       return fail(ADAMW_EALIGN, "tensor %d: a pointer is not aligned to its element size", i);
     d.vec_ok = aligned(t.param, 16) && aligned(t.grad, 16) && aligned(t.exp_avg, svec) &&
-               aligned(t.exp_avg_sq, svec) && (!t.param_rem || aligned(t.param_rem, 16));
+               aligned(t.exp_avg_sq, svec) && (!t.param_rem || aligned(t.param_rem, 16)) &&
+               (!t.exp_avg_slow || aligned(t.exp_avg_slow, 16));
     total += t.numel;
   }
+  if (with_slow != 0 && with_slow != sized)
+    return fail(ADAMW_EINVAL, "exp_avg_slow must be set on every tensor or on none");
+  if (with_slow && mode == ADAMW_MODE_Q8)
+    return fail(ADAMW_EUNSUPPORTED, "AdEMAMix slow states are supported in the fp32 and "
+                                    "bf16+remainder modes");
 
   // Every argument is valid; only now touch the device.
   int device = -1, sms = 0;
@@ -175,7 +190,8 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
   int bps = 0, smem = 0;
   const bool bulk = kUseBulk && mode != ADAMW_MODE_Q8;
   if (bulk) {
-    e = prepare_step_bulk(mode, grad_dtype);
+    e = prepare_step_bulk(mode, grad_dtype, false);
+    if (e == cudaSuccess && with_slow) e = prepare_step_bulk(mode, grad_dtype, true);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bulk step)");
     bps = 1;
   } else {
@@ -199,6 +215,7 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
 
   p->device = device;
   p->bulk = bulk;
+  p->has_slow = with_slow != 0;
   const int64_t resident = static_cast<int64_t>(bps) * sms;
   p->grid = static_cast<int>(p->n_chunks < resident ? (p->n_chunks > 0 ? p->n_chunks : 1) : resident);
   const int64_t check_res = 8LL * sms;
@@ -342,6 +359,8 @@ adamw_status adamw_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev
   a.beta1 = beta1;
   a.beta2 = beta2;
   a.eps = eps;
+  a.beta3 = 0.0f;
+  a.alpha = 0.0f;
   a.scratch = plan->d_scratch;
   a.qt = plan->d_qt;
   a.refine = plan->refine;
@@ -361,6 +380,46 @@ adamw_status adamw_lr_from_table(const float* table, int32_t n, const int32_t* s
     return fail(ADAMW_EALIGN, "pointers must be 4-byte aligned");
   cudaError_t e = launch_lr_from_table(table, n, step_dev, lr_dev, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ADAMW_OK : cuda_fail(e, "launch lr lookup");
+}
+
+adamw_status adamw_ademamix_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev,
+                                 float beta1, float beta2, float beta3, float alpha, float eps,
+                                 const float* grad_scale_dev, const float* found_inf_dev,
+                                 void* stream) {
+  if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
+  if (!plan->has_slow)
+    return fail(ADAMW_EINVAL, "the plan's tensors carry no exp_avg_slow (AdEMAMix slow EMA)");
+  if (!lr_dev || !step_dev) return fail(ADAMW_EINVAL, "lr_dev and step_dev must be set");
+  if (!aligned(lr_dev, 4) || !aligned(step_dev, 4) || !aligned(grad_scale_dev, 4) ||
+      !aligned(found_inf_dev, 4))
+    return fail(ADAMW_EALIGN, "a scalar pointer is not 4-byte aligned");
+  if (!(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f) ||
+      !(beta3 >= 0.0f && beta3 < 1.0f))
+    return fail(ADAMW_EINVAL, "betas must lie in [0, 1)");
+  if (!std::isfinite(alpha)) return fail(ADAMW_EINVAL, "alpha must be finite");
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(ADAMW_EINVAL, "eps must be finite and >= 0");
+  adamw_status st = check_device(plan);
+  if (st != ADAMW_OK) return st;
+  StepArgs a;
+  a.tensors = plan->d_tensors;
+  a.chunks = plan->d_chunks;
+  a.n_chunks = plan->n_chunks;
+  a.lr = lr_dev;
+  a.step = step_dev;
+  a.grad_scale = grad_scale_dev;
+  a.found_inf = found_inf_dev;
+  a.beta1 = beta1;
+  a.beta2 = beta2;
+  a.eps = eps;
+  a.beta3 = beta3;
+  a.alpha = alpha;
+  a.scratch = plan->d_scratch;
+  a.qt = nullptr;
+  a.refine = 1;
+  cudaError_t e = launch_step_bulk(plan->mode, plan->gdt, a, plan->grid,
+                                   static_cast<cudaStream_t>(stream), true);
+  if (e != cudaSuccess) return cuda_fail(e, "launch AdEMAMix step");
+  return ADAMW_OK;
 }
 
 adamw_status adamw_step_amp(adamw_plan* plan, const float* lr_dev, int32_t* step_dev, float beta1,
@@ -391,6 +450,8 @@ adamw_status adamw_step_amp(adamw_plan* plan, const float* lr_dev, int32_t* step
   a.beta1 = beta1;
   a.beta2 = beta2;
   a.eps = eps;
+  a.beta3 = 0.0f;
+  a.alpha = 0.0f;
   a.scratch = plan->d_scratch;
   a.qt = nullptr;
   a.refine = 1;

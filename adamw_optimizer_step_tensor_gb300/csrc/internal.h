@@ -55,6 +55,7 @@ struct TensorDesc {
   void* v;            // fp32 or uint8 codes
   float* am;          // Q8 absmax of m per 256 block
   float* av;          // Q8 absmax of v per 256 block
+  void* m2;           // AdEMAMix slow EMA (fp32), or null
   int64_t numel;
   float wd;
   int32_t vec_ok;     // all pointers 16-byte aligned
@@ -107,6 +108,7 @@ struct StepArgs {
   const float* grad_scale;    // may be null
   const float* found_inf;     // may be null
   float beta1, beta2, eps;
+  float beta3, alpha;         // AdEMAMix only
   StepScratch* scratch;       // plan-owned; ticket zero between launches
   const QTables* qt;          // Q8 only
   int refine;                 // Q8 only: thresholds per lookup (1, 2 or 4)
@@ -137,8 +139,8 @@ cudaError_t launch_step(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int
 cudaError_t step_occupancy(adamw_mode mode, adamw_dtype gdt, int* blocks_per_sm,
                            int* smem_bytes);
 cudaError_t launch_step_bulk(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int grid,
-                             cudaStream_t s);
-cudaError_t prepare_step_bulk(adamw_mode mode, adamw_dtype gdt);
+                             cudaStream_t s, bool ademamix = false);
+cudaError_t prepare_step_bulk(adamw_mode mode, adamw_dtype gdt, bool ademamix = false);
 cudaError_t run_wait_selftest(int limit_us, cudaStream_t s, uint32_t* fault_bits,
                               double* waited_ms);
 cudaError_t launch_nonfinite(adamw_dtype gdt, const TensorDesc* tensors, const Chunk* chunks,

@@ -99,6 +99,8 @@ extern "C" adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t 
     if (!t.param || !t.grad || !t.exp_avg || !t.exp_avg_sq || t.absmax_m || t.absmax_v ||
         (mode == ADAMW_MODE_BF16_REM) != (t.param_rem != nullptr))
       return fail(ADAMW_EINVAL, "a tensor's pointers do not match the mode");
+    if (t.exp_avg_slow)
+      return fail(ADAMW_EUNSUPPORTED, "AdEMAMix slow states need a plan (adamw_ademamix_step)");
     if (!aligned(t.param, psz) || !aligned(t.grad, gsz) || !aligned(t.exp_avg, 4) ||
         !aligned(t.exp_avg_sq, 4) || (t.param_rem && !aligned(t.param_rem, 2)))
       return fail(ADAMW_EALIGN, "a pointer is not aligned to its element size");
@@ -141,6 +143,7 @@ extern "C" adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t 
     d.v = t.exp_avg_sq;
     d.am = nullptr;
     d.av = nullptr;
+    d.m2 = nullptr;
     d.numel = t.numel;
     d.wd = t.weight_decay;
     d.vec_ok = aligned(t.param, 16) && aligned(t.grad, 16) && aligned(t.exp_avg, 16) &&
@@ -182,6 +185,8 @@ extern "C" adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t 
   a.beta1 = beta1;
   a.beta2 = beta2;
   a.eps = eps;
+  a.beta3 = 0.0f;
+  a.alpha = 0.0f;
   a.scratch = d_step;
   a.qt = nullptr;
   a.refine = 1;

@@ -15,6 +15,7 @@ namespace {
 
 struct Scal {
   float b1, b2, omb1, omb2, eps, lr, step_size, inv_sqrt_bc2, inv_scale;
+  float b3, omb3, alpha, rbc1;   // AdEMAMix: slow-EMA beta, 1 - b3, mix weight, fl(1/bc1)
   int scaled;
 };
 
@@ -66,6 +67,10 @@ __device__ bool prologue(const StepArgs& a, Scal& s, int& t_out) {
   s.lr = lr;
   s.inv_sqrt_bc2 = bc.inv_sqrt_bc2;
   s.step_size = __fdiv_rn(lr, bc.bc1);
+  s.b3 = a.beta3;
+  s.omb3 = __fsub_rn(1.0f, a.beta3);
+  s.alpha = a.alpha;
+  s.rbc1 = __fdiv_rn(1.0f, bc.bc1);
   s.scaled = a.grad_scale != nullptr;
   s.inv_scale = s.scaled ? __fdiv_rn(1.0f, gscale) : 1.0f;
   t_out = t;
@@ -100,6 +105,19 @@ __device__ __forceinline__ void update(float& p, float g, float& m, float& v, co
   const float h = __fadd_rn(__fmul_rn(__fsqrt_rn(v), s.inv_sqrt_bc2), s.eps);
   const float u = __fdiv_rn(m, h);
   p = __fsub_rn(__fmul_rn(p, decay), __fmul_rn(s.step_size, u));
+}
+
+// The AdEMAMix element update (strict float32, order as in adamw.h).
+__device__ __forceinline__ void update_ademamix(float& p, float g, float& m1, float& m2, float& v,
+                                                const Scal& s, float decay) {
+  if (s.scaled) g = __fmul_rn(g, s.inv_scale);
+  m1 = __fadd_rn(__fmul_rn(s.b1, m1), __fmul_rn(s.omb1, g));
+  m2 = __fadd_rn(__fmul_rn(s.b3, m2), __fmul_rn(s.omb3, g));
+  v = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, __fmul_rn(g, g)));
+  const float h = __fadd_rn(__fmul_rn(__fsqrt_rn(v), s.inv_sqrt_bc2), s.eps);
+  const float n = __fadd_rn(__fmul_rn(m1, s.rbc1), __fmul_rn(s.alpha, m2));
+  const float u = __fdiv_rn(n, h);
+  p = __fsub_rn(__fmul_rn(p, decay), __fmul_rn(s.lr, u));
 }
 
 // ---------------------------------------------------------------- loads/stores
@@ -178,7 +196,7 @@ __device__ __forceinline__ void rem_split(float x, uint32_t& hi, uint32_t& rem16
 
 // Elements [e, e + n) one at a time: ragged tails and tensors whose pointers
 // are not all 16-byte aligned.
-template <adamw_mode MODE, typename GT>
+template <adamw_mode MODE, typename GT, bool ADX = false>
 __device__ void update_scalar(const TensorDesc& td, int64_t e, int n, const Scal& s,
                               float decay) {
   float* const pf = static_cast<float*>(td.p);
@@ -189,7 +207,14 @@ __device__ void update_scalar(const TensorDesc& td, int64_t e, int n, const Scal
     const int64_t k = e + i;
     float p = MODE == ADAMW_MODE_FP32 ? pf[k] : rem_join(ph[k], static_cast<uint16_t>(td.rem[k]));
     float m = mf[k], v = vf[k];
-    update(p, Grad<GT>::load1(td.g, k), m, v, s, decay);
+    if (ADX) {
+      float* const m2f = static_cast<float*>(td.m2);
+      float m2 = m2f[k];
+      update_ademamix(p, Grad<GT>::load1(td.g, k), m, m2, v, s, decay);
+      m2f[k] = m2;
+    } else {
+      update(p, Grad<GT>::load1(td.g, k), m, v, s, decay);
+    }
     if (MODE == ADAMW_MODE_FP32) {
       pf[k] = p;
     } else {

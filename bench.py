@@ -49,7 +49,8 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gpt2_small",
-                    choices=["gpt2_small", "single", "amp", "amp_fused", "q8", "llama3_8b", "bf16rem"])
+                    choices=["gpt2_small", "single", "amp", "amp_fused", "q8", "llama3_8b", "bf16rem",
+                             "ademamix_gpt2"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -241,6 +242,21 @@ def cpu_sample_bf16rem(n):
     return run, f"{n} elements per step, strict-fp32 oracle with remainder join/split"
 
 
+def cpu_sample_ademamix(n):
+    import numpy as np
+    from oracle import ademamix as OX
+    rng = np.random.default_rng(0)
+    x = OX.Tensor(p=rng.normal(0, 0.02, n), g=rng.normal(0, 1e-3, n), m1=np.zeros(n), m2=np.zeros(n),
+                  v=np.zeros(n), wd=0.1)
+    state = {"t": 0}
+
+    def run():
+        state["t"] += 1
+        OX.step_fp64([x], lr=1e-3, beta1=0.9, beta2=0.999, beta3=0.9999, alpha=5.0, eps=1e-8,
+                     t=state["t"])
+    return run, f"{n} elements per step, float64 AdEMAMix oracle (oracle.ademamix.step_fp64)"
+
+
 CPU_SAMPLES = {
     "gpt2_small": lambda n: cpu_sample_fp32(n),
     "single": lambda n: cpu_sample_fp32(n, lr=0.1),
@@ -249,6 +265,7 @@ CPU_SAMPLES = {
     "q8": cpu_sample_q8,
     "llama3_8b": cpu_sample_bf16rem,
     "bf16rem": cpu_sample_bf16rem,
+    "ademamix_gpt2": lambda n: cpu_sample_ademamix(n),
 }
 
 # ----------------------------------------------------------------------------- workloads
@@ -378,6 +395,29 @@ class Gpt2Small(Workload):
             with torch.cuda.stream(s_out):
                 self._host_p[lo:hi].copy_(self.p_buf[lo:hi], non_blocking=True)
             ev_out[k].record(s_out)
+
+
+class AdemamixGpt2(Gpt2Small):
+    """The GPT-2-small list stepped with AdEMAMix (a third fp32 state: 36 B/element)."""
+    name = "ademamix_gpt2_small_fp32"
+    bytes_per_param = 36.0
+
+    def __init__(self, seed=0):
+        import torch
+        super().__init__(seed)
+        from adamw_optimizer_step_tensor_gb300 import FusedAdamW
+        self.m2_buf, m2s = _flat_views(self.specs, torch.float32, torch.device("cuda"))
+        self.opt = FusedAdamW(self.ps, self.gs, self.ms, self.vs, [s.wd for s in self.specs],
+                              exp_avg_slows=m2s)
+        self.config = dict(self.config, workload="gpt2_small fp32 param list, AdEMAMix (m1, m2, v), "
+                           "cosine lr from a device table", bytes_per_param=self.bytes_per_param)
+
+    def step(self, i):
+        self.C.adamw_ademamix_step(self.opt.plan, self.lr_ptrs[i % 100], self.step_dev.data_ptr(),
+                                   0.9, 0.999, 0.9999, 5.0, 1e-8, None, None, self.stream)
+
+    def e2e_setup(self):
+        return None
 
 
 class Single(Workload):
@@ -573,7 +613,8 @@ def make_workload(name, numel=0):
     return {"gpt2_small": lambda: Gpt2Small(), "single": lambda: Single(numel=numel),
             "amp": lambda: Single(amp=True, numel=numel), "q8": lambda: Q8(numel=numel),
             "amp_fused": lambda: Single(amp=True, numel=numel, fused=True),
-            "llama3_8b": lambda: Llama3(), "bf16rem": lambda: Bf16Rem(numel=numel)}[name]()
+            "llama3_8b": lambda: Llama3(), "bf16rem": lambda: Bf16Rem(numel=numel),
+            "ademamix_gpt2": lambda: AdemamixGpt2()}[name]()
 
 
 # ----------------------------------------------------------------------------- CPU timing

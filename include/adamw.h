@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define ADAMW_ABI_VERSION 1
+#define ADAMW_ABI_VERSION 2
 #define ADAMW_Q8_BLOCK 256
 
 typedef enum {
@@ -94,6 +94,8 @@ typedef struct {
   float* absmax_v;      /* Q8: fp32 [ceil(numel/256)]; otherwise NULL         */
   int64_t numel;        /* >= 0; tensors with numel 0 are ignored             */
   float weight_decay;   /* per tensor (e.g. 0 for norms and biases)           */
+  void* exp_avg_slow;   /* AdEMAMix slow EMA m2: fp32 [numel] on every tensor of
+                           the plan, or NULL on every tensor (AdamW only)      */
 } adamw_tensor;
 
 typedef struct adamw_plan adamw_plan;
@@ -205,6 +207,26 @@ adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t n_tensors,
                                 float beta1, float beta2, float eps,
                                 const float* grad_scale_dev, const float* found_inf_dev,
                                 void* stream);
+
+/*
+ * One AdEMAMix step over every tensor of the plan (plans whose tensors all
+ * carry exp_avg_slow; fp32 and bf16+remainder modes).  "Fix decoupled weight
+ * decay ordering in the CUDA Adam/AdEMAMix kernels" (bitsandbytes PR #2040):
+ * like AdamW, decay and update both take the previous parameter; the update
+ * rule is that of Pagliardini et al. (arXiv:2409.03137):
+ *     m1' = b1*m1 + (1-b1)*g,  m2' = b3*m2 + (1-b3)*g,  v' = b2*v + (1-b2)*g*g
+ *     p'  = p*(1 - lr*wd) - lr * (m1'/bc1 + alpha*m2') / (sqrt(v')/sqrt(bc2) + eps)
+ * (the slow EMA m2 is not bias-corrected; alpha and beta3 are this step's
+ * values, any warm-up schedule is the caller's).  Float32 sequence:
+ *     g = g_raw [* inv_scale]; m1', m2', v' as above (one rounding per op);
+ *     h = sqrt(v') * inv_sqrt_bc2 + eps;  n = m1' * fl(1/bc1) + alpha * m2';
+ *     u = n / h;  p' = p*(1 - lr*wd) - lr*u.
+ * Other arguments, skip and step-count semantics as adamw_step.
+ */
+adamw_status adamw_ademamix_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev,
+                                 float beta1, float beta2, float beta3, float alpha, float eps,
+                                 const float* grad_scale_dev, const float* found_inf_dev,
+                                 void* stream);
 
 /*
  * The AMP step in one launch ("FusedAdam & PyTorch Lightning AMP": the fused

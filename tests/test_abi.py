@@ -40,7 +40,7 @@ def test_binding_wraps_every_declared_symbol():
 
 
 def test_abi_version():
-    assert C.adamw_abi_version() == 1
+    assert C.adamw_abi_version() == 2
 
 
 def test_default_maps_equal_oracle_maps():
