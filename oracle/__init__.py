@@ -12,6 +12,7 @@ adamw      decoupled-weight-decay AdamW step, fp64 definition and a strict-fp32
            mode with one rounding per written operation (AMP unscale and the
            found_inf skip included).
 ademamix   AdEMAMix (fast and slow EMA) with the same decoupled decay, both modes.
+lion       Lion (sign update, one state) with decay before the update, both modes.
 remainder  fp32 master <-> (bf16 model param, int16 remainder) split and join.
 qmap       the dynamic-exponent 8-bit code maps, their decision thresholds and
            nearest-code quantisation.
@@ -24,4 +25,4 @@ the contents of the 8-bit code maps (``qmap.signed_map`` /
 invariants and the quantiser built on top of it are pinned.
 """
 
-from . import adamw, ademamix, remainder, qmap, q8  # noqa: F401
+from . import adamw, ademamix, lion, remainder, qmap, q8  # noqa: F401

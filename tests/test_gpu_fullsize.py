@@ -158,3 +158,36 @@ def test_llama3_8b_bf16_remainders_full_size_sampled():
     finally:
         del w
         _cleanup()
+
+
+def test_single_tensor_beyond_2e31_elements():
+    """One fp32 tensor of 2^31 + 4097 elements: 64-bit indexing inside a tensor and a
+    ragged tail; sampled windows at both ends and across element 2^31."""
+    n = (1 << 31) + 4097
+    if _free_gib() < 40:
+        pytest.skip("needs ~35 GiB of free device memory")
+    from adamw_optimizer_step_tensor_gb300 import FusedAdamW
+    try:
+        p = synth.normal(n, 0.02, 61, "cuda")
+        g = torch.empty(n, device="cuda")
+        m = torch.zeros(n, device="cuda")
+        v = torch.zeros(n, device="cuda")
+        opt = FusedAdamW([p], [g], [m], [v], [OA.f32(0.1)])
+        idx = np.concatenate([np.arange(0, 4096), np.arange((1 << 31) - 2048, (1 << 31) + 2048),
+                              np.arange(n - 4096, n)]).astype(np.int64)
+        orc = OA.Tensor(p=_take(p, idx).cpu().numpy(), g=None, m=np.zeros(idx.size, np.float32),
+                        v=np.zeros(idx.size, np.float32), wd=OA.f32(0.1))
+        lr, step = torch.tensor([OA.f32(1e-3)], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+        for s in range(3):
+            g.copy_(synth.normal(n, 1e-3, 62 + s, "cuda"))
+            orc.g = _take(g, idx).cpu().numpy()
+            opt.step(lr, step)
+            OA.step_f32([orc], lr=OA.f32(1e-3), beta1=OA.f32(0.9), beta2=OA.f32(0.999),
+                        eps=OA.f32(1e-8), t=s + 1)
+        torch.cuda.synchronize()
+        assert np.array_equal(_take(p, idx).cpu().numpy().view(np.uint32), orc.p.view(np.uint32))
+        assert np.array_equal(_take(m, idx).cpu().numpy().view(np.uint32), orc.m.view(np.uint32))
+        assert np.array_equal(_take(v, idx).cpu().numpy().view(np.uint32), orc.v.view(np.uint32))
+        assert int(step.item()) == 3 and opt.status() == 0
+    finally:
+        _cleanup()
