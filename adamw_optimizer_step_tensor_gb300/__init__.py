@@ -13,6 +13,7 @@ from __future__ import annotations
 from . import _capi
 from ._capi import (  # noqa: F401
     AdamWError, adamw_abi_version, adamw_ademamix_step, adamw_bf16rem_join, adamw_bf16rem_split,
+    adamw_lion_step,
     adamw_check_nonfinite, adamw_last_error, adamw_lr_from_table, adamw_plan_create,
     adamw_plan_destroy,
     adamw_plan_info, adamw_plan_status, adamw_q8_default_maps, adamw_q8_dequant, adamw_q8_quant,
@@ -50,6 +51,8 @@ class FusedAdamW:
                      ``absmax_m`` / ``absmax_v`` float32 [ceil(numel/256)].
     Grads: float32, float16 or bfloat16, one dtype for the whole list.
     ``weight_decays``: one float per tensor.
+    ``exp_avg_sqs=None`` (fp32 / bf16_rem only) makes a plan for ``step_lion``
+    alone.
     """
 
     def __init__(self, params, grads, exp_avgs, exp_avg_sqs, weight_decays, *, mode="fp32",
@@ -58,6 +61,8 @@ class FusedAdamW:
         if mode not in MODES:
             raise ValueError(f"mode must be one of {sorted(MODES)}")
         n = len(params)
+        if exp_avg_sqs is None:
+            exp_avg_sqs = [None] * n
         lists = [grads, exp_avgs, exp_avg_sqs, weight_decays]
         if any(len(x) != n for x in lists):
             raise ValueError("all lists must have one entry per param")
@@ -74,6 +79,8 @@ class FusedAdamW:
             p, g, m, v = params[i], grads[i], exp_avgs[i], exp_avg_sqs[i]
             for name, t, dt in (("param", p, pdt), ("exp_avg", m, sdt), ("exp_avg_sq", v, sdt),
                                 ("grad", g, gdt)):
+                if t is None and name == "exp_avg_sq":
+                    continue
                 if t.dtype != dt:
                     raise TypeError(f"tensor {i}: {name} must be {dt}, got {t.dtype}")
                 if not t.is_contiguous() or t.device.type != "cuda":
@@ -120,6 +127,13 @@ class FusedAdamW:
         adamw_ademamix_step(self.plan, _ptr(lr), _ptr(step), float(betas[0]), float(betas[1]),
                             float(betas[2]), float(alpha), float(eps), _ptr(grad_scale),
                             _ptr(found_inf), _stream(stream))
+
+    def step_lion(self, lr, step, *, betas=(0.9, 0.99), grad_scale=None, found_inf=None,
+                  stream=None) -> None:
+        """Lion step (decay, then a step of lr against sign(b1*m + (1-b1)*g));
+        betas = (b1, b2); exp_avg_sqs are not touched."""
+        adamw_lion_step(self.plan, _ptr(lr), _ptr(step), float(betas[0]), float(betas[1]),
+                        _ptr(grad_scale), _ptr(found_inf), _stream(stream))
 
     def step_amp(self, lr, step, found_inf, *, betas=(0.9, 0.999), eps=1e-8, grad_scale=None,
                  stream=None) -> None:

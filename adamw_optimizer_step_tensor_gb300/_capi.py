@@ -68,6 +68,7 @@ _SIGNATURES = {
                                            _vp, _vp, _vp]),
     "adamw_step_amp": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                       _vp, _vp, _vp]),
+    "adamw_lion_step": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_float, ctypes.c_float, _vp, _vp, _vp]),
     "adamw_bf16rem_split": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int64, _vp]),
     "adamw_bf16rem_join": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int64, _vp]),
     "adamw_q8_default_maps": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float),
@@ -178,6 +179,12 @@ def adamw_ademamix_step(plan: int, lr_dev: int, step_dev: int, beta1: float, bet
                         found_inf_dev: int | None, stream: int | None) -> None:
     _check(load().adamw_ademamix_step(plan, lr_dev, step_dev, beta1, beta2, beta3, alpha, eps,
                                       grad_scale_dev, found_inf_dev, stream))
+
+
+def adamw_lion_step(plan: int, lr_dev: int, step_dev: int, beta1: float, beta2: float,
+                    grad_scale_dev: int | None, found_inf_dev: int | None, stream: int | None) -> None:
+    _check(load().adamw_lion_step(plan, lr_dev, step_dev, beta1, beta2, grad_scale_dev,
+                                  found_inf_dev, stream))
 
 
 def adamw_step_amp(plan: int, lr_dev: int, step_dev: int, beta1: float, beta2: float, eps: float,

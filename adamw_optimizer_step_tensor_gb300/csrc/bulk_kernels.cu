@@ -1,5 +1,5 @@
-// bulk_kernels.cu -- the fp32 and bf16+remainder steps (AdamW, AdEMAMix) with
-// bulk-async staging.
+// bulk_kernels.cu -- the fp32 and bf16+remainder steps (AdamW, AdEMAMix, Lion)
+// with bulk-async staging.
 //
 // One CTA per SM: a producer warp streams each 2048-element tile of every
 // input (p [+ remainder], g, m, v) into a ring of shared-memory stages with
@@ -74,10 +74,12 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
-// Byte layout of one stage: p, rem (bf16 mode), g, m, v, m2 (AdEMAMix) --
-// each kTile elements.
-template <adamw_mode MODE, typename GT, bool ADX>
+// Byte layout of one stage: p, rem (bf16 mode), g, m, v (not Lion), m2
+// (AdEMAMix) -- each kTile elements.
+template <adamw_mode MODE, typename GT, int ALGO>
 struct Stage {
+  static constexpr bool kV = ALGO != kAlgoLion;
+  static constexpr bool kM2 = ALGO == kAlgoAdemamix;
   static constexpr int kP = MODE == ADAMW_MODE_FP32 ? 4 : 2;
   static constexpr int kG = sizeof(GT);
   static constexpr int oP = 0;
@@ -85,10 +87,11 @@ struct Stage {
   static constexpr int oG = oR + (MODE == ADAMW_MODE_BF16_REM ? kTile * 2 : 0);
   static constexpr int oM = oG + kTile * kG;
   static constexpr int oV = oM + kTile * 4;
-  static constexpr int oM2 = oV + kTile * 4;
-  static constexpr int kBytes = oM2 + (ADX ? kTile * 4 : 0);
+  static constexpr int oM2 = oV + (kV ? kTile * 4 : 0);
+  static constexpr int kBytes = oM2 + (kM2 ? kTile * 4 : 0);
   // bytes moved per element in bulk
-  static constexpr int kPerElem = kP + (MODE == ADAMW_MODE_BF16_REM ? 2 : 0) + kG + 8 + (ADX ? 4 : 0);
+  static constexpr int kPerElem =
+      kP + (MODE == ADAMW_MODE_BF16_REM ? 2 : 0) + kG + 4 + (kV ? 4 : 0) + (kM2 ? 4 : 0);
   static_assert(kBytes % 128 == 0, "stages stay 128-byte aligned");
 };
 
@@ -97,9 +100,9 @@ struct Stage {
 // stages 97%, 24-30 warps 96-97%.
 template <int MODE> struct BulkTune { static constexpr int stages = 3; };
 
-template <adamw_mode MODE, typename GT, bool ADX>
+template <adamw_mode MODE, typename GT, int ALGO>
 constexpr int bulk_smem_bytes() {
-  return BulkTune<MODE>::stages * Stage<MODE, GT, ADX>::kBytes + 2 * BulkTune<MODE>::stages * 8;
+  return BulkTune<MODE>::stages * Stage<MODE, GT, ALGO>::kBytes + 2 * BulkTune<MODE>::stages * 8;
 }
 
 __device__ __forceinline__ void fault(const StepArgs& a, uint32_t code) {
@@ -107,9 +110,9 @@ __device__ __forceinline__ void fault(const StepArgs& a, uint32_t code) {
 }
 
 // The producer: one thread issues the bulk copies of every tile of this CTA.
-template <adamw_mode MODE, typename GT, bool ADX>
+template <adamw_mode MODE, typename GT, int ALGO>
 __device__ void produce(const StepArgs& a, unsigned char* ring, uint64_t* full, uint64_t* empty) {
-  using L = Stage<MODE, GT, ADX>;
+  using L = Stage<MODE, GT, ALGO>;
   constexpr int S = BulkTune<MODE>::stages;
   uint32_t i = 0;
   bool ok = true;
@@ -135,8 +138,8 @@ __device__ void produce(const StepArgs& a, unsigned char* ring, uint64_t* full, 
           bulk_g2s(st + L::oR, td.rem + e, nb * 2, &full[s]);
         bulk_g2s(st + L::oG, static_cast<const unsigned char*>(td.g) + e * L::kG, nb * L::kG, &full[s]);
         bulk_g2s(st + L::oM, static_cast<const float*>(td.m) + e, nb * 4, &full[s]);
-        bulk_g2s(st + L::oV, static_cast<const float*>(td.v) + e, nb * 4, &full[s]);
-        if (ADX) bulk_g2s(st + L::oM2, static_cast<const float*>(td.m2) + e, nb * 4, &full[s]);
+        if (L::kV) bulk_g2s(st + L::oV, static_cast<const float*>(td.v) + e, nb * 4, &full[s]);
+        if (L::kM2) bulk_g2s(st + L::oM2, static_cast<const float*>(td.m2) + e, nb * 4, &full[s]);
       }
     }
   }
@@ -159,10 +162,10 @@ __device__ __forceinline__ float grad_from_smem(const unsigned char* base, int i
 }
 
 // Four consecutive elements [j, j+4) of a tile from shared memory.
-template <adamw_mode MODE, typename GT, bool ADX>
+template <adamw_mode MODE, typename GT, int ALGO>
 __device__ __forceinline__ void load4_smem(const unsigned char* st, int j, float (&p)[4],
                                            float (&g)[4], float (&m)[4], float (&v)[4]) {
-  using L = Stage<MODE, GT, ADX>;
+  using L = Stage<MODE, GT, ALGO>;
   if (MODE == ADAMW_MODE_FP32) {
     const float4 x = *reinterpret_cast<const float4*>(st + L::oP + j * 4);
     p[0] = x.x; p[1] = x.y; p[2] = x.z; p[3] = x.w;
@@ -177,12 +180,14 @@ __device__ __forceinline__ void load4_smem(const unsigned char* st, int j, float
 #pragma unroll
   for (int q = 0; q < 4; ++q) g[q] = grad_from_smem<GT>(st + L::oG, j + q);
   const float4 mm = *reinterpret_cast<const float4*>(st + L::oM + j * 4);
-  const float4 vv = *reinterpret_cast<const float4*>(st + L::oV + j * 4);
   m[0] = mm.x; m[1] = mm.y; m[2] = mm.z; m[3] = mm.w;
-  v[0] = vv.x; v[1] = vv.y; v[2] = vv.z; v[3] = vv.w;
+  if (L::kV) {
+    const float4 vv = *reinterpret_cast<const float4*>(st + L::oV + j * 4);
+    v[0] = vv.x; v[1] = vv.y; v[2] = vv.z; v[3] = vv.w;
+  }
 }
 
-template <adamw_mode MODE>
+template <adamw_mode MODE, bool kV>
 __device__ __forceinline__ void store4(const TensorDesc& td, int64_t e, const float (&p)[4],
                                        const float (&m)[4], const float (&v)[4]) {
   if (MODE == ADAMW_MODE_FP32) {
@@ -198,12 +203,13 @@ __device__ __forceinline__ void store4(const TensorDesc& td, int64_t e, const fl
     __stcs(reinterpret_cast<uint2*>(td.rem + e), make_uint2(r0 | (r1 << 16), r2 | (r3 << 16)));
   }
   __stcs(reinterpret_cast<float4*>(static_cast<float*>(td.m) + e), make_float4(m[0], m[1], m[2], m[3]));
-  __stcs(reinterpret_cast<float4*>(static_cast<float*>(td.v) + e), make_float4(v[0], v[1], v[2], v[3]));
+  if (kV)
+    __stcs(reinterpret_cast<float4*>(static_cast<float*>(td.v) + e), make_float4(v[0], v[1], v[2], v[3]));
 }
 
-template <adamw_mode MODE, typename GT, bool ADX>
+template <adamw_mode MODE, typename GT, int ALGO>
 __global__ void __launch_bounds__(kBulkThreads, 1) step_bulk_kernel(const StepArgs a) {
-  using L = Stage<MODE, GT, ADX>;
+  using L = Stage<MODE, GT, ALGO>;
   constexpr int S = BulkTune<MODE>::stages;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* ring = smem_raw;
@@ -227,7 +233,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1) step_bulk_kernel(const StepAr
     // no copy is issued for a skipped step
     if (threadIdx.x == kConsumers) {
       const bool skip = a.found_inf != nullptr && *a.found_inf != 0.0f;
-      if (!skip) produce<MODE, GT, ADX>(a, ring, full, empty);
+      if (!skip) produce<MODE, GT, ALGO>(a, ring, full, empty);
     }
     return;
   }
@@ -260,21 +266,24 @@ __global__ void __launch_bounds__(kBulkThreads, 1) step_bulk_kernel(const StepAr
         const int j = threadIdx.x * 4;
         if (j + 4 <= nb) {
           float p[4], g[4], m[4], v[4];
-          load4_smem<MODE, GT, ADX>(st, j, p, g, m, v);
-          if (ADX) {
+          load4_smem<MODE, GT, ALGO>(st, j, p, g, m, v);
+          if (ALGO == kAlgoAdemamix) {
             const float4 w = *reinterpret_cast<const float4*>(st + L::oM2 + j * 4);
             float m2[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
             for (int q = 0; q < 4; ++q) update_ademamix(p[q], g[q], m[q], m2[q], v[q], s, decay);
             __stcs(reinterpret_cast<float4*>(static_cast<float*>(td.m2) + e0 + j),
                    make_float4(m2[0], m2[1], m2[2], m2[3]));
+          } else if (ALGO == kAlgoLion) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) update_lion(p[q], g[q], m[q], s, decay);
           } else {
 #pragma unroll
             for (int q = 0; q < 4; ++q) update(p[q], g[q], m[q], v[q], s, decay);
           }
-          store4<MODE>(td, e0 + j, p, m, v);
+          store4<MODE, L::kV>(td, e0 + j, p, m, v);
         } else if (j < len) {
-          update_scalar<MODE, GT, ADX>(td, e0 + j, min(4, len - j), s, decay);
+          update_scalar<MODE, GT, ALGO>(td, e0 + j, min(4, len - j), s, decay);
         }
       }
       __syncwarp();
@@ -283,35 +292,44 @@ __global__ void __launch_bounds__(kBulkThreads, 1) step_bulk_kernel(const StepAr
   }
 }
 
-template <adamw_mode MODE, typename GT, bool ADX>
+template <adamw_mode MODE, typename GT, int ALGO>
 cudaError_t launch_one(const StepArgs& a, int grid, cudaStream_t st) {
-  step_bulk_kernel<MODE, GT, ADX><<<grid, kBulkThreads, bulk_smem_bytes<MODE, GT, ADX>(), st>>>(a);
+  step_bulk_kernel<MODE, GT, ALGO><<<grid, kBulkThreads, bulk_smem_bytes<MODE, GT, ALGO>(), st>>>(a);
   return cudaGetLastError();
 }
 
-template <adamw_mode MODE, typename GT, bool ADX>
+template <adamw_mode MODE, typename GT, int ALGO>
 cudaError_t prepare_one() {
-  return cudaFuncSetAttribute(step_bulk_kernel<MODE, GT, ADX>,
+  return cudaFuncSetAttribute(step_bulk_kernel<MODE, GT, ALGO>,
                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              bulk_smem_bytes<MODE, GT, ADX>());
+                              bulk_smem_bytes<MODE, GT, ALGO>());
+}
+
+template <adamw_mode MODE, typename GT>
+cudaError_t launch_algo(const StepArgs& a, int grid, cudaStream_t st, int algo) {
+  if (algo == kAlgoAdemamix) return launch_one<MODE, GT, kAlgoAdemamix>(a, grid, st);
+  if (algo == kAlgoLion) return launch_one<MODE, GT, kAlgoLion>(a, grid, st);
+  return launch_one<MODE, GT, kAlgoAdamW>(a, grid, st);
+}
+
+template <adamw_mode MODE, typename GT>
+cudaError_t prepare_algo(int algo) {
+  if (algo == kAlgoAdemamix) return prepare_one<MODE, GT, kAlgoAdemamix>();
+  if (algo == kAlgoLion) return prepare_one<MODE, GT, kAlgoLion>();
+  return prepare_one<MODE, GT, kAlgoAdamW>();
 }
 
 template <typename GT>
 cudaError_t launch_bulk_mode(adamw_mode mode, const StepArgs& a, int grid, cudaStream_t st,
-                             bool adx) {
-  if (mode == ADAMW_MODE_FP32)
-    return adx ? launch_one<ADAMW_MODE_FP32, GT, true>(a, grid, st)
-               : launch_one<ADAMW_MODE_FP32, GT, false>(a, grid, st);
-  return adx ? launch_one<ADAMW_MODE_BF16_REM, GT, true>(a, grid, st)
-             : launch_one<ADAMW_MODE_BF16_REM, GT, false>(a, grid, st);
+                             int algo) {
+  if (mode == ADAMW_MODE_FP32) return launch_algo<ADAMW_MODE_FP32, GT>(a, grid, st, algo);
+  return launch_algo<ADAMW_MODE_BF16_REM, GT>(a, grid, st, algo);
 }
 
 template <typename GT>
-cudaError_t prepare_bulk_mode(adamw_mode mode, bool adx) {
-  if (mode == ADAMW_MODE_FP32)
-    return adx ? prepare_one<ADAMW_MODE_FP32, GT, true>() : prepare_one<ADAMW_MODE_FP32, GT, false>();
-  return adx ? prepare_one<ADAMW_MODE_BF16_REM, GT, true>()
-             : prepare_one<ADAMW_MODE_BF16_REM, GT, false>();
+cudaError_t prepare_bulk_mode(adamw_mode mode, int algo) {
+  if (mode == ADAMW_MODE_FP32) return prepare_algo<ADAMW_MODE_FP32, GT>(algo);
+  return prepare_algo<ADAMW_MODE_BF16_REM, GT>(algo);
 }
 
 // Self-test of the bounded wait: one thread waits on an mbarrier phase that
@@ -347,20 +365,20 @@ cudaError_t run_wait_selftest(int limit_us, cudaStream_t s, uint32_t* fault_bits
 }
 
 cudaError_t launch_step_bulk(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int grid,
-                             cudaStream_t s, bool ademamix) {
+                             cudaStream_t s, int algo) {
   switch (gdt) {
-    case ADAMW_F32: return launch_bulk_mode<float>(mode, a, grid, s, ademamix);
-    case ADAMW_F16: return launch_bulk_mode<__half>(mode, a, grid, s, ademamix);
-    case ADAMW_BF16: return launch_bulk_mode<__nv_bfloat16>(mode, a, grid, s, ademamix);
+    case ADAMW_F32: return launch_bulk_mode<float>(mode, a, grid, s, algo);
+    case ADAMW_F16: return launch_bulk_mode<__half>(mode, a, grid, s, algo);
+    case ADAMW_BF16: return launch_bulk_mode<__nv_bfloat16>(mode, a, grid, s, algo);
   }
   return cudaErrorInvalidValue;
 }
 
-cudaError_t prepare_step_bulk(adamw_mode mode, adamw_dtype gdt, bool ademamix) {
+cudaError_t prepare_step_bulk(adamw_mode mode, adamw_dtype gdt, int algo) {
   switch (gdt) {
-    case ADAMW_F32: return prepare_bulk_mode<float>(mode, ademamix);
-    case ADAMW_F16: return prepare_bulk_mode<__half>(mode, ademamix);
-    case ADAMW_BF16: return prepare_bulk_mode<__nv_bfloat16>(mode, ademamix);
+    case ADAMW_F32: return prepare_bulk_mode<float>(mode, algo);
+    case ADAMW_F16: return prepare_bulk_mode<__half>(mode, algo);
+    case ADAMW_BF16: return prepare_bulk_mode<__nv_bfloat16>(mode, algo);
   }
   return cudaErrorInvalidValue;
 }

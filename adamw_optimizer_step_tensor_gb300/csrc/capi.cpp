@@ -39,6 +39,7 @@ struct adamw_plan {
   int64_t n_chunks_fused = 0;
   int grid_fused = 0;
   bool has_slow = false;       // every tensor carries an AdEMAMix slow EMA
+  bool has_v = true;           // every tensor carries exp_avg_sq (false: Lion-only plan)
 };
 
 namespace {
@@ -135,7 +136,7 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
   std::vector<TensorDesc> td(static_cast<size_t>(n_tensors));
   std::vector<Chunk> chunks;
   int64_t total = 0;
-  int with_slow = 0, sized = 0;
+  int with_slow = 0, with_v = 0, sized = 0;
   for (int32_t i = 0; i < n_tensors; ++i) {
     const adamw_tensor& t = tensors[i];
     if (t.numel < 0) return fail(ADAMW_EINVAL, "tensor %d: numel < 0", i);
@@ -159,8 +160,9 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
       if (!aligned(t.exp_avg_slow, 4))
         return fail(ADAMW_EALIGN, "tensor %d: exp_avg_slow is not 4-byte aligned", i);
     }
-    if (!t.param || !t.grad || !t.exp_avg || !t.exp_avg_sq)
-      return fail(ADAMW_EINVAL, "tensor %d: param, grad, exp_avg and exp_avg_sq must be set", i);
+    if (!t.param || !t.grad || !t.exp_avg)
+      return fail(ADAMW_EINVAL, "tensor %d: param, grad and exp_avg must be set", i);
+    if (t.exp_avg_sq) ++with_v;
     if ((mode == ADAMW_MODE_BF16_REM) != (t.param_rem != nullptr))
       return fail(ADAMW_EINVAL, "tensor %d: param_rem must be set exactly in BF16_REM mode", i);
     if ((mode == ADAMW_MODE_Q8) != (t.absmax_m != nullptr && t.absmax_v != nullptr) ||
@@ -180,6 +182,12 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
   if (with_slow && mode == ADAMW_MODE_Q8)
     return fail(ADAMW_EUNSUPPORTED, "AdEMAMix slow states are supported in the fp32 and "
                                     "bf16+remainder modes");
+  if (with_v != 0 && with_v != sized)
+    return fail(ADAMW_EINVAL, "exp_avg_sq must be set on every tensor or on none");
+  if (sized && !with_v && mode == ADAMW_MODE_Q8)
+    return fail(ADAMW_EINVAL, "Q8 mode needs exp_avg_sq on every tensor");
+  if (sized && !with_v && with_slow)
+    return fail(ADAMW_EINVAL, "an AdEMAMix plan needs exp_avg_sq on every tensor");
 
   // Every argument is valid; only now touch the device.
   int device = -1, sms = 0;
@@ -190,8 +198,9 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
   int bps = 0, smem = 0;
   const bool bulk = kUseBulk && mode != ADAMW_MODE_Q8;
   if (bulk) {
-    e = prepare_step_bulk(mode, grad_dtype, false);
-    if (e == cudaSuccess && with_slow) e = prepare_step_bulk(mode, grad_dtype, true);
+    e = prepare_step_bulk(mode, grad_dtype, kAlgoLion);
+    if (e == cudaSuccess && (with_v || !sized)) e = prepare_step_bulk(mode, grad_dtype, kAlgoAdamW);
+    if (e == cudaSuccess && with_slow) e = prepare_step_bulk(mode, grad_dtype, kAlgoAdemamix);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bulk step)");
     bps = 1;
   } else {
@@ -216,6 +225,7 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
   p->device = device;
   p->bulk = bulk;
   p->has_slow = with_slow != 0;
+  p->has_v = with_v != 0 || sized == 0;
   const int64_t resident = static_cast<int64_t>(bps) * sms;
   p->grid = static_cast<int>(p->n_chunks < resident ? (p->n_chunks > 0 ? p->n_chunks : 1) : resident);
   const int64_t check_res = 8LL * sms;
@@ -346,6 +356,7 @@ adamw_status adamw_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev
   if (!(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f))
     return fail(ADAMW_EINVAL, "betas must lie in [0, 1)");
   if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(ADAMW_EINVAL, "eps must be finite and >= 0");
+  if (!plan->has_v) return fail(ADAMW_EINVAL, "the plan's tensors carry no exp_avg_sq");
   adamw_status st = check_device(plan);
   if (st != ADAMW_OK) return st;
   StepArgs a;
@@ -365,7 +376,7 @@ adamw_status adamw_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev
   a.qt = plan->d_qt;
   a.refine = plan->refine;
   cudaError_t e = plan->bulk ? launch_step_bulk(plan->mode, plan->gdt, a, plan->grid,
-                                                static_cast<cudaStream_t>(stream))
+                                                static_cast<cudaStream_t>(stream), kAlgoAdamW)
                              : launch_step(plan->mode, plan->gdt, a, plan->grid,
                                            static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "launch adamw step");
@@ -417,8 +428,44 @@ adamw_status adamw_ademamix_step(adamw_plan* plan, const float* lr_dev, int32_t*
   a.qt = nullptr;
   a.refine = 1;
   cudaError_t e = launch_step_bulk(plan->mode, plan->gdt, a, plan->grid,
-                                   static_cast<cudaStream_t>(stream), true);
+                                   static_cast<cudaStream_t>(stream), kAlgoAdemamix);
   if (e != cudaSuccess) return cuda_fail(e, "launch AdEMAMix step");
+  return ADAMW_OK;
+}
+
+adamw_status adamw_lion_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev,
+                             float beta1, float beta2, const float* grad_scale_dev,
+                             const float* found_inf_dev, void* stream) {
+  if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
+  if (plan->mode == ADAMW_MODE_Q8)
+    return fail(ADAMW_EUNSUPPORTED, "Lion covers the fp32 and bf16+remainder modes");
+  if (!lr_dev || !step_dev) return fail(ADAMW_EINVAL, "lr_dev and step_dev must be set");
+  if (!aligned(lr_dev, 4) || !aligned(step_dev, 4) || !aligned(grad_scale_dev, 4) ||
+      !aligned(found_inf_dev, 4))
+    return fail(ADAMW_EALIGN, "a scalar pointer is not 4-byte aligned");
+  if (!(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f))
+    return fail(ADAMW_EINVAL, "betas must lie in [0, 1)");
+  adamw_status st = check_device(plan);
+  if (st != ADAMW_OK) return st;
+  StepArgs a;
+  a.tensors = plan->d_tensors;
+  a.chunks = plan->d_chunks;
+  a.n_chunks = plan->n_chunks;
+  a.lr = lr_dev;
+  a.step = step_dev;
+  a.grad_scale = grad_scale_dev;
+  a.found_inf = found_inf_dev;
+  a.beta1 = beta1;
+  a.beta2 = beta2;
+  a.eps = 0.0f;
+  a.beta3 = 0.0f;
+  a.alpha = 0.0f;
+  a.scratch = plan->d_scratch;
+  a.qt = nullptr;
+  a.refine = 1;
+  cudaError_t e = launch_step_bulk(plan->mode, plan->gdt, a, plan->grid,
+                                   static_cast<cudaStream_t>(stream), kAlgoLion);
+  if (e != cudaSuccess) return cuda_fail(e, "launch Lion step");
   return ADAMW_OK;
 }
 
@@ -436,6 +483,7 @@ adamw_status adamw_step_amp(adamw_plan* plan, const float* lr_dev, int32_t* step
   if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(ADAMW_EINVAL, "eps must be finite and >= 0");
   if (plan->mode == ADAMW_MODE_Q8)
     return fail(ADAMW_EUNSUPPORTED, "the fused check + step covers the fp32 and bf16+remainder modes");
+  if (!plan->has_v) return fail(ADAMW_EINVAL, "the plan's tensors carry no exp_avg_sq");
   adamw_status st = check_device(plan);
   if (st != ADAMW_OK) return st;
   // every CTA of the cooperative launch is resident at once (grid sized at plan creation)

@@ -47,6 +47,11 @@ inline int64_t choose_chunk(int64_t total, int sms, int blocks_per_sm) {
 constexpr int kBuckets = 1 + 25 * 128;       // |x| in [0, 2^-24) plus 25 binades x 128
 constexpr int kMaxRefine = 4;                // thresholds compared per lookup, at most
 
+// Update rules of the bulk-staged kernel.
+constexpr int kAlgoAdamW = 0;
+constexpr int kAlgoAdemamix = 1;
+constexpr int kAlgoLion = 2;
+
 struct TensorDesc {
   void* p;            // fp32 or bf16 param
   int16_t* rem;       // remainders (BF16_REM)
@@ -139,8 +144,8 @@ cudaError_t launch_step(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int
 cudaError_t step_occupancy(adamw_mode mode, adamw_dtype gdt, int* blocks_per_sm,
                            int* smem_bytes);
 cudaError_t launch_step_bulk(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int grid,
-                             cudaStream_t s, bool ademamix = false);
-cudaError_t prepare_step_bulk(adamw_mode mode, adamw_dtype gdt, bool ademamix = false);
+                             cudaStream_t s, int algo);
+cudaError_t prepare_step_bulk(adamw_mode mode, adamw_dtype gdt, int algo);
 cudaError_t run_wait_selftest(int limit_us, cudaStream_t s, uint32_t* fault_bits,
                               double* waited_ms);
 cudaError_t launch_nonfinite(adamw_dtype gdt, const TensorDesc* tensors, const Chunk* chunks,

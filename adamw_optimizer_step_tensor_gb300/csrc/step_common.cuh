@@ -120,6 +120,18 @@ __device__ __forceinline__ void update_ademamix(float& p, float g, float& m1, fl
   p = __fsub_rn(__fmul_rn(p, decay), __fmul_rn(s.lr, u));
 }
 
+// The Lion element update: decay first, then a step of exactly lr against the
+// sign of b1*m + (1-b1)*g (0 for a zero or NaN interpolation); the state keeps
+// the b2 EMA.
+__device__ __forceinline__ void update_lion(float& p, float g, float& m, const Scal& s,
+                                            float decay) {
+  if (s.scaled) g = __fmul_rn(g, s.inv_scale);
+  const float c = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
+  const float sg = c > 0.0f ? 1.0f : (c < 0.0f ? -1.0f : 0.0f);
+  p = __fsub_rn(__fmul_rn(p, decay), __fmul_rn(s.lr, sg));
+  m = __fadd_rn(__fmul_rn(s.b2, m), __fmul_rn(s.omb2, g));
+}
+
 // ---------------------------------------------------------------- loads/stores
 __device__ __forceinline__ void ld8f(const float* q, float (&x)[8]) {
   const float4 a = __ldcs(reinterpret_cast<const float4*>(q));
@@ -196,7 +208,7 @@ __device__ __forceinline__ void rem_split(float x, uint32_t& hi, uint32_t& rem16
 
 // Elements [e, e + n) one at a time: ragged tails and tensors whose pointers
 // are not all 16-byte aligned.
-template <adamw_mode MODE, typename GT, bool ADX = false>
+template <adamw_mode MODE, typename GT, int ALGO = kAlgoAdamW>
 __device__ void update_scalar(const TensorDesc& td, int64_t e, int n, const Scal& s,
                               float decay) {
   float* const pf = static_cast<float*>(td.p);
@@ -206,12 +218,15 @@ __device__ void update_scalar(const TensorDesc& td, int64_t e, int n, const Scal
   for (int i = 0; i < n; ++i) {
     const int64_t k = e + i;
     float p = MODE == ADAMW_MODE_FP32 ? pf[k] : rem_join(ph[k], static_cast<uint16_t>(td.rem[k]));
-    float m = mf[k], v = vf[k];
-    if (ADX) {
+    float m = mf[k];
+    float v = ALGO == kAlgoLion ? 0.0f : vf[k];
+    if (ALGO == kAlgoAdemamix) {
       float* const m2f = static_cast<float*>(td.m2);
       float m2 = m2f[k];
       update_ademamix(p, Grad<GT>::load1(td.g, k), m, m2, v, s, decay);
       m2f[k] = m2;
+    } else if (ALGO == kAlgoLion) {
+      update_lion(p, Grad<GT>::load1(td.g, k), m, s, decay);
     } else {
       update(p, Grad<GT>::load1(td.g, k), m, v, s, decay);
     }
@@ -224,7 +239,7 @@ __device__ void update_scalar(const TensorDesc& td, int64_t e, int n, const Scal
       td.rem[k] = static_cast<int16_t>(static_cast<uint16_t>(r));
     }
     mf[k] = m;
-    vf[k] = v;
+    if (ALGO != kAlgoLion) vf[k] = v;
   }
 }
 

@@ -50,7 +50,7 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gpt2_small",
                     choices=["gpt2_small", "single", "amp", "amp_fused", "q8", "llama3_8b", "bf16rem",
-                             "ademamix_gpt2"])
+                             "ademamix_gpt2", "lion_gpt2"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -257,6 +257,17 @@ def cpu_sample_ademamix(n):
     return run, f"{n} elements per step, float64 AdEMAMix oracle (oracle.ademamix.step_fp64)"
 
 
+def cpu_sample_lion(n):
+    import numpy as np
+    from oracle import lion as OL
+    rng = np.random.default_rng(0)
+    x = OL.Tensor(p=rng.normal(0, 0.02, n), g=rng.normal(0, 1e-3, n), m=np.zeros(n), wd=0.1)
+
+    def run():
+        OL.step_fp64([x], lr=1e-4, beta1=0.9, beta2=0.99)
+    return run, f"{n} elements per step, float64 Lion oracle (oracle.lion.step_fp64)"
+
+
 CPU_SAMPLES = {
     "gpt2_small": lambda n: cpu_sample_fp32(n),
     "single": lambda n: cpu_sample_fp32(n, lr=0.1),
@@ -266,6 +277,7 @@ CPU_SAMPLES = {
     "llama3_8b": cpu_sample_bf16rem,
     "bf16rem": cpu_sample_bf16rem,
     "ademamix_gpt2": lambda n: cpu_sample_ademamix(n),
+    "lion_gpt2": lambda n: cpu_sample_lion(n),
 }
 
 # ----------------------------------------------------------------------------- workloads
@@ -346,7 +358,6 @@ class Gpt2Small(Workload):
         device-to-host copy of the one before overlap on three streams.
         """
         import torch
-        from adamw_optimizer_step_tensor_gb300 import FusedAdamW
         self._host_g = torch.empty_like(self.g_buf, device="cpu").pin_memory()
         self._host_g.copy_(self.g_buf)
         self._host_p = torch.empty_like(self.p_buf, device="cpu").pin_memory()
@@ -359,15 +370,23 @@ class Gpt2Small(Workload):
             if acc >= target * (len(self._groups) + 1) or k == len(self.ps) - 1:
                 idx = list(range(start, k + 1))
                 lo, hi = offs[start], offs[k] + self.ps[k].numel()
-                opt = FusedAdamW([self.ps[j] for j in idx], [self.gs[j] for j in idx],
-                                 [self.ms[j] for j in idx], [self.vs[j] for j in idx],
-                                 [self.specs[j].wd for j in idx])
+                opt = self._group_plan(idx)
                 self._groups.append((lo, hi, opt, torch.zeros(1, dtype=torch.int32, device="cuda")))
                 start = k + 1
         self._s = [torch.cuda.Stream() for _ in range(3)]          # in, step, out
         n = len(self._groups)
         self._ev = [[torch.cuda.Event() for _ in range(n)] for _ in range(3)]
         return self._host_g.numel() * 4, self._host_p.numel() * 4
+
+    def _group_plan(self, idx):
+        from adamw_optimizer_step_tensor_gb300 import FusedAdamW
+        return FusedAdamW([self.ps[j] for j in idx], [self.gs[j] for j in idx],
+                          [self.ms[j] for j in idx], [self.vs[j] for j in idx],
+                          [self.specs[j].wd for j in idx])
+
+    def _group_step(self, opt, i, step_dev, stream):
+        self.C.adamw_step(opt.plan, self.lr_ptrs[i % 100], step_dev.data_ptr(), 0.9, 0.999, 1e-8,
+                          None, None, stream)
 
     def e2e_begin(self, stream):
         for s in self._s:
@@ -388,8 +407,7 @@ class Gpt2Small(Workload):
             ev_in[k].record(s_in)
             s_cmp.wait_event(ev_in[k])
             s_cmp.wait_event(ev_out[k])           # the previous copy-out has read these params
-            self.C.adamw_step(opt.plan, self.lr_ptrs[i % 100], step_dev.data_ptr(), 0.9, 0.999,
-                              1e-8, None, None, s_cmp.cuda_stream)
+            self._group_step(opt, i, step_dev, s_cmp.cuda_stream)
             ev_cmp[k].record(s_cmp)
             s_out.wait_event(ev_cmp[k])
             with torch.cuda.stream(s_out):
@@ -407,17 +425,56 @@ class AdemamixGpt2(Gpt2Small):
         super().__init__(seed)
         from adamw_optimizer_step_tensor_gb300 import FusedAdamW
         self.m2_buf, m2s = _flat_views(self.specs, torch.float32, torch.device("cuda"))
+        self.m2s = m2s
         self.opt = FusedAdamW(self.ps, self.gs, self.ms, self.vs, [s.wd for s in self.specs],
                               exp_avg_slows=m2s)
         self.config = dict(self.config, workload="gpt2_small fp32 param list, AdEMAMix (m1, m2, v), "
-                           "cosine lr from a device table", bytes_per_param=self.bytes_per_param)
+                           "cosine lr from a device table", bytes_per_param=self.bytes_per_param,
+                           l2="no flush: 4.48 GB moved per step, larger than the 126 MB L2")
+        self.e2e_what = self.e2e_what.replace("adamw_step", "adamw_ademamix_step")
 
     def step(self, i):
         self.C.adamw_ademamix_step(self.opt.plan, self.lr_ptrs[i % 100], self.step_dev.data_ptr(),
                                    0.9, 0.999, 0.9999, 5.0, 1e-8, None, None, self.stream)
 
-    def e2e_setup(self):
-        return None
+    def _group_plan(self, idx):
+        from adamw_optimizer_step_tensor_gb300 import FusedAdamW
+        return FusedAdamW([self.ps[j] for j in idx], [self.gs[j] for j in idx],
+                          [self.ms[j] for j in idx], [self.vs[j] for j in idx],
+                          [self.specs[j].wd for j in idx], exp_avg_slows=[self.m2s[j] for j in idx])
+
+    def _group_step(self, opt, i, step_dev, stream):
+        self.C.adamw_ademamix_step(opt.plan, self.lr_ptrs[i % 100], step_dev.data_ptr(), 0.9, 0.999,
+                                   0.9999, 5.0, 1e-8, None, None, stream)
+
+
+class LionGpt2(Gpt2Small):
+    """The GPT-2-small list stepped with Lion (one fp32 state, no v: 20 B/element)."""
+    name = "lion_gpt2_small_fp32"
+    bytes_per_param = 20.0
+
+    def __init__(self, seed=0):
+        super().__init__(seed)
+        from adamw_optimizer_step_tensor_gb300 import FusedAdamW
+        self.opt = FusedAdamW(self.ps, self.gs, self.ms, None, [s.wd for s in self.specs])
+        self.vs = self.v_buf = None
+        self.config = dict(self.config, workload="gpt2_small fp32 param list, Lion (m only), "
+                           "cosine lr from a device table", bytes_per_param=self.bytes_per_param,
+                           l2="no flush: 2.49 GB moved per step, larger than the 126 MB L2")
+        self.e2e_what = self.e2e_what.replace("adamw_step", "adamw_lion_step")
+
+    def step(self, i):
+        self.C.adamw_lion_step(self.opt.plan, self.lr_ptrs[i % 100], self.step_dev.data_ptr(),
+                               0.9, 0.99, None, None, self.stream)
+
+    def _group_plan(self, idx):
+        from adamw_optimizer_step_tensor_gb300 import FusedAdamW
+        return FusedAdamW([self.ps[j] for j in idx], [self.gs[j] for j in idx],
+                          [self.ms[j] for j in idx], None, [self.specs[j].wd for j in idx])
+
+    def _group_step(self, opt, i, step_dev, stream):
+        self.C.adamw_lion_step(opt.plan, self.lr_ptrs[i % 100], step_dev.data_ptr(), 0.9, 0.99,
+                               None, None, stream)
 
 
 class Single(Workload):
@@ -614,7 +671,8 @@ def make_workload(name, numel=0):
             "amp": lambda: Single(amp=True, numel=numel), "q8": lambda: Q8(numel=numel),
             "amp_fused": lambda: Single(amp=True, numel=numel, fused=True),
             "llama3_8b": lambda: Llama3(), "bf16rem": lambda: Bf16Rem(numel=numel),
-            "ademamix_gpt2": lambda: AdemamixGpt2()}[name]()
+            "ademamix_gpt2": lambda: AdemamixGpt2(),
+            "lion_gpt2": lambda: LionGpt2()}[name]()
 
 
 # ----------------------------------------------------------------------------- CPU timing
@@ -759,7 +817,8 @@ def main():
                                "pinned-host grads -> device, adamw_step, updated params -> pinned host")}
     else:
         e2e = {"value": None, "unit": UNIT, "h2d_bytes_per_step": None, "d2h_bytes_per_step": None,
-               "note": "no pinned-host copy of this workload's buffers fits beside it"}
+               "note": "this workload has no host-offload arm (its buffers leave no room for a "
+                       "pinned-host copy, or --e2e-steps 0)"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -47,7 +47,7 @@
 extern "C" {
 #endif
 
-#define ADAMW_ABI_VERSION 2
+#define ADAMW_ABI_VERSION 3
 #define ADAMW_Q8_BLOCK 256
 
 typedef enum {
@@ -89,7 +89,10 @@ typedef struct {
   int16_t* param_rem;   /* BF16_REM: int16 [numel]; otherwise must be NULL    */
   const void* grad;     /* grad_dtype [numel], possibly loss-scaled           */
   void* exp_avg;        /* m: fp32 [numel]; uint8 codes [numel] in Q8 mode    */
-  void* exp_avg_sq;     /* v: fp32 [numel]; uint8 codes [numel] in Q8 mode    */
+  void* exp_avg_sq;     /* v: fp32 [numel]; uint8 codes [numel] in Q8 mode.
+                           May be NULL on every tensor of an fp32 or
+                           bf16+remainder plan: such a plan runs only
+                           adamw_lion_step (the others return EINVAL)        */
   float* absmax_m;      /* Q8: fp32 [ceil(numel/256)]; otherwise NULL         */
   float* absmax_v;      /* Q8: fp32 [ceil(numel/256)]; otherwise NULL         */
   int64_t numel;        /* >= 0; tensors with numel 0 are ignored             */
@@ -227,6 +230,29 @@ adamw_status adamw_ademamix_step(adamw_plan* plan, const float* lr_dev, int32_t*
                                  float beta1, float beta2, float beta3, float alpha, float eps,
                                  const float* grad_scale_dev, const float* found_inf_dev,
                                  void* stream);
+
+/*
+ * One Lion step over every tensor of the plan (fp32 and bf16+remainder
+ * modes; exp_avg_sq and exp_avg_slow, if the plan has them, are neither read
+ * nor written).  "Fix decoupled weight decay ordering in the CUDA
+ * Adam/AdEMAMix kernels" (bitsandbytes PR #2040), review of the 1-state
+ * kernels: Lion decays the parameter before its sign update.  The update is
+ * that of Chen et al., "Symbolic Discovery of Optimization Algorithms"
+ * (arXiv:2302.06675), with one state m and no bias correction:
+ *     c  = b1*m + (1-b1)*g
+ *     p' = p*(1 - lr*wd) - lr*sign(c)      sign(0) = sign(NaN) = 0
+ *     m' = b2*m + (1-b2)*g
+ * Float32 sequence, one rounding per operation: g = g_raw [* inv_scale];
+ * c = b1*m + fl(1-b1)*g; p' = p*fl(1 - fl(lr*wd)) - lr*sign(c);
+ * m' = b2*m + fl(1-b2)*g.  Reads p (+ rem), g, m and writes p (+ rem), m:
+ * 20 bytes per element with fp32 params and grads.
+ * lr_dev, step_dev, grad_scale_dev, found_inf_dev, skip and step counting as
+ * adamw_step (*step_dev advances although Lion has no bias correction).
+ * EINVAL for betas outside [0, 1); EUNSUPPORTED for Q8 plans.
+ */
+adamw_status adamw_lion_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev,
+                             float beta1, float beta2, const float* grad_scale_dev,
+                             const float* found_inf_dev, void* stream);
 
 /*
  * The AMP step in one launch ("FusedAdam & PyTorch Lightning AMP": the fused

@@ -40,7 +40,7 @@ def test_binding_wraps_every_declared_symbol():
 
 
 def test_abi_version():
-    assert C.adamw_abi_version() == 2
+    assert C.adamw_abi_version() == 3
 
 
 def test_default_maps_equal_oracle_maps():
@@ -96,3 +96,17 @@ def test_step_and_helpers_reject_bad_arguments_on_the_host():
 
 def test_plan_info_null():
     assert _status(lambda: C.adamw_plan_info(None)) == C.EINVAL
+
+
+def test_one_state_plans_are_checked_on_the_host():
+    no_v = C.adamw_tensor(0x10000, None, 0x110000, 0x210000, None, None, None, 1024, 0.0)
+    # exp_avg_sq on some tensors but not all
+    assert _status(lambda: C.adamw_plan_create([no_v, _t(base=0x400000)], C.MODE_FP32, C.F32)) == C.EINVAL
+    assert "exp_avg_sq" in C.adamw_last_error()
+    # Q8 always needs v
+    q = C.adamw_tensor(0x10000, None, 0x110000, 0x210000, None, 0x310000, 0x320000, 1024, 0.0)
+    assert _status(lambda: C.adamw_plan_create([q], C.MODE_Q8, C.F32)) == C.EINVAL
+    # AdEMAMix needs v
+    slow = C.adamw_tensor(0x10000, None, 0x110000, 0x210000, None, None, None, 1024, 0.0, 0x510000)
+    assert _status(lambda: C.adamw_plan_create([slow], C.MODE_FP32, C.F32)) == C.EINVAL
+    assert _status(lambda: C.adamw_lion_step(None, 0x100, 0x200, 0.9, 0.99, None, None, None)) == C.EINVAL
