@@ -13,6 +13,7 @@ adamw      decoupled-weight-decay AdamW step, fp64 definition and a strict-fp32
            found_inf skip included).
 ademamix   AdEMAMix (fast and slow EMA) with the same decoupled decay, both modes.
 lion       Lion (sign update, one state) with decay before the update, both modes.
+coupled    momentum, RMSprop and Adagrad (one state) with coupled L2 decay, both modes.
 remainder  fp32 master <-> (bf16 model param, int16 remainder) split and join.
 qmap       the dynamic-exponent 8-bit code maps, their decision thresholds and
            nearest-code quantisation.
@@ -25,4 +26,4 @@ the contents of the 8-bit code maps (``qmap.signed_map`` /
 invariants and the quantiser built on top of it are pinned.
 """
 
-from . import adamw, ademamix, lion, remainder, qmap, q8  # noqa: F401
+from . import adamw, ademamix, coupled, lion, remainder, qmap, q8  # noqa: F401
