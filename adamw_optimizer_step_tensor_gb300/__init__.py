@@ -13,7 +13,7 @@ from __future__ import annotations
 from . import _capi
 from ._capi import (  # noqa: F401
     AdamWError, adamw_abi_version, adamw_ademamix_step, adamw_bf16rem_join, adamw_bf16rem_split,
-    adamw_lion_step,
+    adamw_coupled_step, adamw_lion_step,
     adamw_check_nonfinite, adamw_last_error, adamw_lr_from_table, adamw_plan_create,
     adamw_plan_destroy,
     adamw_plan_info, adamw_plan_status, adamw_q8_default_maps, adamw_q8_dequant, adamw_q8_quant,
@@ -51,8 +51,8 @@ class FusedAdamW:
                      ``absmax_m`` / ``absmax_v`` float32 [ceil(numel/256)].
     Grads: float32, float16 or bfloat16, one dtype for the whole list.
     ``weight_decays``: one float per tensor.
-    ``exp_avg_sqs=None`` (fp32 / bf16_rem only) makes a plan for ``step_lion``
-    alone.
+    ``exp_avg_sqs=None`` (fp32 / bf16_rem only) makes a plan for the 1-state
+    steps ``step_lion`` and ``step_coupled`` alone.
     """
 
     def __init__(self, params, grads, exp_avgs, exp_avg_sqs, weight_decays, *, mode="fp32",
@@ -134,6 +134,13 @@ class FusedAdamW:
         betas = (b1, b2); exp_avg_sqs are not touched."""
         adamw_lion_step(self.plan, _ptr(lr), _ptr(step), float(betas[0]), float(betas[1]),
                         _ptr(grad_scale), _ptr(found_inf), _stream(stream))
+
+    def step_coupled(self, rule, lr, step, *, beta=0.9, eps=1e-8, grad_scale=None, found_inf=None,
+                     stream=None) -> None:
+        """Momentum SGD, RMSprop or Adagrad (``rule``) with coupled L2 decay;
+        exp_avgs hold the one state, exp_avg_sqs are not touched."""
+        adamw_coupled_step(self.plan, _capi.RULES[rule], _ptr(lr), _ptr(step), float(beta),
+                           float(eps), _ptr(grad_scale), _ptr(found_inf), _stream(stream))
 
     def step_amp(self, lr, step, found_inf, *, betas=(0.9, 0.999), eps=1e-8, grad_scale=None,
                  stream=None) -> None:

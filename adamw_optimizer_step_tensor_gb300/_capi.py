@@ -69,6 +69,8 @@ _SIGNATURES = {
     "adamw_step_amp": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_float, ctypes.c_float, ctypes.c_float,
                                       _vp, _vp, _vp]),
     "adamw_lion_step": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_float, ctypes.c_float, _vp, _vp, _vp]),
+    "adamw_coupled_step": (ctypes.c_int, [_vp, ctypes.c_int, _vp, _vp, ctypes.c_float, ctypes.c_float,
+                                          _vp, _vp, _vp]),
     "adamw_bf16rem_split": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int64, _vp]),
     "adamw_bf16rem_join": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int64, _vp]),
     "adamw_q8_default_maps": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float),
@@ -185,6 +187,16 @@ def adamw_lion_step(plan: int, lr_dev: int, step_dev: int, beta1: float, beta2: 
                     grad_scale_dev: int | None, found_inf_dev: int | None, stream: int | None) -> None:
     _check(load().adamw_lion_step(plan, lr_dev, step_dev, beta1, beta2, grad_scale_dev,
                                   found_inf_dev, stream))
+
+
+RULES = {"momentum": 0, "rmsprop": 1, "adagrad": 2}
+
+
+def adamw_coupled_step(plan: int, rule: int, lr_dev: int, step_dev: int, beta: float, eps: float,
+                       grad_scale_dev: int | None, found_inf_dev: int | None,
+                       stream: int | None) -> None:
+    _check(load().adamw_coupled_step(plan, rule, lr_dev, step_dev, beta, eps, grad_scale_dev,
+                                     found_inf_dev, stream))
 
 
 def adamw_step_amp(plan: int, lr_dev: int, step_dev: int, beta1: float, beta2: float, eps: float,

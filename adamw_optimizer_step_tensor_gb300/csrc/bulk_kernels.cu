@@ -1,5 +1,5 @@
-// bulk_kernels.cu -- the fp32 and bf16+remainder steps (AdamW, AdEMAMix, Lion)
-// with bulk-async staging.
+// bulk_kernels.cu -- the fp32 and bf16+remainder steps (AdamW, AdEMAMix, Lion,
+// and momentum / RMSprop / Adagrad with coupled L2) with bulk-async staging.
 //
 // One CTA per SM: a producer warp streams each 2048-element tile of every
 // input (p [+ remainder], g, m, v) into a ring of shared-memory stages with
@@ -78,7 +78,7 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
 // (AdEMAMix) -- each kTile elements.
 template <adamw_mode MODE, typename GT, int ALGO>
 struct Stage {
-  static constexpr bool kV = ALGO != kAlgoLion;
+  static constexpr bool kV = algo_two_state(ALGO);
   static constexpr bool kM2 = ALGO == kAlgoAdemamix;
   static constexpr int kP = MODE == ADAMW_MODE_FP32 ? 4 : 2;
   static constexpr int kG = sizeof(GT);
@@ -99,6 +99,13 @@ struct Stage {
 // stages moved 98% of the copy bandwidth; 8 warps x 6 stages 91%, 16 x 4-5
 // stages 97%, 24-30 warps 96-97%.
 template <int MODE> struct BulkTune { static constexpr int stages = 3; };
+// Resident CTAs per SM the register budget targets.  RMSprop and Adagrad do a
+// square root and a division for every 20 bytes (fp32) and hide their latency
+// with two CTAs per SM (GPT-2 list: 0.448 -> 0.403 ms); Lion and momentum,
+// without them, run faster at one (0.371 vs 0.384 ms).
+template <int ALGO> struct AlgoTune {
+  static constexpr int ctas = (ALGO == kAlgoRmsprop || ALGO == kAlgoAdagrad) ? 2 : 1;
+};
 
 template <adamw_mode MODE, typename GT, int ALGO>
 constexpr int bulk_smem_bytes() {
@@ -208,7 +215,7 @@ __device__ __forceinline__ void store4(const TensorDesc& td, int64_t e, const fl
 }
 
 template <adamw_mode MODE, typename GT, int ALGO>
-__global__ void __launch_bounds__(kBulkThreads, 1) step_bulk_kernel(const StepArgs a) {
+__global__ void __launch_bounds__(kBulkThreads, AlgoTune<ALGO>::ctas) step_bulk_kernel(const StepArgs a) {
   using L = Stage<MODE, GT, ALGO>;
   constexpr int S = BulkTune<MODE>::stages;
   extern __shared__ __align__(128) unsigned char smem_raw[];
@@ -250,7 +257,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1) step_bulk_kernel(const StepAr
   for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
     const Chunk ch = a.chunks[c];
     const TensorDesc td = a.tensors[ch.tensor];
-    const float decay = __fsub_rn(1.0f, __fmul_rn(s.lr, td.wd));
+    // the parameter's decay factor; the coupled rules take wd itself
+    const float decay = algo_coupled(ALGO) ? td.wd : __fsub_rn(1.0f, __fmul_rn(s.lr, td.wd));
     for (int k = 0; k * kTile < ch.len; ++k, ++i) {
       const uint32_t st_i = i % S;
       if (!mbar_wait(&full[st_i], (i / S) & 1u)) {
@@ -267,7 +275,10 @@ __global__ void __launch_bounds__(kBulkThreads, 1) step_bulk_kernel(const StepAr
         if (j + 4 <= nb) {
           float p[4], g[4], m[4], v[4];
           load4_smem<MODE, GT, ALGO>(st, j, p, g, m, v);
-          if (ALGO == kAlgoAdemamix) {
+          if (algo_coupled(ALGO)) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) update_coupled<ALGO>(p[q], g[q], m[q], s, decay);
+          } else if (ALGO == kAlgoAdemamix) {
             const float4 w = *reinterpret_cast<const float4*>(st + L::oM2 + j * 4);
             float m2[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -305,18 +316,36 @@ cudaError_t prepare_one() {
                               bulk_smem_bytes<MODE, GT, ALGO>());
 }
 
+template <adamw_mode MODE, typename GT, int ALGO>
+cudaError_t occupancy_one(int* blocks) {
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks, step_bulk_kernel<MODE, GT, ALGO>,
+                                                       kBulkThreads, bulk_smem_bytes<MODE, GT, ALGO>());
+}
+
 template <adamw_mode MODE, typename GT>
 cudaError_t launch_algo(const StepArgs& a, int grid, cudaStream_t st, int algo) {
-  if (algo == kAlgoAdemamix) return launch_one<MODE, GT, kAlgoAdemamix>(a, grid, st);
-  if (algo == kAlgoLion) return launch_one<MODE, GT, kAlgoLion>(a, grid, st);
-  return launch_one<MODE, GT, kAlgoAdamW>(a, grid, st);
+  switch (algo) {
+    case kAlgoAdamW: return launch_one<MODE, GT, kAlgoAdamW>(a, grid, st);
+    case kAlgoAdemamix: return launch_one<MODE, GT, kAlgoAdemamix>(a, grid, st);
+    case kAlgoLion: return launch_one<MODE, GT, kAlgoLion>(a, grid, st);
+    case kAlgoMomentum: return launch_one<MODE, GT, kAlgoMomentum>(a, grid, st);
+    case kAlgoRmsprop: return launch_one<MODE, GT, kAlgoRmsprop>(a, grid, st);
+    case kAlgoAdagrad: return launch_one<MODE, GT, kAlgoAdagrad>(a, grid, st);
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <adamw_mode MODE, typename GT>
 cudaError_t prepare_algo(int algo) {
-  if (algo == kAlgoAdemamix) return prepare_one<MODE, GT, kAlgoAdemamix>();
-  if (algo == kAlgoLion) return prepare_one<MODE, GT, kAlgoLion>();
-  return prepare_one<MODE, GT, kAlgoAdamW>();
+  switch (algo) {
+    case kAlgoAdamW: return prepare_one<MODE, GT, kAlgoAdamW>();
+    case kAlgoAdemamix: return prepare_one<MODE, GT, kAlgoAdemamix>();
+    case kAlgoLion: return prepare_one<MODE, GT, kAlgoLion>();
+    case kAlgoMomentum: return prepare_one<MODE, GT, kAlgoMomentum>();
+    case kAlgoRmsprop: return prepare_one<MODE, GT, kAlgoRmsprop>();
+    case kAlgoAdagrad: return prepare_one<MODE, GT, kAlgoAdagrad>();
+  }
+  return cudaErrorInvalidValue;
 }
 
 template <typename GT>
@@ -370,6 +399,22 @@ cudaError_t launch_step_bulk(adamw_mode mode, adamw_dtype gdt, const StepArgs& a
     case ADAMW_F32: return launch_bulk_mode<float>(mode, a, grid, s, algo);
     case ADAMW_F16: return launch_bulk_mode<__half>(mode, a, grid, s, algo);
     case ADAMW_BF16: return launch_bulk_mode<__nv_bfloat16>(mode, a, grid, s, algo);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t bulk_occupancy_sqrt_div(adamw_mode mode, adamw_dtype gdt, int* blocks) {
+  const bool f = mode == ADAMW_MODE_FP32;
+  switch (gdt) {
+    case ADAMW_F32:
+      return f ? occupancy_one<ADAMW_MODE_FP32, float, kAlgoRmsprop>(blocks)
+               : occupancy_one<ADAMW_MODE_BF16_REM, float, kAlgoRmsprop>(blocks);
+    case ADAMW_F16:
+      return f ? occupancy_one<ADAMW_MODE_FP32, __half, kAlgoRmsprop>(blocks)
+               : occupancy_one<ADAMW_MODE_BF16_REM, __half, kAlgoRmsprop>(blocks);
+    case ADAMW_BF16:
+      return f ? occupancy_one<ADAMW_MODE_FP32, __nv_bfloat16, kAlgoRmsprop>(blocks)
+               : occupancy_one<ADAMW_MODE_BF16_REM, __nv_bfloat16, kAlgoRmsprop>(blocks);
   }
   return cudaErrorInvalidValue;
 }

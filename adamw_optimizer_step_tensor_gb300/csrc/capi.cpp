@@ -40,6 +40,7 @@ struct adamw_plan {
   int grid_fused = 0;
   bool has_slow = false;       // every tensor carries an AdEMAMix slow EMA
   bool has_v = true;           // every tensor carries exp_avg_sq (false: Lion-only plan)
+  int grid_sqrt_div = 1;       // grid of the RMSprop / Adagrad kernels (2 CTAs per SM)
 };
 
 namespace {
@@ -195,13 +196,17 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
   if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-  int bps = 0, smem = 0;
+  int bps = 0, smem = 0, bps_sd = 1;
   const bool bulk = kUseBulk && mode != ADAMW_MODE_Q8;
   if (bulk) {
-    e = prepare_step_bulk(mode, grad_dtype, kAlgoLion);
+    e = cudaSuccess;
+    for (int algo : {kAlgoLion, kAlgoMomentum, kAlgoRmsprop, kAlgoAdagrad})
+      if (e == cudaSuccess) e = prepare_step_bulk(mode, grad_dtype, algo);
     if (e == cudaSuccess && (with_v || !sized)) e = prepare_step_bulk(mode, grad_dtype, kAlgoAdamW);
     if (e == cudaSuccess && with_slow) e = prepare_step_bulk(mode, grad_dtype, kAlgoAdemamix);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bulk step)");
+    e = bulk_occupancy_sqrt_div(mode, grad_dtype, &bps_sd);
+    if (e != cudaSuccess) return cuda_fail(e, "occupancy of the RMSprop/Adagrad step");
     bps = 1;
   } else {
     e = step_occupancy(mode, grad_dtype, &bps, &smem);
@@ -228,6 +233,9 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
   p->has_v = with_v != 0 || sized == 0;
   const int64_t resident = static_cast<int64_t>(bps) * sms;
   p->grid = static_cast<int>(p->n_chunks < resident ? (p->n_chunks > 0 ? p->n_chunks : 1) : resident);
+  const int64_t res_sd = static_cast<int64_t>(bps_sd < 1 ? 1 : bps_sd) * sms;
+  p->grid_sqrt_div =
+      static_cast<int>(p->n_chunks < res_sd ? (p->n_chunks > 0 ? p->n_chunks : 1) : res_sd);
   const int64_t check_res = 8LL * sms;
   p->grid_check = static_cast<int>(p->n_chunks < check_res ? (p->n_chunks > 0 ? p->n_chunks : 1) : check_res);
 
@@ -466,6 +474,51 @@ adamw_status adamw_lion_step(adamw_plan* plan, const float* lr_dev, int32_t* ste
   cudaError_t e = launch_step_bulk(plan->mode, plan->gdt, a, plan->grid,
                                    static_cast<cudaStream_t>(stream), kAlgoLion);
   if (e != cudaSuccess) return cuda_fail(e, "launch Lion step");
+  return ADAMW_OK;
+}
+
+adamw_status adamw_coupled_step(adamw_plan* plan, adamw_coupled_rule rule, const float* lr_dev,
+                                int32_t* step_dev, float beta, float eps,
+                                const float* grad_scale_dev, const float* found_inf_dev,
+                                void* stream) {
+  if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
+  int algo;
+  switch (rule) {
+    case ADAMW_RULE_MOMENTUM: algo = kAlgoMomentum; break;
+    case ADAMW_RULE_RMSPROP: algo = kAlgoRmsprop; break;
+    case ADAMW_RULE_ADAGRAD: algo = kAlgoAdagrad; break;
+    default: return fail(ADAMW_EINVAL, "unknown coupled rule %d", (int)rule);
+  }
+  if (plan->mode == ADAMW_MODE_Q8)
+    return fail(ADAMW_EUNSUPPORTED, "the coupled rules cover the fp32 and bf16+remainder modes");
+  if (!lr_dev || !step_dev) return fail(ADAMW_EINVAL, "lr_dev and step_dev must be set");
+  if (!aligned(lr_dev, 4) || !aligned(step_dev, 4) || !aligned(grad_scale_dev, 4) ||
+      !aligned(found_inf_dev, 4))
+    return fail(ADAMW_EALIGN, "a scalar pointer is not 4-byte aligned");
+  if (!(beta >= 0.0f && beta < 1.0f)) return fail(ADAMW_EINVAL, "beta must lie in [0, 1)");
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(ADAMW_EINVAL, "eps must be finite and >= 0");
+  adamw_status st = check_device(plan);
+  if (st != ADAMW_OK) return st;
+  StepArgs a;
+  a.tensors = plan->d_tensors;
+  a.chunks = plan->d_chunks;
+  a.n_chunks = plan->n_chunks;
+  a.lr = lr_dev;
+  a.step = step_dev;
+  a.grad_scale = grad_scale_dev;
+  a.found_inf = found_inf_dev;
+  a.beta1 = rule == ADAMW_RULE_ADAGRAD ? 0.0f : beta;
+  a.beta2 = 0.0f;
+  a.eps = eps;
+  a.beta3 = 0.0f;
+  a.alpha = 0.0f;
+  a.scratch = plan->d_scratch;
+  a.qt = nullptr;
+  a.refine = 1;
+  const int grid = algo == kAlgoMomentum ? plan->grid : plan->grid_sqrt_div;
+  cudaError_t e = launch_step_bulk(plan->mode, plan->gdt, a, grid,
+                                   static_cast<cudaStream_t>(stream), algo);
+  if (e != cudaSuccess) return cuda_fail(e, "launch coupled-L2 step");
   return ADAMW_OK;
 }
 

@@ -51,6 +51,11 @@ constexpr int kMaxRefine = 4;                // thresholds compared per lookup, 
 constexpr int kAlgoAdamW = 0;
 constexpr int kAlgoAdemamix = 1;
 constexpr int kAlgoLion = 2;
+constexpr int kAlgoMomentum = 3;  // coupled L2, one state
+constexpr int kAlgoRmsprop = 4;
+constexpr int kAlgoAdagrad = 5;
+__host__ __device__ constexpr bool algo_two_state(int algo) { return algo == kAlgoAdamW || algo == kAlgoAdemamix; }
+__host__ __device__ constexpr bool algo_coupled(int algo) { return algo >= kAlgoMomentum; }
 
 struct TensorDesc {
   void* p;            // fp32 or bf16 param
@@ -146,6 +151,9 @@ cudaError_t step_occupancy(adamw_mode mode, adamw_dtype gdt, int* blocks_per_sm,
 cudaError_t launch_step_bulk(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int grid,
                              cudaStream_t s, int algo);
 cudaError_t prepare_step_bulk(adamw_mode mode, adamw_dtype gdt, int algo);
+// Resident CTAs per SM of the RMSprop / Adagrad bulk kernels (one footprint);
+// call after prepare_step_bulk.
+cudaError_t bulk_occupancy_sqrt_div(adamw_mode mode, adamw_dtype gdt, int* blocks);
 cudaError_t run_wait_selftest(int limit_us, cudaStream_t s, uint32_t* fault_bits,
                               double* waited_ms);
 cudaError_t launch_nonfinite(adamw_dtype gdt, const TensorDesc* tensors, const Chunk* chunks,

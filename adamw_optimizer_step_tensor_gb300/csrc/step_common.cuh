@@ -132,6 +132,25 @@ __device__ __forceinline__ void update_lion(float& p, float g, float& m, const S
   m = __fadd_rn(__fmul_rn(s.b2, m), __fmul_rn(s.omb2, g));
 }
 
+// Momentum, RMSprop and Adagrad: the decay joins the (unscaled) grad as
+// g + p*wd when wd > 0 (coupled L2); one state st, no bias correction.
+template <int ALGO>
+__device__ __forceinline__ void update_coupled(float& p, float g, float& st, const Scal& s,
+                                               float wd) {
+  if (s.scaled) g = __fmul_rn(g, s.inv_scale);
+  if (wd > 0.0f) g = __fadd_rn(g, __fmul_rn(p, wd));
+  float d;
+  if (ALGO == kAlgoMomentum) {
+    st = __fadd_rn(__fmul_rn(s.b1, st), g);
+    d = st;
+  } else {
+    st = ALGO == kAlgoRmsprop ? __fadd_rn(__fmul_rn(s.b1, st), __fmul_rn(s.omb1, __fmul_rn(g, g)))
+                              : __fadd_rn(st, __fmul_rn(g, g));
+    d = __fdiv_rn(g, __fadd_rn(__fsqrt_rn(st), s.eps));
+  }
+  p = __fsub_rn(p, __fmul_rn(s.lr, d));
+}
+
 // ---------------------------------------------------------------- loads/stores
 __device__ __forceinline__ void ld8f(const float* q, float (&x)[8]) {
   const float4 a = __ldcs(reinterpret_cast<const float4*>(q));
@@ -219,8 +238,10 @@ __device__ void update_scalar(const TensorDesc& td, int64_t e, int n, const Scal
     const int64_t k = e + i;
     float p = MODE == ADAMW_MODE_FP32 ? pf[k] : rem_join(ph[k], static_cast<uint16_t>(td.rem[k]));
     float m = mf[k];
-    float v = ALGO == kAlgoLion ? 0.0f : vf[k];
-    if (ALGO == kAlgoAdemamix) {
+    float v = algo_two_state(ALGO) ? vf[k] : 0.0f;
+    if (algo_coupled(ALGO)) {
+      update_coupled<ALGO>(p, Grad<GT>::load1(td.g, k), m, s, decay);
+    } else if (ALGO == kAlgoAdemamix) {
       float* const m2f = static_cast<float*>(td.m2);
       float m2 = m2f[k];
       update_ademamix(p, Grad<GT>::load1(td.g, k), m, m2, v, s, decay);
@@ -239,7 +260,7 @@ __device__ void update_scalar(const TensorDesc& td, int64_t e, int n, const Scal
       td.rem[k] = static_cast<int16_t>(static_cast<uint16_t>(r));
     }
     mf[k] = m;
-    if (ALGO != kAlgoLion) vf[k] = v;
+    if (algo_two_state(ALGO)) vf[k] = v;
   }
 }
 

@@ -50,7 +50,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gpt2_small",
                     choices=["gpt2_small", "single", "amp", "amp_fused", "q8", "llama3_8b", "bf16rem",
-                             "ademamix_gpt2", "lion_gpt2"])
+                             "ademamix_gpt2", "lion_gpt2", "momentum_gpt2", "rmsprop_gpt2",
+                             "adagrad_gpt2"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -268,6 +269,17 @@ def cpu_sample_lion(n):
     return run, f"{n} elements per step, float64 Lion oracle (oracle.lion.step_fp64)"
 
 
+def cpu_sample_coupled(n, rule):
+    import numpy as np
+    from oracle import coupled as OC
+    rng = np.random.default_rng(0)
+    x = OC.Tensor(p=rng.normal(0, 0.02, n), g=rng.normal(0, 1e-3, n), s=np.zeros(n), wd=0.1)
+
+    def run():
+        OC.step_fp64([x], rule=rule, lr=1e-3, beta=0.9, eps=1e-8)
+    return run, f"{n} elements per step, float64 {rule} oracle (oracle.coupled.step_fp64)"
+
+
 CPU_SAMPLES = {
     "gpt2_small": lambda n: cpu_sample_fp32(n),
     "single": lambda n: cpu_sample_fp32(n, lr=0.1),
@@ -278,6 +290,9 @@ CPU_SAMPLES = {
     "bf16rem": cpu_sample_bf16rem,
     "ademamix_gpt2": lambda n: cpu_sample_ademamix(n),
     "lion_gpt2": lambda n: cpu_sample_lion(n),
+    "momentum_gpt2": lambda n: cpu_sample_coupled(n, "momentum"),
+    "rmsprop_gpt2": lambda n: cpu_sample_coupled(n, "rmsprop"),
+    "adagrad_gpt2": lambda n: cpu_sample_coupled(n, "adagrad"),
 }
 
 # ----------------------------------------------------------------------------- workloads
@@ -477,6 +492,29 @@ class LionGpt2(Gpt2Small):
                                None, None, stream)
 
 
+class CoupledGpt2(LionGpt2):
+    """The GPT-2-small list stepped with momentum SGD, RMSprop or Adagrad (coupled
+    L2; one fp32 state, no v: 20 B/element)."""
+    bytes_per_param = 20.0
+
+    def __init__(self, rule, seed=0):
+        super().__init__(seed)
+        self.rule = rule
+        self.rule_id = self.C.RULES[rule]
+        self.name = f"{rule}_gpt2_small_fp32"
+        self.config = dict(self.config, workload=f"gpt2_small fp32 param list, {rule} with coupled L2 "
+                           "(one state), cosine lr from a device table")
+        self.e2e_what = self.e2e_what.replace("adamw_lion_step", "adamw_coupled_step")
+
+    def step(self, i):
+        self.C.adamw_coupled_step(self.opt.plan, self.rule_id, self.lr_ptrs[i % 100],
+                                  self.step_dev.data_ptr(), 0.9, 1e-8, None, None, self.stream)
+
+    def _group_step(self, opt, i, step_dev, stream):
+        self.C.adamw_coupled_step(opt.plan, self.rule_id, self.lr_ptrs[i % 100], step_dev.data_ptr(),
+                                  0.9, 1e-8, None, None, stream)
+
+
 class Single(Workload):
     name = "single_fp32_1M_l2flush"
     bytes_per_param = 28.0
@@ -672,7 +710,10 @@ def make_workload(name, numel=0):
             "amp_fused": lambda: Single(amp=True, numel=numel, fused=True),
             "llama3_8b": lambda: Llama3(), "bf16rem": lambda: Bf16Rem(numel=numel),
             "ademamix_gpt2": lambda: AdemamixGpt2(),
-            "lion_gpt2": lambda: LionGpt2()}[name]()
+            "lion_gpt2": lambda: LionGpt2(),
+            "momentum_gpt2": lambda: CoupledGpt2("momentum"),
+            "rmsprop_gpt2": lambda: CoupledGpt2("rmsprop"),
+            "adagrad_gpt2": lambda: CoupledGpt2("adagrad")}[name]()
 
 
 # ----------------------------------------------------------------------------- CPU timing

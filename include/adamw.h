@@ -91,8 +91,9 @@ typedef struct {
   void* exp_avg;        /* m: fp32 [numel]; uint8 codes [numel] in Q8 mode    */
   void* exp_avg_sq;     /* v: fp32 [numel]; uint8 codes [numel] in Q8 mode.
                            May be NULL on every tensor of an fp32 or
-                           bf16+remainder plan: such a plan runs only
-                           adamw_lion_step (the others return EINVAL)        */
+                           bf16+remainder plan: such a plan runs only the
+                           1-state steps adamw_lion_step and
+                           adamw_coupled_step (the others return EINVAL)     */
   float* absmax_m;      /* Q8: fp32 [ceil(numel/256)]; otherwise NULL         */
   float* absmax_v;      /* Q8: fp32 [ceil(numel/256)]; otherwise NULL         */
   int64_t numel;        /* >= 0; tensors with numel 0 are ignored             */
@@ -253,6 +254,38 @@ adamw_status adamw_ademamix_step(adamw_plan* plan, const float* lr_dev, int32_t*
 adamw_status adamw_lion_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev,
                              float beta1, float beta2, const float* grad_scale_dev,
                              const float* found_inf_dev, void* stream);
+
+/* The 1-state rules with coupled L2 decay (adamw_coupled_step). */
+typedef enum {
+  ADAMW_RULE_MOMENTUM = 0, /* s = b*s + g;            p -= lr*s                    */
+  ADAMW_RULE_RMSPROP = 1,  /* s = b*s + (1-b)*g*g;    p -= lr*g/(sqrt(s) + eps)    */
+  ADAMW_RULE_ADAGRAD = 2   /* s = s + g*g;            p -= lr*g/(sqrt(s) + eps)    */
+} adamw_coupled_rule;
+
+/*
+ * One step of momentum SGD, RMSprop or Adagrad over every tensor of the plan
+ * (fp32 and bf16+remainder modes), with exp_avg as the one state s; exp_avg_sq
+ * and exp_avg_slow, if present, are not touched.  "Fix decoupled weight decay
+ * ordering in the CUDA Adam/AdEMAMix kernels" (bitsandbytes PR #2040), review
+ * of the 1-state kernels: these rules fold the decay into the grad,
+ * g = g + p*wd when wd > 0 (coupled L2; a tensor with wd <= 0 gets none), and
+ * never decay the parameter directly.  The update formulas are the rules'
+ * textbook forms (as torch.optim's SGD with momentum and no dampening,
+ * RMSprop without centring, Adagrad without lr decay); no bias correction;
+ * the momentum state starting at 0 makes its first step s = g.
+ * Float32 sequence, one rounding per operation: g = g_raw [* inv_scale];
+ * g = g + p*wd (wd > 0); s' as in the enum above with fl(1-b) for RMSprop;
+ * d = s' (momentum) or g / (sqrt(s') + eps); p' = p - lr*d.
+ * beta: the momentum or the RMSprop smoothing constant, in [0, 1) (ignored by
+ * Adagrad); eps finite and >= 0 (unused by momentum).  20 bytes per element
+ * with fp32 params and grads.  lr_dev, step_dev, grad_scale_dev,
+ * found_inf_dev, skip and step counting as adamw_step.  EINVAL for an unknown
+ * rule, EUNSUPPORTED for Q8 plans.
+ */
+adamw_status adamw_coupled_step(adamw_plan* plan, adamw_coupled_rule rule, const float* lr_dev,
+                                int32_t* step_dev, float beta, float eps,
+                                const float* grad_scale_dev, const float* found_inf_dev,
+                                void* stream);
 
 /*
  * The AMP step in one launch ("FusedAdam & PyTorch Lightning AMP": the fused

@@ -110,3 +110,8 @@ def test_one_state_plans_are_checked_on_the_host():
     slow = C.adamw_tensor(0x10000, None, 0x110000, 0x210000, None, None, None, 1024, 0.0, 0x510000)
     assert _status(lambda: C.adamw_plan_create([slow], C.MODE_FP32, C.F32)) == C.EINVAL
     assert _status(lambda: C.adamw_lion_step(None, 0x100, 0x200, 0.9, 0.99, None, None, None)) == C.EINVAL
+
+
+def test_coupled_step_checks_on_the_host():
+    assert _status(lambda: C.adamw_coupled_step(None, 0, 0x100, 0x200, 0.9, 1e-8, None, None, None)) == C.EINVAL
+    assert C.RULES == {"momentum": 0, "rmsprop": 1, "adagrad": 2}
