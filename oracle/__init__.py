@@ -18,12 +18,14 @@ remainder  fp32 master <-> (bf16 model param, int16 remainder) split and join.
 qmap       the dynamic-exponent 8-bit code maps, their decision thresholds and
            nearest-code quantisation.
 q8         the AdamW step with 8-bit blockwise-quantised moments.
+q4         the same step with 4-bit codes (two per byte) and 128-element blocks.
 
 Pins (what ties each function to something other than itself) live in
 ``tests/test_oracle_*.py``.  One function is **parity unpinned** by the pages:
-the contents of the 8-bit code maps (``qmap.signed_map`` /
-``qmap.unsigned_map``); the pages never print the map, so only its structural
+the contents of the 8-bit and 4-bit code maps (``qmap.signed_map`` /
+``qmap.unsigned_map``, ``qmap.signed_map4`` / ``qmap.unsigned_map4``); the pages never
+print a map, so only its structural
 invariants and the quantiser built on top of it are pinned.
 """
 
-from . import adamw, ademamix, coupled, lion, remainder, qmap, q8  # noqa: F401
+from . import adamw, ademamix, coupled, lion, remainder, qmap, q4, q8  # noqa: F401

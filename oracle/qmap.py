@@ -1,4 +1,4 @@
-"""8-bit dynamic-exponent code maps and nearest-code quantisation -- CPU oracle.
+"""8-bit and 4-bit code maps and nearest-code quantisation -- CPU oracle.
 
 Test infrastructure only.  **parity unpinned**: the pages never print the code
 map.  The bitsandbytes PR ("Fix decoupled weight decay ordering ...") only
@@ -25,6 +25,16 @@ Each value is the exact rational rounded once to the nearest float32; the 256
 values are sorted ascending and the code of a value is its index.  Exact 0
 makes an all-zero state quantise exactly (the first-step closed form of the
 bitsandbytes PR relies on that) and exact 1.0 keeps the block maximum exact.
+
+4-bit maps (**parity unpinned** too): the pages name torchao's AdamW4bit
+("4 bit Adam should support non constant lr"; the torchtitan job config of
+"Adam-mini <> DTensor") but print no format.  Reading taken: the format of
+Li, Chen, Zhu, "Memory Efficient Optimizers with 4-bit States" (NeurIPS
+2023), which that optimizer implements -- the first moment on the same
+dynamic tree at 4 bits (3 magnitude bits: E = 0..2, F = 2 - E, both signs,
+plus 0 and +1.0: 16 values), the second moment on the linear map without
+zero, k/16 for k = 1..16 (zero is left out because a v quantised to 0 turns
+the update into m/eps -- the paper's zero-point problem).
 
 Quantisation rule (also a reading: the pages are silent): the code of a
 float32 ``x`` is the index of the nearest map value, an exact tie going to the
@@ -54,9 +64,10 @@ def _round_to_f32(q: Fraction) -> np.float32:
     return F32(best[1])
 
 
-def _dynamic_values(frac_bits_at_e0: int, signed: bool) -> np.ndarray:
+def _dynamic_values(frac_bits_at_e0: int, signed: bool, n_exp: int = 7,
+                    size: int = 256) -> np.ndarray:
     vals = [Fraction(0), Fraction(1)]
-    for e in range(7):
+    for e in range(n_exp):
         f = frac_bits_at_e0 - e
         n = 2 ** f
         for k in range(n):
@@ -65,8 +76,8 @@ def _dynamic_values(frac_bits_at_e0: int, signed: bool) -> np.ndarray:
             if signed:
                 vals.append(-mag)
     out = np.array(sorted(_round_to_f32(q) for q in vals), dtype=F32)
-    if out.size != 256 or np.unique(out).size != 256:
-        raise AssertionError("code map must hold 256 distinct values")
+    if out.size != size or np.unique(out).size != size:
+        raise AssertionError(f"code map must hold {size} distinct values")
     return out
 
 
@@ -80,10 +91,27 @@ def unsigned_map() -> np.ndarray:
     return _dynamic_values(7, signed=False)
 
 
+def signed_map4() -> np.ndarray:
+    """16 sorted float32 values in [-1, 1] for the 4-bit first moment."""
+    return _dynamic_values(2, signed=True, n_exp=3, size=16)
+
+
+def unsigned_map4() -> np.ndarray:
+    """k/16 for k = 1..16 (no zero), the 4-bit second-moment map."""
+    return (np.arange(1, 17, dtype=np.float64) / 16).astype(F32)
+
+
 def zero_code(qmap: np.ndarray) -> int:
     """Index of the exact 0.0 entry."""
     (idx,) = np.nonzero(qmap == 0)
     return int(idx[0])
+
+
+def empty_block_code(qmap: np.ndarray) -> int:
+    """Code stored for an all-zero block (absmax 0): the zero entry, or code 0
+    for a map without one (it dequantises to 0 through the zero absmax)."""
+    (idx,) = np.nonzero(qmap == 0)
+    return int(idx[0]) if idx.size else 0
 
 
 def quantize_bruteforce(x: np.ndarray, qmap: np.ndarray) -> np.ndarray:
@@ -114,8 +142,8 @@ def thresholds(qmap: np.ndarray) -> np.ndarray:
     magnitude <= 1 whose exponents differ by fewer than 29 binades.
     """
     q = qmap.astype(np.float64)
-    out = np.empty(255, dtype=F32)
-    for k in range(255):
+    out = np.empty(q.size - 1, dtype=F32)
+    for k in range(q.size - 1):
         mid = (q[k] + q[k + 1]) / 2.0
         assert Fraction(mid) == (Fraction(q[k]) + Fraction(q[k + 1])) / 2
         c = F32(mid)
