@@ -13,14 +13,15 @@ from __future__ import annotations
 from . import _capi
 from ._capi import (  # noqa: F401
     AdamWError, adamw_abi_version, adamw_ademamix_step, adamw_bf16rem_join, adamw_bf16rem_split,
-    adamw_coupled_step, adamw_lion_step,
+    adamw_coupled_step, adamw_lion_step, adamw_q4_default_maps,
     adamw_check_nonfinite, adamw_last_error, adamw_lr_from_table, adamw_plan_create,
     adamw_plan_destroy,
     adamw_plan_info, adamw_plan_status, adamw_q8_default_maps, adamw_q8_dequant, adamw_q8_quant,
     adamw_q8_set_maps, adamw_step, adamw_step_amp, adamw_step_noalloc, adamw_wait_selftest,
 )
 
-MODES = {"fp32": _capi.MODE_FP32, "bf16_rem": _capi.MODE_BF16_REM, "q8": _capi.MODE_Q8}
+MODES = {"fp32": _capi.MODE_FP32, "bf16_rem": _capi.MODE_BF16_REM, "q8": _capi.MODE_Q8,
+         "q4": _capi.MODE_Q4}
 
 
 def _ptr(t) -> int | None:
@@ -49,6 +50,8 @@ class FusedAdamW:
     mode "bf16_rem": params bfloat16 + ``param_rems`` int16; states float32.
     mode "q8":       params float32; exp_avgs / exp_avg_sqs uint8 codes plus
                      ``absmax_m`` / ``absmax_v`` float32 [ceil(numel/256)].
+    mode "q4":       params float32; exp_avgs / exp_avg_sqs uint8 [ceil(numel/2)],
+                     two 4-bit codes per byte; absmax float32 [ceil(numel/128)].
     Grads: float32, float16 or bfloat16, one dtype for the whole list.
     ``weight_decays``: one float per tensor.
     ``exp_avg_sqs=None`` (fp32 / bf16_rem only) makes a plan for the 1-state
@@ -72,7 +75,7 @@ class FusedAdamW:
         avs = absmax_v if absmax_v is not None else [None] * n
         slows = exp_avg_slows if exp_avg_slows is not None else [None] * n
         pdt = torch.bfloat16 if mode == "bf16_rem" else torch.float32
-        sdt = torch.uint8 if mode == "q8" else torch.float32
+        sdt = torch.uint8 if mode in ("q8", "q4") else torch.float32
         gdt = grads[0].dtype if n else torch.float32
         recs = []
         for i in range(n):
@@ -85,16 +88,19 @@ class FusedAdamW:
                     raise TypeError(f"tensor {i}: {name} must be {dt}, got {t.dtype}")
                 if not t.is_contiguous() or t.device.type != "cuda":
                     raise ValueError(f"tensor {i}: {name} must be a contiguous CUDA tensor")
-                if t.numel() != p.numel():
-                    raise ValueError(f"tensor {i}: {name} has {t.numel()} elements, param {p.numel()}")
+                want = (p.numel() + 1) // 2 if (mode == "q4" and name in ("exp_avg", "exp_avg_sq")) \
+                    else p.numel()
+                if t.numel() != want:
+                    raise ValueError(f"tensor {i}: {name} has {t.numel()} elements, expected {want}")
             if mode == "bf16_rem" and (rems[i] is None or rems[i].dtype != torch.int16
                                        or rems[i].numel() != p.numel()):
                 raise TypeError(f"tensor {i}: bf16_rem mode needs an int16 remainder per element")
-            if mode == "q8":
-                nb = (p.numel() + _capi.Q8_BLOCK - 1) // _capi.Q8_BLOCK
+            if mode in ("q8", "q4"):
+                blk = _capi.Q8_BLOCK if mode == "q8" else _capi.Q4_BLOCK
+                nb = (p.numel() + blk - 1) // blk
                 for name, a in (("absmax_m", ams[i]), ("absmax_v", avs[i])):
                     if a is None or a.dtype != torch.float32 or a.numel() < nb:
-                        raise TypeError(f"tensor {i}: q8 mode needs {name} float32 [{nb}]")
+                        raise TypeError(f"tensor {i}: {mode} mode needs {name} float32 [{nb}]")
             if slows[i] is not None and (slows[i].dtype != torch.float32
                                          or slows[i].numel() != p.numel()):
                 raise TypeError(f"tensor {i}: exp_avg_slow must be float32 with one entry per element")

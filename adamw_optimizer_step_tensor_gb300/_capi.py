@@ -18,8 +18,9 @@ LIB_PATH = os.path.join(HERE, "_build", "libadamw.so")
 OK, EINVAL, EALIGN, EDTYPE, ENOMEM, ECUDA, EUNSUPPORTED, ETIMEOUT = range(8)
 STATUS_NAMES = ["OK", "EINVAL", "EALIGN", "EDTYPE", "ENOMEM", "ECUDA", "EUNSUPPORTED", "ETIMEOUT"]
 F32, F16, BF16 = 0, 1, 2
-MODE_FP32, MODE_BF16_REM, MODE_Q8 = 0, 1, 2
+MODE_FP32, MODE_BF16_REM, MODE_Q8, MODE_Q4 = 0, 1, 2, 3
 Q8_BLOCK = 256
+Q4_BLOCK = 128
 
 _vp = ctypes.c_void_p
 
@@ -73,6 +74,8 @@ _SIGNATURES = {
                                           _vp, _vp, _vp]),
     "adamw_bf16rem_split": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int64, _vp]),
     "adamw_bf16rem_join": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_int64, _vp]),
+    "adamw_q4_default_maps": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float),
+                                             ctypes.POINTER(ctypes.c_float)]),
     "adamw_q8_default_maps": (ctypes.c_int, [ctypes.POINTER(ctypes.c_float),
                                              ctypes.POINTER(ctypes.c_float)]),
     "adamw_q8_set_maps": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_float),
@@ -215,6 +218,13 @@ def adamw_bf16rem_split(master: int, bf16: int, rem: int, n: int, stream: int | 
 
 def adamw_bf16rem_join(bf16: int, rem: int, master: int, n: int, stream: int | None) -> None:
     _check(load().adamw_bf16rem_join(bf16, rem, master, n, stream))
+
+
+def adamw_q4_default_maps():
+    """Host call: returns (signed_map, unsigned_map) of the Q4 mode, two lists of 16 floats."""
+    s, u = (ctypes.c_float * 16)(), (ctypes.c_float * 16)()
+    _check(load().adamw_q4_default_maps(s, u))
+    return list(s), list(u)
 
 
 def adamw_q8_default_maps():

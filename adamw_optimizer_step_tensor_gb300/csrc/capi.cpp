@@ -12,8 +12,9 @@
 
 namespace adamw {
 void default_maps(float smap[256], float umap[256]);
-int build_qmap(const float value[256], QMapDev* out);
-int zero_code_of(const float value[256]);
+void default_maps4(float smap[16], float umap[16]);
+int build_qmap(const float* value, int n, QMapDev* out);
+int zero_code_of(const float* value, int n);
 }  // namespace adamw
 
 using namespace adamw;
@@ -67,8 +68,12 @@ size_t dtype_size(adamw_dtype d) { return d == ADAMW_F32 ? 4 : 2; }
 
 bool valid_dtype(int d) { return d == ADAMW_F32 || d == ADAMW_F16 || d == ADAMW_BF16; }
 bool valid_mode(int m) {
-  return m == ADAMW_MODE_FP32 || m == ADAMW_MODE_BF16_REM || m == ADAMW_MODE_Q8;
+  return m == ADAMW_MODE_FP32 || m == ADAMW_MODE_BF16_REM || m == ADAMW_MODE_Q8 ||
+         m == ADAMW_MODE_Q4;
 }
+
+// Modes whose moments are stored as codes with a per-block absmax.
+bool quantized(int m) { return m == ADAMW_MODE_Q8 || m == ADAMW_MODE_Q4; }
 
 void free_plan(adamw_plan* p) {
   if (!p) return;
@@ -90,15 +95,18 @@ adamw_status check_device(const adamw_plan* p) {
   return ADAMW_OK;
 }
 
-adamw_status build_qtables(const float smap[256], const float umap[256], QTables* qt) {
+// n = 256 (8-bit maps, both must contain 0.0) or 16 (the 4-bit maps; the v
+// map has no zero and an all-zero block stores code 0).
+adamw_status build_qtables(const float* smap, const float* umap, int n, QTables* qt) {
   std::memset(qt, 0, sizeof(QTables));
-  const int r0 = build_qmap(smap, &qt->map[0]);
-  const int r1 = build_qmap(umap, &qt->map[1]);
+  const int r0 = build_qmap(smap, n, &qt->map[0]);
+  const int r1 = build_qmap(umap, n, &qt->map[1]);
   if (r0 < 0 || r1 < 0)
-    return fail(ADAMW_EINVAL, "code maps must hold 256 strictly ascending finite floats "
-                              "whose neighbour sums are exact in float64");
-  qt->zero_code[0] = zero_code_of(smap);
-  qt->zero_code[1] = zero_code_of(umap);
+    return fail(ADAMW_EINVAL, "code maps must hold %d strictly ascending finite floats "
+                              "whose neighbour sums are exact in float64", n);
+  qt->zero_code[0] = zero_code_of(smap, n);
+  qt->zero_code[1] = zero_code_of(umap, n);
+  if (n == 16 && qt->zero_code[1] < 0) qt->zero_code[1] = 0;
   if (qt->zero_code[0] < 0 || qt->zero_code[1] < 0)
     return fail(ADAMW_EINVAL, "code maps must contain 0.0");
   const int r = r0 > r1 ? r0 : r1;
@@ -130,9 +138,9 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
   if (!valid_dtype(grad_dtype)) return fail(ADAMW_EDTYPE, "unknown grad dtype %d", (int)grad_dtype);
 
   const size_t psz = mode == ADAMW_MODE_BF16_REM ? 2 : 4;
-  const size_t ssz = mode == ADAMW_MODE_Q8 ? 1 : 4;
+  const size_t ssz = quantized(mode) ? 1 : 4;
   const size_t gsz = dtype_size(grad_dtype);
-  const size_t svec = mode == ADAMW_MODE_Q8 ? 8 : 16;
+  const size_t svec = mode == ADAMW_MODE_Q8 ? 8 : (mode == ADAMW_MODE_Q4 ? 4 : 16);
 
   std::vector<TensorDesc> td(static_cast<size_t>(n_tensors));
   std::vector<Chunk> chunks;
@@ -166,9 +174,9 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
     if (t.exp_avg_sq) ++with_v;
     if ((mode == ADAMW_MODE_BF16_REM) != (t.param_rem != nullptr))
       return fail(ADAMW_EINVAL, "tensor %d: param_rem must be set exactly in BF16_REM mode", i);
-    if ((mode == ADAMW_MODE_Q8) != (t.absmax_m != nullptr && t.absmax_v != nullptr) ||
-        (mode != ADAMW_MODE_Q8 && (t.absmax_m || t.absmax_v)))
-      return fail(ADAMW_EINVAL, "tensor %d: absmax_m/absmax_v must be set exactly in Q8 mode", i);
+    if (quantized(mode) != (t.absmax_m != nullptr && t.absmax_v != nullptr) ||
+        (!quantized(mode) && (t.absmax_m || t.absmax_v)))
+      return fail(ADAMW_EINVAL, "tensor %d: absmax_m/absmax_v must be set exactly in the Q8 and Q4 modes", i);
     if (!aligned(t.param, psz) || !aligned(t.grad, gsz) || !aligned(t.exp_avg, ssz) ||
         !aligned(t.exp_avg_sq, ssz) || (t.param_rem && !aligned(t.param_rem, 2)) ||
         (t.absmax_m && !aligned(t.absmax_m, 4)) || (t.absmax_v && !aligned(t.absmax_v, 4)))
@@ -180,13 +188,13 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
   }
   if (with_slow != 0 && with_slow != sized)
     return fail(ADAMW_EINVAL, "exp_avg_slow must be set on every tensor or on none");
-  if (with_slow && mode == ADAMW_MODE_Q8)
+  if (with_slow && quantized(mode))
     return fail(ADAMW_EUNSUPPORTED, "AdEMAMix slow states are supported in the fp32 and "
                                     "bf16+remainder modes");
   if (with_v != 0 && with_v != sized)
     return fail(ADAMW_EINVAL, "exp_avg_sq must be set on every tensor or on none");
-  if (sized && !with_v && mode == ADAMW_MODE_Q8)
-    return fail(ADAMW_EINVAL, "Q8 mode needs exp_avg_sq on every tensor");
+  if (sized && !with_v && quantized(mode))
+    return fail(ADAMW_EINVAL, "the Q8 and Q4 modes need exp_avg_sq on every tensor");
   if (sized && !with_v && with_slow)
     return fail(ADAMW_EINVAL, "an AdEMAMix plan needs exp_avg_sq on every tensor");
 
@@ -197,7 +205,7 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
   int bps = 0, smem = 0, bps_sd = 1;
-  const bool bulk = kUseBulk && mode != ADAMW_MODE_Q8;
+  const bool bulk = kUseBulk && !quantized(mode);
   if (bulk) {
     e = cudaSuccess;
     for (int algo : {kAlgoLion, kAlgoMomentum, kAlgoRmsprop, kAlgoAdagrad})
@@ -208,6 +216,9 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
     e = bulk_occupancy_sqrt_div(mode, grad_dtype, &bps_sd);
     if (e != cudaSuccess) return cuda_fail(e, "occupancy of the RMSprop/Adagrad step");
     bps = 1;
+  } else if (mode == ADAMW_MODE_Q4) {
+    e = q4_occupancy(grad_dtype, &bps, &smem);
+    if (e != cudaSuccess) return cuda_fail(e, "occupancy of the 4-bit step");
   } else {
     e = step_occupancy(mode, grad_dtype, &bps, &smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor");
@@ -252,7 +263,7 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
     return cuda_fail(e, "upload chunk table");
   if ((e = cudaMemset(p->d_scratch, 0, sizeof(StepScratch))) != cudaSuccess)
     return cuda_fail(e, "clear step scratch");
-  if (mode != ADAMW_MODE_Q8) {
+  if (!quantized(mode)) {
     int bpf = 0;
     if ((e = fused_occupancy(mode, grad_dtype, &bpf)) != cudaSuccess)
       return cuda_fail(e, "occupancy of the fused step");
@@ -274,11 +285,17 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
     if (fb && (e = cudaMemcpy(p->d_chunks_fused, fchunks.data(), fb, cudaMemcpyHostToDevice)) != cudaSuccess)
       return cuda_fail(e, "upload fused chunk table");
   }
-  if (mode == ADAMW_MODE_Q8) {
+  if (quantized(mode)) {
     std::unique_ptr<QTables> qt(new QTables);
     float smap[256], umap[256];
-    default_maps(smap, umap);
-    adamw_status st = build_qtables(smap, umap, qt.get());
+    int n = 256;
+    if (mode == ADAMW_MODE_Q4) {
+      default_maps4(smap, umap);
+      n = 16;
+    } else {
+      default_maps(smap, umap);
+    }
+    adamw_status st = build_qtables(smap, umap, n, qt.get());
     if (st != ADAMW_OK) return st;
     p->refine = qt->refine;
     if ((e = cudaMalloc(&p->d_qt, sizeof(QTables))) != cudaSuccess)
@@ -383,10 +400,10 @@ adamw_status adamw_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev
   a.scratch = plan->d_scratch;
   a.qt = plan->d_qt;
   a.refine = plan->refine;
-  cudaError_t e = plan->bulk ? launch_step_bulk(plan->mode, plan->gdt, a, plan->grid,
-                                                static_cast<cudaStream_t>(stream), kAlgoAdamW)
-                             : launch_step(plan->mode, plan->gdt, a, plan->grid,
-                                           static_cast<cudaStream_t>(stream));
+  cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+  cudaError_t e = plan->bulk ? launch_step_bulk(plan->mode, plan->gdt, a, plan->grid, st_, kAlgoAdamW)
+                  : plan->mode == ADAMW_MODE_Q4 ? launch_step_q4(plan->gdt, a, plan->grid, st_)
+                                                : launch_step(plan->mode, plan->gdt, a, plan->grid, st_);
   if (e != cudaSuccess) return cuda_fail(e, "launch adamw step");
   return ADAMW_OK;
 }
@@ -445,7 +462,7 @@ adamw_status adamw_lion_step(adamw_plan* plan, const float* lr_dev, int32_t* ste
                              float beta1, float beta2, const float* grad_scale_dev,
                              const float* found_inf_dev, void* stream) {
   if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
-  if (plan->mode == ADAMW_MODE_Q8)
+  if (quantized(plan->mode))
     return fail(ADAMW_EUNSUPPORTED, "Lion covers the fp32 and bf16+remainder modes");
   if (!lr_dev || !step_dev) return fail(ADAMW_EINVAL, "lr_dev and step_dev must be set");
   if (!aligned(lr_dev, 4) || !aligned(step_dev, 4) || !aligned(grad_scale_dev, 4) ||
@@ -489,7 +506,7 @@ adamw_status adamw_coupled_step(adamw_plan* plan, adamw_coupled_rule rule, const
     case ADAMW_RULE_ADAGRAD: algo = kAlgoAdagrad; break;
     default: return fail(ADAMW_EINVAL, "unknown coupled rule %d", (int)rule);
   }
-  if (plan->mode == ADAMW_MODE_Q8)
+  if (quantized(plan->mode))
     return fail(ADAMW_EUNSUPPORTED, "the coupled rules cover the fp32 and bf16+remainder modes");
   if (!lr_dev || !step_dev) return fail(ADAMW_EINVAL, "lr_dev and step_dev must be set");
   if (!aligned(lr_dev, 4) || !aligned(step_dev, 4) || !aligned(grad_scale_dev, 4) ||
@@ -534,7 +551,7 @@ adamw_status adamw_step_amp(adamw_plan* plan, const float* lr_dev, int32_t* step
   if (!(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f))
     return fail(ADAMW_EINVAL, "betas must lie in [0, 1)");
   if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(ADAMW_EINVAL, "eps must be finite and >= 0");
-  if (plan->mode == ADAMW_MODE_Q8)
+  if (quantized(plan->mode))
     return fail(ADAMW_EUNSUPPORTED, "the fused check + step covers the fp32 and bf16+remainder modes");
   if (!plan->has_v) return fail(ADAMW_EINVAL, "the plan's tensors carry no exp_avg_sq");
   adamw_status st = check_device(plan);
@@ -590,13 +607,19 @@ adamw_status adamw_q8_default_maps(float signed_map[256], float unsigned_map[256
   return ADAMW_OK;
 }
 
+adamw_status adamw_q4_default_maps(float signed_map[16], float unsigned_map[16]) {
+  if (!signed_map || !unsigned_map) return fail(ADAMW_EINVAL, "NULL output");
+  default_maps4(signed_map, unsigned_map);
+  return ADAMW_OK;
+}
+
 adamw_status adamw_q8_set_maps(adamw_plan* plan, const float signed_map[256],
                                const float unsigned_map[256]) {
   if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
   if (plan->mode != ADAMW_MODE_Q8 || !plan->d_qt) return fail(ADAMW_EINVAL, "plan is not in Q8 mode");
   if (!signed_map || !unsigned_map) return fail(ADAMW_EINVAL, "NULL map");
   std::unique_ptr<QTables> qt(new QTables);
-  adamw_status st = build_qtables(signed_map, unsigned_map, qt.get());
+  adamw_status st = build_qtables(signed_map, unsigned_map, 256, qt.get());
   if (st != ADAMW_OK) return st;
   cudaError_t e = cudaMemcpy(plan->d_qt, qt.get(), sizeof(QTables), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_fail(e, "upload code maps");

@@ -151,6 +151,9 @@ cudaError_t step_occupancy(adamw_mode mode, adamw_dtype gdt, int* blocks_per_sm,
 cudaError_t launch_step_bulk(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int grid,
                              cudaStream_t s, int algo);
 cudaError_t prepare_step_bulk(adamw_mode mode, adamw_dtype gdt, int algo);
+// 4-bit states (q4_kernels.cu).
+cudaError_t launch_step_q4(adamw_dtype gdt, const StepArgs& a, int grid, cudaStream_t s);
+cudaError_t q4_occupancy(adamw_dtype gdt, int* bps, int* smem);
 // Resident CTAs per SM of the RMSprop / Adagrad bulk kernels (one footprint);
 // call after prepare_step_bulk.
 cudaError_t bulk_occupancy_sqrt_div(adamw_mode mode, adamw_dtype gdt, int* blocks);

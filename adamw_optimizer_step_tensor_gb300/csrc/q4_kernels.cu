@@ -1,0 +1,185 @@
+// q4_kernels.cu -- the AdamW step with 4-bit blockwise-quantised moments.
+//
+// The 8-bit blockwise 2-state step of "Fix decoupled weight decay ordering in
+// the CUDA Adam/AdEMAMix kernels" (bitsandbytes PR #2040) with 4-bit codes:
+// dequantise m and v, run the strict-fp32 AdamW element update on the
+// unquantised values, then re-quantise m' and v' per block of 128 elements
+// (one fp32 absmax per block and per moment; nearest code, ties to the lower
+// code).  Two codes per byte, the even element in the low nibble.
+//
+// Layout of the work: as in the 8-bit kernel every lane owns 8 consecutive
+// elements of a 256-element warp span, so one half-warp owns one 128-element
+// block; its absmax is a 16-lane xor-shuffle maximum over float32 bit
+// patterns (exact and order-free).  The 8 codes of a lane are one 32-bit word.
+#include "step_common.cuh"
+
+namespace adamw {
+namespace {
+
+constexpr int kQ4Block = 128;
+constexpr int kQ4Span = 2 * kQ4Block;       // one warp: two blocks
+constexpr int kQ4MinBlocks = 4;             // resident CTAs per SM the registers target
+static_assert(16 * kVec == kQ4Block, "a half-warp holds one block");
+static_assert(kQBlock % kQ4Span == 0, "chunks start on whole warp spans");
+
+__device__ __forceinline__ uint32_t half_warp_max(uint32_t x) {
+#pragma unroll
+  for (int o = 8; o > 0; o >>= 1) x = max(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
+  return x;
+}
+
+__device__ __forceinline__ uint32_t pack_nibbles(const uint32_t (&q)[8]) {
+  uint32_t w = 0u;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) w |= q[i] << (4 * i);
+  return w;
+}
+
+template <typename GT, int R>
+__global__ void __launch_bounds__(kThreads, kQ4MinBlocks) step_q4_kernel(const StepArgs a) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  QTables& qt = *reinterpret_cast<QTables*>(smem_raw);
+  __shared__ Scal s_sc;
+  __shared__ int s_skip;
+  int t = 0;
+  if (threadIdx.x == 0) s_skip = prologue(a, s_sc, t);
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(a.qt);
+    uint4* dst = reinterpret_cast<uint4*>(smem_raw);
+    for (int i = threadIdx.x; i < static_cast<int>(sizeof(QTables) / 16); i += kThreads)
+      dst[i] = src[i];
+  }
+  __syncthreads();
+  if (s_skip) return;
+  const Scal s = s_sc;
+  if (threadIdx.x == 0) take_ticket(a, t);
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+  const int half = lane >> 4;
+  const uint32_t zc_m = qt.zero_code[0], zc_v = qt.zero_code[1];
+
+  for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
+    const Chunk ch = a.chunks[c];
+    const TensorDesc td = a.tensors[ch.tensor];
+    const float decay = __fsub_rn(1.0f, __fmul_rn(s.lr, td.wd));
+    const bool vec = td.vec_ok != 0;
+    float* const pf = static_cast<float*>(td.p);
+    uint8_t* const cm = static_cast<uint8_t*>(td.m);
+    uint8_t* const cv = static_cast<uint8_t*>(td.v);
+
+    // warp w owns the two blocks starting at `wb` of every pass; `e` is even
+    for (int wb = warp * kQ4Span; wb < ch.len; wb += kPass) {
+      const int64_t blk = (ch.start + wb) / kQ4Block + half;
+      const int off = wb + lane * kVec;
+      const int64_t e = ch.start + off;
+      float m[8], v[8];
+      uint32_t q_m[8], q_v[8];
+      if (vec && wb + kQ4Span <= ch.len) {
+        float p[8], gr[8];
+        const float am = td.am[blk], av = td.av[blk];
+        ld8f(pf + e, p);
+        Grad<GT>::load8(td.g, e, gr);
+        const uint32_t wm = __ldcs(reinterpret_cast<const uint32_t*>(cm + e / 2));
+        const uint32_t wv = __ldcs(reinterpret_cast<const uint32_t*>(cv + e / 2));
+        uint32_t mx_m = 0u, mx_v = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          m[i] = __fmul_rn(qt.map[0].value[(wm >> (4 * i)) & 0xFu], am);
+          v[i] = __fmul_rn(qt.map[1].value[(wv >> (4 * i)) & 0xFu], av);
+          update(p[i], gr[i], m[i], v[i], s, decay);
+          mx_m = max(mx_m, __float_as_uint(m[i]) & 0x7FFFFFFFu);
+          mx_v = max(mx_v, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+        }
+        st8f(pf + e, p);
+        const BlockNorm nm = block_norm(half_warp_max(mx_m));
+        quant8<R>(m, nm, qt.map[0], zc_m, q_m);
+        __stcs(reinterpret_cast<uint32_t*>(cm + e / 2), pack_nibbles(q_m));
+        const BlockNorm nv = block_norm(half_warp_max(mx_v));
+        quant8<R>(v, nv, qt.map[1], zc_v, q_v);
+        __stcs(reinterpret_cast<uint32_t*>(cv + e / 2), pack_nibbles(q_v));
+        if ((lane & 15) == 0) {
+          td.am[blk] = __uint_as_float(nm.bits);
+          td.av[blk] = __uint_as_float(nv.bits);
+        }
+      } else {
+        // the tail of a tensor (a half-warp's block may be partial or empty),
+        // or a misaligned tensor: element by element
+        const int n = max(0, min(kVec, ch.len - off));
+        const bool has_block = wb + half * kQ4Block < ch.len;
+        const float am = has_block ? td.am[blk] : 0.0f;
+        const float av = has_block ? td.av[blk] : 0.0f;
+        uint32_t mx_m = 0u, mx_v = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          m[i] = v[i] = 0.0f;
+          if (i < n) {
+            const int sh = 4 * (i & 1);
+            float pi = pf[e + i];
+            m[i] = __fmul_rn(qt.map[0].value[(cm[(e + i) / 2] >> sh) & 0xFu], am);
+            v[i] = __fmul_rn(qt.map[1].value[(cv[(e + i) / 2] >> sh) & 0xFu], av);
+            update(pi, Grad<GT>::load1(td.g, e + i), m[i], v[i], s, decay);
+            pf[e + i] = pi;
+            mx_m = max(mx_m, __float_as_uint(m[i]) & 0x7FFFFFFFu);
+            mx_v = max(mx_v, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+          }
+        }
+        const BlockNorm nm = block_norm(half_warp_max(mx_m));
+        const BlockNorm nv = block_norm(half_warp_max(mx_v));
+        quant8<R>(m, nm, qt.map[0], zc_m, q_m);
+        quant8<R>(v, nv, qt.map[1], zc_v, q_v);
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+          if (i < n) {
+            const bool pair = i + 1 < n;
+            cm[(e + i) / 2] = static_cast<uint8_t>(q_m[i] | (pair ? q_m[i + 1] << 4 : 0u));
+            cv[(e + i) / 2] = static_cast<uint8_t>(q_v[i] | (pair ? q_v[i + 1] << 4 : 0u));
+          }
+        }
+        if ((lane & 15) == 0 && has_block) {
+          td.am[blk] = __uint_as_float(nm.bits);
+          td.av[blk] = __uint_as_float(nv.bits);
+        }
+      }
+    }
+  }
+}
+
+template <typename GT>
+cudaError_t launch_q4(const StepArgs& a, int grid, cudaStream_t st) {
+  if (a.refine <= 1)
+    step_q4_kernel<GT, 1><<<grid, kThreads, sizeof(QTables), st>>>(a);
+  else if (a.refine <= 2)
+    step_q4_kernel<GT, 2><<<grid, kThreads, sizeof(QTables), st>>>(a);
+  else
+    step_q4_kernel<GT, kMaxRefine><<<grid, kThreads, sizeof(QTables), st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_step_q4(adamw_dtype gdt, const StepArgs& a, int grid, cudaStream_t s) {
+  switch (gdt) {
+    case ADAMW_F32: return launch_q4<float>(a, grid, s);
+    case ADAMW_F16: return launch_q4<__half>(a, grid, s);
+    case ADAMW_BF16: return launch_q4<__nv_bfloat16>(a, grid, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t q4_occupancy(adamw_dtype gdt, int* bps, int* smem) {
+  *smem = static_cast<int>(sizeof(QTables));
+  switch (gdt) {
+    case ADAMW_F32:
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, step_q4_kernel<float, kMaxRefine>,
+                                                           kThreads, *smem);
+    case ADAMW_F16:
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, step_q4_kernel<__half, kMaxRefine>,
+                                                           kThreads, *smem);
+    case ADAMW_BF16:
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          bps, step_q4_kernel<__nv_bfloat16, kMaxRefine>, kThreads, *smem);
+  }
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace adamw

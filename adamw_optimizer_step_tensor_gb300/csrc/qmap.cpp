@@ -1,5 +1,5 @@
-// qmap.cpp -- host construction of the 8-bit code maps and of the tables the
-// kernels use to find the nearest code.
+// qmap.cpp -- host construction of the 8-bit and 4-bit code maps and of the
+// tables the kernels use to find the nearest code.
 //
 // Default maps: dynamic-exponent quantisation as described by Dettmers et
 // al., "8-bit Optimizers via Block-wise Quantization" (arXiv:2110.02861):
@@ -12,6 +12,11 @@
 //
 // Each value is the rational (2n + 18k + 9) / (20 n 10^E) with n = 2^F, bin k,
 // rounded once to the nearest float32 with integer arithmetic only.
+//
+// 4-bit maps (the format of Li, Chen, Zhu, "Memory Efficient Optimizers with
+// 4-bit States", as torchao's 4-bit AdamW uses it): the first moment on the
+// same tree with three magnitude bits (E = 0..2, F = 2 - E, both signs, plus
+// 0 and +1.0: 16 values), the second moment on k/16, k = 1..16 (no zero).
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -35,10 +40,10 @@ float round_ratio(uint64_t num, uint64_t p5, int k) {
   return std::ldexp(static_cast<float>(keep), 2 - s - k);
 }
 
-void dynamic_map(int frac_bits_e0, bool is_signed, float out[256]) {
+void dynamic_map(int frac_bits_e0, bool is_signed, int n_exp, int size, float* out) {
   std::vector<float> v = {0.0f, 1.0f};
   uint64_t p5 = 5;                                      // 5^(E+1)
-  for (int e = 0; e < 7; ++e, p5 *= 5) {
+  for (int e = 0; e < n_exp; ++e, p5 *= 5) {
     const int f = frac_bits_e0 - e;
     const uint64_t n = 1ull << f;
     for (uint64_t b = 0; b < n; ++b) {
@@ -49,13 +54,13 @@ void dynamic_map(int frac_bits_e0, bool is_signed, float out[256]) {
     }
   }
   std::sort(v.begin(), v.end());
-  std::memcpy(out, v.data(), 256 * sizeof(float));
+  std::memcpy(out, v.data(), static_cast<size_t>(size) * sizeof(float));
 }
 
-// #{k : thr[k] <= x} over 255 ascending thresholds (float comparisons).
-int count_le(const float* thr, float x) {
+// #{k : thr[k] <= x} over n - 1 ascending thresholds (float comparisons).
+int count_le(const float* thr, int n, float x) {
   int c = 0;
-  while (c < 255 && thr[c] <= x) ++c;
+  while (c < n - 1 && thr[c] <= x) ++c;
   return c;
 }
 
@@ -68,20 +73,28 @@ float bits_to_float(uint32_t b) {
 }  // namespace
 
 void default_maps(float smap[256], float umap[256]) {
-  dynamic_map(6, true, smap);
-  dynamic_map(7, false, umap);
+  dynamic_map(6, true, 7, 256, smap);
+  dynamic_map(7, false, 7, 256, umap);
 }
 
-// Fill one QMapDev from 256 ascending finite values.  Returns the largest
-// number of thresholds inside one bucket, or -1 if the values are unusable.
-int build_qmap(const float value[256], QMapDev* out) {
-  for (int k = 0; k < 256; ++k) {
+void default_maps4(float smap[16], float umap[16]) {
+  dynamic_map(2, true, 3, 16, smap);
+  for (int k = 0; k < 16; ++k) umap[k] = static_cast<float>(k + 1) / 16.0f;   // exact
+}
+
+// Fill one QMapDev from n (16 or 256) ascending finite values.  Returns the
+// largest number of thresholds inside one bucket, or -1 if the values are
+// unusable.
+int build_qmap(const float* value, int n, QMapDev* out) {
+  if (n < 2 || n > 256) return -1;
+  for (int k = 0; k < n; ++k) {
     if (!std::isfinite(value[k])) return -1;
     if (k > 0 && !(value[k - 1] < value[k])) return -1;
   }
-  std::memcpy(out->value, value, sizeof(out->value));
+  std::memset(out->value, 0, sizeof(out->value));
+  std::memcpy(out->value, value, static_cast<size_t>(n) * sizeof(float));
   // thr[k]: smallest float strictly above the exact midpoint of value[k], value[k+1]
-  for (int k = 0; k < 255; ++k) {
+  for (int k = 0; k < n - 1; ++k) {
     const double a = value[k], b = value[k + 1];
     const double s = a + b;
     const double bb = s - a;                            // two-sum: the sum must be exact
@@ -91,7 +104,7 @@ int build_qmap(const float value[256], QMapDev* out) {
     if (static_cast<double>(c) <= mid) c = std::nextafter(c, INFINITY);
     out->thr[k] = c;
   }
-  for (int k = 255; k < 256 + kMaxRefine; ++k) out->thr[k] = INFINITY;
+  for (int k = n - 1; k < 256 + kMaxRefine; ++k) out->thr[k] = INFINITY;
   // Normalised values satisfy |x| <= 1, so the last bucket (|x| >= 1.9921875)
   // is reached only by NaN: its lowest code is 0 and, since no threshold
   // compares true against NaN, NaN quantises to code 0.
@@ -113,8 +126,8 @@ int build_qmap(const float value[256], QMapDev* out) {
       hi_bits = lo_bits | 0xFFFFu;
     }
     const float lo = bits_to_float(lo_bits), hi = bits_to_float(hi_bits);
-    const int pos_lo = count_le(out->thr, lo), pos_hi = count_le(out->thr, hi);
-    const int neg_lo = count_le(out->thr, -hi), neg_hi = count_le(out->thr, -lo);
+    const int pos_lo = count_le(out->thr, n, lo), pos_hi = count_le(out->thr, n, hi);
+    const int neg_lo = count_le(out->thr, n, -hi), neg_hi = count_le(out->thr, n, -lo);
     out->lo_pos[k] = static_cast<uint8_t>(pos_lo);
     out->lo_neg[k] = static_cast<uint8_t>(neg_lo);
     refine = std::max(refine, std::max(pos_hi - pos_lo, neg_hi - neg_lo));
@@ -122,8 +135,8 @@ int build_qmap(const float value[256], QMapDev* out) {
   return refine;
 }
 
-int zero_code_of(const float value[256]) {
-  for (int k = 0; k < 256; ++k)
+int zero_code_of(const float* value, int n) {
+  for (int k = 0; k < n; ++k)
     if (value[k] == 0.0f) return k;
   return -1;
 }

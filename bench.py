@@ -51,7 +51,7 @@ def parse_args():
     ap.add_argument("--workload", default="gpt2_small",
                     choices=["gpt2_small", "single", "amp", "amp_fused", "q8", "llama3_8b", "bf16rem",
                              "ademamix_gpt2", "lion_gpt2", "momentum_gpt2", "rmsprop_gpt2",
-                             "adagrad_gpt2"])
+                             "adagrad_gpt2", "q4"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -243,6 +243,25 @@ def cpu_sample_bf16rem(n):
     return run, f"{n} elements per step, strict-fp32 oracle with remainder join/split"
 
 
+def cpu_sample_q4(n):
+    import numpy as np
+    from oracle import q4 as O4
+    n = max(128, n // 128 * 128)
+    rng = np.random.default_rng(0)
+    p = rng.normal(0, 0.02, n).astype(np.float32)
+    g = rng.normal(0, 1e-3, n).astype(np.float32)
+    pm, pv = np.zeros(n // 2, np.uint8), np.zeros(n // 2, np.uint8)
+    am, av = np.zeros(n // 128, np.float32), np.zeros(n // 128, np.float32)
+    maps = O4.Maps4()
+    state = {"t": 0}
+
+    def run():
+        state["t"] += 1
+        O4.step_f32(p, g, pm, pv, am, av, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, wd=0.01,
+                    t=state["t"], maps=maps)
+    return run, f"{n} elements per step, strict-fp32 4-bit oracle (oracle.q4.step_f32)"
+
+
 def cpu_sample_ademamix(n):
     import numpy as np
     from oracle import ademamix as OX
@@ -293,6 +312,7 @@ CPU_SAMPLES = {
     "momentum_gpt2": lambda n: cpu_sample_coupled(n, "momentum"),
     "rmsprop_gpt2": lambda n: cpu_sample_coupled(n, "rmsprop"),
     "adagrad_gpt2": lambda n: cpu_sample_coupled(n, "adagrad"),
+    "q4": lambda n: cpu_sample_q4(n),
 }
 
 # ----------------------------------------------------------------------------- workloads
@@ -626,6 +646,37 @@ class Q8(Workload):
 
 
 
+class Q4(Q8):
+    """The q8 workload with 4-bit packed codes and 128-element blocks."""
+    name = "q4_blockwise_1G"
+    bytes_per_param = 12.125      # p 4+4, g 2, codes 0.5+0.5 each way, absmax 8/128 each way
+
+    def __init__(self, seed=4, numel=0):
+        import torch
+        import synth
+        from adamw_optimizer_step_tensor_gb300 import FusedAdamW, _capi
+        dev = torch.device("cuda")
+        self.C = _capi
+        n = self.n_params = numel or (1 << 30)
+        self.p = synth.normal(n, 0.02, seed, dev)
+        self.g = synth.normal(n, 1e-3, seed + 1, dev, dtype=torch.bfloat16)
+        self.cm = torch.zeros((n + 1) // 2, dtype=torch.uint8, device=dev)
+        self.cv = torch.zeros((n + 1) // 2, dtype=torch.uint8, device=dev)
+        nb = (n + 127) // 128
+        self.am = torch.zeros(nb, device=dev)
+        self.av = torch.zeros(nb, device=dev)
+        self.opt = FusedAdamW([self.p], [self.g], [self.cm], [self.cv], [0.01], mode="q4",
+                              absmax_m=[self.am], absmax_v=[self.av])
+        self.lr = torch.tensor([1e-3], dtype=torch.float32, device=dev)
+        self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream().cuda_stream
+        self.dtype = "f32 (4-bit states)"
+        self.config = {"workload": "4-bit blockwise m,v (128-element blocks); one flat fp32 param "
+                                   "of 2^30, bf16 grads",
+                       "tensors": 1, "numel": n, "bytes_per_param": self.bytes_per_param,
+                       "l2": "no flush: 13.0 GB moved per step"}
+
+
 class Llama3(Workload):
     name = "llama3_8b_bf16_rem"
     bytes_per_param = 26.0
@@ -713,7 +764,8 @@ def make_workload(name, numel=0):
             "lion_gpt2": lambda: LionGpt2(),
             "momentum_gpt2": lambda: CoupledGpt2("momentum"),
             "rmsprop_gpt2": lambda: CoupledGpt2("rmsprop"),
-            "adagrad_gpt2": lambda: CoupledGpt2("adagrad")}[name]()
+            "adagrad_gpt2": lambda: CoupledGpt2("adagrad"),
+            "q4": lambda: Q4(numel=numel)}[name]()
 
 
 # ----------------------------------------------------------------------------- CPU timing

@@ -49,6 +49,7 @@ extern "C" {
 
 #define ADAMW_ABI_VERSION 3
 #define ADAMW_Q8_BLOCK 256
+#define ADAMW_Q4_BLOCK 128
 
 typedef enum {
   ADAMW_OK = 0,
@@ -80,7 +81,16 @@ typedef enum {
    * unquantised m', v', then absmax = max|m'| and code = nearest map entry
    * to m'/absmax (exact tie -> lower code; all-zero block -> absmax 0 and
    * the code of 0.0). */
-  ADAMW_MODE_Q8 = 2
+  ADAMW_MODE_Q8 = 2,
+  /* The Q8 step with 4-bit codes and 128-element blocks (the 4-bit AdamW of
+   * torchao named in "4 bit Adam should support non constant lr"; format of
+   * Li, Chen, Zhu, "Memory Efficient Optimizers with 4-bit States"): m on a
+   * 16-entry signed dynamic map, v on k/16 (k = 1..16, no zero; an all-zero
+   * block stores absmax 0 and code 0).  exp_avg and exp_avg_sq are uint8
+   * [ceil(numel/2)], two codes per byte, the even element in the low nibble
+   * (an odd numel leaves the last high nibble 0); absmax_m/absmax_v fp32
+   * [ceil(numel/128)].  The maps are fixed (adamw_q4_default_maps). */
+  ADAMW_MODE_Q4 = 3
 } adamw_mode;
 
 /* One parameter tensor, flat and contiguous (numel elements). */
@@ -88,14 +98,16 @@ typedef struct {
   void* param;          /* fp32 [numel]; bf16 [numel] in BF16_REM mode       */
   int16_t* param_rem;   /* BF16_REM: int16 [numel]; otherwise must be NULL    */
   const void* grad;     /* grad_dtype [numel], possibly loss-scaled           */
-  void* exp_avg;        /* m: fp32 [numel]; uint8 codes [numel] in Q8 mode    */
+  void* exp_avg;        /* m: fp32 [numel]; uint8 codes [numel] in Q8 mode;
+                           packed 4-bit codes [ceil(numel/2)] in Q4 mode      */
   void* exp_avg_sq;     /* v: fp32 [numel]; uint8 codes [numel] in Q8 mode.
                            May be NULL on every tensor of an fp32 or
                            bf16+remainder plan: such a plan runs only the
                            1-state steps adamw_lion_step and
                            adamw_coupled_step (the others return EINVAL)     */
-  float* absmax_m;      /* Q8: fp32 [ceil(numel/256)]; otherwise NULL         */
-  float* absmax_v;      /* Q8: fp32 [ceil(numel/256)]; otherwise NULL         */
+  float* absmax_m;      /* Q8: fp32 [ceil(numel/256)]; Q4: [ceil(numel/128)];
+                           otherwise NULL                                      */
+  float* absmax_v;      /* as absmax_m                                         */
   int64_t numel;        /* >= 0; tensors with numel 0 are ignored             */
   float weight_decay;   /* per tensor (e.g. 0 for norms and biases)           */
   void* exp_avg_slow;   /* AdEMAMix slow EMA m2: fp32 [numel] on every tensor of
@@ -336,6 +348,14 @@ adamw_status adamw_bf16rem_join(const uint16_t* bf16, const int16_t* rem, float*
  * both signs; unsigned: F = 7-E; each plus exact 0 and +1.0.  Host only.
  */
 adamw_status adamw_q8_default_maps(float signed_map[256], float unsigned_map[256]);
+
+/*
+ * The Q4 mode's code maps (host arrays of 16 floats, ascending): signed, the
+ * dynamic tree above with three magnitude bits (E = 0..2, F = 2-E, both signs,
+ * plus 0 and +1.0); unsigned, k/16 for k = 1..16 (no zero: the zero-point
+ * problem of "Memory Efficient Optimizers with 4-bit States").  Host only.
+ */
+adamw_status adamw_q4_default_maps(float signed_map[16], float unsigned_map[16]);
 
 /* Replace a Q8 plan's maps (host arrays, 256 strictly ascending finite
  * floats each).  Synchronous.  EUNSUPPORTED if the maps are too dense for the

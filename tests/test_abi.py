@@ -115,3 +115,17 @@ def test_one_state_plans_are_checked_on_the_host():
 def test_coupled_step_checks_on_the_host():
     assert _status(lambda: C.adamw_coupled_step(None, 0, 0x100, 0x200, 0.9, 1e-8, None, None, None)) == C.EINVAL
     assert C.RULES == {"momentum": 0, "rmsprop": 1, "adagrad": 2}
+
+
+def test_q4_default_maps_equal_oracle_maps():
+    s, u = C.adamw_q4_default_maps()
+    assert np.array_equal(np.array(s, np.float32).view(np.uint32), qmap.signed_map4().view(np.uint32))
+    assert np.array_equal(np.array(u, np.float32).view(np.uint32), qmap.unsigned_map4().view(np.uint32))
+
+
+def test_q4_plans_are_checked_on_the_host():
+    # absmax pointers are required in Q4 mode, param_rem is not allowed
+    assert _status(lambda: C.adamw_plan_create([_t()], C.MODE_Q4, C.BF16)) == C.EINVAL
+    assert _status(lambda: C.adamw_plan_create([_t(rem=0x900000, am=0x910000, av=0x920000)],
+                                               C.MODE_Q4, C.BF16)) == C.EINVAL
+    assert _status(lambda: C.adamw_plan_create([_t()], 4, C.BF16)) == C.EDTYPE

@@ -1,0 +1,121 @@
+"""GPU parity: AdamW with 4-bit blockwise-quantised moments (mode "q4").
+
+Params, packed codes and per-block absmax are bit-exact against the
+strict-fp32 4-bit oracle on ragged tensor lists (odd sizes leave a lone low
+nibble, partial and empty half-warp blocks, a misaligned tensor on the
+element path) for fp32/fp16/bf16 grads; the first step from zero state also
+matches the closed form of "Fix decoupled weight decay ordering in the CUDA
+Adam/AdEMAMix kernels" (bitsandbytes PR #2040); the AMP skip leaves
+everything as it was.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from adamw_optimizer_step_tensor_gb300 import FusedAdamW
+from oracle import adamw as OA
+from oracle import q4 as O4
+from oracle import q8 as OQ
+
+from _support import bits_equal, dev, first_mismatch, grads_of, host, scalar_f32, scalar_i32
+
+pytestmark = pytest.mark.gpu
+f32 = OA.f32
+B1, B2, EPS = f32(0.9), f32(0.999), f32(1e-8)
+SIZES = [1, 7, 127, 128, 129, 255, 256, 257, 2048 + 100, 8192 + 301, 70001, 0]
+
+
+def _view(a, misalign):
+    if not misalign:
+        return dev(a)
+    return dev(np.concatenate([np.zeros(1, a.dtype), a]))[1:]   # 4 bytes off the 16-byte grid
+
+
+def _build(sizes, gdtype, seed, zero_state, misalign=False):
+    rng = np.random.default_rng(seed)
+    st = []
+    for n in sizes:
+        nb = OQ.n_blocks(n, O4.BLOCK)
+        p = rng.normal(0, 0.02, n).astype(np.float32)
+        pm = O4.pack(rng.integers(0, 16, n).astype(np.uint8))
+        pv = O4.pack(rng.integers(0, 16, n).astype(np.uint8))
+        am = np.zeros(nb, np.float32) if zero_state else rng.uniform(0, 1e-3, nb).astype(np.float32)
+        av = np.zeros(nb, np.float32) if zero_state else rng.uniform(0, 1e-6, nb).astype(np.float32)
+        st.append(dict(p=p, cm=pm, cv=pv, am=am, av=av))
+    d = [{k: (_view(v, misalign) if k == "p" else dev(v)) for k, v in s.items()} for s in st]
+    gs = [torch.empty(n, dtype=gdtype, device="cuda") for n in sizes]
+    opt = FusedAdamW([x["p"] for x in d], gs, [x["cm"] for x in d], [x["cv"] for x in d],
+                     [f32(0.01) if i % 2 else 0.0 for i in range(len(sizes))], mode="q4",
+                     absmax_m=[x["am"] for x in d], absmax_v=[x["av"] for x in d])
+    return opt, st, d, gs, rng
+
+
+def _steps(opt, st, d, gs, rng, gdtype, n_steps, lr=1e-3):
+    maps = O4.Maps4()
+    lr_d, step = scalar_f32(f32(lr)), scalar_i32(0)
+    for t in range(1, n_steps + 1):
+        wide = []
+        for g in gs:
+            tg, w = grads_of(rng.normal(0, 1e-3, g.numel()).astype(np.float32), gdtype)
+            g.copy_(tg)
+            wide.append(w)
+        opt.step(lr_d, step, betas=(B1, B2), eps=EPS)
+        for i, (s, w) in enumerate(zip(st, wide)):
+            O4.step_f32(s["p"], w, s["cm"], s["cv"], s["am"], s["av"], lr=f32(lr), beta1=B1,
+                        beta2=B2, eps=EPS, wd=f32(0.01) if i % 2 else 0.0, t=t, maps=maps)
+        torch.cuda.synchronize()
+        for i, (s, x) in enumerate(zip(st, d)):
+            assert bits_equal(host(x["p"]), s["p"]), f"t{t} tensor {i} p: {first_mismatch(host(x['p']), s['p'])}"
+            assert np.array_equal(host(x["cm"]), s["cm"]), f"t{t} tensor {i} m codes"
+            assert np.array_equal(host(x["cv"]), s["cv"]), f"t{t} tensor {i} v codes"
+            assert bits_equal(host(x["am"]), s["am"]), f"t{t} tensor {i} absmax m"
+            assert bits_equal(host(x["av"]), s["av"]), f"t{t} tensor {i} absmax v"
+    assert int(step.item()) == n_steps
+
+
+@pytest.mark.parametrize("gdtype", [torch.bfloat16, torch.float32, torch.float16])
+def test_q4_steps_bitexact(gdtype):
+    opt, st, d, gs, rng = _build(SIZES, gdtype, seed=31, zero_state=False)
+    _steps(opt, st, d, gs, rng, gdtype, 4)
+
+
+def test_q4_from_zero_state_bitexact():
+    opt, st, d, gs, rng = _build(SIZES, torch.bfloat16, seed=32, zero_state=True)
+    _steps(opt, st, d, gs, rng, torch.bfloat16, 3, lr=1e-2)
+
+
+def test_q4_element_path_on_misaligned_params():
+    opt, st, d, gs, rng = _build([1, 129, 1000, 4099], torch.float32, seed=33, zero_state=False,
+                                 misalign=True)
+    _steps(opt, st, d, gs, rng, torch.float32, 2)
+
+
+def test_q4_first_step_closed_form():
+    n = 100_001
+    opt, st, d, gs, rng = _build([n], torch.float32, seed=34, zero_state=True)
+    g = rng.normal(0, 1e-3, n).astype(np.float32)
+    gs[0].copy_(dev(g))
+    p0 = st[0]["p"].astype(np.float64)
+    opt.step(scalar_f32(f32(0.1)), scalar_i32(0), betas=(B1, B2), eps=EPS)
+    torch.cuda.synchronize()
+    lr = f32(0.1)
+    want = p0 - lr * g / (np.abs(g) + EPS)           # tensor 0 has wd 0
+    got = host(d[0]["p"]).astype(np.float64)
+    assert np.max(np.abs(got - want) / (np.abs(want) + lr)) < 8 * 2.0 ** -24
+    assert host(d[0]["cm"])[-1] >> 4 == 0             # odd n: the last high nibble stays 0
+
+
+def test_q4_amp_skip_leaves_codes_and_absmax():
+    n = 3001
+    opt, st, d, gs, rng = _build([n], torch.float16, seed=35, zero_state=False)
+    gs[0].copy_(dev((rng.normal(0, 1e-3, n) * 1024).astype(np.float16)))
+    gs[0][5] = float("nan")
+    before = {k: host(v) for k, v in d[0].items()}
+    found, step = scalar_f32(0.0), scalar_i32(7)
+    opt.check_nonfinite(found)
+    opt.step(scalar_f32(1e-3), step, grad_scale=scalar_f32(1024.0), found_inf=found)
+    torch.cuda.synchronize()
+    for k, v in d[0].items():
+        assert np.array_equal(host(v).view(np.uint8), before[k].view(np.uint8)), k
+    assert int(step.item()) == 7
