@@ -2,10 +2,13 @@
 """Throughput of the fused AdamW step on GB300 (params/s and achieved HBM GB/s).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload gpt2_small|single|amp|q8|llama3_8b]
+                    [--workload gpt2_small|single|amp|amp_fused|q8|q4|llama3_8b|bf16rem|
+                                ademamix_gpt2|lion_gpt2|momentum_gpt2|rmsprop_gpt2|adagrad_gpt2]
 
-One "step" is one AdamW update of every tensor of the workload (one launch of
-the library's step kernel; plus the non-finite check in the AMP workload).
+One "step" is one optimizer update of every tensor of the workload (one launch
+of the library's step kernel; plus the non-finite check in the AMP workload).
+The default is AdamW; the *_gpt2 variants step the same list with AdEMAMix,
+Lion or the coupled-L2 rules, q8 / q4 keep 8-bit / 4-bit moments.
 The default workload is the GPT-2-small fp32 parameter list (148 tensors,
 124,439,808 elements) with a device learning rate on a cosine schedule.  Its
 inputs (3.48 GB moved per step) are larger than L2, so no flush is needed
@@ -71,10 +74,20 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, one earlier GB300 measurement)"
 
 
-def kernel_source_sha() -> str:
+# The source files that make up the dominant kernel of each workload; a
+# committed ncu summary counts only while their hash matches.
+KERNEL_SOURCES = {
+    "q8": ("step_kernels.cu", "step_common.cuh", "internal.h"),
+    "q4": ("q4_kernels.cu", "step_common.cuh", "internal.h"),
+    "amp_fused": ("step_kernels.cu", "step_common.cuh", "internal.h"),
+}
+BULK_SOURCES = ("bulk_kernels.cu", "step_common.cuh", "internal.h")
+
+
+def kernel_source_sha(workload: str = "gpt2_small") -> str:
     h = hashlib.sha256()
     d = os.path.join(ROOT, "adamw_optimizer_step_tensor_gb300", "csrc")
-    for name in ("step_kernels.cu", "bulk_kernels.cu", "step_common.cuh", "internal.h"):
+    for name in KERNEL_SOURCES.get(workload, BULK_SOURCES):
         with open(os.path.join(d, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -88,7 +101,7 @@ def ncu_traffic(workload: str):
     txt = open(path).read()
     sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", txt)
     tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    if not sha or not tr or sha.group(1) != kernel_source_sha():
+    if not sha or not tr or sha.group(1) != kernel_source_sha(workload):
         return None
     return float(tr.group(1))
 
