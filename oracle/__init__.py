@@ -14,6 +14,7 @@ adamw      decoupled-weight-decay AdamW step, fp64 definition and a strict-fp32
 ademamix   AdEMAMix (fast and slow EMA) with the same decoupled decay, both modes.
 lion       Lion (sign update, one state) with decay before the update, both modes.
 coupled    momentum, RMSprop and Adagrad (one state) with coupled L2 decay, both modes.
+mini       Adam-mini: one second moment per block (element, head or tensor), both modes.
 remainder  fp32 master <-> (bf16 model param, int16 remainder) split and join.
 qmap       the dynamic-exponent 8-bit code maps, their decision thresholds and
            nearest-code quantisation.
@@ -28,4 +29,4 @@ print a map, so only its structural
 invariants and the quantiser built on top of it are pinned.
 """
 
-from . import adamw, ademamix, coupled, lion, remainder, qmap, q4, q8  # noqa: F401
+from . import adamw, ademamix, coupled, lion, mini, remainder, qmap, q4, q8  # noqa: F401
