@@ -13,7 +13,8 @@ from __future__ import annotations
 from . import _capi
 from ._capi import (  # noqa: F401
     AdamWError, adamw_abi_version, adamw_ademamix_step, adamw_bf16rem_join, adamw_bf16rem_split,
-    adamw_coupled_step, adamw_lion_step, adamw_q4_default_maps,
+    adamw_coupled_step, adamw_lion_step, adamw_mini_plan_create, adamw_mini_step,
+    adamw_q4_default_maps,
     adamw_check_nonfinite, adamw_last_error, adamw_lr_from_table, adamw_plan_create,
     adamw_plan_destroy,
     adamw_plan_info, adamw_plan_status, adamw_q8_default_maps, adamw_q8_dequant, adamw_q8_quant,
@@ -56,10 +57,13 @@ class FusedAdamW:
     ``weight_decays``: one float per tensor.
     ``exp_avg_sqs=None`` (fp32 / bf16_rem only) makes a plan for the 1-state
     steps ``step_lion`` and ``step_coupled`` alone.
+    ``v_blocks`` (fp32 / bf16_rem): one Adam-mini block length per tensor; the
+    tensor's exp_avg_sq then holds numel / block values and the plan steps with
+    ``step_mini``.
     """
 
     def __init__(self, params, grads, exp_avgs, exp_avg_sqs, weight_decays, *, mode="fp32",
-                 param_rems=None, absmax_m=None, absmax_v=None, exp_avg_slows=None):
+                 param_rems=None, absmax_m=None, absmax_v=None, exp_avg_slows=None, v_blocks=None):
         import torch
         if mode not in MODES:
             raise ValueError(f"mode must be one of {sorted(MODES)}")
@@ -90,6 +94,8 @@ class FusedAdamW:
                     raise ValueError(f"tensor {i}: {name} must be a contiguous CUDA tensor")
                 want = (p.numel() + 1) // 2 if (mode == "q4" and name in ("exp_avg", "exp_avg_sq")) \
                     else p.numel()
+                if v_blocks is not None and name == "exp_avg_sq":
+                    want = p.numel() // max(1, int(v_blocks[i]))
                 if t.numel() != want:
                     raise ValueError(f"tensor {i}: {name} has {t.numel()} elements, expected {want}")
             if mode == "bf16_rem" and (rems[i] is None or rems[i].dtype != torch.int16
@@ -109,7 +115,13 @@ class FusedAdamW:
                 int(p.numel()), float(weight_decays[i]), _ptr(slows[i])))
         self._keep = (list(params), list(grads), list(exp_avgs), list(exp_avg_sqs), rems, ams, avs,
                       slows)
-        self.plan = adamw_plan_create(recs, MODES[mode], _grad_dtype(gdt))
+        if v_blocks is not None:
+            if len(v_blocks) != n:
+                raise ValueError("v_blocks must have one entry per param")
+            self.plan = adamw_mini_plan_create(recs, [int(b) for b in v_blocks], MODES[mode],
+                                               _grad_dtype(gdt))
+        else:
+            self.plan = adamw_plan_create(recs, MODES[mode], _grad_dtype(gdt))
 
     def info(self) -> dict:
         return adamw_plan_info(self.plan)
@@ -133,6 +145,12 @@ class FusedAdamW:
         adamw_ademamix_step(self.plan, _ptr(lr), _ptr(step), float(betas[0]), float(betas[1]),
                             float(betas[2]), float(alpha), float(eps), _ptr(grad_scale),
                             _ptr(found_inf), _stream(stream))
+
+    def step_mini(self, lr, step, *, betas=(0.9, 0.999), eps=1e-8, grad_scale=None, found_inf=None,
+                  stream=None) -> None:
+        """Adam-mini step (plans made with ``v_blocks``)."""
+        adamw_mini_step(self.plan, _ptr(lr), _ptr(step), float(betas[0]), float(betas[1]),
+                        float(eps), _ptr(grad_scale), _ptr(found_inf), _stream(stream))
 
     def step_lion(self, lr, step, *, betas=(0.9, 0.99), grad_scale=None, found_inf=None,
                   stream=None) -> None:

@@ -50,6 +50,11 @@ class adamw_tensor(ctypes.Structure):
 _SIGNATURES = {
     "adamw_plan_create": (ctypes.c_int, [ctypes.POINTER(adamw_tensor), ctypes.c_int32, ctypes.c_int,
                                          ctypes.c_int, ctypes.POINTER(_vp)]),
+    "adamw_mini_plan_create": (ctypes.c_int, [ctypes.POINTER(adamw_tensor), ctypes.POINTER(ctypes.c_int64),
+                                              ctypes.c_int32, ctypes.c_int, ctypes.c_int,
+                                              ctypes.POINTER(_vp)]),
+    "adamw_mini_step": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_float, ctypes.c_float, ctypes.c_float,
+                                       _vp, _vp, _vp]),
     "adamw_plan_destroy": (ctypes.c_int, [_vp]),
     "adamw_plan_info": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_int64),
                                        ctypes.POINTER(ctypes.c_int64),
@@ -127,6 +132,22 @@ def adamw_plan_create(tensors: list[adamw_tensor], mode: int, grad_dtype: int) -
     out = _vp()
     _check(load().adamw_plan_create(arr, len(tensors), mode, grad_dtype, ctypes.byref(out)))
     return out.value
+
+
+def adamw_mini_plan_create(tensors: list[adamw_tensor], v_block: list[int], mode: int,
+                           grad_dtype: int) -> int:
+    arr = (adamw_tensor * max(1, len(tensors)))(*tensors)
+    blocks = (ctypes.c_int64 * max(1, len(v_block)))(*v_block)
+    out = _vp()
+    _check(load().adamw_mini_plan_create(arr, blocks if v_block else None, len(tensors), mode,
+                                         grad_dtype, ctypes.byref(out)))
+    return out.value
+
+
+def adamw_mini_step(plan: int, lr_dev: int, step_dev: int, beta1: float, beta2: float, eps: float,
+                    grad_scale_dev: int | None, found_inf_dev: int | None, stream: int | None) -> None:
+    _check(load().adamw_mini_step(plan, lr_dev, step_dev, beta1, beta2, eps, grad_scale_dev,
+                                  found_inf_dev, stream))
 
 
 def adamw_plan_destroy(plan: int) -> None:

@@ -20,6 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libadamw.so")
 SOURCES = ["capi.cpp", "qmap.cpp", "step_kernels.cu", "bulk_kernels.cu", "aux_kernels.cu", "noalloc.cu",
+           "mini_kernels.cu",
            "q4_kernels.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

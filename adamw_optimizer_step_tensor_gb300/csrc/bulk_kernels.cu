@@ -1,5 +1,6 @@
 // bulk_kernels.cu -- the fp32 and bf16+remainder steps (AdamW, AdEMAMix, Lion,
-// and momentum / RMSprop / Adagrad with coupled L2) with bulk-async staging.
+// momentum / RMSprop / Adagrad with coupled L2, and the element update of
+// Adam-mini) with bulk-async staging.
 //
 // One CTA per SM: a producer warp streams each 2048-element tile of every
 // input (p [+ remainder], g, m, v) into a ring of shared-memory stages with
@@ -126,6 +127,9 @@ __device__ void produce(const StepArgs& a, unsigned char* ring, uint64_t* full, 
   for (int64_t c = blockIdx.x; ok && c < a.n_chunks; c += gridDim.x) {
     const Chunk ch = a.chunks[c];
     const TensorDesc td = a.tensors[ch.tensor];
+    // Adam-mini chunks of a shared-v block stream no v
+    const bool copy_v = L::kV && !(ALGO == kAlgoMini && a.chunk_blk[c] >= 0);
+    const uint32_t per_elem = L::kPerElem - ((L::kV && !copy_v) ? 4u : 0u);
     for (int k = 0; k * kTile < ch.len; ++k, ++i) {
       const uint32_t s = i % S;
       if (!mbar_wait(&empty[s], ((i / S) & 1u) ^ 1u)) {
@@ -137,7 +141,7 @@ __device__ void produce(const StepArgs& a, unsigned char* ring, uint64_t* full, 
       const int nb = td.vec_ok ? (len & ~(kVec - 1)) : 0;  // elements moved in bulk
       const int64_t e = ch.start + static_cast<int64_t>(k) * kTile;
       unsigned char* st = ring + static_cast<size_t>(s) * L::kBytes;
-      const uint32_t bytes = nb * L::kPerElem;
+      const uint32_t bytes = nb * per_elem;
       mbar_expect_tx(&full[s], bytes);
       if (nb > 0) {
         bulk_g2s(st + L::oP, static_cast<const unsigned char*>(td.p) + e * L::kP, nb * L::kP, &full[s]);
@@ -145,7 +149,7 @@ __device__ void produce(const StepArgs& a, unsigned char* ring, uint64_t* full, 
           bulk_g2s(st + L::oR, td.rem + e, nb * 2, &full[s]);
         bulk_g2s(st + L::oG, static_cast<const unsigned char*>(td.g) + e * L::kG, nb * L::kG, &full[s]);
         bulk_g2s(st + L::oM, static_cast<const float*>(td.m) + e, nb * 4, &full[s]);
-        if (L::kV) bulk_g2s(st + L::oV, static_cast<const float*>(td.v) + e, nb * 4, &full[s]);
+        if (copy_v) bulk_g2s(st + L::oV, static_cast<const float*>(td.v) + e, nb * 4, &full[s]);
         if (L::kM2) bulk_g2s(st + L::oM2, static_cast<const float*>(td.m2) + e, nb * 4, &full[s]);
       }
     }
@@ -257,8 +261,17 @@ __global__ void __launch_bounds__(kBulkThreads, AlgoTune<ALGO>::ctas) step_bulk_
   for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
     const Chunk ch = a.chunks[c];
     const TensorDesc td = a.tensors[ch.tensor];
-    // the parameter's decay factor; the coupled rules take wd itself
-    const float decay = algo_coupled(ALGO) ? td.wd : __fsub_rn(1.0f, __fmul_rn(s.lr, td.wd));
+    // the parameter's decay factor; the coupled rules take wd itself, Adam-mini
+    // decays only when wd > 0
+    const float decay = algo_coupled(ALGO) ? td.wd
+                        : (ALGO == kAlgoMini && !(td.wd > 0.0f)) ? 1.0f
+                        : __fsub_rn(1.0f, __fmul_rn(s.lr, td.wd));
+    int32_t mini_blk = -1;
+    float mini_r = 0.0f;
+    if (ALGO == kAlgoMini) {
+      mini_blk = a.chunk_blk[c];
+      if (mini_blk >= 0) mini_r = a.blk_r[mini_blk];
+    }
     for (int k = 0; k * kTile < ch.len; ++k, ++i) {
       const uint32_t st_i = i % S;
       if (!mbar_wait(&full[st_i], (i / S) & 1u)) {
@@ -275,7 +288,10 @@ __global__ void __launch_bounds__(kBulkThreads, AlgoTune<ALGO>::ctas) step_bulk_
         if (j + 4 <= nb) {
           float p[4], g[4], m[4], v[4];
           load4_smem<MODE, GT, ALGO>(st, j, p, g, m, v);
-          if (algo_coupled(ALGO)) {
+          if (ALGO == kAlgoMini && mini_blk >= 0) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) update_mini(p[q], g[q], m[q], mini_r, s, decay);
+          } else if (algo_coupled(ALGO)) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) update_coupled<ALGO>(p[q], g[q], m[q], s, decay);
           } else if (ALGO == kAlgoAdemamix) {
@@ -292,9 +308,12 @@ __global__ void __launch_bounds__(kBulkThreads, AlgoTune<ALGO>::ctas) step_bulk_
 #pragma unroll
             for (int q = 0; q < 4; ++q) update(p[q], g[q], m[q], v[q], s, decay);
           }
-          store4<MODE, L::kV>(td, e0 + j, p, m, v);
+          if (ALGO == kAlgoMini && mini_blk >= 0)
+            store4<MODE, false>(td, e0 + j, p, m, v);
+          else
+            store4<MODE, L::kV>(td, e0 + j, p, m, v);
         } else if (j < len) {
-          update_scalar<MODE, GT, ALGO>(td, e0 + j, min(4, len - j), s, decay);
+          update_scalar<MODE, GT, ALGO>(td, e0 + j, min(4, len - j), s, decay, mini_r, mini_blk >= 0);
         }
       }
       __syncwarp();
@@ -331,6 +350,7 @@ cudaError_t launch_algo(const StepArgs& a, int grid, cudaStream_t st, int algo) 
     case kAlgoMomentum: return launch_one<MODE, GT, kAlgoMomentum>(a, grid, st);
     case kAlgoRmsprop: return launch_one<MODE, GT, kAlgoRmsprop>(a, grid, st);
     case kAlgoAdagrad: return launch_one<MODE, GT, kAlgoAdagrad>(a, grid, st);
+    case kAlgoMini: return launch_one<MODE, GT, kAlgoMini>(a, grid, st);
   }
   return cudaErrorInvalidValue;
 }
@@ -344,6 +364,7 @@ cudaError_t prepare_algo(int algo) {
     case kAlgoMomentum: return prepare_one<MODE, GT, kAlgoMomentum>();
     case kAlgoRmsprop: return prepare_one<MODE, GT, kAlgoRmsprop>();
     case kAlgoAdagrad: return prepare_one<MODE, GT, kAlgoAdagrad>();
+    case kAlgoMini: return prepare_one<MODE, GT, kAlgoMini>();
   }
   return cudaErrorInvalidValue;
 }

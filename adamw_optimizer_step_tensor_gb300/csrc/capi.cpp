@@ -42,6 +42,16 @@ struct adamw_plan {
   bool has_slow = false;       // every tensor carries an AdEMAMix slow EMA
   bool has_v = true;           // every tensor carries exp_avg_sq (false: Lion-only plan)
   int grid_sqrt_div = 1;       // grid of the RMSprop / Adagrad kernels (2 CTAs per SM)
+  // Adam-mini plans (adamw_mini_plan_create): blocks sharing one v
+  bool mini = false;
+  int64_t n_blocks = 0, n_red = 0;
+  int grid_red = 1;
+  MiniBlock* d_blocks = nullptr;
+  int32_t* d_chunk_blk = nullptr;
+  int64_t* d_red_chunks = nullptr;
+  double* d_partial = nullptr;
+  uint32_t* d_arrived = nullptr;
+  float* d_blk_r = nullptr;
 };
 
 namespace {
@@ -82,6 +92,12 @@ void free_plan(adamw_plan* p) {
   cudaFree(p->d_chunks_fused);
   cudaFree(p->d_scratch);
   cudaFree(p->d_qt);
+  cudaFree(p->d_blocks);
+  cudaFree(p->d_chunk_blk);
+  cudaFree(p->d_red_chunks);
+  cudaFree(p->d_partial);
+  cudaFree(p->d_arrived);
+  cudaFree(p->d_blk_r);
   delete p;
 }
 
@@ -122,6 +138,10 @@ adamw_status build_qtables(const float* smap, const float* umap, int n, QTables*
 
 void adamw::set_last_error(const char* msg) { g_err = msg; }
 
+static adamw_status create_plan(const adamw_tensor* tensors, int32_t n_tensors, adamw_mode mode,
+                                adamw_dtype grad_dtype, const int64_t* v_block,
+                                adamw_plan** out);
+
 extern "C" {
 
 const char* adamw_last_error(void) { return g_err.c_str(); }
@@ -130,6 +150,21 @@ int32_t adamw_abi_version(void) { return ADAMW_ABI_VERSION; }
 
 adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, adamw_mode mode,
                                adamw_dtype grad_dtype, adamw_plan** out) {
+  return create_plan(tensors, n_tensors, mode, grad_dtype, nullptr, out);
+}
+
+adamw_status adamw_mini_plan_create(const adamw_tensor* tensors, const int64_t* v_block,
+                                    int32_t n_tensors, adamw_mode mode, adamw_dtype grad_dtype,
+                                    adamw_plan** out) {
+  if (n_tensors > 0 && !v_block) return fail(ADAMW_EINVAL, "v_block is NULL");
+  return create_plan(tensors, n_tensors, mode, grad_dtype, v_block, out);
+}
+
+}  // extern "C"
+
+static adamw_status create_plan(const adamw_tensor* tensors, int32_t n_tensors, adamw_mode mode,
+                                adamw_dtype grad_dtype, const int64_t* v_block,
+                                adamw_plan** out) {
   if (!out) return fail(ADAMW_EINVAL, "out is NULL");
   *out = nullptr;
   if (n_tensors < 0) return fail(ADAMW_EINVAL, "n_tensors < 0");
@@ -197,6 +232,21 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
     return fail(ADAMW_EINVAL, "the Q8 and Q4 modes need exp_avg_sq on every tensor");
   if (sized && !with_v && with_slow)
     return fail(ADAMW_EINVAL, "an AdEMAMix plan needs exp_avg_sq on every tensor");
+  if (v_block) {
+    if (mode != ADAMW_MODE_FP32 && mode != ADAMW_MODE_BF16_REM)
+      return fail(ADAMW_EUNSUPPORTED, "Adam-mini plans cover the fp32 and bf16+remainder modes");
+    if (with_slow) return fail(ADAMW_EINVAL, "an Adam-mini plan carries no exp_avg_slow");
+    if (with_v != sized) return fail(ADAMW_EINVAL, "an Adam-mini plan needs exp_avg_sq on every tensor");
+    for (int32_t i = 0; i < n_tensors; ++i) {
+      const int64_t n = td[i].numel, b = v_block[i];
+      if (n == 0) continue;
+      if (b < 1 || n % b != 0)
+        return fail(ADAMW_EINVAL, "tensor %d: v_block %lld must divide numel %lld", i,
+                    (long long)b, (long long)n);
+      if (b != 1 && b != n && b % kVec != 0)
+        return fail(ADAMW_EINVAL, "tensor %d: v_block must be 1, numel or a multiple of %d", i, kVec);
+    }
+  }
 
   // Every argument is valid; only now touch the device.
   int device = -1, sms = 0;
@@ -225,11 +275,40 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
   }
   if (bps < 1) bps = 1;
   const int64_t chunk = choose_chunk(total, sms, bps);
-  for (int32_t i = 0; i < n_tensors; ++i)
-    for (int64_t s = 0; s < td[i].numel; s += chunk) {
-      const int64_t len = td[i].numel - s < chunk ? td[i].numel - s : chunk;
-      chunks.push_back(Chunk{s, i, static_cast<int32_t>(len)});
+  // Adam-mini: chunks of a shared-v block stay inside it; chunk_blk maps each
+  // chunk to its block (-1: v per element)
+  std::vector<int32_t> chunk_blk;
+  std::vector<MiniBlock> blocks;
+  std::vector<int64_t> red_chunks;
+  for (int32_t i = 0; i < n_tensors; ++i) {
+    const int64_t b = v_block ? v_block[i] : 1;
+    if (b == 1 || td[i].numel == 0) {
+      for (int64_t s = 0; s < td[i].numel; s += chunk) {
+        const int64_t len = td[i].numel - s < chunk ? td[i].numel - s : chunk;
+        chunks.push_back(Chunk{s, i, static_cast<int32_t>(len)});
+        chunk_blk.push_back(-1);
+      }
+      continue;
     }
+    for (int64_t b0 = 0; b0 < td[i].numel; b0 += b) {
+      MiniBlock mb;
+      mb.v_index = b0 / b;
+      mb.first_chunk = static_cast<int64_t>(chunks.size());
+      mb.len = b;
+      mb.tensor = i;
+      mb.n_chunks = 0;
+      for (int64_t s = 0; s < b; s += chunk) {
+        const int64_t len = b - s < chunk ? b - s : chunk;
+        red_chunks.push_back(static_cast<int64_t>(chunks.size()));
+        chunks.push_back(Chunk{b0 + s, i, static_cast<int32_t>(len)});
+        chunk_blk.push_back(static_cast<int32_t>(blocks.size()));
+        ++mb.n_chunks;
+      }
+      blocks.push_back(mb);
+    }
+  }
+  if (blocks.size() > static_cast<size_t>(INT32_MAX))
+    return fail(ADAMW_EUNSUPPORTED, "more than 2^31 - 1 Adam-mini blocks");
 
   std::unique_ptr<adamw_plan, void (*)(adamw_plan*)> p(new adamw_plan, free_plan);
   p->mode = mode;
@@ -263,6 +342,35 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
     return cuda_fail(e, "upload chunk table");
   if ((e = cudaMemset(p->d_scratch, 0, sizeof(StepScratch))) != cudaSuccess)
     return cuda_fail(e, "clear step scratch");
+  if (v_block) {
+    p->mini = true;
+    p->n_blocks = static_cast<int64_t>(blocks.size());
+    p->n_red = static_cast<int64_t>(red_chunks.size());
+    const int64_t red_res = 8LL * sms;
+    p->grid_red = static_cast<int>(p->n_red < 1 ? 1 : (p->n_red < red_res ? p->n_red : red_res));
+    if ((e = prepare_step_bulk(mode, grad_dtype, kAlgoMini)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(Adam-mini step)");
+    const size_t nb = blocks.size(), nc = chunks.size(), nr = red_chunks.size();
+    if (nc && (e = cudaMalloc(&p->d_chunk_blk, nc * sizeof(int32_t))) != cudaSuccess)
+      return fail(ADAMW_ENOMEM, "cudaMalloc(chunk blocks): %s", cudaGetErrorString(e));
+    if (nc && (e = cudaMemcpy(p->d_chunk_blk, chunk_blk.data(), nc * sizeof(int32_t),
+                              cudaMemcpyHostToDevice)) != cudaSuccess)
+      return cuda_fail(e, "upload chunk blocks");
+    if (nb) {
+      if ((e = cudaMalloc(&p->d_blocks, nb * sizeof(MiniBlock))) != cudaSuccess ||
+          (e = cudaMalloc(&p->d_red_chunks, nr * sizeof(int64_t))) != cudaSuccess ||
+          (e = cudaMalloc(&p->d_partial, nc * sizeof(double))) != cudaSuccess ||
+          (e = cudaMalloc(&p->d_arrived, nb * sizeof(uint32_t))) != cudaSuccess ||
+          (e = cudaMalloc(&p->d_blk_r, nb * sizeof(float))) != cudaSuccess)
+        return fail(ADAMW_ENOMEM, "cudaMalloc(Adam-mini tables): %s", cudaGetErrorString(e));
+      if ((e = cudaMemcpy(p->d_blocks, blocks.data(), nb * sizeof(MiniBlock),
+                          cudaMemcpyHostToDevice)) != cudaSuccess ||
+          (e = cudaMemcpy(p->d_red_chunks, red_chunks.data(), nr * sizeof(int64_t),
+                          cudaMemcpyHostToDevice)) != cudaSuccess ||
+          (e = cudaMemset(p->d_arrived, 0, nb * sizeof(uint32_t))) != cudaSuccess)
+        return cuda_fail(e, "upload Adam-mini tables");
+    }
+  }
   if (!quantized(mode)) {
     int bpf = 0;
     if ((e = fused_occupancy(mode, grad_dtype, &bpf)) != cudaSuccess)
@@ -306,6 +414,8 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors, a
   *out = p.release();
   return ADAMW_OK;
 }
+
+extern "C" {
 
 adamw_status adamw_plan_destroy(adamw_plan* plan) {
   if (!plan) return ADAMW_OK;
@@ -382,6 +492,7 @@ adamw_status adamw_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev
     return fail(ADAMW_EINVAL, "betas must lie in [0, 1)");
   if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(ADAMW_EINVAL, "eps must be finite and >= 0");
   if (!plan->has_v) return fail(ADAMW_EINVAL, "the plan's tensors carry no exp_avg_sq");
+  if (plan->mini) return fail(ADAMW_EINVAL, "an Adam-mini plan steps with adamw_mini_step");
   adamw_status st = check_device(plan);
   if (st != ADAMW_OK) return st;
   StepArgs a;
@@ -455,6 +566,56 @@ adamw_status adamw_ademamix_step(adamw_plan* plan, const float* lr_dev, int32_t*
   cudaError_t e = launch_step_bulk(plan->mode, plan->gdt, a, plan->grid,
                                    static_cast<cudaStream_t>(stream), kAlgoAdemamix);
   if (e != cudaSuccess) return cuda_fail(e, "launch AdEMAMix step");
+  return ADAMW_OK;
+}
+
+adamw_status adamw_mini_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev,
+                             float beta1, float beta2, float eps, const float* grad_scale_dev,
+                             const float* found_inf_dev, void* stream) {
+  if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
+  if (!plan->mini) return fail(ADAMW_EINVAL, "the plan was not made by adamw_mini_plan_create");
+  if (!lr_dev || !step_dev) return fail(ADAMW_EINVAL, "lr_dev and step_dev must be set");
+  if (!aligned(lr_dev, 4) || !aligned(step_dev, 4) || !aligned(grad_scale_dev, 4) ||
+      !aligned(found_inf_dev, 4))
+    return fail(ADAMW_EALIGN, "a scalar pointer is not 4-byte aligned");
+  if (!(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f))
+    return fail(ADAMW_EINVAL, "betas must lie in [0, 1)");
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(ADAMW_EINVAL, "eps must be finite and >= 0");
+  adamw_status st = check_device(plan);
+  if (st != ADAMW_OK) return st;
+  StepArgs a;
+  a.tensors = plan->d_tensors;
+  a.chunks = plan->d_chunks;
+  a.n_chunks = plan->n_chunks;
+  a.lr = lr_dev;
+  a.step = step_dev;
+  a.grad_scale = grad_scale_dev;
+  a.found_inf = found_inf_dev;
+  a.beta1 = beta1;
+  a.beta2 = beta2;
+  a.eps = eps;
+  a.beta3 = 0.0f;
+  a.alpha = 0.0f;
+  a.scratch = plan->d_scratch;
+  a.qt = nullptr;
+  a.refine = 1;
+  a.chunk_blk = plan->d_chunk_blk;
+  a.blk_r = plan->d_blk_r;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (plan->n_red > 0) {
+    MiniArgs ma;
+    ma.red_chunks = plan->d_red_chunks;
+    ma.n_red = plan->n_red;
+    ma.blocks = plan->d_blocks;
+    ma.partial = plan->d_partial;
+    ma.arrived = plan->d_arrived;
+    ma.blk_r = plan->d_blk_r;
+    e = launch_mini_reduce(plan->gdt, a, ma, plan->grid_red, s);
+    if (e != cudaSuccess) return cuda_fail(e, "launch Adam-mini reduction");
+  }
+  e = launch_step_bulk(plan->mode, plan->gdt, a, plan->grid, s, kAlgoMini);
+  if (e != cudaSuccess) return cuda_fail(e, "launch Adam-mini step");
   return ADAMW_OK;
 }
 
@@ -554,6 +715,7 @@ adamw_status adamw_step_amp(adamw_plan* plan, const float* lr_dev, int32_t* step
   if (quantized(plan->mode))
     return fail(ADAMW_EUNSUPPORTED, "the fused check + step covers the fp32 and bf16+remainder modes");
   if (!plan->has_v) return fail(ADAMW_EINVAL, "the plan's tensors carry no exp_avg_sq");
+  if (plan->mini) return fail(ADAMW_EINVAL, "an Adam-mini plan steps with adamw_mini_step");
   adamw_status st = check_device(plan);
   if (st != ADAMW_OK) return st;
   // every CTA of the cooperative launch is resident at once (grid sized at plan creation)

@@ -54,8 +54,13 @@ constexpr int kAlgoLion = 2;
 constexpr int kAlgoMomentum = 3;  // coupled L2, one state
 constexpr int kAlgoRmsprop = 4;
 constexpr int kAlgoAdagrad = 5;
-__host__ __device__ constexpr bool algo_two_state(int algo) { return algo == kAlgoAdamW || algo == kAlgoAdemamix; }
-__host__ __device__ constexpr bool algo_coupled(int algo) { return algo >= kAlgoMomentum; }
+constexpr int kAlgoMini = 6;      // Adam-mini: v per element or shared per block
+__host__ __device__ constexpr bool algo_two_state(int algo) {
+  return algo == kAlgoAdamW || algo == kAlgoAdemamix || algo == kAlgoMini;
+}
+__host__ __device__ constexpr bool algo_coupled(int algo) {
+  return algo == kAlgoMomentum || algo == kAlgoRmsprop || algo == kAlgoAdagrad;
+}
 
 struct TensorDesc {
   void* p;            // fp32 or bf16 param
@@ -122,6 +127,28 @@ struct StepArgs {
   StepScratch* scratch;       // plan-owned; ticket zero between launches
   const QTables* qt;          // Q8 only
   int refine;                 // Q8 only: thresholds per lookup (1, 2 or 4)
+  const int32_t* chunk_blk = nullptr;   // Adam-mini: v block of each chunk (-1: v per element)
+  const float* blk_r = nullptr;         // Adam-mini: fl(1/bc1) / h of each block, this step
+};
+
+// Adam-mini: one block of `len` contiguous elements sharing one v value
+// (exp_avg_sq[v_index] of its tensor); its chunks are contiguous in the
+// chunk table.
+struct MiniBlock {
+  int64_t v_index;
+  int64_t first_chunk;
+  int64_t len;
+  int32_t tensor;
+  int32_t n_chunks;
+};
+
+struct MiniArgs {
+  const int64_t* red_chunks;  // chunks of the blocks longer than one element
+  int64_t n_red;
+  const MiniBlock* blocks;
+  double* partial;            // per chunk: sum of g*g over the chunk
+  uint32_t* arrived;          // per block: chunks summed this step (0 between launches)
+  float* blk_r;               // per block: fl(1/bc1) / h, read by the update
 };
 
 // Bucket of a non-negative float bit pattern: 0 for |x| < 2^-24, then 128
@@ -151,6 +178,10 @@ cudaError_t step_occupancy(adamw_mode mode, adamw_dtype gdt, int* blocks_per_sm,
 cudaError_t launch_step_bulk(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int grid,
                              cudaStream_t s, int algo);
 cudaError_t prepare_step_bulk(adamw_mode mode, adamw_dtype gdt, int algo);
+// Adam-mini block reduction and v update (mini_kernels.cu); the element
+// update is the bulk kernel with kAlgoMini.
+cudaError_t launch_mini_reduce(adamw_dtype gdt, const StepArgs& a, const MiniArgs& ma, int grid,
+                               cudaStream_t s);
 // 4-bit states (q4_kernels.cu).
 cudaError_t launch_step_q4(adamw_dtype gdt, const StepArgs& a, int grid, cudaStream_t s);
 cudaError_t q4_occupancy(adamw_dtype gdt, int* bps, int* smem);

@@ -151,6 +151,15 @@ __device__ __forceinline__ void update_coupled(float& p, float g, float& st, con
   p = __fsub_rn(p, __fmul_rn(s.lr, d));
 }
 
+// Adam-mini, an element of a block with shared v: r = fl(1/bc1) / h of the
+// block; the parameter moves by lr * (m' * r) after the decay.
+__device__ __forceinline__ void update_mini(float& p, float g, float& m, float r, const Scal& s,
+                                            float decay) {
+  if (s.scaled) g = __fmul_rn(g, s.inv_scale);
+  m = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
+  p = __fsub_rn(__fmul_rn(p, decay), __fmul_rn(s.lr, __fmul_rn(m, r)));
+}
+
 // ---------------------------------------------------------------- loads/stores
 __device__ __forceinline__ void ld8f(const float* q, float (&x)[8]) {
   const float4 a = __ldcs(reinterpret_cast<const float4*>(q));
@@ -229,7 +238,7 @@ __device__ __forceinline__ void rem_split(float x, uint32_t& hi, uint32_t& rem16
 // are not all 16-byte aligned.
 template <adamw_mode MODE, typename GT, int ALGO = kAlgoAdamW>
 __device__ void update_scalar(const TensorDesc& td, int64_t e, int n, const Scal& s,
-                              float decay) {
+                              float decay, float mini_r = 0.0f, bool mini_shared = false) {
   float* const pf = static_cast<float*>(td.p);
   uint16_t* const ph = static_cast<uint16_t*>(td.p);
   float* const mf = static_cast<float*>(td.m);
@@ -238,8 +247,11 @@ __device__ void update_scalar(const TensorDesc& td, int64_t e, int n, const Scal
     const int64_t k = e + i;
     float p = MODE == ADAMW_MODE_FP32 ? pf[k] : rem_join(ph[k], static_cast<uint16_t>(td.rem[k]));
     float m = mf[k];
-    float v = algo_two_state(ALGO) ? vf[k] : 0.0f;
-    if (algo_coupled(ALGO)) {
+    const bool has_v = algo_two_state(ALGO) && !(ALGO == kAlgoMini && mini_shared);
+    float v = has_v ? vf[k] : 0.0f;
+    if (ALGO == kAlgoMini && mini_shared) {
+      update_mini(p, Grad<GT>::load1(td.g, k), m, mini_r, s, decay);
+    } else if (algo_coupled(ALGO)) {
       update_coupled<ALGO>(p, Grad<GT>::load1(td.g, k), m, s, decay);
     } else if (ALGO == kAlgoAdemamix) {
       float* const m2f = static_cast<float*>(td.m2);
@@ -260,7 +272,7 @@ __device__ void update_scalar(const TensorDesc& td, int64_t e, int n, const Scal
       td.rem[k] = static_cast<int16_t>(static_cast<uint16_t>(r));
     }
     mf[k] = m;
-    if (algo_two_state(ALGO)) vf[k] = v;
+    if (has_v) vf[k] = v;
   }
 }
 

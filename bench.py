@@ -3,7 +3,8 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload gpt2_small|single|amp|amp_fused|q8|q4|llama3_8b|bf16rem|
-                                ademamix_gpt2|lion_gpt2|momentum_gpt2|rmsprop_gpt2|adagrad_gpt2]
+                                ademamix_gpt2|lion_gpt2|momentum_gpt2|rmsprop_gpt2|adagrad_gpt2|
+                                adam_mini_llama3]
 
 One "step" is one optimizer update of every tensor of the workload (one launch
 of the library's step kernel; plus the non-finite check in the AMP workload).
@@ -54,7 +55,7 @@ def parse_args():
     ap.add_argument("--workload", default="gpt2_small",
                     choices=["gpt2_small", "single", "amp", "amp_fused", "q8", "llama3_8b", "bf16rem",
                              "ademamix_gpt2", "lion_gpt2", "momentum_gpt2", "rmsprop_gpt2",
-                             "adagrad_gpt2", "q4"])
+                             "adagrad_gpt2", "q4", "adam_mini_llama3"])
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -275,6 +276,22 @@ def cpu_sample_q4(n):
     return run, f"{n} elements per step, strict-fp32 4-bit oracle (oracle.q4.step_f32)"
 
 
+def cpu_sample_mini(n):
+    import numpy as np
+    from oracle import mini as OM
+    block = 524288
+    n = max(block, n // block * block)
+    rng = np.random.default_rng(0)
+    x = OM.Tensor(p=rng.normal(0, 0.02, n), g=rng.normal(0, 1e-4, n), m=np.zeros(n),
+                  v=np.zeros(n // block), wd=0.1, block=block)
+    state = {"t": 0}
+
+    def run():
+        state["t"] += 1
+        OM.step_fp64([x], lr=3e-4, beta1=0.9, beta2=0.999, eps=1e-8, t=state["t"])
+    return run, f"{n} elements per step in heads of {block}, float64 Adam-mini oracle (oracle.mini.step_fp64)"
+
+
 def cpu_sample_ademamix(n):
     import numpy as np
     from oracle import ademamix as OX
@@ -326,6 +343,7 @@ CPU_SAMPLES = {
     "rmsprop_gpt2": lambda n: cpu_sample_coupled(n, "rmsprop"),
     "adagrad_gpt2": lambda n: cpu_sample_coupled(n, "adagrad"),
     "q4": lambda n: cpu_sample_q4(n),
+    "adam_mini_llama3": lambda n: cpu_sample_mini(n),
 }
 
 # ----------------------------------------------------------------------------- workloads
@@ -737,6 +755,66 @@ class Llama3(Workload):
 
 
 
+class MiniLlama3(Workload):
+    """Adam-mini on the Llama-3-8B list (bf16 params + int16 remainders, bf16 grads).
+
+    Two launches per step: the block reduction reads g of every tensor with a
+    shared v (2 B per element), the update streams p, remainder, g, m (and v
+    for the per-element embedding and output tensors)."""
+    name = "adam_mini_llama3_8b_bf16_rem"
+    launches_per_step = 2
+
+    def __init__(self, seed=5):
+        import torch
+        import synth
+        from adamw_optimizer_step_tensor_gb300 import FusedAdamW, _capi
+        dev = torch.device("cuda")
+        self.C = _capi
+        self.specs = synth.llama3_8b()
+        self.n_params = synth.total_numel(self.specs)
+        blocks = synth.adam_mini_blocks(self.specs, dim=4096, n_heads=32)
+        _, hs = _flat_views(self.specs, torch.bfloat16, dev)
+        _, rs = _flat_views(self.specs, torch.int16, dev)
+        _, gs = _flat_views(self.specs, torch.bfloat16, dev)
+        _, ms = _flat_views(self.specs, torch.float32, dev)
+        vs = [torch.zeros(s.numel // b, device=dev) for s, b in zip(self.specs, blocks)]
+        for i, (h, r, g, s) in enumerate(zip(hs, rs, gs, self.specs)):
+            if "norm" in s.name:
+                h.fill_(1.0)
+            else:
+                hi, rem = synth.bf16_params_with_remainders(s.numel, 0.02, seed + i, dev)
+                h.copy_(hi)
+                r.copy_(rem)
+                del hi, rem
+            g.copy_(synth.normal(s.numel, 1e-4, synth.grad_seed(seed, 0, i), dev, torch.bfloat16))
+        wds = [0.0 if "norm" in s.name else 0.1 for s in self.specs]
+        self.opt = FusedAdamW(hs, gs, ms, vs, wds, mode="bf16_rem", param_rems=rs, v_blocks=blocks)
+        self._views = (hs, rs, gs, ms, vs)
+        n_elem_v = sum(s.numel for s, b in zip(self.specs, blocks) if b == 1)
+        n_shared = self.n_params - n_elem_v
+        # reduction: g (2); update: p 2 + rem 2 + g 2 + m 4 read, p 2 + rem 2 + m 4 written;
+        # per-element v (embeddings, output) adds 4 + 4
+        total = 2 * n_shared + 18 * self.n_params + 8 * n_elem_v
+        self.bytes_per_param = total / self.n_params
+        self.lr = torch.tensor([3e-4], dtype=torch.float32, device=dev)
+        self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.stream = torch.cuda.current_stream().cuda_stream
+        self.dtype = "f32 (bf16+int16 params)"
+        self.config = {"workload": "Adam-mini on the Llama-3-8B param list (v per element for "
+                                   "embeddings/output, per head for wq/wk, per tensor elsewhere), "
+                                   "bf16 params + int16 remainders",
+                       "tensors": len(self.specs), "numel": self.n_params,
+                       "v_blocks": len(set(blocks)), "bytes_per_param": round(self.bytes_per_param, 4),
+                       "l2": f"no flush: {total / 1e9:.0f} GB moved per step"}
+
+    def step(self, i):
+        self.C.adamw_mini_step(self.opt.plan, self.lr.data_ptr(), self.step_dev.data_ptr(), 0.9, 0.999,
+                               1e-8, None, None, self.stream)
+
+    def e2e_setup(self):
+        return None
+
+
 class Bf16Rem(Workload):
     """One flat bf16+remainder tensor: a small stand-in for the Llama-3-8B list (profiling)."""
     name = "bf16rem_flat"
@@ -778,7 +856,8 @@ def make_workload(name, numel=0):
             "momentum_gpt2": lambda: CoupledGpt2("momentum"),
             "rmsprop_gpt2": lambda: CoupledGpt2("rmsprop"),
             "adagrad_gpt2": lambda: CoupledGpt2("adagrad"),
-            "q4": lambda: Q4(numel=numel)}[name]()
+            "q4": lambda: Q4(numel=numel),
+            "adam_mini_llama3": lambda: MiniLlama3()}[name]()
 
 
 # ----------------------------------------------------------------------------- CPU timing

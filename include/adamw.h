@@ -267,6 +267,48 @@ adamw_status adamw_lion_step(adamw_plan* plan, const float* lr_dev, int32_t* ste
                              float beta1, float beta2, const float* grad_scale_dev,
                              const float* found_inf_dev, void* stream);
 
+/*
+ * Adam-mini plan ("Adam-mini <> DTensor", the AdamWMini listing): like
+ * adamw_plan_create (fp32 and bf16+remainder modes), plus one block length per
+ * tensor, v_block[i]: the elements of tensor i form blocks of v_block[i]
+ * contiguous elements that share one second moment, and exp_avg_sq of that
+ * tensor holds numel / v_block[i] fp32 values.  1 gives the listing's AdamW
+ * branch (embeddings and the output layer), a head's dim*dim/n_heads elements
+ * its query/key branch, numel its one-v-per-tensor branch; the partition is
+ * the caller's.  v_block[i] must divide numel and be 1, numel or a multiple
+ * of 8 (EINVAL otherwise); exp_avg_sq is required on every tensor and
+ * exp_avg_slow must be NULL.  Chunks never straddle blocks.  Such a plan steps
+ * with adamw_mini_step (and, touching no v, adamw_lion_step and
+ * adamw_coupled_step); adamw_step and adamw_step_amp return EINVAL.
+ */
+adamw_status adamw_mini_plan_create(const adamw_tensor* tensors, const int64_t* v_block,
+                                    int32_t n_tensors, adamw_mode mode, adamw_dtype grad_dtype,
+                                    adamw_plan** out);
+
+/*
+ * One Adam-mini step: two launches on `stream`.  The first sums g*g over
+ * every block longer than one element (per thread an error-free pair of
+ * float32 -- exact squares by fma, TwoSum additions, after Ogita, Rump and
+ * Oishi -- combined in float64 in a fixed order, the block's chunks in chunk
+ * order), then per block, one rounding per operation:
+ *     mean = fl32(sum / len);  v' = b2*v + fl(1-b2)*mean
+ *     h = sqrt(v')*fl32(1/sqrt(1-b2^t)) + eps;  r = fl(1/fl32(1-b1^t)) / h
+ * The second updates every element:
+ *     block of 1: exactly adamw_step's sequence
+ *     longer:     g = g_raw [* inv_scale];  m' = b1*m + fl(1-b1)*g
+ *                 p' = p*decay - lr*(m'*r)
+ * with decay = fl(1 - fl(lr*wd)) when wd > 0 and no decay otherwise (the
+ * listing decays only for wd > 0).  The sum's relative error stays below
+ * about 2^-35 (64 squares per thread and chunk), so the mean is the correctly
+ * rounded mean of the squares except within that distance of a float32
+ * rounding boundary (one ulp off then), or when a square leaves the float32
+ * range.  lr_dev, step_dev, grad_scale_dev, found_inf_dev, skip
+ * (both launches) and step counting (the second launch) as adamw_step.
+ */
+adamw_status adamw_mini_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev,
+                             float beta1, float beta2, float eps, const float* grad_scale_dev,
+                             const float* found_inf_dev, void* stream);
+
 /* The 1-state rules with coupled L2 decay (adamw_coupled_step). */
 typedef enum {
   ADAMW_RULE_MOMENTUM = 0, /* s = b*s + g;            p -= lr*s                    */

@@ -92,6 +92,22 @@ def llama3_8b(wd: float = 0.1) -> list[TensorSpec]:
     return out
 
 
+def adam_mini_blocks(specs: list[TensorSpec], dim: int, n_heads: int) -> list[int]:
+    """Adam-mini block length per tensor by parameter name, as the AdamWMini
+    listing of "Adam-mini <> DTensor" partitions a model: embeddings and the
+    output layer keep one v per element, query and key weights one per head
+    (dim*dim/n_heads elements), every other tensor one v for the whole tensor."""
+    out = []
+    for s in specs:
+        if any(k in s.name for k in ("embed", "embd", "wte", "lm_head", "output")):
+            out.append(1)
+        elif any(k in s.name for k in ("wq", "wk", "q_proj", "k_proj")):
+            out.append(dim * dim // n_heads)
+        else:
+            out.append(s.numel)
+    return out
+
+
 def total_numel(specs: list[TensorSpec]) -> int:
     return sum(s.numel for s in specs)
 

@@ -129,3 +129,15 @@ def test_q4_plans_are_checked_on_the_host():
     assert _status(lambda: C.adamw_plan_create([_t(rem=0x900000, am=0x910000, av=0x920000)],
                                                C.MODE_Q4, C.BF16)) == C.EINVAL
     assert _status(lambda: C.adamw_plan_create([_t()], 4, C.BF16)) == C.EDTYPE
+
+
+def test_mini_plans_are_checked_on_the_host():
+    t = _t(numel=1024)
+    assert _status(lambda: C.adamw_mini_plan_create([t], [3], C.MODE_FP32, C.F32)) == C.EINVAL   # 3 does not divide
+    assert _status(lambda: C.adamw_mini_plan_create([t], [4], C.MODE_FP32, C.F32)) == C.EINVAL   # not a multiple of 8
+    assert _status(lambda: C.adamw_mini_plan_create([t], [0], C.MODE_FP32, C.F32)) == C.EINVAL
+    q = _t(numel=1024, am=0x910000, av=0x920000)
+    assert _status(lambda: C.adamw_mini_plan_create([q], [256], C.MODE_Q8, C.F32)) == C.EUNSUPPORTED
+    no_v = C.adamw_tensor(0x10000, None, 0x110000, 0x210000, None, None, None, 1024, 0.0)
+    assert _status(lambda: C.adamw_mini_plan_create([no_v], [1024], C.MODE_FP32, C.F32)) == C.EINVAL
+    assert _status(lambda: C.adamw_mini_step(None, 0x100, 0x200, 0.9, 0.999, 1e-8, None, None, None)) == C.EINVAL
