@@ -191,3 +191,162 @@ def test_single_tensor_beyond_2e31_elements():
         assert int(step.item()) == 3 and opt.status() == 0
     finally:
         _cleanup()
+
+
+def _elementwise_full_size(w, step_fn, make_orc, check, n_steps, seed):
+    """Shared driver for the GPT-2-list variants: sampled windows of every tensor."""
+    rng = np.random.default_rng(seed)
+    idx = _windows([p.numel() for p in w.ps], rng)
+    orc = make_orc(idx)
+    for s in range(n_steps):
+        for k, g in enumerate(w.gs):
+            g.copy_(synth.normal(g.numel(), 1e-3, synth.grad_seed(seed, s, k), "cuda"))
+        for o, g, i in zip(orc, w.gs, idx):
+            o.g = _take(g, i).cpu().numpy()
+        w.step(s)
+        step_fn(orc, float(w.lr_table[s % 100].item()), s)
+    torch.cuda.synchronize()
+    check(orc, idx)
+    assert int(w.step_dev.item()) == n_steps
+    assert w.opt.status() == 0
+
+
+def test_lion_gpt2_full_size_sampled():
+    """The GPT-2-small list stepped with Lion (1-state plan, no exp_avg_sq), 10 steps."""
+    from oracle import lion as OL
+    w = bench.LionGpt2()
+    try:
+        def make(idx):
+            return [OL.Tensor(p=_take(p, i).cpu().numpy(), g=None, m=_take(m, i).cpu().numpy(), wd=s.wd)
+                    for p, m, i, s in zip(w.ps, w.ms, idx, w.specs)]
+
+        def step(orc, lr, s):
+            OL.step_f32(orc, lr=lr, beta1=OA.f32(0.9), beta2=OA.f32(0.99))
+
+        def check(orc, idx):
+            for k, (p, m, i, o) in enumerate(zip(w.ps, w.ms, idx, orc)):
+                assert np.array_equal(_take(p, i).cpu().numpy().view(np.uint32), o.p.view(np.uint32)), k
+                assert np.array_equal(_take(m, i).cpu().numpy().view(np.uint32), o.m.view(np.uint32)), k
+        _elementwise_full_size(w, step, make, check, 10, 31)
+    finally:
+        del w
+        _cleanup()
+
+
+@pytest.mark.parametrize("rule", ["momentum", "rmsprop", "adagrad"])
+def test_coupled_gpt2_full_size_sampled(rule):
+    """The GPT-2-small list stepped with a coupled-L2 rule, 5 steps."""
+    from oracle import coupled as OC
+    w = bench.CoupledGpt2(rule)
+    try:
+        def make(idx):
+            return [OC.Tensor(p=_take(p, i).cpu().numpy(), g=None, s=_take(m, i).cpu().numpy(), wd=s.wd)
+                    for p, m, i, s in zip(w.ps, w.ms, idx, w.specs)]
+
+        def step(orc, lr, s):
+            OC.step_f32(orc, rule=rule, lr=lr, beta=OA.f32(0.9), eps=OA.f32(1e-8))
+
+        def check(orc, idx):
+            for k, (p, m, i, o) in enumerate(zip(w.ps, w.ms, idx, orc)):
+                assert np.array_equal(_take(p, i).cpu().numpy().view(np.uint32), o.p.view(np.uint32)), k
+                assert np.array_equal(_take(m, i).cpu().numpy().view(np.uint32), o.s.view(np.uint32)), k
+        _elementwise_full_size(w, step, make, check, 5, 32)
+    finally:
+        del w
+        _cleanup()
+
+
+def test_q4_full_size_2e30_sampled_blocks():
+    """One 2^30 fp32 tensor, 4-bit m and v, bf16 grads, lr 1e-3, wd 0.01, 10 steps."""
+    from oracle import q4 as O4
+    if _free_gib() < 10:
+        pytest.skip("needs ~8 GiB of free device memory")
+    w = bench.Q4()
+    try:
+        rng = np.random.default_rng(33)
+        n = w.n_params
+        blocks = np.unique(np.concatenate([[0, 1, n // 128 - 1], rng.integers(0, n // 128, 64)]))
+        idx = (blocks[:, None] * 128 + np.arange(128)[None, :]).ravel()
+        bidx = torch.from_numpy(blocks).cuda()
+        byte_idx = (blocks[:, None] * 64 + np.arange(64)[None, :]).ravel()
+        p = _take(w.p, idx).cpu().numpy()
+        pm = _take(w.cm, byte_idx).cpu().numpy()
+        pv = _take(w.cv, byte_idx).cpu().numpy()
+        am = w.am[bidx].cpu().numpy()
+        av = w.av[bidx].cpu().numpy()
+        maps = O4.Maps4()
+        for s in range(10):
+            w.g.copy_(synth.normal(n, 1e-3, synth.grad_seed(10, s), "cuda", torch.bfloat16))
+            g = _take(w.g, idx).float().cpu().numpy()
+            w.step(s)
+            O4.step_f32(p, g, pm, pv, am, av, lr=OA.f32(1e-3), beta1=OA.f32(0.9), beta2=OA.f32(0.999),
+                        eps=OA.f32(1e-8), wd=OA.f32(0.01), t=s + 1, maps=maps)
+        torch.cuda.synchronize()
+        assert np.array_equal(_take(w.p, idx).cpu().numpy().view(np.uint32), p.view(np.uint32))
+        assert np.array_equal(_take(w.cm, byte_idx).cpu().numpy(), pm)
+        assert np.array_equal(_take(w.cv, byte_idx).cpu().numpy(), pv)
+        assert np.array_equal(w.am[bidx].cpu().numpy().view(np.uint32), am.view(np.uint32))
+        assert np.array_equal(w.av[bidx].cpu().numpy().view(np.uint32), av.view(np.uint32))
+        assert int(w.step_dev.item()) == 10
+    finally:
+        del w
+        _cleanup()
+
+
+def test_adam_mini_llama3_full_size_sampled_blocks():
+    """Adam-mini on the Llama-3-8B list (v per element / head / tensor), 3 steps: whole
+    blocks sampled -- two query heads and one key head of layer 0, the whole wv of
+    layer 31, two norm tensors -- plus windows of the per-element embedding and output."""
+    from oracle import mini as OM
+    if _free_gib() < 95:
+        pytest.skip("needs ~90 GiB of free device memory")
+    w = bench.MiniLlama3()
+    try:
+        hs, rs, gs, ms, vs = w._views
+        blocks = synth.adam_mini_blocks(w.specs, dim=4096, n_heads=32)
+        names = [s.name for s in w.specs]
+        rng = np.random.default_rng(34)
+        picks = []   # (tensor index, element indices, block length, v indices)
+        for name, heads in (("layers.0.attention.wq", (0, 31)), ("layers.0.attention.wk", (5,))):
+            k = names.index(name)
+            for h in heads:
+                picks.append((k, np.arange(h * blocks[k], (h + 1) * blocks[k]), blocks[k], np.array([h])))
+        for name in ("layers.31.attention.wv", "layers.3.ffn_norm", "norm"):
+            k = names.index(name)
+            picks.append((k, np.arange(hs[k].numel()), blocks[k], np.array([0])))
+        for name in ("tok_embeddings", "output"):
+            k = names.index(name)
+            i = _windows([hs[k].numel()], rng, n_rand=8)[0]
+            picks.append((k, i, 1, i))
+        orc = []
+        for k, i, b, vi in picks:
+            hi = _take(hs[k].view(torch.int16), i).cpu().numpy().view(np.uint16)
+            orc.append(OM.Tensor(p=OR.join(hi, _take(rs[k], i).cpu().numpy()), g=None,
+                                 m=_take(ms[k], i).cpu().numpy(), v=_take(vs[k], vi).cpu().numpy(),
+                                 wd=0.0 if "norm" in names[k] else OA.f32(0.1), block=b))
+        for s in range(3):
+            for k, g in enumerate(gs):
+                g.copy_(synth.normal(g.numel(), 1e-4, synth.grad_seed(11, s, k), "cuda", torch.bfloat16))
+            for o, (k, i, b, vi) in zip(orc, picks):
+                o.g = _take(gs[k], i).float().cpu().numpy()
+            w.step(s)
+            OM.step_f32(orc, lr=OA.f32(3e-4), beta1=OA.f32(0.9), beta2=OA.f32(0.999), eps=OA.f32(1e-8),
+                        t=s + 1)
+        torch.cuda.synchronize()
+        for o, (k, i, b, vi) in zip(orc, picks):
+            v = _take(vs[k], vi).cpu().numpy()
+            ulps = np.abs(v.view(np.int32).astype(np.int64) - o.v.view(np.int32).astype(np.int64))
+            assert ulps.max() <= 3, (names[k], int(ulps.max()))
+            assert np.array_equal(_take(ms[k], i).cpu().numpy().view(np.uint32), o.m.view(np.uint32)), names[k]
+            ohi, orem = OR.split(o.p)
+            got = OR.join(_take(hs[k].view(torch.int16), i).cpu().numpy().view(np.uint16),
+                          _take(rs[k], i).cpu().numpy())
+            if b == 1:
+                assert np.array_equal(got.view(np.uint32), o.p.view(np.uint32)), names[k]
+            else:
+                assert np.all(np.abs(got.astype(np.float64) - o.p) <= 2.0 ** -21 * (np.abs(o.p) + 1e-6)), names[k]
+        assert int(w.step_dev.item()) == 3
+        assert w.opt.status() == 0
+    finally:
+        del w
+        _cleanup()
