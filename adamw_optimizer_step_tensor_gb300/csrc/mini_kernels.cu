@@ -38,16 +38,49 @@ __device__ __forceinline__ void add_square(float& s, float& c, float x) {
   c = __fadd_rn(c, __fadd_rn(err, e));
 }
 
-// The float64 sum of one value per thread, in a fixed order (xor tree in each
-// warp, then the warps in order); every thread gets the result.
+// (s, c) += (s2, c2) for two error-free pairs: TwoSum of the leading parts,
+// the rounding error joins the trailing parts.
+__device__ __forceinline__ void add_pair(float& s, float& c, float s2, float c2) {
+  const float t = __fadd_rn(s, s2);
+  const float bp = __fsub_rn(t, s);
+  const float err = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(s2, bp));
+  s = t;
+  c = __fadd_rn(__fadd_rn(c, c2), err);
+}
+
+// The sum over the CTA of one pair per thread, in a fixed order (xor tree of
+// pairs in each warp, then the warps' pairs in float64 in order).  The result
+// is valid in thread 0.  Float64 work stays at 16 additions per CTA: GB300
+// issues float64 at a small fraction of its float32 rate.
+__device__ __forceinline__ double cta_pair_sum(float s, float c, float2* s_pair) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1)
+    add_pair(s, c, __shfl_xor_sync(0xFFFFFFFFu, s, o), __shfl_xor_sync(0xFFFFFFFFu, c, o));
+  if ((threadIdx.x & 31) == 0) s_pair[threadIdx.x >> 5] = make_float2(s, c);
+  __syncthreads();
+  double total = 0.0;
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int w = 0; w < kRedThreads / 32; ++w) {
+      total += static_cast<double>(s_pair[w].x);
+      total += static_cast<double>(s_pair[w].y);
+    }
+  }
+  __syncthreads();
+  return total;
+}
+
+// The float64 sum of one value per thread, in a fixed order; valid in thread 0.
 __device__ __forceinline__ double cta_sum(double x, double* s_warp) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
   if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = x;
   __syncthreads();
   double total = 0.0;
+  if (threadIdx.x == 0) {
 #pragma unroll
-  for (int w = 0; w < kRedThreads / 32; ++w) total += s_warp[w];
+    for (int w = 0; w < kRedThreads / 32; ++w) total += s_warp[w];
+  }
   __syncthreads();
   return total;
 }
@@ -70,6 +103,7 @@ __global__ void __launch_bounds__(kRedThreads) mini_reduce_kernel(const StepArgs
   __shared__ Scal s_sc;
   __shared__ int s_skip;
   __shared__ double s_warp[kRedThreads / 32];
+  __shared__ float2 s_pair[kRedThreads / 32];
   __shared__ int s_last;
   int t = 0;
   if (threadIdx.x == 0) s_skip = prologue(a, s_sc, t);
@@ -98,7 +132,7 @@ __global__ void __launch_bounds__(kRedThreads) mini_reduce_kernel(const StepArgs
         add_square(sum, comp, x);
       }
     }
-    double d = cta_sum(static_cast<double>(sum) + static_cast<double>(comp), s_warp);
+    const double d = cta_pair_sum(sum, comp, s_pair);
     const int32_t b = a.chunk_blk[c];
     const MiniBlock blk = ma.blocks[b];
     if (blk.n_chunks == 1) {
