@@ -86,6 +86,8 @@ _SIGNATURES = {
     "adamw_q8_set_maps": (ctypes.c_int, [_vp, ctypes.POINTER(ctypes.c_float),
                                          ctypes.POINTER(ctypes.c_float)]),
     "adamw_q8_dequant": (ctypes.c_int, [_vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int64, _vp]),
+    "adamw_q4_dequant": (ctypes.c_int, [_vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int64, _vp]),
+    "adamw_q4_quant": (ctypes.c_int, [_vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int64, _vp]),
     "adamw_q8_quant": (ctypes.c_int, [_vp, ctypes.c_int32, _vp, _vp, _vp, ctypes.c_int64, _vp]),
     "adamw_last_error": (ctypes.c_char_p, []),
     "adamw_abi_version": (ctypes.c_int32, []),
@@ -269,3 +271,13 @@ def adamw_q8_dequant(plan: int, which: int, codes: int, absmax: int, out: int, n
 def adamw_q8_quant(plan: int, which: int, x: int, codes: int, absmax: int, n: int,
                    stream: int | None) -> None:
     _check(load().adamw_q8_quant(plan, which, x, codes, absmax, n, stream))
+
+
+def adamw_q4_dequant(plan: int, which: int, codes: int, absmax: int, out: int, n: int,
+                     stream: int | None) -> None:
+    _check(load().adamw_q4_dequant(plan, which, codes, absmax, out, n, stream))
+
+
+def adamw_q4_quant(plan: int, which: int, x: int, codes: int, absmax: int, n: int,
+                   stream: int | None) -> None:
+    _check(load().adamw_q4_quant(plan, which, x, codes, absmax, n, stream))

@@ -152,6 +152,72 @@ int grid_for(int64_t n, int per_block) {
   return static_cast<int>(g);
 }
 
+
+// ---------------------------------------------------------------- 4-bit export / import
+// Packed 4-bit codes (even element in the low nibble), one absmax per 128.
+__global__ void q4_dequant_kernel(const QTables* __restrict__ qt, int which,
+                                  const uint8_t* __restrict__ codes,
+                                  const float* __restrict__ absmax, float* __restrict__ out,
+                                  int64_t n) {
+  const float* value = qt->map[which].value;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const uint32_t c = (codes[i >> 1] >> ((i & 1) * 4)) & 0xFu;
+    out[i] = __fmul_rn(value[c], absmax[i / 128]);
+  }
+}
+
+// One half-warp per 128-element block (8 elements per lane): absmax over bit
+// patterns by a 16-lane xor maximum, then the nearest code of x / absmax.
+__global__ void q4_quant_kernel(const QTables* __restrict__ qt, int which,
+                                const float* __restrict__ x, uint8_t* __restrict__ codes,
+                                float* __restrict__ absmax, int64_t n) {
+  const QMapDev& t = qt->map[which];
+  const int refine = qt->refine;
+  const int lane = threadIdx.x & 31, l16 = lane & 15;
+  const int64_t warps = (int64_t)gridDim.x * (blockDim.x / 32);
+  const int64_t nblk = (n + 127) / 128;
+  for (int64_t w = blockIdx.x * (int64_t)(blockDim.x / 32) + (threadIdx.x >> 5); 2 * w < nblk;
+       w += warps) {
+    const int64_t b = 2 * w + (lane >> 4);
+    float v[8];
+    uint32_t mx = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int64_t e = b * 128 + l16 * 8 + i;
+      v[i] = (b < nblk && e < n) ? x[e] : 0.0f;
+      mx = max(mx, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+    }
+#pragma unroll
+    for (int o = 8; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+    if (b >= nblk) continue;
+    const float A = __uint_as_float(mx);
+    const float scale = A < kTinyAbsmax ? kTinyScale : 1.0f;
+    const float inv = __frcp_rn(__fmul_rn(A, scale));
+    uint32_t q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      if (mx == 0u) {
+        q[i] = static_cast<uint32_t>(qt->zero_code[which]);
+      } else {
+        const float y = __fmul_rn(__fmul_rn(v[i], scale), inv);
+        const uint32_t bits = __float_as_uint(y);
+        const int k = bucket_of(bits & 0x7FFFFFFFu);
+        const uint32_t lo = (bits >> 31) ? t.lo_neg[k] : t.lo_pos[k];
+        uint32_t c = lo;
+        for (int r = 0; r < refine; ++r) c += (t.thr[lo + r] <= y) ? 1u : 0u;
+        q[i] = c;
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+      const int64_t e = b * 128 + l16 * 8 + i;
+      if (e < n) codes[e >> 1] = static_cast<uint8_t>(q[i] | (e + 1 < n ? q[i + 1] << 4 : 0u));
+    }
+    if (l16 == 0) absmax[b] = A;
+  }
+}
+
 }  // namespace
 
 cudaError_t launch_nonfinite(adamw_dtype gdt, const TensorDesc* tensors, const Chunk* chunks,
@@ -201,6 +267,19 @@ cudaError_t launch_q8_quant(const QTables* qt, int which, const float* x, uint8_
   const int64_t nblk = (n + kQBlock - 1) / kQBlock;
   q8_quant_kernel<<<grid_for(nblk, kThreads / 32), kThreads, 0, s>>>(qt, which, x, codes,
                                                                     absmax, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_q4_dequant(const QTables* qt, int which, const uint8_t* codes,
+                              const float* absmax, float* out, int64_t n, cudaStream_t s) {
+  q4_dequant_kernel<<<grid_for(n, kThreads), kThreads, 0, s>>>(qt, which, codes, absmax, out, n);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_q4_quant(const QTables* qt, int which, const float* x, uint8_t* codes,
+                            float* absmax, int64_t n, cudaStream_t s) {
+  const int64_t nwarp = ((n + 127) / 128 + 1) / 2;
+  q4_quant_kernel<<<grid_for(nwarp, kThreads / 32), kThreads, 0, s>>>(qt, which, x, codes, absmax, n);
   return cudaGetLastError();
 }
 

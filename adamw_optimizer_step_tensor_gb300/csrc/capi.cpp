@@ -13,6 +13,11 @@
 namespace adamw {
 void default_maps(float smap[256], float umap[256]);
 void default_maps4(float smap[16], float umap[16]);
+// 4-bit export / import (aux_kernels.cu)
+cudaError_t launch_q4_dequant(const QTables* qt, int which, const uint8_t* codes,
+                              const float* absmax, float* out, int64_t n, cudaStream_t s);
+cudaError_t launch_q4_quant(const QTables* qt, int which, const float* x, uint8_t* codes,
+                            float* absmax, int64_t n, cudaStream_t s);
 int build_qmap(const float* value, int n, QMapDev* out);
 int zero_code_of(const float* value, int n);
 }  // namespace adamw
@@ -790,9 +795,11 @@ adamw_status adamw_q8_set_maps(adamw_plan* plan, const float signed_map[256],
 }
 
 static adamw_status q8_io_check(const adamw_plan* plan, int32_t which, const void* a,
-                                const void* b, const void* c, int64_t n) {
+                                const void* b, const void* c, int64_t n,
+                                adamw_mode mode = ADAMW_MODE_Q8) {
   if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
-  if (plan->mode != ADAMW_MODE_Q8 || !plan->d_qt) return fail(ADAMW_EINVAL, "plan is not in Q8 mode");
+  if (plan->mode != mode || !plan->d_qt)
+    return fail(ADAMW_EINVAL, "plan is not in %s mode", mode == ADAMW_MODE_Q8 ? "Q8" : "Q4");
   if (which != 0 && which != 1) return fail(ADAMW_EINVAL, "which must be 0 (m) or 1 (v)");
   if (n < 0) return fail(ADAMW_EINVAL, "n < 0");
   if (n > 0 && (!a || !b || !c)) return fail(ADAMW_EINVAL, "NULL pointer");
@@ -817,6 +824,26 @@ adamw_status adamw_q8_quant(const adamw_plan* plan, int32_t which, const float* 
   cudaError_t e = launch_q8_quant(plan->d_qt, which, x, codes, absmax, n,
                                   static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? ADAMW_OK : cuda_fail(e, "launch q8 quant");
+}
+
+adamw_status adamw_q4_dequant(const adamw_plan* plan, int32_t which, const uint8_t* codes,
+                              const float* absmax, float* out, int64_t n, void* stream) {
+  adamw_status st = q8_io_check(plan, which, codes, absmax, out, n, ADAMW_MODE_Q4);
+  if (st != ADAMW_OK || n == 0) return st;
+  if (!aligned(absmax, 4) || !aligned(out, 4)) return fail(ADAMW_EALIGN, "misaligned float pointer");
+  cudaError_t e = launch_q4_dequant(plan->d_qt, which, codes, absmax, out, n,
+                                    static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ADAMW_OK : cuda_fail(e, "launch q4 dequant");
+}
+
+adamw_status adamw_q4_quant(const adamw_plan* plan, int32_t which, const float* x, uint8_t* codes,
+                            float* absmax, int64_t n, void* stream) {
+  adamw_status st = q8_io_check(plan, which, x, codes, absmax, n, ADAMW_MODE_Q4);
+  if (st != ADAMW_OK || n == 0) return st;
+  if (!aligned(absmax, 4) || !aligned(x, 4)) return fail(ADAMW_EALIGN, "misaligned float pointer");
+  cudaError_t e = launch_q4_quant(plan->d_qt, which, x, codes, absmax, n,
+                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ADAMW_OK : cuda_fail(e, "launch q4 quant");
 }
 
 }  // extern "C"

@@ -399,6 +399,21 @@ adamw_status adamw_q8_default_maps(float signed_map[256], float unsigned_map[256
  */
 adamw_status adamw_q4_default_maps(float signed_map[16], float unsigned_map[16]);
 
+/*
+ * Export / import of Q4-mode states (plans in ADAMW_MODE_Q4 only), the 4-bit
+ * counterparts of adamw_q8_dequant / adamw_q8_quant: codes are packed
+ * [ceil(n/2)] bytes (even element in the low nibble), absmax [ceil(n/128)].
+ * dequant: out[i] = map[code(i)] * absmax[i/128].  quant: per 128-element
+ * block the absmax of the bit patterns of |x|, then the nearest map entry of
+ * x * fl(1/absmax) (both scaled by 2^64 below 2^-64; exact tie -> lower code,
+ * NaN -> code 0); an all-zero block stores absmax 0 and the map's zero code
+ * (code 0 for the v map, which has no zero).  which: 0 = m map, 1 = v map.
+ */
+adamw_status adamw_q4_dequant(const adamw_plan* plan, int32_t which, const uint8_t* codes,
+                              const float* absmax, float* out, int64_t n, void* stream);
+adamw_status adamw_q4_quant(const adamw_plan* plan, int32_t which, const float* x,
+                            uint8_t* codes, float* absmax, int64_t n, void* stream);
+
 /* Replace a Q8 plan's maps (host arrays, 256 strictly ascending finite
  * floats each).  Synchronous.  EUNSUPPORTED if the maps are too dense for the
  * kernel's bucketed nearest-code search. */

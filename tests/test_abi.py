@@ -141,3 +141,8 @@ def test_mini_plans_are_checked_on_the_host():
     no_v = C.adamw_tensor(0x10000, None, 0x110000, 0x210000, None, None, None, 1024, 0.0)
     assert _status(lambda: C.adamw_mini_plan_create([no_v], [1024], C.MODE_FP32, C.F32)) == C.EINVAL
     assert _status(lambda: C.adamw_mini_step(None, 0x100, 0x200, 0.9, 0.999, 1e-8, None, None, None)) == C.EINVAL
+
+
+def test_q4_io_checks_on_the_host():
+    assert _status(lambda: C.adamw_q4_dequant(None, 0, 0x100, 0x200, 0x300, 5, None)) == C.EINVAL
+    assert _status(lambda: C.adamw_q4_quant(None, 0, 0x100, 0x200, 0x300, 5, None)) == C.EINVAL

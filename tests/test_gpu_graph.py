@@ -126,3 +126,89 @@ def test_graph_walks_a_device_lr_schedule():
         assert float(lr.item()) == OA.f32(synth.cosine_lr(t - 1, total=7))
         assert np.array_equal(p.cpu().numpy().view(np.uint32), ref.p.view(np.uint32)), t
     assert int(step.item()) == 7
+
+
+def _build_kind(kind, seed):
+    """Two identical optimizers of one kind (state on the device), and a step function."""
+    sizes = [4099, 70_000, 33 * 64]
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    st = []
+    for n in sizes:
+        d = {"p": torch.randn(n, generator=g, device="cuda") * 0.02,
+             "g": torch.zeros(n, dtype=torch.float16, device="cuda"),
+             "m": torch.zeros(n, device="cuda")}
+        if kind in ("q8", "q4"):
+            nb = (n + (255 if kind == "q8" else 127)) // (256 if kind == "q8" else 128)
+            nc = n if kind == "q8" else (n + 1) // 2
+            d.update(m=torch.zeros(nc, dtype=torch.uint8, device="cuda"),
+                     v=torch.zeros(nc, dtype=torch.uint8, device="cuda"),
+                     am=torch.zeros(nb, device="cuda"), av=torch.zeros(nb, device="cuda"))
+        elif kind == "mini":
+            d["v"] = torch.zeros(n // (n if n != 33 * 64 else 64), device="cuda")
+        elif kind in ("ademamix",):
+            d["v"] = torch.zeros(n, device="cuda")
+            d["m2"] = torch.zeros(n, device="cuda")
+        elif kind not in ("lion", "rmsprop"):
+            d["v"] = torch.zeros(n, device="cuda")
+        st.append(d)
+    kw = {}
+    if kind in ("q8", "q4"):
+        kw = dict(mode=kind, absmax_m=[d["am"] for d in st], absmax_v=[d["av"] for d in st])
+    if kind == "ademamix":
+        kw = dict(exp_avg_slows=[d["m2"] for d in st])
+    if kind == "mini":
+        kw = dict(v_blocks=[4099, 70_000, 64])
+    opt = FusedAdamW([d["p"] for d in st], [d["g"] for d in st], [d["m"] for d in st],
+                     [d.get("v") for d in st] if "v" in st[0] else None, [0.1, 0.0, 0.1], **kw)
+
+    def step(sc):
+        opt.check_nonfinite(sc["found"])
+        args = dict(grad_scale=sc["scale"], found_inf=sc["found"])
+        if kind == "lion":
+            opt.step_lion(sc["lr"], sc["step"], **args)
+        elif kind == "rmsprop":
+            opt.step_coupled("rmsprop", sc["lr"], sc["step"], beta=0.99, **args)
+        elif kind == "ademamix":
+            opt.step_ademamix(sc["lr"], sc["step"], **args)
+        elif kind == "mini":
+            opt.step_mini(sc["lr"], sc["step"], **args)
+        else:
+            opt.step(sc["lr"], sc["step"], **args)
+    return st, opt, step
+
+
+@pytest.mark.parametrize("kind", ["lion", "rmsprop", "ademamix", "mini", "q8", "q4"])
+def test_graph_replay_matches_eager_for_every_rule(kind):
+    st_e, opt_e, step_e = _build_kind(kind, 5)
+    st_g, opt_g, step_g = _build_kind(kind, 5)
+    sc = {name: dict(lr=torch.tensor([1e-3], device="cuda"), step=torch.zeros(1, dtype=torch.int32, device="cuda"),
+                     scale=torch.tensor([1024.0], device="cuda"), found=torch.zeros(1, device="cuda"))
+          for name in ("e", "g")}
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        step_g(sc["g"])
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(6)
+    for it in range(6):
+        for a, b in zip(st_e, st_g):
+            x = torch.from_numpy((rng.normal(0, 1e-3, a["g"].numel()) * 1024).astype(np.float16))
+            a["g"].copy_(x)
+            b["g"].copy_(x)
+        if it == 3:
+            st_e[1]["g"][5] = float("inf")
+            st_g[1]["g"][5] = float("inf")
+        for name in ("e", "g"):
+            sc[name]["lr"].fill_(float(np.float32(1e-3 * 0.8 ** it)))
+        step_e(sc["e"])
+        graph.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(st_e, st_g):
+            for k in a:
+                if k == "g":
+                    continue
+                x, y = a[k], b[k]
+                assert torch.equal(x.view(torch.uint8), y.view(torch.uint8)), (kind, it, k)
+    assert int(sc["g"]["step"].item()) == int(sc["e"]["step"].item()) == 5

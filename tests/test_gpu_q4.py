@@ -119,3 +119,36 @@ def test_q4_amp_skip_leaves_codes_and_absmax():
     for k, v in d[0].items():
         assert np.array_equal(host(v).view(np.uint8), before[k].view(np.uint8)), k
     assert int(step.item()) == 7
+
+
+def test_q4_export_import_match_oracle():
+    from adamw_optimizer_step_tensor_gb300 import _capi as C
+    from oracle import qmap
+    n = 10_001
+    opt, st, d, gs, rng = _build([n], torch.bfloat16, seed=36, zero_state=False)
+    maps = O4.Maps4()
+    x = (rng.normal(0, 1e-3, n) * rng.uniform(0, 1, n)).astype(np.float32)
+    x[:128] = 0.0                        # an all-zero block
+    x[300] = np.nan                      # NaN poisons its block's absmax and codes 0
+    nb = OQ.n_blocks(n, O4.BLOCK)
+    sh = torch.cuda.current_stream().cuda_stream
+    for which, table, thr in ((0, maps.smap, maps.sthr), (1, maps.umap, maps.uthr)):
+        xs = x if which == 0 else np.abs(x)
+        xd = dev(xs)
+        codes = torch.empty((n + 1) // 2, dtype=torch.uint8, device="cuda")
+        am = torch.empty(nb, dtype=torch.float32, device="cuda")
+        C.adamw_q4_quant(opt.plan, which, xd.data_ptr(), codes.data_ptr(), am.data_ptr(), n, sh)
+        out = torch.empty(n, dtype=torch.float32, device="cuda")
+        C.adamw_q4_dequant(opt.plan, which, codes.data_ptr(), am.data_ptr(), out.data_ptr(), n, sh)
+        torch.cuda.synchronize()
+        oc, oa = O4.quantize_blockwise(xs, table, thr)
+        assert np.array_equal(host(codes), O4.pack(oc)), which
+        assert bits_equal(host(am), oa), which
+        assert np.array_equal(host(out), OQ.dequantize(oc, oa, table, O4.BLOCK), equal_nan=True), which
+    assert qmap.empty_block_code(maps.umap) == 0
+    with pytest.raises(C.AdamWError):   # an 8-bit plan refuses the 4-bit calls
+        opt8 = FusedAdamW([d[0]["p"]], [gs[0]], [torch.zeros(n, dtype=torch.uint8, device="cuda")],
+                          [torch.zeros(n, dtype=torch.uint8, device="cuda")], [0.0], mode="q8",
+                          absmax_m=[torch.zeros(OQ.n_blocks(n), device="cuda")],
+                          absmax_v=[torch.zeros(OQ.n_blocks(n), device="cuda")])
+        C.adamw_q4_dequant(opt8.plan, 0, codes.data_ptr(), am.data_ptr(), out.data_ptr(), n, sh)
