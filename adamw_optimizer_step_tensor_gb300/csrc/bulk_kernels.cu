@@ -2,10 +2,11 @@
 // momentum / RMSprop / Adagrad with coupled L2, and the element update of
 // Adam-mini) with bulk-async staging.
 //
-// One CTA per SM: a producer warp streams each 2048-element tile of every
-// input (p [+ remainder], g, m, v) into a ring of shared-memory stages with
+// One CTA per SM (two for RMSprop and Adagrad): a producer warp streams each
+// 2048-element tile of every input the rule reads (p [+ remainder], g, m, and
+// v / the slow EMA where it has them) into a ring of shared-memory stages with
 // cp.async.bulk (the TMA engine, completion counted on an mbarrier per stage),
-// and eight consumer warps update the tile from shared memory and store the
+// and sixteen consumer warps update the tile from shared memory and store the
 // results straight to global memory.  Many tiles are in flight per SM without
 // holding them in registers, which is what an HBM-bound stream needs.
 //

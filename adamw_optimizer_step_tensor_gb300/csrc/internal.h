@@ -25,8 +25,8 @@ template <> struct Tune<ADAMW_MODE_Q8> { static constexpr int unroll = 1, min_bl
 constexpr int kChunkMax = 8 * kPass;         // chunks hold up to 16384 elements (chosen per plan)
 // fp32 and bf16+remainder steps stage tiles through shared memory with bulk
 // async copies (bulk_kernels.cu) instead of 128-bit register loads.  The
-// 8-bit step keeps register loads: it is bound by instruction issue, and a
-// bulk-staged version of it measured 5% slower on GB300.
+// 8-bit and 4-bit steps keep register loads: they are bound by instruction
+// issue, and a bulk-staged 8-bit step measured 5% slower on GB300.
 constexpr bool kUseBulk = true;
 constexpr int kQBlock = ADAMW_Q8_BLOCK;      // 256
 static_assert(kPass % kQBlock == 0, "chunks must hold whole Q8 blocks");
@@ -43,7 +43,7 @@ inline int64_t choose_chunk(int64_t total, int sms, int blocks_per_sm) {
   return chunk < kQBlock ? kQBlock : (chunk > kChunkMax ? kChunkMax : chunk);
 }
 
-// Q8 nearest-code search tables (see qmap.cpp for how they are built).
+// Nearest-code search tables of the 8-bit and 4-bit maps (see qmap.cpp).
 constexpr int kBuckets = 1 + 25 * 128;       // |x| in [0, 2^-24) plus 25 binades x 128
 constexpr int kMaxRefine = 4;                // thresholds compared per lookup, at most
 

@@ -59,6 +59,8 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-l2-flush", action="store_true",
+                    help="single/amp workloads: keep L2 between timed launches (L2-resident rate)")
     ap.add_argument("--numel", type=int, default=0,
                     help="element count override for the single/amp/q8 workloads (profiling)")
     return ap.parse_args()
@@ -925,6 +927,10 @@ def main():
         return 1
     torch.cuda.set_device(local)
     w = make_workload(args.workload, args.numel)
+    if args.no_l2_flush and w.flush_l2:
+        w.flush_l2 = False
+        w.config = dict(w.config, l2="not flushed: the inputs stay resident in the 126 MB L2 "
+                                     "between timed launches (an L2-resident rate, not HBM)")
     stream = torch.cuda.current_stream()
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device="cuda") if w.flush_l2 else None
 
