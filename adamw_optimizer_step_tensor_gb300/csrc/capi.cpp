@@ -162,7 +162,8 @@ adamw_status adamw_mini_plan_create(const adamw_tensor* tensors, const int64_t* 
                                     int32_t n_tensors, adamw_mode mode, adamw_dtype grad_dtype,
                                     adamw_plan** out) {
   if (n_tensors > 0 && !v_block) return fail(ADAMW_EINVAL, "v_block is NULL");
-  return create_plan(tensors, n_tensors, mode, grad_dtype, v_block, out);
+  static const int64_t kNoBlocks = 1;   // an empty list is still an Adam-mini plan
+  return create_plan(tensors, n_tensors, mode, grad_dtype, v_block ? v_block : &kNoBlocks, out);
 }
 
 }  // extern "C"
@@ -266,7 +267,7 @@ static adamw_status create_plan(const adamw_tensor* tensors, int32_t n_tensors, 
     for (int algo : {kAlgoLion, kAlgoMomentum, kAlgoRmsprop, kAlgoAdagrad})
       if (e == cudaSuccess) e = prepare_step_bulk(mode, grad_dtype, algo);
     if (e == cudaSuccess && (with_v || !sized)) e = prepare_step_bulk(mode, grad_dtype, kAlgoAdamW);
-    if (e == cudaSuccess && with_slow) e = prepare_step_bulk(mode, grad_dtype, kAlgoAdemamix);
+    if (e == cudaSuccess && (with_slow || !sized)) e = prepare_step_bulk(mode, grad_dtype, kAlgoAdemamix);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(bulk step)");
     e = bulk_occupancy_sqrt_div(mode, grad_dtype, &bps_sd);
     if (e != cudaSuccess) return cuda_fail(e, "occupancy of the RMSprop/Adagrad step");
@@ -324,7 +325,7 @@ static adamw_status create_plan(const adamw_tensor* tensors, int32_t n_tensors, 
 
   p->device = device;
   p->bulk = bulk;
-  p->has_slow = with_slow != 0;
+  p->has_slow = with_slow != 0 || (sized == 0 && !quantized(mode));
   p->has_v = with_v != 0 || sized == 0;
   const int64_t resident = static_cast<int64_t>(bps) * sms;
   p->grid = static_cast<int>(p->n_chunks < resident ? (p->n_chunks > 0 ? p->n_chunks : 1) : resident);
