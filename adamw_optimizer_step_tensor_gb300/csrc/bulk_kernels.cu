@@ -97,21 +97,24 @@ struct Stage {
   static_assert(kBytes % 128 == 0, "stages stay 128-byte aligned");
 };
 
-// Measured on GB300 (GPT-2 list, fp32 states): 16 consumer warps with 3
-// stages moved 98% of the copy bandwidth; 8 warps x 6 stages 91%, 16 x 4-5
-// stages 97%, 24-30 warps 96-97%.
-template <int MODE> struct BulkTune { static constexpr int stages = 3; };
-// Resident CTAs per SM the register budget targets.  RMSprop and Adagrad do a
-// square root and a division for every 20 bytes (fp32) and hide their latency
-// with two CTAs per SM (GPT-2 list: 0.448 -> 0.403 ms); Lion and momentum,
-// without them, run faster at one (0.371 vs 0.384 ms).
+// Resident CTAs per SM the register budget targets, and pipeline stages per
+// CTA.  Measured on GB300 (GPT-2 list, fp32): AdamW with 16 consumer warps and
+// 3 stages moved 98% of the copy bandwidth (8 warps x 6 stages 91%, 16 x 4-5
+// stages 97%, 16 x 2 stages 96%, 24-30 warps 96-97%); Lion 3 stages 0.368 ms,
+// 4 stages 0.371, 2 stages 0.419.  RMSprop and Adagrad do a square root and a
+// division for every 20 bytes and hide their latency with two CTAs per SM of
+// two stages each (0.448 ms at 1 x 3, 0.398 at 2 x 3, 0.377 at 2 x 2, 0.412 at
+// 2 x 4); Lion and momentum, without them, run faster at one CTA (0.371 vs
+// 0.384 ms).
 template <int ALGO> struct AlgoTune {
-  static constexpr int ctas = (ALGO == kAlgoRmsprop || ALGO == kAlgoAdagrad) ? 2 : 1;
+  static constexpr bool sqrt_div = ALGO == kAlgoRmsprop || ALGO == kAlgoAdagrad;
+  static constexpr int ctas = sqrt_div ? 2 : 1;
+  static constexpr int stages = sqrt_div ? 2 : 3;
 };
 
 template <adamw_mode MODE, typename GT, int ALGO>
 constexpr int bulk_smem_bytes() {
-  return BulkTune<MODE>::stages * Stage<MODE, GT, ALGO>::kBytes + 2 * BulkTune<MODE>::stages * 8;
+  return AlgoTune<ALGO>::stages * Stage<MODE, GT, ALGO>::kBytes + 2 * AlgoTune<ALGO>::stages * 8;
 }
 
 __device__ __forceinline__ void fault(const StepArgs& a, uint32_t code) {
@@ -122,7 +125,7 @@ __device__ __forceinline__ void fault(const StepArgs& a, uint32_t code) {
 template <adamw_mode MODE, typename GT, int ALGO>
 __device__ void produce(const StepArgs& a, unsigned char* ring, uint64_t* full, uint64_t* empty) {
   using L = Stage<MODE, GT, ALGO>;
-  constexpr int S = BulkTune<MODE>::stages;
+  constexpr int S = AlgoTune<ALGO>::stages;
   uint32_t i = 0;
   bool ok = true;
   for (int64_t c = blockIdx.x; ok && c < a.n_chunks; c += gridDim.x) {
@@ -222,7 +225,7 @@ __device__ __forceinline__ void store4(const TensorDesc& td, int64_t e, const fl
 template <adamw_mode MODE, typename GT, int ALGO>
 __global__ void __launch_bounds__(kBulkThreads, AlgoTune<ALGO>::ctas) step_bulk_kernel(const StepArgs a) {
   using L = Stage<MODE, GT, ALGO>;
-  constexpr int S = BulkTune<MODE>::stages;
+  constexpr int S = AlgoTune<ALGO>::stages;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   unsigned char* ring = smem_raw;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + S * L::kBytes);
