@@ -351,7 +351,10 @@ adamw_status adamw_coupled_step(adamw_plan* plan, adamw_coupled_rule rule, const
  * adamw_check_nonfinite + adamw_step would.  *found_inf_dev (output) receives
  * 1.0f or 0.0f for the caller's loss-scale logic.  Meant for plans whose grads
  * stay in L2 between the scan and the update (the scan then costs one read of
- * the grads); other arguments as adamw_step.  fp32 and bf16+remainder modes.
+ * the grads): plans of more than 6 Mi (6,291,456) elements run
+ * adamw_check_nonfinite + adamw_step instead, with the same results and the
+ * same *found_inf_dev, because past that size the two launches are faster.
+ * Other arguments as adamw_step.  fp32 and bf16+remainder modes.
  */
 adamw_status adamw_step_amp(adamw_plan* plan, const float* lr_dev, int32_t* step_dev,
                             float beta1, float beta2, float eps,

@@ -57,8 +57,10 @@ def test_fused_amp_matches_oracle_and_skips():
 
 
 @pytest.mark.parametrize("mode", ["fp32", "bf16_rem"])
-def test_fused_amp_equals_two_launch_path(mode):
-    sizes = [1, 4099, 70000, 0, 257]
+@pytest.mark.parametrize("big", [False, True])
+def test_fused_amp_equals_two_launch_path(mode, big):
+    # big: more than 6 Mi elements, where adamw_step_amp itself runs the two launches
+    sizes = [1, 4099, 7_000_000 if big else 70000, 0, 257]
     rng = np.random.default_rng(32)
     sides = []
     for _ in range(2):
