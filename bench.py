@@ -405,13 +405,19 @@ class Gpt2Small(Workload):
         self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)
         self.lr_ptrs = [self.lr_table.data_ptr() + 4 * s for s in range(100)]
         self.stream = torch.cuda.current_stream().cuda_stream
-        self.config = {"workload": "gpt2_small fp32 param list, cosine lr from a device table",
-                       "tensors": len(self.specs), "numel": self.n_params,
-                       "bytes_per_param": self.bytes_per_param,
-                       "grad_dtype": "f32", "state_dtype": "f32",
-                       "l2": "no flush: 3.48 GB moved per step, larger than the 126 MB L2",
-                       "lr_schedule": "cosine 1e-3 -> 1e-4 over 100 steps, lr_dev points into it"}
+        self.config = Gpt2Small.describe()
         self._host = None
+
+    @classmethod
+    def describe(cls, seed=0):
+        import synth
+        specs = synth.gpt2_small()
+        return {"workload": "gpt2_small fp32 param list, cosine lr from a device table",
+                "tensors": len(specs), "numel": synth.total_numel(specs),
+                "bytes_per_param": Gpt2Small.bytes_per_param,
+                "grad_dtype": "f32", "state_dtype": "f32",
+                "l2": "no flush: 3.48 GB moved per step, larger than the 126 MB L2",
+                "lr_schedule": "cosine 1e-3 -> 1e-4 over 100 steps, lr_dev points into it"}
 
     def step(self, i):
         self.C.adamw_step(self.opt.plan, self.lr_ptrs[i % 100], self.step_dev.data_ptr(), 0.9, 0.999,
@@ -496,10 +502,14 @@ class AdemamixGpt2(Gpt2Small):
         self.m2s = m2s
         self.opt = FusedAdamW(self.ps, self.gs, self.ms, self.vs, [s.wd for s in self.specs],
                               exp_avg_slows=m2s)
-        self.config = dict(self.config, workload="gpt2_small fp32 param list, AdEMAMix (m1, m2, v), "
-                           "cosine lr from a device table", bytes_per_param=self.bytes_per_param,
-                           l2="no flush: 4.48 GB moved per step, larger than the 126 MB L2")
+        self.config = AdemamixGpt2.describe()
         self.e2e_what = self.e2e_what.replace("adamw_step", "adamw_ademamix_step")
+
+    @classmethod
+    def describe(cls, seed=0):
+        return dict(Gpt2Small.describe(), workload="gpt2_small fp32 param list, AdEMAMix (m1, m2, v), "
+                    "cosine lr from a device table", bytes_per_param=AdemamixGpt2.bytes_per_param,
+                    l2="no flush: 4.48 GB moved per step, larger than the 126 MB L2")
 
     def step(self, i):
         self.C.adamw_ademamix_step(self.opt.plan, self.lr_ptrs[i % 100], self.step_dev.data_ptr(),
@@ -526,10 +536,14 @@ class LionGpt2(Gpt2Small):
         from adamw_optimizer_step_tensor_gb300 import FusedAdamW
         self.opt = FusedAdamW(self.ps, self.gs, self.ms, None, [s.wd for s in self.specs])
         self.vs = self.v_buf = None
-        self.config = dict(self.config, workload="gpt2_small fp32 param list, Lion (m only), "
-                           "cosine lr from a device table", bytes_per_param=self.bytes_per_param,
-                           l2="no flush: 2.49 GB moved per step, larger than the 126 MB L2")
+        self.config = LionGpt2.describe()
         self.e2e_what = self.e2e_what.replace("adamw_step", "adamw_lion_step")
+
+    @classmethod
+    def describe(cls, seed=0):
+        return dict(Gpt2Small.describe(), workload="gpt2_small fp32 param list, Lion (m only), "
+                    "cosine lr from a device table", bytes_per_param=LionGpt2.bytes_per_param,
+                    l2="no flush: 2.49 GB moved per step, larger than the 126 MB L2")
 
     def step(self, i):
         self.C.adamw_lion_step(self.opt.plan, self.lr_ptrs[i % 100], self.step_dev.data_ptr(),
@@ -555,9 +569,13 @@ class CoupledGpt2(LionGpt2):
         self.rule = rule
         self.rule_id = self.C.RULES[rule]
         self.name = f"{rule}_gpt2_small_fp32"
-        self.config = dict(self.config, workload=f"gpt2_small fp32 param list, {rule} with coupled L2 "
-                           "(one state), cosine lr from a device table")
+        self.config = CoupledGpt2.describe(rule)
         self.e2e_what = self.e2e_what.replace("adamw_lion_step", "adamw_coupled_step")
+
+    @classmethod
+    def describe(cls, rule, seed=0):
+        return dict(LionGpt2.describe(), workload=f"gpt2_small fp32 param list, {rule} with coupled "
+                    "L2 (one state), cosine lr from a device table")
 
     def step(self, i):
         self.C.adamw_coupled_step(self.opt.plan, self.rule_id, self.lr_ptrs[i % 100],
@@ -598,13 +616,17 @@ class Single(Workload):
             self.name = "amp_fp16_grads_1M_l2flush"
             self.bytes_per_param = 28.0
             self.inject = synth.amp_injection(10 ** 6, n, seed=3)
-        self.config = {"workload": ("AMP fp16 grads x65536, unscale + found_inf skip, 1 tensor, "
-                                    + ("check and step in one cooperative launch" if fused
-                                       else "check and step as two launches")
-                                    if amp else "single fp32 tensor"),
-                       "tensors": 1, "numel": n, "bytes_per_param": self.bytes_per_param,
-                       "l2": f"L2 flushed ({L2_FLUSH_BYTES >> 20} MB write) before every timed launch; "
-                             "launch times summed"}
+        self.config = Single.describe(amp=amp, numel=numel, fused=fused)
+
+    @classmethod
+    def describe(cls, amp=False, seed=1, numel=0, fused=False):
+        return {"workload": ("AMP fp16 grads x65536, unscale + found_inf skip, 1 tensor, "
+                             + ("check and step in one launch (adamw_step_amp)" if fused
+                                else "check and step as two launches")
+                             if amp else "single fp32 tensor"),
+                "tensors": 1, "numel": numel or (1 << 20), "bytes_per_param": 28.0,
+                "l2": f"L2 flushed ({L2_FLUSH_BYTES >> 20} MB write) before every timed launch; "
+                      "launch times summed"}
 
     def step(self, i):
         if self.amp and self.fused:
@@ -657,9 +679,13 @@ class Q8(Workload):
         self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)
         self.stream = torch.cuda.current_stream().cuda_stream
         self.dtype = "f32 (u8 states)"
-        self.config = {"workload": "8-bit blockwise m,v; one flat fp32 param of 2^30, bf16 grads",
-                       "tensors": 1, "numel": n, "bytes_per_param": self.bytes_per_param,
-                       "l2": "no flush: 15.1 GB moved per step"}
+        self.config = Q8.describe(numel=numel)
+
+    @classmethod
+    def describe(cls, seed=4, numel=0):
+        return {"workload": "8-bit blockwise m,v; one flat fp32 param of 2^30, bf16 grads",
+                "tensors": 1, "numel": numel or (1 << 30), "bytes_per_param": Q8.bytes_per_param,
+                "l2": "no flush: 15.1 GB moved per step"}
 
     def step(self, i):
         self.C.adamw_step(self.opt.plan, self.lr.data_ptr(), self.step_dev.data_ptr(), 0.9, 0.999,
@@ -704,10 +730,14 @@ class Q4(Q8):
         self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)
         self.stream = torch.cuda.current_stream().cuda_stream
         self.dtype = "f32 (4-bit states)"
-        self.config = {"workload": "4-bit blockwise m,v (128-element blocks); one flat fp32 param "
-                                   "of 2^30, bf16 grads",
-                       "tensors": 1, "numel": n, "bytes_per_param": self.bytes_per_param,
-                       "l2": "no flush: 13.0 GB moved per step"}
+        self.config = Q4.describe(numel=numel)
+
+    @classmethod
+    def describe(cls, seed=4, numel=0):
+        return {"workload": "4-bit blockwise m,v (128-element blocks); one flat fp32 param "
+                            "of 2^30, bf16 grads",
+                "tensors": 1, "numel": numel or (1 << 30), "bytes_per_param": Q4.bytes_per_param,
+                "l2": "no flush: 13.0 GB moved per step"}
 
 
 class Llama3(Workload):
@@ -743,10 +773,15 @@ class Llama3(Workload):
         self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)
         self.stream = torch.cuda.current_stream().cuda_stream
         self.dtype = "f32 (bf16+int16 params)"
-        self.config = {"workload": "Llama-3-8B param list, bf16 params + int16 remainders",
-                       "tensors": len(self.specs), "numel": self.n_params,
-                       "bytes_per_param": self.bytes_per_param,
-                       "l2": "no flush: 209 GB moved per step"}
+        self.config = Llama3.describe()
+
+    @classmethod
+    def describe(cls, seed=5):
+        import synth
+        specs = synth.llama3_8b()
+        return {"workload": "Llama-3-8B param list, bf16 params + int16 remainders",
+                "tensors": len(specs), "numel": synth.total_numel(specs),
+                "bytes_per_param": Llama3.bytes_per_param, "l2": "no flush: 209 GB moved per step"}
 
     def step(self, i):
         self.C.adamw_step(self.opt.plan, self.lr.data_ptr(), self.step_dev.data_ptr(), 0.9, 0.999,
@@ -792,22 +827,28 @@ class MiniLlama3(Workload):
         wds = [0.0 if "norm" in s.name else 0.1 for s in self.specs]
         self.opt = FusedAdamW(hs, gs, ms, vs, wds, mode="bf16_rem", param_rems=rs, v_blocks=blocks)
         self._views = (hs, rs, gs, ms, vs)
-        n_elem_v = sum(s.numel for s, b in zip(self.specs, blocks) if b == 1)
-        n_shared = self.n_params - n_elem_v
-        # reduction: g (2); update: p 2 + rem 2 + g 2 + m 4 read, p 2 + rem 2 + m 4 written;
-        # per-element v (embeddings, output) adds 4 + 4
-        total = 2 * n_shared + 18 * self.n_params + 8 * n_elem_v
-        self.bytes_per_param = total / self.n_params
+        self.config = MiniLlama3.describe()
+        self.bytes_per_param = self.config["bytes_per_param"]
         self.lr = torch.tensor([3e-4], dtype=torch.float32, device=dev)
         self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)
         self.stream = torch.cuda.current_stream().cuda_stream
         self.dtype = "f32 (bf16+int16 params)"
-        self.config = {"workload": "Adam-mini on the Llama-3-8B param list (v per element for "
-                                   "embeddings/output, per head for wq/wk, per tensor elsewhere), "
-                                   "bf16 params + int16 remainders",
-                       "tensors": len(self.specs), "numel": self.n_params,
-                       "v_blocks": len(set(blocks)), "bytes_per_param": round(self.bytes_per_param, 4),
-                       "l2": f"no flush: {total / 1e9:.0f} GB moved per step"}
+
+    @classmethod
+    def describe(cls, seed=5):
+        import synth
+        specs = synth.llama3_8b()
+        blocks = synth.adam_mini_blocks(specs, dim=4096, n_heads=32)
+        n = synth.total_numel(specs)
+        n_elem_v = sum(s.numel for s, b in zip(specs, blocks) if b == 1)
+        # reduction: g (2) of the shared-v tensors; update: p 2 + rem 2 + g 2 + m 4 read,
+        # p 2 + rem 2 + m 4 written; per-element v (embeddings, output) adds 4 + 4
+        total = 2 * (n - n_elem_v) + 18 * n + 8 * n_elem_v
+        return {"workload": "Adam-mini on the Llama-3-8B param list (v per element for "
+                            "embeddings/output, per head for wq/wk, per tensor elsewhere), "
+                            "bf16 params + int16 remainders",
+                "tensors": len(specs), "numel": n, "v_blocks": len(set(blocks)),
+                "bytes_per_param": total / n, "l2": f"no flush: {total / 1e9:.0f} GB moved per step"}
 
     def step(self, i):
         self.C.adamw_mini_step(self.opt.plan, self.lr.data_ptr(), self.step_dev.data_ptr(), 0.9, 0.999,
@@ -839,27 +880,41 @@ class Bf16Rem(Workload):
         self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)
         self.stream = torch.cuda.current_stream().cuda_stream
         self.dtype = "f32 (bf16+int16 params)"
-        self.config = {"workload": "one flat bf16+remainder tensor, bf16 grads", "tensors": 1,
-                       "numel": n, "bytes_per_param": self.bytes_per_param,
-                       "l2": "no flush: inputs larger than L2"}
+        self.config = Bf16Rem.describe(numel=numel)
+
+    @classmethod
+    def describe(cls, seed=6, numel=0):
+        return {"workload": "one flat bf16+remainder tensor, bf16 grads", "tensors": 1,
+                "numel": numel or (1 << 26), "bytes_per_param": Bf16Rem.bytes_per_param,
+                "l2": "no flush: inputs larger than L2"}
 
     def step(self, i):
         self.C.adamw_step(self.opt.plan, self.lr.data_ptr(), self.step_dev.data_ptr(), 0.9, 0.999,
                           1e-8, None, None, self.stream)
 
 
+def _workload_table(numel):
+    """name -> (class, constructor arguments); the constructor builds the workload on the
+    device, ``describe`` with the same arguments gives its config without a device."""
+    return {"gpt2_small": (Gpt2Small, {}), "single": (Single, dict(numel=numel)),
+            "amp": (Single, dict(amp=True, numel=numel)), "q8": (Q8, dict(numel=numel)),
+            "amp_fused": (Single, dict(amp=True, numel=numel, fused=True)),
+            "llama3_8b": (Llama3, {}), "bf16rem": (Bf16Rem, dict(numel=numel)),
+            "ademamix_gpt2": (AdemamixGpt2, {}), "lion_gpt2": (LionGpt2, {}),
+            "momentum_gpt2": (CoupledGpt2, dict(rule="momentum")),
+            "rmsprop_gpt2": (CoupledGpt2, dict(rule="rmsprop")),
+            "adagrad_gpt2": (CoupledGpt2, dict(rule="adagrad")),
+            "q4": (Q4, dict(numel=numel)), "adam_mini_llama3": (MiniLlama3, {})}
+
+
 def make_workload(name, numel=0):
-    return {"gpt2_small": lambda: Gpt2Small(), "single": lambda: Single(numel=numel),
-            "amp": lambda: Single(amp=True, numel=numel), "q8": lambda: Q8(numel=numel),
-            "amp_fused": lambda: Single(amp=True, numel=numel, fused=True),
-            "llama3_8b": lambda: Llama3(), "bf16rem": lambda: Bf16Rem(numel=numel),
-            "ademamix_gpt2": lambda: AdemamixGpt2(),
-            "lion_gpt2": lambda: LionGpt2(),
-            "momentum_gpt2": lambda: CoupledGpt2("momentum"),
-            "rmsprop_gpt2": lambda: CoupledGpt2("rmsprop"),
-            "adagrad_gpt2": lambda: CoupledGpt2("adagrad"),
-            "q4": lambda: Q4(numel=numel),
-            "adam_mini_llama3": lambda: MiniLlama3()}[name]()
+    cls, kw = _workload_table(numel)[name]
+    return cls(**kw)
+
+
+def describe_workload(name, numel=0):
+    cls, kw = _workload_table(numel)[name]
+    return cls.describe(**kw)
 
 
 # ----------------------------------------------------------------------------- CPU timing
@@ -907,7 +962,7 @@ def run_reference(args, rank, world):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": args.workload, "sample_elements_per_step": n},
+            "config": dict(describe_workload(args.workload, args.numel), parallelism="1 GPU"),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
