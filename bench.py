@@ -611,7 +611,8 @@ class Single(Workload):
         self.found = torch.zeros(1, device=dev)
         self.stream = torch.cuda.current_stream().cuda_stream
         self.fused = fused
-        self.launches_per_step = 2 if amp and not fused else 1
+        # adamw_step_amp runs the check and the step as two launches above 6 Mi elements
+        self.launches_per_step = 2 if amp and (not fused or n > (6 << 20)) else 1
         if amp:
             self.name = "amp_fp16_grads_1M_l2flush"
             self.bytes_per_param = 28.0
