@@ -95,7 +95,7 @@ __global__ void __launch_bounds__(kThreads, kQ4MinBlocks) step_q4_kernel(const S
         quant8<R>(m, nm, qt.map[0], zc_m, q_m);
         __stcs(reinterpret_cast<uint32_t*>(cm + e / 2), pack_nibbles(q_m));
         const BlockNorm nv = block_norm(half_warp_max(mx_v));
-        quant8<R>(v, nv, qt.map[1], zc_v, q_v);
+        quant8<R, false>(v, nv, qt.map[1], zc_v, q_v);
         __stcs(reinterpret_cast<uint32_t*>(cv + e / 2), pack_nibbles(q_v));
         if ((lane & 15) == 0) {
           td.am[blk] = __uint_as_float(nm.bits);
@@ -126,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, kQ4MinBlocks) step_q4_kernel(const S
         const BlockNorm nm = block_norm(half_warp_max(mx_m));
         const BlockNorm nv = block_norm(half_warp_max(mx_v));
         quant8<R>(m, nm, qt.map[0], zc_m, q_m);
-        quant8<R>(v, nv, qt.map[1], zc_v, q_v);
+        quant8<R, false>(v, nv, qt.map[1], zc_v, q_v);
 #pragma unroll
         for (int i = 0; i < 8; i += 2) {
           if (i < n) {

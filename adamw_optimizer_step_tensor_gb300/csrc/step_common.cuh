@@ -282,11 +282,13 @@ __device__ void update_scalar(const TensorDesc& td, int64_t e, int n, const Scal
 // thresholds lie inside a bucket, and code = lo + #{r < R : thr[lo + r] <= x}
 // because thr is ascending.  NaN lands in the last bucket, whose lowest code
 // is 0 and whose thresholds never compare true: code 0.
-template <int R>
+template <int R, bool kSigned = true>
 __device__ __forceinline__ uint32_t nearest_code(float x, const QMapDev& t) {
   const uint32_t b = __float_as_uint(x);
   const int k = bucket_of(b & 0x7FFFFFFFu);
-  const uint32_t lo = (b >> 31) ? t.lo_neg[k] : t.lo_pos[k];
+  // the second moment is never negative (a NaN of either sign reaches the last
+  // bucket of either table, whose lowest code is 0): its lookups skip the sign
+  const uint32_t lo = (kSigned && (b >> 31)) ? t.lo_neg[k] : t.lo_pos[k];
   uint32_t c = lo;
 #pragma unroll
   for (int r = 0; r < R; ++r) c += (t.thr[lo + r] <= x) ? 1u : 0u;
@@ -312,7 +314,7 @@ __device__ __forceinline__ BlockNorm block_norm(uint32_t amax_bits) {
 // Codes of the 8 values one lane owns.  All branches are warp-uniform (the
 // block constants are the same in every lane); x * 1 is exact, so the
 // scaled multiply is skipped when the scale is 1.
-template <int R>
+template <int R, bool kSigned = true>
 __device__ __forceinline__ void quant8(const float (&x)[8], const BlockNorm& n,
                                        const QMapDev& t, uint32_t zero_code, uint32_t (&q)[8]) {
   if (n.bits == 0u) {
@@ -320,11 +322,11 @@ __device__ __forceinline__ void quant8(const float (&x)[8], const BlockNorm& n,
     for (int i = 0; i < 8; ++i) q[i] = zero_code;
   } else if (n.scale == 1.0f) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = nearest_code<R>(__fmul_rn(x[i], n.inv), t);
+    for (int i = 0; i < 8; ++i) q[i] = nearest_code<R, kSigned>(__fmul_rn(x[i], n.inv), t);
   } else {
 #pragma unroll
     for (int i = 0; i < 8; ++i)
-      q[i] = nearest_code<R>(__fmul_rn(__fmul_rn(x[i], n.scale), n.inv), t);
+      q[i] = nearest_code<R, kSigned>(__fmul_rn(__fmul_rn(x[i], n.scale), n.inv), t);
   }
 }
 

@@ -337,7 +337,7 @@ step_q8_kernel(const StepArgs a) {
         quant8<R>(m, nm, qt.map[0], zc_m, q_m);
         __stcs(reinterpret_cast<uint2*>(cm + e), pack8(q_m));
         const BlockNorm nv = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_v));
-        quant8<R>(v, nv, qt.map[1], zc_v, q_v);
+        quant8<R, false>(v, nv, qt.map[1], zc_v, q_v);
         __stcs(reinterpret_cast<uint2*>(cv + e), pack8(q_v));
         if (lane == 0) {
           td.am[blk] = __uint_as_float(nm.bits);
@@ -363,7 +363,7 @@ step_q8_kernel(const StepArgs a) {
         const BlockNorm nm = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_m));
         const BlockNorm nv = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_v));
         quant8<R>(m, nm, qt.map[0], zc_m, q_m);
-        quant8<R>(v, nv, qt.map[1], zc_v, q_v);
+        quant8<R, false>(v, nv, qt.map[1], zc_v, q_v);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           if (i < n) {
