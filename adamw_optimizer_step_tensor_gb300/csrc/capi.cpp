@@ -355,7 +355,7 @@ static adamw_status create_plan(const adamw_tensor* tensors, int32_t n_tensors, 
     p->mini = true;
     p->n_blocks = static_cast<int64_t>(blocks.size());
     p->n_red = static_cast<int64_t>(red_chunks.size());
-    const int64_t red_res = 8LL * sms;
+    const int64_t red_res = 32LL * sms;   // several waves: the grid-stride tail balances
     p->grid_red = static_cast<int>(p->n_red < 1 ? 1 : (p->n_red < red_res ? p->n_red : red_res));
     if ((e = prepare_step_bulk(mode, grad_dtype, kAlgoMini)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(Adam-mini step)");
