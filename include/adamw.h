@@ -22,7 +22,10 @@
  * float32 (the bias correction of sqrt(v) is a multiplication by its
  * reciprocal rather than a per-element division).
  * Results are therefore reproducible bit for bit by any IEEE float32
- * implementation of the same sequence.
+ * implementation of the same sequence.  The other rules (AdEMAMix, Lion, the
+ * coupled-L2 rules, Adam-mini) and the 8-bit and 4-bit modes state their own
+ * sequences below in the same terms; the one fused multiply-add in the library
+ * is the exact split of a square in the Adam-mini block reduction.
  *
  * Conventions shared by all entry points
  *   - Every tensor, scalar and stream is owned by the caller.  Pointers named
@@ -30,7 +33,9 @@
  *     was current when the plan was created.
  *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *     stream).  Device work is asynchronous on it; no entry point that takes
- *     a stream synchronises the host or allocates memory.
+ *     a stream allocates memory, and none synchronises the host except
+ *     adamw_step_noalloc (its table upload is a pageable copy) and the
+ *     self-test.
  *   - Arguments are validated before any launch; a non-OK status means
  *     nothing was enqueued.  adamw_last_error() returns a message for the
  *     last non-OK status of the calling thread.  Nothing is thrown across
@@ -178,7 +183,7 @@ adamw_status adamw_check_nonfinite(const adamw_plan* plan, float* found_inf_dev,
  *                  rebuilt ("4 bit Adam should support non constant lr").
  *   step_dev       device int32 count of completed steps; this step uses
  *                  t = *step_dev + 1 and stores t there unless skipped.
- *   beta1, beta2   in [0, 1); eps > 0 (float32).
+ *   beta1, beta2   in [0, 1); eps finite and >= 0 (float32); EINVAL otherwise.
  *   grad_scale_dev NULL, or device fp32 loss scale: grads are multiplied by
  *                  1 / *grad_scale_dev before use.
  *   found_inf_dev  NULL, or device fp32 flag: when non-zero at run time the
