@@ -119,6 +119,50 @@ adamw_status check_device(const adamw_plan* p) {
   return ADAMW_OK;
 }
 
+// Checks every step entry point shares: the plan, the run-time scalar pointers
+// (lr and step required, grad scale and found-inf optional) and betas in [0, 1).
+adamw_status check_step(const adamw_plan* plan, const float* lr_dev, const int32_t* step_dev,
+                        const float* grad_scale_dev, const float* found_inf_dev,
+                        float beta1, float beta2) {
+  if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
+  if (!lr_dev || !step_dev) return fail(ADAMW_EINVAL, "lr_dev and step_dev must be set");
+  if (!aligned(lr_dev, 4) || !aligned(step_dev, 4) || !aligned(grad_scale_dev, 4) ||
+      !aligned(found_inf_dev, 4))
+    return fail(ADAMW_EALIGN, "a scalar pointer is not 4-byte aligned");
+  if (!(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f))
+    return fail(ADAMW_EINVAL, "betas must lie in [0, 1)");
+  return ADAMW_OK;
+}
+
+adamw_status check_eps(float eps) {
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(ADAMW_EINVAL, "eps must be finite and >= 0");
+  return ADAMW_OK;
+}
+
+// The launch arguments every step shares; rule-specific fields keep their
+// neutral values (no slow EMA, no code maps, no Adam-mini blocks).
+StepArgs step_args(const adamw_plan* plan, const float* lr_dev, int32_t* step_dev,
+                   const float* grad_scale_dev, const float* found_inf_dev, float beta1,
+                   float beta2, float eps) {
+  StepArgs a;
+  a.tensors = plan->d_tensors;
+  a.chunks = plan->d_chunks;
+  a.n_chunks = plan->n_chunks;
+  a.lr = lr_dev;
+  a.step = step_dev;
+  a.grad_scale = grad_scale_dev;
+  a.found_inf = found_inf_dev;
+  a.beta1 = beta1;
+  a.beta2 = beta2;
+  a.eps = eps;
+  a.beta3 = 0.0f;
+  a.alpha = 0.0f;
+  a.scratch = plan->d_scratch;
+  a.qt = nullptr;
+  a.refine = 1;
+  return a;
+}
+
 // n = 256 (8-bit maps, both must contain 0.0) or 16 (the 4-bit maps; the v
 // map has no zero and an all-zero block stores code 0).
 adamw_status build_qtables(const float* smap, const float* umap, int n, QTables* qt) {
@@ -492,32 +536,13 @@ adamw_status adamw_check_nonfinite(const adamw_plan* plan, float* found_inf_dev,
 adamw_status adamw_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev, float beta1,
                         float beta2, float eps, const float* grad_scale_dev,
                         const float* found_inf_dev, void* stream) {
-  if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
-  if (!lr_dev || !step_dev) return fail(ADAMW_EINVAL, "lr_dev and step_dev must be set");
-  if (!aligned(lr_dev, 4) || !aligned(step_dev, 4) || !aligned(grad_scale_dev, 4) ||
-      !aligned(found_inf_dev, 4))
-    return fail(ADAMW_EALIGN, "a scalar pointer is not 4-byte aligned");
-  if (!(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f))
-    return fail(ADAMW_EINVAL, "betas must lie in [0, 1)");
-  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(ADAMW_EINVAL, "eps must be finite and >= 0");
+  adamw_status st = check_step(plan, lr_dev, step_dev, grad_scale_dev, found_inf_dev, beta1, beta2);
+  if (st == ADAMW_OK) st = check_eps(eps);
+  if (st != ADAMW_OK) return st;
   if (!plan->has_v) return fail(ADAMW_EINVAL, "the plan's tensors carry no exp_avg_sq");
   if (plan->mini) return fail(ADAMW_EINVAL, "an Adam-mini plan steps with adamw_mini_step");
-  adamw_status st = check_device(plan);
-  if (st != ADAMW_OK) return st;
-  StepArgs a;
-  a.tensors = plan->d_tensors;
-  a.chunks = plan->d_chunks;
-  a.n_chunks = plan->n_chunks;
-  a.lr = lr_dev;
-  a.step = step_dev;
-  a.grad_scale = grad_scale_dev;
-  a.found_inf = found_inf_dev;
-  a.beta1 = beta1;
-  a.beta2 = beta2;
-  a.eps = eps;
-  a.beta3 = 0.0f;
-  a.alpha = 0.0f;
-  a.scratch = plan->d_scratch;
+  if ((st = check_device(plan)) != ADAMW_OK) return st;
+  StepArgs a = step_args(plan, lr_dev, step_dev, grad_scale_dev, found_inf_dev, beta1, beta2, eps);
   a.qt = plan->d_qt;
   a.refine = plan->refine;
   cudaStream_t st_ = static_cast<cudaStream_t>(stream);
@@ -542,36 +567,17 @@ adamw_status adamw_ademamix_step(adamw_plan* plan, const float* lr_dev, int32_t*
                                  float beta1, float beta2, float beta3, float alpha, float eps,
                                  const float* grad_scale_dev, const float* found_inf_dev,
                                  void* stream) {
-  if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
+  adamw_status st = check_step(plan, lr_dev, step_dev, grad_scale_dev, found_inf_dev, beta1, beta2);
+  if (st == ADAMW_OK) st = check_eps(eps);
+  if (st != ADAMW_OK) return st;
   if (!plan->has_slow)
     return fail(ADAMW_EINVAL, "the plan's tensors carry no exp_avg_slow (AdEMAMix slow EMA)");
-  if (!lr_dev || !step_dev) return fail(ADAMW_EINVAL, "lr_dev and step_dev must be set");
-  if (!aligned(lr_dev, 4) || !aligned(step_dev, 4) || !aligned(grad_scale_dev, 4) ||
-      !aligned(found_inf_dev, 4))
-    return fail(ADAMW_EALIGN, "a scalar pointer is not 4-byte aligned");
-  if (!(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f) ||
-      !(beta3 >= 0.0f && beta3 < 1.0f))
-    return fail(ADAMW_EINVAL, "betas must lie in [0, 1)");
+  if (!(beta3 >= 0.0f && beta3 < 1.0f)) return fail(ADAMW_EINVAL, "betas must lie in [0, 1)");
   if (!std::isfinite(alpha)) return fail(ADAMW_EINVAL, "alpha must be finite");
-  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(ADAMW_EINVAL, "eps must be finite and >= 0");
-  adamw_status st = check_device(plan);
-  if (st != ADAMW_OK) return st;
-  StepArgs a;
-  a.tensors = plan->d_tensors;
-  a.chunks = plan->d_chunks;
-  a.n_chunks = plan->n_chunks;
-  a.lr = lr_dev;
-  a.step = step_dev;
-  a.grad_scale = grad_scale_dev;
-  a.found_inf = found_inf_dev;
-  a.beta1 = beta1;
-  a.beta2 = beta2;
-  a.eps = eps;
+  if ((st = check_device(plan)) != ADAMW_OK) return st;
+  StepArgs a = step_args(plan, lr_dev, step_dev, grad_scale_dev, found_inf_dev, beta1, beta2, eps);
   a.beta3 = beta3;
   a.alpha = alpha;
-  a.scratch = plan->d_scratch;
-  a.qt = nullptr;
-  a.refine = 1;
   cudaError_t e = launch_step_bulk(plan->mode, plan->gdt, a, plan->grid,
                                    static_cast<cudaStream_t>(stream), kAlgoAdemamix);
   if (e != cudaSuccess) return cuda_fail(e, "launch AdEMAMix step");
@@ -581,33 +587,12 @@ adamw_status adamw_ademamix_step(adamw_plan* plan, const float* lr_dev, int32_t*
 adamw_status adamw_mini_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev,
                              float beta1, float beta2, float eps, const float* grad_scale_dev,
                              const float* found_inf_dev, void* stream) {
-  if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
-  if (!plan->mini) return fail(ADAMW_EINVAL, "the plan was not made by adamw_mini_plan_create");
-  if (!lr_dev || !step_dev) return fail(ADAMW_EINVAL, "lr_dev and step_dev must be set");
-  if (!aligned(lr_dev, 4) || !aligned(step_dev, 4) || !aligned(grad_scale_dev, 4) ||
-      !aligned(found_inf_dev, 4))
-    return fail(ADAMW_EALIGN, "a scalar pointer is not 4-byte aligned");
-  if (!(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f))
-    return fail(ADAMW_EINVAL, "betas must lie in [0, 1)");
-  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(ADAMW_EINVAL, "eps must be finite and >= 0");
-  adamw_status st = check_device(plan);
+  adamw_status st = check_step(plan, lr_dev, step_dev, grad_scale_dev, found_inf_dev, beta1, beta2);
+  if (st == ADAMW_OK) st = check_eps(eps);
   if (st != ADAMW_OK) return st;
-  StepArgs a;
-  a.tensors = plan->d_tensors;
-  a.chunks = plan->d_chunks;
-  a.n_chunks = plan->n_chunks;
-  a.lr = lr_dev;
-  a.step = step_dev;
-  a.grad_scale = grad_scale_dev;
-  a.found_inf = found_inf_dev;
-  a.beta1 = beta1;
-  a.beta2 = beta2;
-  a.eps = eps;
-  a.beta3 = 0.0f;
-  a.alpha = 0.0f;
-  a.scratch = plan->d_scratch;
-  a.qt = nullptr;
-  a.refine = 1;
+  if (!plan->mini) return fail(ADAMW_EINVAL, "the plan was not made by adamw_mini_plan_create");
+  if ((st = check_device(plan)) != ADAMW_OK) return st;
+  StepArgs a = step_args(plan, lr_dev, step_dev, grad_scale_dev, found_inf_dev, beta1, beta2, eps);
   a.chunk_blk = plan->d_chunk_blk;
   a.blk_r = plan->d_blk_r;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -631,33 +616,12 @@ adamw_status adamw_mini_step(adamw_plan* plan, const float* lr_dev, int32_t* ste
 adamw_status adamw_lion_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev,
                              float beta1, float beta2, const float* grad_scale_dev,
                              const float* found_inf_dev, void* stream) {
-  if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
+  adamw_status st = check_step(plan, lr_dev, step_dev, grad_scale_dev, found_inf_dev, beta1, beta2);
+  if (st != ADAMW_OK) return st;
   if (quantized(plan->mode))
     return fail(ADAMW_EUNSUPPORTED, "Lion covers the fp32 and bf16+remainder modes");
-  if (!lr_dev || !step_dev) return fail(ADAMW_EINVAL, "lr_dev and step_dev must be set");
-  if (!aligned(lr_dev, 4) || !aligned(step_dev, 4) || !aligned(grad_scale_dev, 4) ||
-      !aligned(found_inf_dev, 4))
-    return fail(ADAMW_EALIGN, "a scalar pointer is not 4-byte aligned");
-  if (!(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f))
-    return fail(ADAMW_EINVAL, "betas must lie in [0, 1)");
-  adamw_status st = check_device(plan);
-  if (st != ADAMW_OK) return st;
-  StepArgs a;
-  a.tensors = plan->d_tensors;
-  a.chunks = plan->d_chunks;
-  a.n_chunks = plan->n_chunks;
-  a.lr = lr_dev;
-  a.step = step_dev;
-  a.grad_scale = grad_scale_dev;
-  a.found_inf = found_inf_dev;
-  a.beta1 = beta1;
-  a.beta2 = beta2;
-  a.eps = 0.0f;
-  a.beta3 = 0.0f;
-  a.alpha = 0.0f;
-  a.scratch = plan->d_scratch;
-  a.qt = nullptr;
-  a.refine = 1;
+  if ((st = check_device(plan)) != ADAMW_OK) return st;
+  StepArgs a = step_args(plan, lr_dev, step_dev, grad_scale_dev, found_inf_dev, beta1, beta2, 0.0f);
   cudaError_t e = launch_step_bulk(plan->mode, plan->gdt, a, plan->grid,
                                    static_cast<cudaStream_t>(stream), kAlgoLion);
   if (e != cudaSuccess) return cuda_fail(e, "launch Lion step");
@@ -668,7 +632,9 @@ adamw_status adamw_coupled_step(adamw_plan* plan, adamw_coupled_rule rule, const
                                 int32_t* step_dev, float beta, float eps,
                                 const float* grad_scale_dev, const float* found_inf_dev,
                                 void* stream) {
-  if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
+  adamw_status st = check_step(plan, lr_dev, step_dev, grad_scale_dev, found_inf_dev, beta, 0.0f);
+  if (st == ADAMW_OK) st = check_eps(eps);
+  if (st != ADAMW_OK) return st;
   int algo;
   switch (rule) {
     case ADAMW_RULE_MOMENTUM: algo = kAlgoMomentum; break;
@@ -678,30 +644,9 @@ adamw_status adamw_coupled_step(adamw_plan* plan, adamw_coupled_rule rule, const
   }
   if (quantized(plan->mode))
     return fail(ADAMW_EUNSUPPORTED, "the coupled rules cover the fp32 and bf16+remainder modes");
-  if (!lr_dev || !step_dev) return fail(ADAMW_EINVAL, "lr_dev and step_dev must be set");
-  if (!aligned(lr_dev, 4) || !aligned(step_dev, 4) || !aligned(grad_scale_dev, 4) ||
-      !aligned(found_inf_dev, 4))
-    return fail(ADAMW_EALIGN, "a scalar pointer is not 4-byte aligned");
-  if (!(beta >= 0.0f && beta < 1.0f)) return fail(ADAMW_EINVAL, "beta must lie in [0, 1)");
-  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(ADAMW_EINVAL, "eps must be finite and >= 0");
-  adamw_status st = check_device(plan);
-  if (st != ADAMW_OK) return st;
-  StepArgs a;
-  a.tensors = plan->d_tensors;
-  a.chunks = plan->d_chunks;
-  a.n_chunks = plan->n_chunks;
-  a.lr = lr_dev;
-  a.step = step_dev;
-  a.grad_scale = grad_scale_dev;
-  a.found_inf = found_inf_dev;
-  a.beta1 = rule == ADAMW_RULE_ADAGRAD ? 0.0f : beta;
-  a.beta2 = 0.0f;
-  a.eps = eps;
-  a.beta3 = 0.0f;
-  a.alpha = 0.0f;
-  a.scratch = plan->d_scratch;
-  a.qt = nullptr;
-  a.refine = 1;
+  if ((st = check_device(plan)) != ADAMW_OK) return st;
+  StepArgs a = step_args(plan, lr_dev, step_dev, grad_scale_dev, found_inf_dev,
+                         rule == ADAMW_RULE_ADAGRAD ? 0.0f : beta, 0.0f, eps);
   const int grid = algo == kAlgoMomentum ? plan->grid : plan->grid_sqrt_div;
   cudaError_t e = launch_step_bulk(plan->mode, plan->gdt, a, grid,
                                    static_cast<cudaStream_t>(stream), algo);
@@ -712,21 +657,15 @@ adamw_status adamw_coupled_step(adamw_plan* plan, adamw_coupled_rule rule, const
 adamw_status adamw_step_amp(adamw_plan* plan, const float* lr_dev, int32_t* step_dev, float beta1,
                             float beta2, float eps, const float* grad_scale_dev, float* found_inf_dev,
                             void* stream) {
-  if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
-  if (!lr_dev || !step_dev || !found_inf_dev)
-    return fail(ADAMW_EINVAL, "lr_dev, step_dev and found_inf_dev must be set");
-  if (!aligned(lr_dev, 4) || !aligned(step_dev, 4) || !aligned(grad_scale_dev, 4) ||
-      !aligned(found_inf_dev, 4))
-    return fail(ADAMW_EALIGN, "a scalar pointer is not 4-byte aligned");
-  if (!(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f))
-    return fail(ADAMW_EINVAL, "betas must lie in [0, 1)");
-  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(ADAMW_EINVAL, "eps must be finite and >= 0");
+  adamw_status st = check_step(plan, lr_dev, step_dev, grad_scale_dev, found_inf_dev, beta1, beta2);
+  if (st == ADAMW_OK) st = check_eps(eps);
+  if (st != ADAMW_OK) return st;
+  if (!found_inf_dev) return fail(ADAMW_EINVAL, "found_inf_dev must be set");
   if (quantized(plan->mode))
     return fail(ADAMW_EUNSUPPORTED, "the fused check + step covers the fp32 and bf16+remainder modes");
   if (!plan->has_v) return fail(ADAMW_EINVAL, "the plan's tensors carry no exp_avg_sq");
   if (plan->mini) return fail(ADAMW_EINVAL, "an Adam-mini plan steps with adamw_mini_step");
-  adamw_status st = check_device(plan);
-  if (st != ADAMW_OK) return st;
+  if ((st = check_device(plan)) != ADAMW_OK) return st;
   // Past a few million elements the grads no longer stay in L2 between the
   // scan and the update, and the bulk-staged step outruns the cooperative one
   // (fp16 grads on GB300: fused 33.5 us vs 35.9 us at 4 Mi elements, 57.3 vs
@@ -737,23 +676,11 @@ adamw_status adamw_step_amp(adamw_plan* plan, const float* lr_dev, int32_t* step
     return adamw_step(plan, lr_dev, step_dev, beta1, beta2, eps, grad_scale_dev, found_inf_dev,
                       stream);
   }
-  // every CTA of the cooperative launch is resident at once (grid sized at plan creation)
-  StepArgs a;
-  a.tensors = plan->d_tensors;
+  // every CTA of the cooperative launch is resident at once (grid sized at plan
+  // creation, with its own chunk table); the skip is decided inside the launch
+  StepArgs a = step_args(plan, lr_dev, step_dev, grad_scale_dev, nullptr, beta1, beta2, eps);
   a.chunks = plan->d_chunks_fused;
   a.n_chunks = plan->n_chunks_fused;
-  a.lr = lr_dev;
-  a.step = step_dev;
-  a.grad_scale = grad_scale_dev;
-  a.found_inf = nullptr;      // decided inside the launch
-  a.beta1 = beta1;
-  a.beta2 = beta2;
-  a.eps = eps;
-  a.beta3 = 0.0f;
-  a.alpha = 0.0f;
-  a.scratch = plan->d_scratch;
-  a.qt = nullptr;
-  a.refine = 1;
   cudaError_t e = launch_step_fused_amp(plan->mode, plan->gdt, a, plan->grid_fused, found_inf_dev,
                                         static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cooperative launch of the fused step");
