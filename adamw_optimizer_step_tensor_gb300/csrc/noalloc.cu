@@ -122,12 +122,13 @@ extern "C" adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t 
     if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
     ds.ready = true;
   }
+  // The plan path's bulk-staged kernel, one CTA per SM; its shared-memory
+  // size is raised once per device, mode and grad dtype (no allocation).
   int& bps = ds.blocks_per_sm[mode][grad_dtype];
   if (bps == 0) {
-    int smem = 0;
-    e = step_occupancy(mode, grad_dtype, &bps, &smem);
-    if (e != cudaSuccess) return fail_cuda(e, "occupancy query");
-    if (bps < 1) bps = 1;
+    e = prepare_step_bulk(mode, grad_dtype, kAlgoAdamW);
+    if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(bulk step)");
+    bps = 1;
   }
 
   // Same chunking rule as a plan: the largest chunk that gives every SM work.
@@ -192,7 +193,7 @@ extern "C" adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t 
   a.refine = 1;
   const int64_t resident = static_cast<int64_t>(bps) * ds.sms;
   const int grid = static_cast<int>(n_chunks < 1 ? 1 : (n_chunks < resident ? n_chunks : resident));
-  e = launch_step(mode, grad_dtype, a, grid, st);
+  e = launch_step_bulk(mode, grad_dtype, a, grid, st, kAlgoAdamW);
   if (e != cudaSuccess) return fail_cuda(e, "launch adamw step");
   return ADAMW_OK;
 }
