@@ -23,8 +23,7 @@
 namespace adamw {
 namespace {
 
-constexpr int kConsumers = 2 * kThreads;        // consumer threads (16 warps)
-constexpr int kBulkThreads = kConsumers + 32;   // + 1 producer warp
+constexpr int kConsumers = kBulkConsumers;     // consumer threads (16 warps)
 constexpr int kTile = kConsumers * 4;           // elements per stage: 4 per consumer thread
 static_assert(kTile % kVec == 0, "bulk copies move whole 8-element groups");
 constexpr uint64_t kWaitLimitNs = 2000000000ull;

@@ -32,6 +32,7 @@ struct adamw_plan {
   int64_t total_numel = 0;
   int64_t n_chunks = 0;
   int grid = 1;
+  int block_threads = kThreads;   // threads per CTA of the step kernel
   int grid_check = 1;
   TensorDesc* d_tensors = nullptr;
   Chunk* d_chunks = nullptr;
@@ -372,6 +373,7 @@ static adamw_status create_plan(const adamw_tensor* tensors, int32_t n_tensors, 
 
   p->device = device;
   p->bulk = bulk;
+  p->block_threads = bulk ? kBulkThreads : (mode == ADAMW_MODE_Q8 ? kQ8Threads : kThreads);
   p->has_slow = with_slow != 0 || (sized == 0 && !quantized(mode));
   p->has_v = with_v != 0 || sized == 0;
   const int64_t resident = static_cast<int64_t>(bps) * sms;
@@ -487,7 +489,7 @@ adamw_status adamw_plan_info(const adamw_plan* plan, int64_t* total_numel, int64
   if (total_numel) *total_numel = plan->total_numel;
   if (n_chunks) *n_chunks = plan->n_chunks;
   if (grid_blocks) *grid_blocks = plan->grid;
-  if (block_threads) *block_threads = kThreads;
+  if (block_threads) *block_threads = plan->block_threads;
   return ADAMW_OK;
 }
 

@@ -15,19 +15,26 @@ constexpr int kThreads = 256;
 constexpr int kVec = 8;
 constexpr int kPass = kThreads * kVec;       // 2048 elements per CTA pass
 // Passes whose loads a thread issues together, and the resident CTAs per SM
-// the register budget targets, per storage mode.  Measured on GB300: the
-// register-load fp32 kernel (now only behind adamw_step_noalloc) 2 x 2 -> 92%
-// of copy bandwidth vs 88% for 1 x 3; the instruction-bound 8-bit kernel runs
-// best at 4 CTAs/SM (64 registers: 3.37 ms for 2^30 elements vs 3.63 ms at 3).
+// the register budget targets, of the register-load fp32 / bf16+remainder
+// kernel (the A/B baseline of the bulk-staged one, see kUseBulk).  Measured on
+// GB300: 2 x 2 -> 92% of copy bandwidth vs 88% for 1 x 3.
 template <int MODE> struct Tune { static constexpr int unroll = 1, min_blocks = 3; };
 template <> struct Tune<ADAMW_MODE_FP32> { static constexpr int unroll = 2, min_blocks = 2; };
-template <> struct Tune<ADAMW_MODE_Q8> { static constexpr int unroll = 1, min_blocks = 4; };
 constexpr int kChunkMax = 8 * kPass;         // chunks hold up to 16384 elements (chosen per plan)
 // fp32 and bf16+remainder steps stage tiles through shared memory with bulk
 // async copies (bulk_kernels.cu) instead of 128-bit register loads.  The
-// 8-bit and 4-bit steps keep register loads: they are bound by instruction
-// issue, and a bulk-staged 8-bit step measured 5% slower on GB300.
+// 8-bit and 4-bit steps load into registers: their bound is the
+// shared-memory pipe (code-table lookups), which staging would load further
+// (a bulk-staged 8-bit step measured 5% slower, a per-warp cp.async-staged
+// one 38% slower).
 constexpr bool kUseBulk = true;
+// The bulk-staged step: 16 consumer warps and one producer warp per CTA.
+constexpr int kBulkConsumers = 2 * kThreads;
+constexpr int kBulkThreads = kBulkConsumers + 32;
+// The 8-bit step runs one CTA of kQ8Threads per SM (64 registers a thread):
+// its lane-private code tables (lane_tables.cuh, 139 KB) fit once per SM.
+constexpr int kQ8Threads = 1024;
+constexpr int kQ8Pass = kQ8Threads * kVec;   // 8192 elements per CTA pass
 constexpr int kQBlock = ADAMW_Q8_BLOCK;      // 256
 static_assert(kPass % kQBlock == 0, "chunks must hold whole Q8 blocks");
 static_assert(32 * kVec == kQBlock, "one warp pass covers exactly one Q8 block");

@@ -18,6 +18,7 @@
 
 #include "internal.h"
 #include "step_common.cuh"
+#include "lane_tables.cuh"
 
 namespace adamw {
 namespace {
@@ -273,28 +274,27 @@ cudaError_t launch_fused_mode(adamw_mode mode, const StepArgs& a, int grid, floa
 }
 
 // ---------------------------------------------------------------- 8-bit states
+// One CTA of kQ8Threads per SM; every warp owns one 256-element block per
+// pass, each lane 8 consecutive elements.  The code tables are lane-private
+// copies in shared memory (lane_tables.cuh).
+constexpr int kQ8Smem = static_cast<int>(sizeof(LaneTables<256>));
+
 template <typename GT, int R>
-__global__ void __launch_bounds__(kThreads, Tune<ADAMW_MODE_Q8>::min_blocks)
-step_q8_kernel(const StepArgs a) {
+__global__ void __launch_bounds__(kQ8Threads, 1) step_q8_kernel(const StepArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  QTables& qt = *reinterpret_cast<QTables*>(smem_raw);
+  LaneTables<256>& lt = *reinterpret_cast<LaneTables<256>*>(smem_raw);
   __shared__ Scal s_sc;
   __shared__ int s_skip;
   int t = 0;
   if (threadIdx.x == 0) s_skip = prologue(a, s_sc, t);
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(a.qt);
-    uint4* dst = reinterpret_cast<uint4*>(smem_raw);
-    for (int i = threadIdx.x; i < static_cast<int>(sizeof(QTables) / 16); i += kThreads)
-      dst[i] = src[i];
-  }
+  fill_lane_tables<256>(lt, a.qt);
   __syncthreads();
   if (s_skip) return;
   const Scal s = s_sc;
   if (threadIdx.x == 0) take_ticket(a, t);
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
-  const uint32_t zc_m = qt.zero_code[0], zc_v = qt.zero_code[1];
+  const uint32_t zc_m = a.qt->zero_code[0], zc_v = a.qt->zero_code[1];
 
   for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
     const Chunk ch = a.chunks[c];
@@ -306,7 +306,7 @@ step_q8_kernel(const StepArgs a) {
     uint8_t* const cv = static_cast<uint8_t*>(td.v);
 
     // warp w owns the 256-element block starting at `wb` of every pass
-    for (int wb = warp * kQBlock; wb < ch.len; wb += kPass) {
+    for (int wb = warp * kQBlock; wb < ch.len; wb += kQ8Pass) {
       const int64_t blk = (ch.start + wb) / kQBlock;   // block-aligned within the tensor
       const int off = wb + lane * kVec;
       const int64_t e = ch.start + off;
@@ -324,20 +324,20 @@ step_q8_kernel(const StepArgs a) {
         for (int i = 0; i < 8; ++i) {
           const uint32_t wm = i < 4 ? qm.x : qm.y, wv = i < 4 ? qv.x : qv.y;
           const int sh = (i & 3) * 8;
-          m[i] = __fmul_rn(qt.map[0].value[(wm >> sh) & 0xFFu], am);
-          v[i] = __fmul_rn(qt.map[1].value[(wv >> sh) & 0xFFu], av);
+          m[i] = __fmul_rn(lt.value[0][(wm >> sh) & 0xFFu][lane], am);
+          v[i] = __fmul_rn(lt.value[1][(wv >> sh) & 0xFFu][lane], av);
           update(p[i], gr[i], m[i], v[i], s, decay);
           mx_m = max(mx_m, __float_as_uint(m[i]) & 0x7FFFFFFFu);
           mx_v = max(mx_v, __float_as_uint(v[i]) & 0x7FFFFFFFu);
         }
         // store each result as soon as it is final: short live ranges keep the
-        // kernel within the register budget of 3 CTAs per SM
+        // kernel within its 64 registers
         st8f(pf + e, p);
         const BlockNorm nm = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_m));
-        quant8<R>(m, nm, qt.map[0], zc_m, q_m);
+        lane_quant8<256, 0, R>(lt, m, nm, zc_m, lane, q_m);
         __stcs(reinterpret_cast<uint2*>(cm + e), pack8(q_m));
         const BlockNorm nv = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_v));
-        quant8<R, false>(v, nv, qt.map[1], zc_v, q_v);
+        lane_quant8<256, 1, R>(lt, v, nv, zc_v, lane, q_v);
         __stcs(reinterpret_cast<uint2*>(cv + e), pack8(q_v));
         if (lane == 0) {
           td.am[blk] = __uint_as_float(nm.bits);
@@ -353,8 +353,8 @@ step_q8_kernel(const StepArgs a) {
           if (i < n) {
             p[i] = pf[e + i];
             gr[i] = Grad<GT>::load1(td.g, e + i);
-            m[i] = __fmul_rn(qt.map[0].value[cm[e + i]], am);
-            v[i] = __fmul_rn(qt.map[1].value[cv[e + i]], av);
+            m[i] = __fmul_rn(lt.value[0][cm[e + i]][lane], am);
+            v[i] = __fmul_rn(lt.value[1][cv[e + i]][lane], av);
             update(p[i], gr[i], m[i], v[i], s, decay);
             mx_m = max(mx_m, __float_as_uint(m[i]) & 0x7FFFFFFFu);
             mx_v = max(mx_v, __float_as_uint(v[i]) & 0x7FFFFFFFu);
@@ -362,8 +362,8 @@ step_q8_kernel(const StepArgs a) {
         }
         const BlockNorm nm = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_m));
         const BlockNorm nv = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_v));
-        quant8<R>(m, nm, qt.map[0], zc_m, q_m);
-        quant8<R, false>(v, nv, qt.map[1], zc_v, q_v);
+        lane_quant8<256, 0, R>(lt, m, nm, zc_m, lane, q_m);
+        lane_quant8<256, 1, R>(lt, v, nv, zc_v, lane, q_v);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
           if (i < n) {
@@ -397,11 +397,11 @@ cudaError_t launch_mode(adamw_mode mode, const StepArgs& a, int grid, cudaStream
       break;
     case ADAMW_MODE_Q8:
       if (a.refine <= 1)
-        step_q8_kernel<GT, 1><<<grid, kThreads, sizeof(QTables), st>>>(a);
+        step_q8_kernel<GT, 1><<<grid, kQ8Threads, kQ8Smem, st>>>(a);
       else if (a.refine <= 2)
-        step_q8_kernel<GT, 2><<<grid, kThreads, sizeof(QTables), st>>>(a);
+        step_q8_kernel<GT, 2><<<grid, kQ8Threads, kQ8Smem, st>>>(a);
       else
-        step_q8_kernel<GT, kMaxRefine><<<grid, kThreads, sizeof(QTables), st>>>(a);
+        step_q8_kernel<GT, kMaxRefine><<<grid, kQ8Threads, kQ8Smem, st>>>(a);
       break;
     default:
       return cudaErrorInvalidValue;
@@ -418,9 +418,22 @@ cudaError_t occupancy_mode(adamw_mode mode, int* bps, int* smem) {
     case ADAMW_MODE_BF16_REM:
       *smem = 0;
       return occ(step_kernel<ADAMW_MODE_BF16_REM, GT>, 0, bps);
-    case ADAMW_MODE_Q8:
-      *smem = static_cast<int>(sizeof(QTables));
-      return occ(step_q8_kernel<GT, kMaxRefine>, *smem, bps);
+    case ADAMW_MODE_Q8: {
+      // the lane-private tables exceed the 48 KB default: raise the limit of
+      // each refine variant (before any launch), then ask for the occupancy
+      *smem = kQ8Smem;
+      cudaError_t e = cudaFuncSetAttribute(step_q8_kernel<GT, 1>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kQ8Smem);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(step_q8_kernel<GT, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kQ8Smem);
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(step_q8_kernel<GT, kMaxRefine>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kQ8Smem);
+      if (e != cudaSuccess) return e;
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, step_q8_kernel<GT, kMaxRefine>,
+                                                           kQ8Threads, kQ8Smem);
+    }
     default:
       return cudaErrorInvalidValue;
   }

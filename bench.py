@@ -80,9 +80,9 @@ def measured_peak():
 # The source files that make up the dominant kernel of each workload; a
 # committed ncu summary counts only while their hash matches.
 KERNEL_SOURCES = {
-    "q8": ("step_kernels.cu", "step_common.cuh", "internal.h"),
+    "q8": ("step_kernels.cu", "step_common.cuh", "internal.h", "lane_tables.cuh"),
     "q4": ("q4_kernels.cu", "step_common.cuh", "internal.h"),
-    "amp_fused": ("step_kernels.cu", "step_common.cuh", "internal.h"),
+    "amp_fused": ("step_kernels.cu", "step_common.cuh", "internal.h", "lane_tables.cuh"),
 }
 BULK_SOURCES = ("bulk_kernels.cu", "step_common.cuh", "internal.h")
 

@@ -139,8 +139,10 @@ adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors,
 /* Free a plan (NULL is allowed).  Synchronises with the device first. */
 adamw_status adamw_plan_destroy(adamw_plan* plan);
 
-/* Plan facts for logging: element count, chunk count, launch grid. Any
- * output pointer may be NULL. */
+/* Plan facts for logging: element count, chunk count, and the launch shape
+ * of the plan's step kernel (grid, threads per CTA; the fused AMP step and
+ * the rules other than AdamW may launch other shapes).  Any output pointer
+ * may be NULL. */
 adamw_status adamw_plan_info(const adamw_plan* plan, int64_t* total_numel,
                              int64_t* n_chunks, int32_t* grid_blocks,
                              int32_t* block_threads);

@@ -49,3 +49,31 @@ def test_degenerate_plans_count_steps(n):
         assert int(st.item()) == 3, name
         assert opt.status() == 0, name
         opt.close()
+
+
+def test_plan_info_reports_the_launch_shape():
+    """Every plan reports the CTA size of the kernel its step launches: the
+    bulk-staged kernel (16 consumer warps + 1 producer warp), the 8-bit
+    kernel (one 1024-thread CTA per SM with lane-private code tables) and the
+    4-bit kernel (256 threads); the grid never exceeds the SM count times the
+    CTAs that fit on one SM."""
+    n = 1 << 22
+    f = lambda dt=torch.float32: torch.zeros(n, dtype=dt, device="cuda")
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    blocks = n // 256
+    absq8 = torch.zeros(blocks, device="cuda")
+    absq4 = torch.zeros(2 * blocks, device="cuda")
+    cases = {
+        "fp32": (FusedAdamW([f()], [f()], [f()], [f()], [0.1]), 544, 1),
+        "q8": (FusedAdamW([f()], [f(torch.bfloat16)], [f(torch.uint8)], [f(torch.uint8)], [0.1],
+                          mode="q8", absmax_m=[absq8], absmax_v=[absq8.clone()]), 1024, 1),
+        "q4": (FusedAdamW([f()], [f(torch.bfloat16)], [torch.zeros(n // 2, dtype=torch.uint8, device="cuda")],
+                          [torch.zeros(n // 2, dtype=torch.uint8, device="cuda")], [0.1], mode="q4",
+                          absmax_m=[absq4], absmax_v=[absq4.clone()]), 256, 4),
+    }
+    for name, (opt, threads, per_sm) in cases.items():
+        info = opt.info()
+        assert info["block_threads"] == threads, name
+        assert info["total_numel"] == n, name
+        assert 1 <= info["grid_blocks"] <= per_sm * sms, name
+        opt.close()
