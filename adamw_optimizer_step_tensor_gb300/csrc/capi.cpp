@@ -363,6 +363,9 @@ static adamw_status create_plan(const adamw_tensor* tensors, int32_t n_tensors, 
   }
   if (blocks.size() > static_cast<size_t>(INT32_MAX))
     return fail(ADAMW_EUNSUPPORTED, "more than 2^31 - 1 Adam-mini blocks");
+  // the quantised kernels walk the chunk table with a 32-bit index
+  if (chunks.size() > (static_cast<size_t>(1) << 30))
+    return fail(ADAMW_EUNSUPPORTED, "more than 2^30 chunks");
 
   std::unique_ptr<adamw_plan, void (*)(adamw_plan*)> p(new adamw_plan, free_plan);
   p->mode = mode;

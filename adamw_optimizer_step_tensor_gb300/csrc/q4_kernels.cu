@@ -28,6 +28,8 @@ __device__ __forceinline__ uint32_t half_warp_max(uint32_t x) {
   return x;
 }
 
+__device__ __forceinline__ uint8_t* codes(void* p) { return static_cast<uint8_t*>(p); }
+
 __device__ __forceinline__ uint32_t pack_nibbles(const uint32_t (&q)[8]) {
   uint32_t w = 0u;
 #pragma unroll
@@ -58,14 +60,16 @@ __global__ void __launch_bounds__(kThreads, kQ4MinBlocks) step_q4_kernel(const S
   const int half = lane >> 4;
   const uint32_t zc_m = qt.zero_code[0], zc_v = qt.zero_code[1];
 
-  for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
+  for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
     const Chunk ch = a.chunks[c];
     const TensorDesc td = a.tensors[ch.tensor];
+    // the code and absmax pointers are read again where they are used (the
+    // step's stores may alias the descriptor, so the compiler keeps no copy
+    // live across the pass): fewer spills at 64 registers
+    const TensorDesc* const tdp = a.tensors + ch.tensor;
     const float decay = __fsub_rn(1.0f, __fmul_rn(s.lr, td.wd));
     const bool vec = td.vec_ok != 0;
     float* const pf = static_cast<float*>(td.p);
-    uint8_t* const cm = static_cast<uint8_t*>(td.m);
-    uint8_t* const cv = static_cast<uint8_t*>(td.v);
 
     // warp w owns the two blocks starting at `wb` of every pass; `e` is even
     for (int wb = warp * kQ4Span; wb < ch.len; wb += kPass) {
@@ -76,11 +80,11 @@ __global__ void __launch_bounds__(kThreads, kQ4MinBlocks) step_q4_kernel(const S
       uint32_t q_m[8], q_v[8];
       if (vec && wb + kQ4Span <= ch.len) {
         float p[8], gr[8];
-        const float am = td.am[blk], av = td.av[blk];
+        const float am = tdp->am[blk], av = tdp->av[blk];
         ld8f(pf + e, p);
         Grad<GT>::load8(td.g, e, gr);
-        const uint32_t wm = __ldcs(reinterpret_cast<const uint32_t*>(cm + e / 2));
-        const uint32_t wv = __ldcs(reinterpret_cast<const uint32_t*>(cv + e / 2));
+        const uint32_t wm = __ldcs(reinterpret_cast<const uint32_t*>(codes(tdp->m) + e / 2));
+        const uint32_t wv = __ldcs(reinterpret_cast<const uint32_t*>(codes(tdp->v) + e / 2));
         uint32_t mx_m = 0u, mx_v = 0u;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -93,21 +97,21 @@ __global__ void __launch_bounds__(kThreads, kQ4MinBlocks) step_q4_kernel(const S
         st8f(pf + e, p);
         const BlockNorm nm = block_norm(half_warp_max(mx_m));
         quant8<R>(m, nm, qt.map[0], zc_m, q_m);
-        __stcs(reinterpret_cast<uint32_t*>(cm + e / 2), pack_nibbles(q_m));
+        __stcs(reinterpret_cast<uint32_t*>(codes(tdp->m) + e / 2), pack_nibbles(q_m));
         const BlockNorm nv = block_norm(half_warp_max(mx_v));
         quant8<R, false>(v, nv, qt.map[1], zc_v, q_v);
-        __stcs(reinterpret_cast<uint32_t*>(cv + e / 2), pack_nibbles(q_v));
+        __stcs(reinterpret_cast<uint32_t*>(codes(tdp->v) + e / 2), pack_nibbles(q_v));
         if ((lane & 15) == 0) {
-          td.am[blk] = __uint_as_float(nm.bits);
-          td.av[blk] = __uint_as_float(nv.bits);
+          tdp->am[blk] = __uint_as_float(nm.bits);
+          tdp->av[blk] = __uint_as_float(nv.bits);
         }
       } else {
         // the tail of a tensor (a half-warp's block may be partial or empty),
         // or a misaligned tensor: element by element
         const int n = max(0, min(kVec, ch.len - off));
         const bool has_block = wb + half * kQ4Block < ch.len;
-        const float am = has_block ? td.am[blk] : 0.0f;
-        const float av = has_block ? td.av[blk] : 0.0f;
+        const float am = has_block ? tdp->am[blk] : 0.0f;
+        const float av = has_block ? tdp->av[blk] : 0.0f;
         uint32_t mx_m = 0u, mx_v = 0u;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -115,8 +119,8 @@ __global__ void __launch_bounds__(kThreads, kQ4MinBlocks) step_q4_kernel(const S
           if (i < n) {
             const int sh = 4 * (i & 1);
             float pi = pf[e + i];
-            m[i] = __fmul_rn(qt.map[0].value[(cm[(e + i) / 2] >> sh) & 0xFu], am);
-            v[i] = __fmul_rn(qt.map[1].value[(cv[(e + i) / 2] >> sh) & 0xFu], av);
+            m[i] = __fmul_rn(qt.map[0].value[(codes(tdp->m)[(e + i) / 2] >> sh) & 0xFu], am);
+            v[i] = __fmul_rn(qt.map[1].value[(codes(tdp->v)[(e + i) / 2] >> sh) & 0xFu], av);
             update(pi, Grad<GT>::load1(td.g, e + i), m[i], v[i], s, decay);
             pf[e + i] = pi;
             mx_m = max(mx_m, __float_as_uint(m[i]) & 0x7FFFFFFFu);
@@ -131,13 +135,13 @@ __global__ void __launch_bounds__(kThreads, kQ4MinBlocks) step_q4_kernel(const S
         for (int i = 0; i < 8; i += 2) {
           if (i < n) {
             const bool pair = i + 1 < n;
-            cm[(e + i) / 2] = static_cast<uint8_t>(q_m[i] | (pair ? q_m[i + 1] << 4 : 0u));
-            cv[(e + i) / 2] = static_cast<uint8_t>(q_v[i] | (pair ? q_v[i + 1] << 4 : 0u));
+            codes(tdp->m)[(e + i) / 2] = static_cast<uint8_t>(q_m[i] | (pair ? q_m[i + 1] << 4 : 0u));
+            codes(tdp->v)[(e + i) / 2] = static_cast<uint8_t>(q_v[i] | (pair ? q_v[i + 1] << 4 : 0u));
           }
         }
         if ((lane & 15) == 0 && has_block) {
-          td.am[blk] = __uint_as_float(nm.bits);
-          td.av[blk] = __uint_as_float(nv.bits);
+          tdp->am[blk] = __uint_as_float(nm.bits);
+          tdp->av[blk] = __uint_as_float(nv.bits);
         }
       }
     }

@@ -279,6 +279,13 @@ cudaError_t launch_fused_mode(adamw_mode mode, const StepArgs& a, int grid, floa
 // copies in shared memory (lane_tables.cuh).
 constexpr int kQ8Smem = static_cast<int>(sizeof(LaneTables<256>));
 
+__device__ __forceinline__ uint8_t* codes_m(const TensorDesc* td) {
+  return static_cast<uint8_t*>(td->m);
+}
+__device__ __forceinline__ uint8_t* codes_v(const TensorDesc* td) {
+  return static_cast<uint8_t*>(td->v);
+}
+
 template <typename GT, int R>
 __global__ void __launch_bounds__(kQ8Threads, 1) step_q8_kernel(const StepArgs a) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
@@ -296,29 +303,31 @@ __global__ void __launch_bounds__(kQ8Threads, 1) step_q8_kernel(const StepArgs a
   const int warp = threadIdx.x >> 5;
   const uint32_t zc_m = a.qt->zero_code[0], zc_v = a.qt->zero_code[1];
 
-  for (int64_t c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
+  for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
     const Chunk ch = a.chunks[c];
     const TensorDesc td = a.tensors[ch.tensor];
+    // the code and absmax pointers are read again where they are used (the
+    // step's stores may alias the descriptor, so the compiler keeps no copy
+    // live across the pass): no spills at 64 registers
+    const TensorDesc* const tdp = a.tensors + ch.tensor;
     const float decay = __fsub_rn(1.0f, __fmul_rn(s.lr, td.wd));
     const bool vec = td.vec_ok != 0;
     float* const pf = static_cast<float*>(td.p);
-    uint8_t* const cm = static_cast<uint8_t*>(td.m);
-    uint8_t* const cv = static_cast<uint8_t*>(td.v);
 
     // warp w owns the 256-element block starting at `wb` of every pass
     for (int wb = warp * kQBlock; wb < ch.len; wb += kQ8Pass) {
       const int64_t blk = (ch.start + wb) / kQBlock;   // block-aligned within the tensor
       const int off = wb + lane * kVec;
       const int64_t e = ch.start + off;
-      const float am = td.am[blk], av = td.av[blk];
+      const float am = tdp->am[blk], av = tdp->av[blk];
       float p[8], gr[8], m[8], v[8];
       uint32_t q_m[8], q_v[8];
       // a whole block on the 128-bit path: no per-element predicates
       if (vec && wb + kQBlock <= ch.len) {
         ld8f(pf + e, p);
         Grad<GT>::load8(td.g, e, gr);
-        const uint2 qm = __ldcs(reinterpret_cast<const uint2*>(cm + e));
-        const uint2 qv = __ldcs(reinterpret_cast<const uint2*>(cv + e));
+        const uint2 qm = __ldcs(reinterpret_cast<const uint2*>(codes_m(tdp) + e));
+        const uint2 qv = __ldcs(reinterpret_cast<const uint2*>(codes_v(tdp) + e));
         uint32_t mx_m = 0u, mx_v = 0u;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
@@ -335,13 +344,13 @@ __global__ void __launch_bounds__(kQ8Threads, 1) step_q8_kernel(const StepArgs a
         st8f(pf + e, p);
         const BlockNorm nm = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_m));
         lane_quant8<256, 0, R>(lt, m, nm, zc_m, lane, q_m);
-        __stcs(reinterpret_cast<uint2*>(cm + e), pack8(q_m));
+        __stcs(reinterpret_cast<uint2*>(codes_m(tdp) + e), pack8(q_m));
         const BlockNorm nv = block_norm(__reduce_max_sync(0xFFFFFFFFu, mx_v));
         lane_quant8<256, 1, R>(lt, v, nv, zc_v, lane, q_v);
-        __stcs(reinterpret_cast<uint2*>(cv + e), pack8(q_v));
+        __stcs(reinterpret_cast<uint2*>(codes_v(tdp) + e), pack8(q_v));
         if (lane == 0) {
-          td.am[blk] = __uint_as_float(nm.bits);
-          td.av[blk] = __uint_as_float(nv.bits);
+          tdp->am[blk] = __uint_as_float(nm.bits);
+          tdp->av[blk] = __uint_as_float(nv.bits);
         }
       } else {
         // the last (partial) block of a tensor, or a misaligned tensor
@@ -353,8 +362,8 @@ __global__ void __launch_bounds__(kQ8Threads, 1) step_q8_kernel(const StepArgs a
           if (i < n) {
             p[i] = pf[e + i];
             gr[i] = Grad<GT>::load1(td.g, e + i);
-            m[i] = __fmul_rn(lt.value[0][cm[e + i]][lane], am);
-            v[i] = __fmul_rn(lt.value[1][cv[e + i]][lane], av);
+            m[i] = __fmul_rn(lt.value[0][codes_m(tdp)[e + i]][lane], am);
+            v[i] = __fmul_rn(lt.value[1][codes_v(tdp)[e + i]][lane], av);
             update(p[i], gr[i], m[i], v[i], s, decay);
             mx_m = max(mx_m, __float_as_uint(m[i]) & 0x7FFFFFFFu);
             mx_v = max(mx_v, __float_as_uint(v[i]) & 0x7FFFFFFFu);
@@ -368,13 +377,13 @@ __global__ void __launch_bounds__(kQ8Threads, 1) step_q8_kernel(const StepArgs a
         for (int i = 0; i < 8; ++i) {
           if (i < n) {
             pf[e + i] = p[i];
-            cm[e + i] = static_cast<uint8_t>(q_m[i]);
-            cv[e + i] = static_cast<uint8_t>(q_v[i]);
+            codes_m(tdp)[e + i] = static_cast<uint8_t>(q_m[i]);
+            codes_v(tdp)[e + i] = static_cast<uint8_t>(q_v[i]);
           }
         }
         if (lane == 0) {
-          td.am[blk] = __uint_as_float(nm.bits);
-          td.av[blk] = __uint_as_float(nv.bits);
+          tdp->am[blk] = __uint_as_float(nm.bits);
+          tdp->av[blk] = __uint_as_float(nv.bits);
         }
       }
     }
