@@ -456,6 +456,8 @@ static adamw_status create_plan(const adamw_tensor* tensors, int32_t n_tensors, 
     float smap[256], umap[256];
     int n = 256;
     if (mode == ADAMW_MODE_Q4) {
+      // fixed maps: the 4-bit step finds the nearest v code arithmetically,
+      // which holds for the map k/16 (k = 1..16) only
       default_maps4(smap, umap);
       n = 16;
     } else {

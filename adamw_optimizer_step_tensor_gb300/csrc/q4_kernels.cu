@@ -30,6 +30,35 @@ __device__ __forceinline__ uint32_t half_warp_max(uint32_t x) {
 
 __device__ __forceinline__ uint8_t* codes(void* p) { return static_cast<uint8_t*>(p); }
 
+// Nearest code of a normalised second moment x on the 4-bit v map, value
+// (k+1)/16 for code k.  Its thresholds are the exact midpoints (k + 1.5)/16,
+// so with y = 16x (exact: a power-of-two scaling) the code is
+// #{k in 0..14 : y > k + 1.5} = clamp(ceil(y - 1.5), 0, 15), ties to the
+// lower code.  The fma rounds 16x - 1.5 once: exactly wherever the result
+// is at or above -0.75, and a result below that stays below 0 whatever its
+// rounding; x is never negative, and a NaN converts to 0: code 0, as the
+// table search gives.
+__device__ __forceinline__ uint32_t v4_code(float x) {
+  const int c = __float2int_ru(__fmaf_rn(x, 16.0f, -1.5f));
+  return static_cast<uint32_t>(min(max(c, 0), 15));
+}
+
+// Codes of the 8 second moments one lane owns (the map has no zero: an
+// all-zero block stores code 0, which dequantises to 0 through its absmax).
+__device__ __forceinline__ void quant_v4(const float (&x)[8], const BlockNorm& n,
+                                         uint32_t (&q)[8]) {
+  if (n.bits == 0u) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = 0u;
+  } else if (n.scale == 1.0f) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = v4_code(__fmul_rn(x[i], n.inv));
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = v4_code(__fmul_rn(__fmul_rn(x[i], n.scale), n.inv));
+  }
+}
+
 __device__ __forceinline__ uint32_t pack_nibbles(const uint32_t (&q)[8]) {
   uint32_t w = 0u;
 #pragma unroll
@@ -58,7 +87,7 @@ __global__ void __launch_bounds__(kThreads, kQ4MinBlocks) step_q4_kernel(const S
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
   const int half = lane >> 4;
-  const uint32_t zc_m = qt.zero_code[0], zc_v = qt.zero_code[1];
+  const uint32_t zc_m = qt.zero_code[0];
 
   for (int c = blockIdx.x; c < a.n_chunks; c += gridDim.x) {
     const Chunk ch = a.chunks[c];
@@ -99,7 +128,7 @@ __global__ void __launch_bounds__(kThreads, kQ4MinBlocks) step_q4_kernel(const S
         quant8<R>(m, nm, qt.map[0], zc_m, q_m);
         __stcs(reinterpret_cast<uint32_t*>(codes(tdp->m) + e / 2), pack_nibbles(q_m));
         const BlockNorm nv = block_norm(half_warp_max(mx_v));
-        quant8<R, false>(v, nv, qt.map[1], zc_v, q_v);
+        quant_v4(v, nv, q_v);
         __stcs(reinterpret_cast<uint32_t*>(codes(tdp->v) + e / 2), pack_nibbles(q_v));
         if ((lane & 15) == 0) {
           tdp->am[blk] = __uint_as_float(nm.bits);
@@ -130,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, kQ4MinBlocks) step_q4_kernel(const S
         const BlockNorm nm = block_norm(half_warp_max(mx_m));
         const BlockNorm nv = block_norm(half_warp_max(mx_v));
         quant8<R>(m, nm, qt.map[0], zc_m, q_m);
-        quant8<R, false>(v, nv, qt.map[1], zc_v, q_v);
+        quant_v4(v, nv, q_v);
 #pragma unroll
         for (int i = 0; i < 8; i += 2) {
           if (i < n) {

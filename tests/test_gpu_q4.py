@@ -152,3 +152,34 @@ def test_q4_export_import_match_oracle():
                           absmax_m=[torch.zeros(OQ.n_blocks(n), device="cuda")],
                           absmax_v=[torch.zeros(OQ.n_blocks(n), device="cuda")])
         C.adamw_q4_dequant(opt8.plan, 0, codes.data_ptr(), am.data_ptr(), out.data_ptr(), n, sh)
+
+
+def _same_or_both_nan(a, b):
+    a, b = np.asarray(a, np.float32), np.asarray(b, np.float32)
+    nan = np.isnan(a)
+    return np.array_equal(nan, np.isnan(b)) and bits_equal(a[~nan], b[~nan])
+
+
+def test_q4_nonfinite_grads_without_skip_match_oracle():
+    """A step that is not skipped on non-finite grads (no found_inf given):
+    NaN and +-inf reach the moments, the block absmax (a maximum over float
+    bits, so a NaN wins) and the nearest-code searches of both maps, whose
+    NaN inputs take code 0.  Codes bit-exact, params and absmax equal up to
+    NaN payloads (the CPU and the GPU make different default NaNs)."""
+    n = 1000
+    opt, st, d, gs, rng = _build([n], torch.float32, seed=37, zero_state=False)
+    g = rng.normal(0, 1e-3, n).astype(np.float32)
+    g[5], g[300], g[700], g[701] = np.nan, np.inf, -np.inf, np.inf
+    gs[0].copy_(dev(g))
+    opt.step(scalar_f32(f32(1e-3)), scalar_i32(0), betas=(B1, B2), eps=EPS)
+    s = st[0]
+    with np.errstate(invalid="ignore", over="ignore", divide="ignore"):
+        O4.step_f32(s["p"], g, s["cm"], s["cv"], s["am"], s["av"], lr=f32(1e-3), beta1=B1,
+                    beta2=B2, eps=EPS, wd=0.0, t=1, maps=O4.Maps4())
+    torch.cuda.synchronize()
+    x = d[0]
+    assert np.array_equal(host(x["cm"]), s["cm"])
+    assert np.array_equal(host(x["cv"]), s["cv"])
+    for k in ("p", "am", "av"):
+        assert _same_or_both_nan(host(x[k]), s[k]), k
+    assert np.isnan(host(x["am"])[0]) and np.isinf(host(x["av"])[2])
