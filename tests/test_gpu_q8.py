@@ -3,7 +3,9 @@
 Params, codes and per-block absmax are bit-exact against the strict-fp32
 oracle (the discrete outputs are defined against that mode); the first step
 from zero state also matches the closed form of "Fix decoupled weight decay
-ordering in the CUDA Adam/AdEMAMix kernels" (bitsandbytes PR #2040).
+ordering in the CUDA Adam/AdEMAMix kernels" (bitsandbytes PR #2040).  User
+maps dense enough to need 2 and 4 threshold compares per lookup, and
+non-finite grads on a step that is not skipped, stay bit-exact too.
 """
 
 import numpy as np
@@ -148,3 +150,83 @@ def test_q8_amp_skip_leaves_codes_and_absmax():
     for k, v in d[0].items():
         assert np.array_equal(host(v).view(np.uint8), before[k].view(np.uint8)), k
     assert int(step.item()) == 7
+
+
+def _cluster_map(k):
+    """A signed map with k extra levels 0.0008 apart just above 0.6, where a
+    bucket of the nearest-code search is 2^-8 wide: its thresholds crowd
+    into one bucket, so the search must compare more of them (the plan's
+    refine count: 2 for k = 3, 3 for k = 5, 5 for k = 7)."""
+    grid = np.linspace(-1, 1, 241)
+    cluster = 0.6 + 0.0008 * np.arange(1, k + 1)
+    n_pad = 256 - grid.size - k
+    pads = (grid[12:12 + n_pad] + grid[13:13 + n_pad]) / 2
+    m = np.sort(np.concatenate([grid, cluster, pads])).astype(np.float32)
+    assert m.size == 256 and np.unique(m).size == 256 and 0.0 in m
+    return m
+
+
+@pytest.mark.parametrize("k", [3, 5])
+def test_q8_dense_maps_take_more_compares(k):
+    """Maps whose thresholds crowd a bucket run the kernel variants with 2 and
+    4 threshold compares per lookup; codes, absmax and params stay bit-exact."""
+    n = 60_000
+    opt, st, d, gs, rng = _build([n], torch.bfloat16, seed=17, zero_state=False)
+    smap = _cluster_map(k)
+    umap = np.linspace(0, 1, 256).astype(np.float32)
+    opt.set_maps(smap, umap)
+    maps = OQ.Maps(smap, umap)
+    lr, step = scalar_f32(f32(1e-3)), scalar_i32(0)
+    s, x = st[0], d[0]
+    in_cluster = 0
+    for t in range(1, 3):
+        tg, w = grads_of(rng.normal(0, 1e-3, n).astype(np.float32), torch.bfloat16)
+        gs[0].copy_(tg)
+        opt.step(lr, step, betas=(B1, B2), eps=EPS)
+        OQ.step_f32(s["p"], w, s["cm"], s["cv"], s["am"], s["av"], lr=f32(1e-3), beta1=B1,
+                    beta2=B2, eps=EPS, wd=f32(0.01), t=t, maps=maps)
+        torch.cuda.synchronize()
+        assert bits_equal(host(x["p"]), s["p"]), f"t{t} p: {first_mismatch(host(x['p']), s['p'])}"
+        assert np.array_equal(host(x["cm"]), s["cm"]), f"t{t} m codes"
+        assert np.array_equal(host(x["cv"]), s["cv"]), f"t{t} v codes"
+        assert bits_equal(host(x["am"]), s["am"]) and bits_equal(host(x["av"]), s["av"]), f"t{t}"
+        in_cluster += int(np.sum((smap[s["cm"]] > 0.6) & (smap[s["cm"]] < 0.607)))
+    assert in_cluster > 100        # the crowded bucket was exercised
+
+
+def test_q8_maps_too_dense_for_the_search_are_refused():
+    n = 300
+    opt, st, d, gs, rng = _build([n], torch.bfloat16, seed=18, zero_state=True)
+    with pytest.raises(C.AdamWError, match="too dense"):
+        opt.set_maps(_cluster_map(7), np.linspace(0, 1, 256).astype(np.float32))
+
+
+def _same_or_both_nan(a, b):
+    a, b = np.asarray(a, np.float32), np.asarray(b, np.float32)
+    nan = np.isnan(a)
+    return np.array_equal(nan, np.isnan(b)) and bits_equal(a[~nan], b[~nan])
+
+
+def test_q8_nonfinite_grads_without_skip_match_oracle():
+    """A step that is not skipped on non-finite grads (no found_inf given):
+    NaN and +-inf reach the moments, the block absmax (a maximum over float
+    bits, so a NaN wins) and both nearest-code searches, whose NaN inputs
+    take code 0.  Codes bit-exact, params and absmax equal up to NaN payloads
+    (the CPU and the GPU make different default NaNs)."""
+    n = 2000
+    opt, st, d, gs, rng = _build([n], torch.float32, seed=19, zero_state=False)
+    g = rng.normal(0, 1e-3, n).astype(np.float32)
+    g[5], g[600], g[1400], g[1401] = np.nan, np.inf, -np.inf, np.inf
+    gs[0].copy_(dev(g))
+    opt.step(scalar_f32(f32(1e-3)), scalar_i32(0), betas=(B1, B2), eps=EPS)
+    s = st[0]
+    with np.errstate(invalid="ignore", over="ignore", divide="ignore"):
+        OQ.step_f32(s["p"], g, s["cm"], s["cv"], s["am"], s["av"], lr=f32(1e-3), beta1=B1,
+                    beta2=B2, eps=EPS, wd=f32(0.01), t=1, maps=OQ.Maps())
+    torch.cuda.synchronize()
+    x = d[0]
+    assert np.array_equal(host(x["cm"]), s["cm"])
+    assert np.array_equal(host(x["cv"]), s["cv"])
+    for k in ("p", "am", "av"):
+        assert _same_or_both_nan(host(x[k]), s[k]), k
+    assert np.isnan(host(x["am"])[0]) and np.isinf(host(x["av"])[2])
