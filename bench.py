@@ -43,6 +43,7 @@ sys.path.insert(0, ROOT)
 METRIC = "optimizer-step params/sec and achieved HBM GB/s (% of GB300 peak)"
 UNIT = "params/s"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 7900.0        # the GB300's nominal HBM3e bandwidth, reported beside the measured peak
 L2_FLUSH_BYTES = 512 << 20
 
 
@@ -96,17 +97,41 @@ def kernel_source_sha(workload: str = "gpt2_small") -> str:
     return h.hexdigest()[:16]
 
 
-def ncu_traffic(workload: str):
-    """DRAM bytes per launch from the committed ncu summary, if it still matches the source."""
+def ncu_figure(workload: str, key: str):
+    """A figure from the committed ncu summary of the workload's kernel, if the
+    summary still matches the source."""
     path = os.path.join(ROOT, "profiles", f"step_kernel_{workload}.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
     sha = re.search(r"kernel_source_sha:\s*([0-9a-f]+)", txt)
-    tr = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    if not sha or not tr or sha.group(1) != kernel_source_sha(workload):
+    val = re.search(key + r":\s*([0-9.eE+]+)", txt)
+    if not sha or not val or sha.group(1) != kernel_source_sha(workload):
         return None
-    return float(tr.group(1))
+    return float(val.group(1))
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)."""
+    return ncu_figure(workload, "dram_bytes_per_launch")
+
+
+def issue_roofline(workload: str, elems_per_s: float, sm_mhz):
+    """The second roofline of the step kernels, instruction issue: ncu's warp
+    instructions per element times the element rate, against one warp
+    instruction per scheduler per cycle (4 schedulers per SM) at the SM clock
+    sampled during the timed region."""
+    wpe = ncu_figure(workload, "warp_instructions_per_element")
+    if wpe is None:
+        return None
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    mhz = sm_mhz or 2070.0
+    peak = sms * 4 * mhz * 1e6
+    achieved = wpe * elems_per_s
+    return {"bound": "issue", "warp_inst_per_element": wpe, "achieved": achieved, "peak": peak,
+            "unit": "warp-inst/s", "frac": achieved / peak,
+            "peak_source": f"{sms} SMs x 4 schedulers x {mhz:.0f} MHz (sampled SM clock)"}
 
 
 class ClockSampler:
@@ -1132,7 +1157,10 @@ def main():
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": ncu_traffic(args.workload),
                          "peak_source": peak_src, "kernel_ms": kernel_ms,
-                         "algorithmic_bytes_per_launch": alg_bytes},
+                         "algorithmic_bytes_per_launch": alg_bytes,
+                         "nominal_peak": NOMINAL_HBM_GBS, "frac_nominal": achieved / NOMINAL_HBM_GBS,
+                         "issue": issue_roofline(args.workload, w.n_params / (kernel_ms * 1e-3),
+                                                 (clk or {}).get("sm_mhz"))},
             "e2e": e2e,
             "gpu_launches": K * w.launches_per_step,
             **({"graph_replay": graph} if graph else {}),
