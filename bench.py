@@ -247,6 +247,24 @@ def cpu_sample_fp32(n, amp=False, lr=1e-3, wd=0.1):
     return run, f"{n} elements per step, float64 oracle (oracle.adamw.step_fp64)"
 
 
+def cpu_sample_fp32_strict(n, amp=False, lr=1e-3, wd=0.1):
+    """One strict-fp32-oracle step over n elements per call (fp32-state workloads)."""
+    import numpy as np
+    from oracle import adamw as OA
+    rng = np.random.default_rng(0)
+    scale = 65536.0 if amp else None
+    g = (rng.normal(0, 1e-3, n) * (scale or 1.0)).astype(np.float32)
+    x = OA.Tensor(p=rng.normal(0, 0.02, n).astype(np.float32), g=g,
+                  m=np.zeros(n, np.float32), v=np.zeros(n, np.float32), wd=OA.f32(wd))
+    state = {"t": 0}
+
+    def run():
+        state["t"] += 1
+        OA.step_f32([x], lr=OA.f32(lr), beta1=OA.f32(0.9), beta2=OA.f32(0.999), eps=OA.f32(1e-8),
+                    t=state["t"], grad_scale=scale)
+    return run, f"{n} elements per step, strict-fp32 oracle (oracle.adamw.step_f32)"
+
+
 def cpu_sample_q8(n):
     import numpy as np
     from oracle import q8 as OQ
@@ -355,6 +373,14 @@ def cpu_sample_coupled(n, rule):
         OC.step_fp64([x], rule=rule, lr=1e-3, beta=0.9, eps=1e-8)
     return run, f"{n} elements per step, float64 {rule} oracle (oracle.coupled.step_fp64)"
 
+
+# The strict-fp32 oracle, timed beside the float64 one for the fp32-state AdamW workloads.
+CPU_SAMPLES_STRICT = {
+    "gpt2_small": lambda n: cpu_sample_fp32_strict(n),
+    "single": lambda n: cpu_sample_fp32_strict(n, lr=0.1),
+    "amp": lambda n: cpu_sample_fp32_strict(n, amp=True, lr=0.1),
+    "amp_fused": lambda n: cpu_sample_fp32_strict(n, amp=True, lr=0.1),
+}
 
 CPU_SAMPLES = {
     "gpt2_small": lambda n: cpu_sample_fp32(n),
@@ -1146,6 +1172,11 @@ def main():
         cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": f"{desc}; {calls} steps in {dt:.1f} s, numpy single-threaded "
                          f"({cpu_threads()} host cores present)"}
+        if args.workload in CPU_SAMPLES_STRICT:
+            run, desc = CPU_SAMPLES_STRICT[args.workload](n)
+            v, calls, dt = time_cpu(run, n, args.cpu_seconds / 2)
+            cpu["strict_fp32"] = {"value": v, "unit": UNIT, "cores": 1,
+                                  "sample": f"{desc}; {calls} steps in {dt:.1f} s"}
 
     if rank == 0:
         line = {
