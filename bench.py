@@ -444,13 +444,18 @@ class Gpt2Small(Workload):
         self.n_params = synth.total_numel(self.specs)
         self.p_buf, ps = _flat_views(self.specs, torch.float32, dev)
         self.g_buf, gs = _flat_views(self.specs, torch.float32, dev)
+        self.g2_buf, gs2 = _flat_views(self.specs, torch.float32, dev)
         self.m_buf, ms = _flat_views(self.specs, torch.float32, dev)
         self.v_buf, vs = _flat_views(self.specs, torch.float32, dev)
-        for i, (p, g) in enumerate(zip(ps, gs)):
+        for i, (p, g, g2) in enumerate(zip(ps, gs, gs2)):
             p.copy_(synth.normal(p.numel(), 0.02, seed + i, dev))
             g.copy_(synth.normal(g.numel(), 1e-3, synth.grad_seed(seed, 0, i), dev))
-        self.opt = FusedAdamW(ps, gs, ms, vs, [s.wd for s in self.specs])
-        self.ps, self.gs, self.ms, self.vs = ps, gs, ms, vs
+            g2.copy_(synth.normal(g2.numel(), 1e-3, synth.grad_seed(seed, 1, i), dev))
+        self.ps, self.gs, self.gs2, self.ms, self.vs = ps, gs, gs2, ms, vs
+        # two grad sets, one plan each, alternating step by step: with one
+        # fixed set, coupled weight decay drives p to -g/wd and the state of
+        # RMSprop towards subnormal values (slow division and square root)
+        self.opts = [FusedAdamW(ps, g, ms, vs, [s.wd for s in self.specs]) for g in (gs, gs2)]
         self.lr_table = torch.tensor([synth.cosine_lr(s) for s in range(100)], dtype=torch.float32,
                                      device=dev)
         self.step_dev = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -467,12 +472,13 @@ class Gpt2Small(Workload):
                 "tensors": len(specs), "numel": synth.total_numel(specs),
                 "bytes_per_param": Gpt2Small.bytes_per_param,
                 "grad_dtype": "f32", "state_dtype": "f32",
+                "grads": "two seeded N(0,1e-3) sets, alternating step by step",
                 "l2": "no flush: 3.48 GB moved per step, larger than the 126 MB L2",
                 "lr_schedule": "cosine 1e-3 -> 1e-4 over 100 steps, lr_dev points into it"}
 
     def step(self, i):
-        self.C.adamw_step(self.opt.plan, self.lr_ptrs[i % 100], self.step_dev.data_ptr(), 0.9, 0.999,
-                          1e-8, None, None, self.stream)
+        self.C.adamw_step(self.opts[i % 2].plan, self.lr_ptrs[i % 100], self.step_dev.data_ptr(),
+                          0.9, 0.999, 1e-8, None, None, self.stream)
 
     def e2e_setup(self, groups=8):
         """Host-offload step: grads arrive from pinned host memory, params go back.
@@ -551,8 +557,8 @@ class AdemamixGpt2(Gpt2Small):
         from adamw_optimizer_step_tensor_gb300 import FusedAdamW
         self.m2_buf, m2s = _flat_views(self.specs, torch.float32, torch.device("cuda"))
         self.m2s = m2s
-        self.opt = FusedAdamW(self.ps, self.gs, self.ms, self.vs, [s.wd for s in self.specs],
-                              exp_avg_slows=m2s)
+        self.opts = [FusedAdamW(self.ps, g, self.ms, self.vs, [s.wd for s in self.specs],
+                                exp_avg_slows=m2s) for g in (self.gs, self.gs2)]
         self.config = AdemamixGpt2.describe()
         self.e2e_what = self.e2e_what.replace("adamw_step", "adamw_ademamix_step")
 
@@ -563,7 +569,7 @@ class AdemamixGpt2(Gpt2Small):
                     l2="no flush: 4.48 GB moved per step, larger than the 126 MB L2")
 
     def step(self, i):
-        self.C.adamw_ademamix_step(self.opt.plan, self.lr_ptrs[i % 100], self.step_dev.data_ptr(),
+        self.C.adamw_ademamix_step(self.opts[i % 2].plan, self.lr_ptrs[i % 100], self.step_dev.data_ptr(),
                                    0.9, 0.999, 0.9999, 5.0, 1e-8, None, None, self.stream)
 
     def _group_plan(self, idx):
@@ -585,7 +591,8 @@ class LionGpt2(Gpt2Small):
     def __init__(self, seed=0):
         super().__init__(seed)
         from adamw_optimizer_step_tensor_gb300 import FusedAdamW
-        self.opt = FusedAdamW(self.ps, self.gs, self.ms, None, [s.wd for s in self.specs])
+        self.opts = [FusedAdamW(self.ps, g, self.ms, None, [s.wd for s in self.specs])
+                     for g in (self.gs, self.gs2)]
         self.vs = self.v_buf = None
         self.config = LionGpt2.describe()
         self.e2e_what = self.e2e_what.replace("adamw_step", "adamw_lion_step")
@@ -597,7 +604,7 @@ class LionGpt2(Gpt2Small):
                     l2="no flush: 2.49 GB moved per step, larger than the 126 MB L2")
 
     def step(self, i):
-        self.C.adamw_lion_step(self.opt.plan, self.lr_ptrs[i % 100], self.step_dev.data_ptr(),
+        self.C.adamw_lion_step(self.opts[i % 2].plan, self.lr_ptrs[i % 100], self.step_dev.data_ptr(),
                                0.9, 0.99, None, None, self.stream)
 
     def _group_plan(self, idx):
@@ -629,7 +636,7 @@ class CoupledGpt2(LionGpt2):
                     "L2 (one state), cosine lr from a device table")
 
     def step(self, i):
-        self.C.adamw_coupled_step(self.opt.plan, self.rule_id, self.lr_ptrs[i % 100],
+        self.C.adamw_coupled_step(self.opts[i % 2].plan, self.rule_id, self.lr_ptrs[i % 100],
                                   self.step_dev.data_ptr(), 0.9, 1e-8, None, None, self.stream)
 
     def _group_step(self, opt, i, step_dev, stream):
