@@ -24,7 +24,13 @@ B1, B2, EPS = f32(0.9), f32(0.999), f32(1e-8)
 SIZES = [1, 255, 256, 257, 2048 + 100, 8192 + 300, 70001, 0]
 
 
-def _build(sizes, gdtype, seed, zero_state):
+def _view(a, misalign):
+    if not misalign:
+        return dev(a)
+    return dev(np.concatenate([np.zeros(1, a.dtype), a]))[1:]   # 4 bytes off the 16-byte grid
+
+
+def _build(sizes, gdtype, seed, zero_state, misalign=False):
     rng = np.random.default_rng(seed)
     st = []
     for n in sizes:
@@ -35,7 +41,7 @@ def _build(sizes, gdtype, seed, zero_state):
         am = np.zeros(nb, np.float32) if zero_state else rng.uniform(0, 1e-3, nb).astype(np.float32)
         av = np.zeros(nb, np.float32) if zero_state else rng.uniform(0, 1e-6, nb).astype(np.float32)
         st.append(dict(p=p, cm=cm, cv=cv, am=am, av=av))
-    d = [{k: dev(v) for k, v in s.items()} for s in st]
+    d = [{k: (_view(v, misalign) if k == "p" else dev(v)) for k, v in s.items()} for s in st]
     gs = [torch.empty(n, dtype=gdtype, device="cuda") for n in sizes]
     opt = FusedAdamW([x["p"] for x in d], gs, [x["cm"] for x in d], [x["cv"] for x in d],
                      [f32(0.01)] * len(sizes), mode="q8", absmax_m=[x["am"] for x in d],
@@ -65,6 +71,32 @@ def test_q8_steps_bitexact(gdtype):
             assert np.array_equal(host(x["cv"]), s["cv"]), f"t{t} tensor {i} v codes"
             assert bits_equal(host(x["am"]), s["am"]), f"t{t} tensor {i} absmax m"
             assert bits_equal(host(x["av"]), s["av"]), f"t{t} tensor {i} absmax v"
+
+
+def test_q8_element_path_on_misaligned_params():
+    """Params 4 bytes off the 16-byte grid: every block of those tensors takes
+    the element path (scalar loads, per-element predicates), several warps of
+    the 1024-thread CTA at once; still bit-exact."""
+    opt, st, d, gs, rng = _build([1, 257, 1000, 9000], torch.float32, seed=20, zero_state=False,
+                                 misalign=True)
+    maps = OQ.Maps()
+    lr, step = scalar_f32(f32(1e-3)), scalar_i32(0)
+    for t in range(1, 3):
+        wide = []
+        for g in gs:
+            tg, w = grads_of(rng.normal(0, 1e-3, g.numel()).astype(np.float32), torch.float32)
+            g.copy_(tg)
+            wide.append(w)
+        opt.step(lr, step, betas=(B1, B2), eps=EPS)
+        for s, w in zip(st, wide):
+            OQ.step_f32(s["p"], w, s["cm"], s["cv"], s["am"], s["av"], lr=f32(1e-3), beta1=B1,
+                        beta2=B2, eps=EPS, wd=f32(0.01), t=t, maps=maps)
+        torch.cuda.synchronize()
+        for i, (s, x) in enumerate(zip(st, d)):
+            assert bits_equal(host(x["p"]), s["p"]), f"t{t} tensor {i} p"
+            assert np.array_equal(host(x["cm"]), s["cm"]), f"t{t} tensor {i} m codes"
+            assert np.array_equal(host(x["cv"]), s["cv"]), f"t{t} tensor {i} v codes"
+            assert bits_equal(host(x["am"]), s["am"]) and bits_equal(host(x["av"]), s["av"])
 
 
 def test_q8_first_step_closed_form():
