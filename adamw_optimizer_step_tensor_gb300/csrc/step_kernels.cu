@@ -1,9 +1,12 @@
-// step_kernels.cu -- the fused AdamW step kernels for sm_103a.
+// step_kernels.cu -- the register-load step kernels for sm_103a: the 8-bit
+// step, the fused non-finite check + step of adamw_step_amp, and the fp32 /
+// bf16+remainder step that the bulk-staged kernel (bulk_kernels.cu) replaced,
+// kept behind kUseBulk as its A/B baseline.
 //
 // One persistent launch covers every tensor of a plan: CTAs stride over the
-// plan's chunk table (2048-16384 contiguous elements of one tensor per chunk),
-// and each thread moves 8 consecutive elements per pass with 128-bit
-// streaming loads and stores.  The step is a pure HBM stream (28 B per element in fp32
+// plan's chunk table (up to 16384 contiguous elements of one tensor per chunk,
+// a multiple of 256 but at a tensor's end), and each thread moves 8
+// consecutive elements per pass with 128-bit streaming loads and stores.  The step is a pure HBM stream (28 B per element in fp32
 // mode, 26 in bf16+remainder mode, 14.06 in 8-bit mode), so there is no
 // tensor-core work; the kernel's job is to keep enough bytes in flight.
 //

@@ -213,8 +213,9 @@ adamw_status adamw_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev
  *
  * Instead of plan memory the call uses one static device array built into the
  * library (about 1.1 MB on every GPU that loads it, held until the process
- * exits).  Limits: at most 1024 tensors and 65536 chunks per call (chunks are
- * 2048-16384 elements, about 1.07e9 elements in all); larger lists are rejected
+ * exits).  Limits: at most 1024 tensors and 65536 chunks per call (a chunk
+ * holds at most 16384 elements, so about 1.07e9 elements in all); larger lists
+ * are rejected
  * with ADAMW_EINVAL before anything is enqueued.  Each call copies the tensor
  * and chunk tables from a static host buffer into the array (a pageable
  * host-to-device copy, which may make the host wait for the stream) and clears
