@@ -428,7 +428,56 @@ class Workload:
 
 
 
-class Gpt2Small(Workload):
+class PipelinedE2E:
+    """The host-offload arm of a workload: every step its grads arrive from
+    pinned host memory and its updated params go back.  The elements are cut
+    into groups with one plan (and step counter) each, so that the
+    host-to-device copy of one group, the step of the previous one and the
+    device-to-host copy of the one before overlap on three streams."""
+
+    def _pipeline(self, g_dev, p_dev, groups):
+        """groups: (lo, hi, plan) over the flat element ranges of g_dev / p_dev."""
+        import torch
+        self._g_dev, self._p_dev = g_dev, p_dev
+        self._host_g = torch.empty_like(g_dev, device="cpu").pin_memory()
+        self._host_g.copy_(g_dev)
+        self._host_p = torch.empty_like(p_dev, device="cpu").pin_memory()
+        self._groups = [(lo, hi, opt, torch.zeros(1, dtype=torch.int32, device="cuda"))
+                        for lo, hi, opt in groups]
+        self._s = [torch.cuda.Stream() for _ in range(3)]          # in, step, out
+        n = len(self._groups)
+        self._ev = [[torch.cuda.Event() for _ in range(n)] for _ in range(3)]
+        return (self._host_g.numel() * self._host_g.element_size(),
+                self._host_p.numel() * self._host_p.element_size())
+
+    def e2e_begin(self, stream):
+        for s in self._s:
+            s.wait_stream(stream)
+
+    def e2e_end(self, stream):
+        for s in self._s:
+            stream.wait_stream(s)
+
+    def e2e_step(self, i):
+        import torch
+        s_in, s_cmp, s_out = self._s
+        ev_in, ev_cmp, ev_out = self._ev
+        for k, (lo, hi, opt, step_dev) in enumerate(self._groups):
+            s_in.wait_event(ev_cmp[k])            # the previous step has consumed these grads
+            with torch.cuda.stream(s_in):
+                self._g_dev[lo:hi].copy_(self._host_g[lo:hi], non_blocking=True)
+            ev_in[k].record(s_in)
+            s_cmp.wait_event(ev_in[k])
+            s_cmp.wait_event(ev_out[k])           # the previous copy-out has read these params
+            self._group_step(opt, i, step_dev, s_cmp.cuda_stream)
+            ev_cmp[k].record(s_cmp)
+            s_out.wait_event(ev_cmp[k])
+            with torch.cuda.stream(s_out):
+                self._host_p[lo:hi].copy_(self._p_dev[lo:hi], non_blocking=True)
+            ev_out[k].record(s_out)
+
+
+class Gpt2Small(PipelinedE2E, Workload):
     name = "gpt2_small_fp32_cosine_lr"
     bytes_per_param = 28.0
     e2e_what = ("pinned-host grads -> device, adamw_step, updated params -> pinned host; the list "
@@ -481,33 +530,19 @@ class Gpt2Small(Workload):
                           0.9, 0.999, 1e-8, None, None, self.stream)
 
     def e2e_setup(self, groups=8):
-        """Host-offload step: grads arrive from pinned host memory, params go back.
-
-        The list is split into `groups` contiguous runs of tensors with about
-        equal element counts, one plan (and step counter) each, so that the
-        host-to-device copy of one group, the step of the previous one and the
-        device-to-host copy of the one before overlap on three streams.
-        """
-        import torch
-        self._host_g = torch.empty_like(self.g_buf, device="cpu").pin_memory()
-        self._host_g.copy_(self.g_buf)
-        self._host_p = torch.empty_like(self.p_buf, device="cpu").pin_memory()
+        """The list in `groups` contiguous runs of tensors of about equal element
+        counts (PipelinedE2E)."""
         base = self.p_buf.data_ptr()
         offs = [(p.data_ptr() - base) // 4 for p in self.ps]
         target = self.n_params / groups
-        self._groups, start, acc = [], 0, 0
+        runs, start, acc = [], 0, 0
         for k, p in enumerate(self.ps):
             acc += p.numel()
-            if acc >= target * (len(self._groups) + 1) or k == len(self.ps) - 1:
+            if acc >= target * (len(runs) + 1) or k == len(self.ps) - 1:
                 idx = list(range(start, k + 1))
-                lo, hi = offs[start], offs[k] + self.ps[k].numel()
-                opt = self._group_plan(idx)
-                self._groups.append((lo, hi, opt, torch.zeros(1, dtype=torch.int32, device="cuda")))
+                runs.append((offs[start], offs[k] + self.ps[k].numel(), self._group_plan(idx)))
                 start = k + 1
-        self._s = [torch.cuda.Stream() for _ in range(3)]          # in, step, out
-        n = len(self._groups)
-        self._ev = [[torch.cuda.Event() for _ in range(n)] for _ in range(3)]
-        return self._host_g.numel() * 4, self._host_p.numel() * 4
+        return self._pipeline(self.g_buf, self.p_buf, runs)
 
     def _group_plan(self, idx):
         from adamw_optimizer_step_tensor_gb300 import FusedAdamW
@@ -518,32 +553,6 @@ class Gpt2Small(Workload):
     def _group_step(self, opt, i, step_dev, stream):
         self.C.adamw_step(opt.plan, self.lr_ptrs[i % 100], step_dev.data_ptr(), 0.9, 0.999, 1e-8,
                           None, None, stream)
-
-    def e2e_begin(self, stream):
-        for s in self._s:
-            s.wait_stream(stream)
-
-    def e2e_end(self, stream):
-        for s in self._s:
-            stream.wait_stream(s)
-
-    def e2e_step(self, i):
-        import torch
-        s_in, s_cmp, s_out = self._s
-        ev_in, ev_cmp, ev_out = self._ev
-        for k, (lo, hi, opt, step_dev) in enumerate(self._groups):
-            s_in.wait_event(ev_cmp[k])            # the previous step has consumed these grads
-            with torch.cuda.stream(s_in):
-                self.g_buf[lo:hi].copy_(self._host_g[lo:hi], non_blocking=True)
-            ev_in[k].record(s_in)
-            s_cmp.wait_event(ev_in[k])
-            s_cmp.wait_event(ev_out[k])           # the previous copy-out has read these params
-            self._group_step(opt, i, step_dev, s_cmp.cuda_stream)
-            ev_cmp[k].record(s_cmp)
-            s_out.wait_event(ev_cmp[k])
-            with torch.cuda.stream(s_out):
-                self._host_p[lo:hi].copy_(self.p_buf[lo:hi], non_blocking=True)
-            ev_out[k].record(s_out)
 
 
 class AdemamixGpt2(Gpt2Small):
@@ -714,9 +723,13 @@ class Single(Workload):
 
 
 
-class Q8(Workload):
+class Q8(PipelinedE2E, Workload):
     name = "q8_blockwise_1G"
     bytes_per_param = 14.0625
+    mode, block, codes_per_byte = "q8", 256, 1
+    e2e_what = ("pinned-host grads -> device, adamw_step, updated params -> pinned host; the "
+                "tensor in 8 slices (one plan each) so copies in, steps and copies out overlap "
+                "on 3 streams")
 
     def __init__(self, seed=4, numel=0):
         import torch
@@ -750,17 +763,25 @@ class Q8(Workload):
         self.C.adamw_step(self.opt.plan, self.lr.data_ptr(), self.step_dev.data_ptr(), 0.9, 0.999,
                           1e-8, None, None, self.stream)
 
-    def e2e_setup(self):
-        import torch
-        self._host_g = torch.empty_like(self.g, device="cpu").pin_memory()
-        self._host_g.copy_(self.g)
-        self._host_p = torch.empty_like(self.p, device="cpu").pin_memory()
-        return self._host_g.numel() * 2, self._host_p.numel() * 4
+    def e2e_setup(self, groups=8):
+        """The tensor in `groups` slices of whole blocks, one plan each (PipelinedE2E)."""
+        from adamw_optimizer_step_tensor_gb300 import FusedAdamW
+        n, b, cpb = self.n_params, self.block, self.codes_per_byte
+        size = -(-n // groups // b) * b
+        runs = []
+        for lo in range(0, n, size):
+            hi = min(n, lo + size)
+            c0, c1 = lo // cpb, -(-hi // cpb)
+            a0, a1 = lo // b, -(-hi // b)
+            opt = FusedAdamW([self.p[lo:hi]], [self.g[lo:hi]], [self.cm[c0:c1]], [self.cv[c0:c1]],
+                             [0.01], mode=self.mode, absmax_m=[self.am[a0:a1]],
+                             absmax_v=[self.av[a0:a1]])
+            runs.append((lo, hi, opt))
+        return self._pipeline(self.g, self.p, runs)
 
-    def e2e_step(self, i):
-        self.g.copy_(self._host_g, non_blocking=True)
-        self.step(i)
-        self._host_p.copy_(self.p, non_blocking=True)
+    def _group_step(self, opt, i, step_dev, stream):
+        self.C.adamw_step(opt.plan, self.lr.data_ptr(), step_dev.data_ptr(), 0.9, 0.999, 1e-8,
+                          None, None, stream)
 
 
 
@@ -768,6 +789,7 @@ class Q4(Q8):
     """The q8 workload with 4-bit packed codes and 128-element blocks."""
     name = "q4_blockwise_1G"
     bytes_per_param = 12.125      # p 4+4, g 2, codes 0.5+0.5 each way, absmax 8/128 each way
+    mode, block, codes_per_byte = "q4", 128, 2
 
     def __init__(self, seed=4, numel=0):
         import torch
