@@ -529,6 +529,17 @@ class Gpt2Small(PipelinedE2E, Workload):
         self.C.adamw_step(self.opts[i % 2].plan, self.lr_ptrs[i % 100], self.step_dev.data_ptr(),
                           0.9, 0.999, 1e-8, None, None, self.stream)
 
+    def step_grads(self, i):
+        """The grad tensors that step i reads (the two sets alternate)."""
+        return self.gs if i % 2 == 0 else self.gs2
+
+    def status(self) -> int:
+        """Device-side fault bits of every plan, or-ed."""
+        out = 0
+        for o in self.opts:
+            out |= o.status()
+        return out
+
     def e2e_setup(self, groups=8):
         """The list in `groups` contiguous runs of tensors of about equal element
         counts (PipelinedE2E)."""

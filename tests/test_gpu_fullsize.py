@@ -63,9 +63,10 @@ def test_gpt2_small_full_size_cosine_lr_sampled():
         ref = [OA.Tensor(p=o.p.astype(np.float64), g=None, m=o.m.astype(np.float64),
                          v=o.v.astype(np.float64), wd=o.wd) for o in orc]
         for s in range(100):
-            for k, g in enumerate(w.gs):
+            gs = w.step_grads(s)
+            for k, g in enumerate(gs):
                 g.copy_(synth.normal(g.numel(), 1e-3, synth.grad_seed(7, s, k), "cuda"))
-            for o, r, g, i in zip(orc, ref, w.gs, idx):
+            for o, r, g, i in zip(orc, ref, gs, idx):
                 o.g = _take(g, i).cpu().numpy()
                 r.g = o.g.astype(np.float64)
             w.step(s)
@@ -79,7 +80,7 @@ def test_gpt2_small_full_size_cosine_lr_sampled():
                     assert np.array_equal(_take(m, i).cpu().numpy().view(np.uint32), o.m.view(np.uint32)), (s, k)
                     assert np.array_equal(_take(v, i).cpu().numpy().view(np.uint32), o.v.view(np.uint32)), (s, k)
         assert int(w.step_dev.item()) == 100
-        assert w.opt.status() == 0
+        assert w.status() == 0
         worst = max(np.max(np.abs(o.p.astype(np.float64) - r.p)) for o, r in zip(orc, ref))
         assert worst <= 5e-5
     finally:
@@ -199,16 +200,17 @@ def _elementwise_full_size(w, step_fn, make_orc, check, n_steps, seed):
     idx = _windows([p.numel() for p in w.ps], rng)
     orc = make_orc(idx)
     for s in range(n_steps):
-        for k, g in enumerate(w.gs):
+        gs = w.step_grads(s)
+        for k, g in enumerate(gs):
             g.copy_(synth.normal(g.numel(), 1e-3, synth.grad_seed(seed, s, k), "cuda"))
-        for o, g, i in zip(orc, w.gs, idx):
+        for o, g, i in zip(orc, gs, idx):
             o.g = _take(g, i).cpu().numpy()
         w.step(s)
         step_fn(orc, float(w.lr_table[s % 100].item()), s)
     torch.cuda.synchronize()
     check(orc, idx)
     assert int(w.step_dev.item()) == n_steps
-    assert w.opt.status() == 0
+    assert w.status() == 0
 
 
 def test_lion_gpt2_full_size_sampled():
