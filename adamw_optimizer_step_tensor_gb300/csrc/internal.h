@@ -23,16 +23,16 @@ template <> struct Tune<ADAMW_MODE_FP32> { static constexpr int unroll = 2, min_
 constexpr int kChunkMax = 8 * kPass;         // chunks hold up to 16384 elements (chosen per plan)
 // fp32 and bf16+remainder steps stage tiles through shared memory with bulk
 // async copies (bulk_kernels.cu) instead of 128-bit register loads.  The
-// 8-bit and 4-bit steps load into registers: their bound is the
-// shared-memory pipe (code-table lookups), which staging would load further
-// (a bulk-staged 8-bit step measured 5% slower, a per-warp cp.async-staged
-// one 38% slower).
+// 8-bit and 4-bit steps load into registers: they are bound by instruction
+// issue and load latency, and staging would spend shared-memory bandwidth
+// that their code-table lookups need (a bulk-staged 8-bit step measured 5%
+// slower, per-warp cp.async staging 24-38% slower).
 constexpr bool kUseBulk = true;
 // The bulk-staged step: 16 consumer warps and one producer warp per CTA.
 constexpr int kBulkConsumers = 2 * kThreads;
 constexpr int kBulkThreads = kBulkConsumers + 32;
 // The 8-bit step runs one CTA of kQ8Threads per SM (64 registers a thread):
-// its lane-private code tables (lane_tables.cuh, 139 KB) fit once per SM.
+// its lane-private code tables (lane_tables.cuh, 141.7 KB) fit once per SM.
 constexpr int kQ8Threads = 1024;
 constexpr int kQ8Pass = kQ8Threads * kVec;   // 8192 elements per CTA pass
 constexpr int kQBlock = ADAMW_Q8_BLOCK;      // 256
