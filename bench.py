@@ -116,16 +116,17 @@ def ncu_traffic(workload: str):
     return ncu_figure(workload, "dram_bytes_per_launch")
 
 
-def issue_roofline(workload: str, elems_per_s: float, sm_mhz):
+def issue_roofline(workload: str, elems_per_s: float, sm_mhz, sms: int | None = None):
     """The second roofline of the step kernels, instruction issue: ncu's warp
     instructions per element times the element rate, against one warp
     instruction per scheduler per cycle (4 schedulers per SM) at the SM clock
-    sampled during the timed region."""
+    sampled during the timed region (the device's SM count unless given)."""
     wpe = ncu_figure(workload, "warp_instructions_per_element")
     if wpe is None:
         return None
-    import torch
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    if sms is None:
+        import torch
+        sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
     mhz = sm_mhz or 2070.0
     peak = sms * 4 * mhz * 1e6
     achieved = wpe * elems_per_s
