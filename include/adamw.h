@@ -221,9 +221,11 @@ adamw_status adamw_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev
  * host-to-device copy, which may make the host wait for the stream) and clears
  * the array's step counter, then launches the step kernel.
  * The first call on each device looks up the array's device address with that
- * device current; make that first call before any stream capture.  All calls
- * share the one array: calls whose work may overlap on the GPU (different
- * streams without ordering between them) race and must not be issued.
+ * device current.  The entry point is not meant for stream capture (every call
+ * uploads its tables with a pageable host-to-device copy); a captured step is
+ * adamw_step on a plan.  All calls share the one array: calls whose work may
+ * overlap on the GPU (different streams without ordering between them) race
+ * and must not be issued.
  */
 adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t n_tensors,
                                 adamw_mode mode, adamw_dtype grad_dtype,
