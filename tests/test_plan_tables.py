@@ -296,3 +296,37 @@ def test_fused_amp_table_and_threshold(lib):
                 assert lib.probe_kind(0).decode() == "bulk"
         finally:
             lib.adamw_plan_destroy(plan)
+
+
+def _cluster_map(k):
+    """A signed map with k extra levels 0.0008 apart just above 0.6: their
+    thresholds crowd one bucket of the nearest-code search."""
+    grid = np.linspace(-1, 1, 241)
+    pads = (grid[12:12 + 15 - k] + grid[13:13 + 15 - k]) / 2
+    return np.sort(np.concatenate([grid, 0.6 + 0.0008 * np.arange(1, k + 1), pads])).astype(np.float32)
+
+
+def test_q8_maps_set_the_compares_per_lookup(lib):
+    lib.adamw_q8_set_maps.restype = ctypes.c_int
+    lib.adamw_q8_set_maps.argtypes = [_vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_float)]
+    lib.probe_refine.restype, lib.probe_refine.argtypes = ctypes.c_int, [ctypes.c_int]
+    fake = Fake()
+    plan = _create(lib, _records([100_000], C.MODE_Q8, fake), C.MODE_Q8)
+    try:
+        lr, step = _scalars(fake)
+        umap = np.linspace(0, 1, 256).astype(np.float32)
+        fp = ctypes.POINTER(ctypes.c_float)
+        assert lib.adamw_step(plan, lr, step, 0.9, 0.999, 1e-8, None, None, None) == C.OK
+        assert lib.probe_refine(0) == 1                       # the default maps: one compare
+        for k, refine in ((3, 2), (5, 3)):
+            smap = _cluster_map(k)
+            assert lib.adamw_q8_set_maps(plan, smap.ctypes.data_as(fp), umap.ctypes.data_as(fp)) == C.OK
+            assert lib.adamw_step(plan, lr, step, 0.9, 0.999, 1e-8, None, None, None) == C.OK
+            assert lib.probe_refine(0) == refine, k
+        assert lib.adamw_q8_set_maps(plan, _cluster_map(7).ctypes.data_as(fp),
+                                     umap.ctypes.data_as(fp)) == C.EUNSUPPORTED
+        assert b"too dense" in lib.adamw_last_error()
+        assert lib.adamw_step(plan, lr, step, 0.9, 0.999, 1e-8, None, None, None) == C.OK
+        assert lib.probe_refine(0) == 3                       # a refused map leaves the plan as it was
+    finally:
+        lib.adamw_plan_destroy(plan)
