@@ -330,3 +330,45 @@ def test_q8_maps_set_the_compares_per_lookup(lib):
         assert lib.probe_refine(0) == 3                       # a refused map leaves the plan as it was
     finally:
         lib.adamw_plan_destroy(plan)
+
+
+def test_rule_launches_and_empty_plans(lib):
+    lib.adamw_ademamix_step.restype = ctypes.c_int
+    lib.adamw_ademamix_step.argtypes = [_vp, _vp, _vp] + [ctypes.c_float] * 5 + [_vp, _vp, _vp]
+    lib.adamw_lion_step.restype = ctypes.c_int
+    lib.adamw_lion_step.argtypes = [_vp, _vp, _vp, ctypes.c_float, ctypes.c_float, _vp, _vp, _vp]
+    fake = Fake()
+    lr, step = _scalars(fake)
+    # AdEMAMix: the slow EMA reaches the tensor table, the bulk kernel runs rule 1
+    recs = _records([5000, 300], C.MODE_FP32, fake)
+    for r in recs:
+        r.exp_avg_slow = fake(r.numel * 4)
+    plan = _create(lib, recs, C.MODE_FP32, C.F32)
+    try:
+        assert lib.adamw_ademamix_step(plan, lr, step, 0.9, 0.999, 0.9999, 5.0, 1e-8, None, None,
+                                       None) == C.OK
+        assert lib.probe_kind(0).decode() == "bulk" and lib.probe_algo(0) == 1
+        tds = _read(lib.probe_tensors(0), TDESC, 2)
+        assert [int(t["m2"]) for t in tds] == [r.exp_avg_slow for r in recs]
+        assert lib.adamw_step(plan, lr, step, 0.9, 0.999, 1e-8, None, None, None) == C.OK
+        assert lib.probe_algo(0) == 0
+    finally:
+        lib.adamw_plan_destroy(plan)
+    # Lion on a 1-state plan: rule 2, one CTA per SM
+    plan = _create(lib, _records([1 << 22], C.MODE_BF16_REM, fake, with_v=False), C.MODE_BF16_REM)
+    try:
+        assert lib.adamw_lion_step(plan, lr, step, 0.9, 0.99, None, None, None) == C.OK
+        assert lib.probe_algo(0) == 2
+        assert lib.probe_grid(0) == min(lib.probe_n_chunks(0), SMS)
+        tds = _read(lib.probe_tensors(0), TDESC, 1)
+        assert tds[0]["v"] == 0 and tds[0]["rem"] != 0
+    finally:
+        lib.adamw_plan_destroy(plan)
+    # an empty plan still launches (one CTA, no chunks): the step counter advances on device
+    for mode in (C.MODE_FP32, C.MODE_Q8, C.MODE_Q4):
+        plan = _create(lib, [], mode)
+        try:
+            assert lib.adamw_step(plan, lr, step, 0.9, 0.999, 1e-8, None, None, None) == C.OK
+            assert lib.probe_n_chunks(0) == 0 and lib.probe_grid(0) == 1, mode
+        finally:
+            lib.adamw_plan_destroy(plan)
