@@ -18,7 +18,8 @@ from ._capi import (  # noqa: F401
     adamw_check_nonfinite, adamw_last_error, adamw_lr_from_table, adamw_plan_create,
     adamw_plan_destroy,
     adamw_plan_info, adamw_plan_status, adamw_q8_default_maps, adamw_q8_dequant, adamw_q8_quant,
-    adamw_q8_set_maps, adamw_step, adamw_step_amp, adamw_step_noalloc, adamw_wait_selftest,
+    adamw_q8_set_maps, adamw_step, adamw_step_amp, adamw_step_noalloc, adamw_step_noalloc_status,
+    adamw_wait_selftest,
 )
 
 MODES = {"fp32": _capi.MODE_FP32, "bf16_rem": _capi.MODE_BF16_REM, "q8": _capi.MODE_Q8,

@@ -68,6 +68,7 @@ _SIGNATURES = {
     "adamw_step_noalloc": (ctypes.c_int, [ctypes.POINTER(adamw_tensor), ctypes.c_int32, ctypes.c_int,
                                           ctypes.c_int, _vp, _vp, ctypes.c_float, ctypes.c_float,
                                           ctypes.c_float, _vp, _vp, _vp]),
+    "adamw_step_noalloc_status": (ctypes.c_int, [ctypes.POINTER(ctypes.c_uint32)]),
     "adamw_lr_from_table": (ctypes.c_int, [_vp, ctypes.c_int32, _vp, _vp, _vp]),
     "adamw_ademamix_step": (ctypes.c_int, [_vp, _vp, _vp, ctypes.c_float, ctypes.c_float,
                                            ctypes.c_float, ctypes.c_float, ctypes.c_float,
@@ -200,6 +201,14 @@ def adamw_step_noalloc(tensors: list[adamw_tensor], mode: int, grad_dtype: int, 
     arr = (adamw_tensor * max(1, len(tensors)))(*tensors)
     _check(load().adamw_step_noalloc(arr, len(tensors), mode, grad_dtype, lr_dev, step_dev, beta1,
                                      beta2, eps, grad_scale_dev, found_inf_dev, stream))
+
+
+def adamw_step_noalloc_status() -> int:
+    """Fault bits of adamw_step_noalloc's static array on the current device
+    (read, then cleared); raises AdamWError (ETIMEOUT) if any was set."""
+    bits = ctypes.c_uint32()
+    _check(load().adamw_step_noalloc_status(ctypes.byref(bits)))
+    return bits.value
 
 
 def adamw_ademamix_step(plan: int, lr_dev: int, step_dev: int, beta1: float, beta2: float,

@@ -8,7 +8,7 @@
 #include <string>
 #include <vector>
 
-#include "internal.h"
+#include "entry_checks.h"
 
 namespace adamw {
 void default_maps(float smap[256], float umap[256]);
@@ -120,48 +120,19 @@ adamw_status check_device(const adamw_plan* p) {
   return ADAMW_OK;
 }
 
-// Checks every step entry point shares: the plan, the run-time scalar pointers
-// (lr and step required, grad scale and found-inf optional) and betas in [0, 1).
+// Checks every step entry point shares: the plan, then the run-time scalars.
 adamw_status check_step(const adamw_plan* plan, const float* lr_dev, const int32_t* step_dev,
                         const float* grad_scale_dev, const float* found_inf_dev,
                         float beta1, float beta2) {
   if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
-  if (!lr_dev || !step_dev) return fail(ADAMW_EINVAL, "lr_dev and step_dev must be set");
-  if (!aligned(lr_dev, 4) || !aligned(step_dev, 4) || !aligned(grad_scale_dev, 4) ||
-      !aligned(found_inf_dev, 4))
-    return fail(ADAMW_EALIGN, "a scalar pointer is not 4-byte aligned");
-  if (!(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f))
-    return fail(ADAMW_EINVAL, "betas must lie in [0, 1)");
-  return ADAMW_OK;
+  return check_step_scalars(lr_dev, step_dev, grad_scale_dev, found_inf_dev, beta1, beta2);
 }
 
-adamw_status check_eps(float eps) {
-  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(ADAMW_EINVAL, "eps must be finite and >= 0");
-  return ADAMW_OK;
-}
-
-// The launch arguments every step shares; rule-specific fields keep their
-// neutral values (no slow EMA, no code maps, no Adam-mini blocks).
 StepArgs step_args(const adamw_plan* plan, const float* lr_dev, int32_t* step_dev,
                    const float* grad_scale_dev, const float* found_inf_dev, float beta1,
                    float beta2, float eps) {
-  StepArgs a;
-  a.tensors = plan->d_tensors;
-  a.chunks = plan->d_chunks;
-  a.n_chunks = plan->n_chunks;
-  a.lr = lr_dev;
-  a.step = step_dev;
-  a.grad_scale = grad_scale_dev;
-  a.found_inf = found_inf_dev;
-  a.beta1 = beta1;
-  a.beta2 = beta2;
-  a.eps = eps;
-  a.beta3 = 0.0f;
-  a.alpha = 0.0f;
-  a.scratch = plan->d_scratch;
-  a.qt = nullptr;
-  a.refine = 1;
-  return a;
+  return base_step_args(plan->d_tensors, plan->d_chunks, plan->n_chunks, plan->d_scratch, lr_dev,
+                        step_dev, grad_scale_dev, found_inf_dev, beta1, beta2, eps);
 }
 
 // n = 256 (8-bit maps, both must contain 0.0) or 16 (the 4-bit maps; the v
@@ -190,6 +161,31 @@ adamw_status build_qtables(const float* smap, const float* umap, int n, QTables*
 }  // namespace
 
 void adamw::set_last_error(const char* msg) { g_err = msg; }
+
+adamw_status adamw::check_mode_dtype(int mode, int grad_dtype) {
+  if (!valid_mode(mode)) return fail(ADAMW_EDTYPE, "unknown mode %d", mode);
+  if (!valid_dtype(grad_dtype)) return fail(ADAMW_EDTYPE, "unknown grad dtype %d", grad_dtype);
+  return ADAMW_OK;
+}
+
+// The run-time scalar pointers (lr and step required, grad scale and
+// found-inf optional, all 4-byte aligned) and betas in [0, 1).
+adamw_status adamw::check_step_scalars(const float* lr_dev, const int32_t* step_dev,
+                                       const float* grad_scale_dev, const float* found_inf_dev,
+                                       float beta1, float beta2) {
+  if (!lr_dev || !step_dev) return fail(ADAMW_EINVAL, "lr_dev and step_dev must be set");
+  if (!aligned(lr_dev, 4) || !aligned(step_dev, 4) || !aligned(grad_scale_dev, 4) ||
+      !aligned(found_inf_dev, 4))
+    return fail(ADAMW_EALIGN, "a scalar pointer is not 4-byte aligned");
+  if (!(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f))
+    return fail(ADAMW_EINVAL, "betas must lie in [0, 1)");
+  return ADAMW_OK;
+}
+
+adamw_status adamw::check_eps(float eps) {
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return fail(ADAMW_EINVAL, "eps must be finite and >= 0");
+  return ADAMW_OK;
+}
 
 static adamw_status create_plan(const adamw_tensor* tensors, int32_t n_tensors, adamw_mode mode,
                                 adamw_dtype grad_dtype, const int64_t* v_block,
@@ -223,8 +219,7 @@ static adamw_status create_plan(const adamw_tensor* tensors, int32_t n_tensors, 
   *out = nullptr;
   if (n_tensors < 0) return fail(ADAMW_EINVAL, "n_tensors < 0");
   if (n_tensors > 0 && !tensors) return fail(ADAMW_EINVAL, "tensors is NULL");
-  if (!valid_mode(mode)) return fail(ADAMW_EDTYPE, "unknown mode %d", (int)mode);
-  if (!valid_dtype(grad_dtype)) return fail(ADAMW_EDTYPE, "unknown grad dtype %d", (int)grad_dtype);
+  if (adamw_status st = check_mode_dtype(mode, grad_dtype); st != ADAMW_OK) return st;
 
   const size_t psz = mode == ADAMW_MODE_BF16_REM ? 2 : 4;
   const size_t ssz = quantized(mode) ? 1 : 4;

@@ -14,10 +14,14 @@
 // call (chunks are at most 16384 elements, so up to about 1.07e9 elements);
 // the array is about 1.1 MB and every GPU that loads the library holds it
 // until the process exits.  fp32 and bf16+remainder modes only.
+//
+// A bounded wait of the kernel that gives up sets a bit in the array's fault
+// word; calls never clear it, adamw_step_noalloc_status reads and clears it.
+#include <cmath>
 #include <cstdio>
 #include <mutex>
 
-#include "internal.h"
+#include "entry_checks.h"
 
 namespace adamw {
 namespace {
@@ -68,32 +72,33 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 using namespace adamw;
 
-extern "C" adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t n_tensors,
-                                           adamw_mode mode, adamw_dtype grad_dtype,
-                                           const float* lr_dev, int32_t* step_dev, float beta1,
-                                           float beta2, float eps, const float* grad_scale_dev,
-                                           const float* found_inf_dev, void* stream) {
+// Validation that touches no device: arguments, and the chunk count's lower
+// bound (every chunk holds at most kChunkMax elements), so that a list the
+// array cannot hold is refused before anything is enqueued.
+static adamw_status check_noalloc_args(const adamw_tensor* tensors, int32_t n_tensors,
+                                       adamw_mode mode, adamw_dtype grad_dtype,
+                                       const float* lr_dev, const int32_t* step_dev, float beta1,
+                                       float beta2, float eps, const float* grad_scale_dev,
+                                       const float* found_inf_dev, int64_t* total_out) {
   if (n_tensors < 0 || (n_tensors > 0 && !tensors)) return fail(ADAMW_EINVAL, "bad tensor list");
   if (n_tensors > kNoAllocMaxTensors)
     return fail(ADAMW_EINVAL, "more tensors than the static scratch holds (limit 1024)");
+  adamw_status st = check_mode_dtype(mode, grad_dtype);
+  if (st != ADAMW_OK) return st;
   if (mode != ADAMW_MODE_FP32 && mode != ADAMW_MODE_BF16_REM)
     return fail(ADAMW_EUNSUPPORTED, "only the fp32 and bf16+remainder modes have a no-allocation form");
-  if (grad_dtype != ADAMW_F32 && grad_dtype != ADAMW_F16 && grad_dtype != ADAMW_BF16)
-    return fail(ADAMW_EDTYPE, "unknown grad dtype");
-  if (!lr_dev || !step_dev) return fail(ADAMW_EINVAL, "lr_dev and step_dev must be set");
-  if (!aligned(lr_dev, 4) || !aligned(step_dev, 4) || !aligned(grad_scale_dev, 4) ||
-      !aligned(found_inf_dev, 4))
-    return fail(ADAMW_EALIGN, "a scalar pointer is not 4-byte aligned");
-  if (!(beta1 >= 0.0f && beta1 < 1.0f) || !(beta2 >= 0.0f && beta2 < 1.0f) || !(eps >= 0.0f))
-    return fail(ADAMW_EINVAL, "betas must lie in [0, 1) and eps must be >= 0");
+  if ((st = check_step_scalars(lr_dev, step_dev, grad_scale_dev, found_inf_dev, beta1, beta2)) !=
+          ADAMW_OK ||
+      (st = check_eps(eps)) != ADAMW_OK)
+    return st;
 
   const size_t psz = mode == ADAMW_MODE_BF16_REM ? 2 : 4;
   const size_t gsz = grad_dtype == ADAMW_F32 ? 4 : 2;
-  int64_t total = 0;
+  int64_t total = 0, min_chunks = 0;
   for (int32_t i = 0; i < n_tensors; ++i) {
     const adamw_tensor& t = tensors[i];
     if (t.numel < 0) return fail(ADAMW_EINVAL, "a tensor has numel < 0");
-    if (!(t.weight_decay == t.weight_decay) || t.weight_decay - t.weight_decay != 0.0f)
+    if (!std::isfinite(t.weight_decay))
       return fail(ADAMW_EINVAL, "a tensor's weight_decay is not finite");
     if (t.numel == 0) continue;
     if (!t.param || !t.grad || !t.exp_avg || !t.exp_avg_sq || t.absmax_m || t.absmax_v ||
@@ -105,26 +110,53 @@ extern "C" adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t 
         !aligned(t.exp_avg_sq, 4) || (t.param_rem && !aligned(t.param_rem, 2)))
       return fail(ADAMW_EALIGN, "a pointer is not aligned to its element size");
     total += t.numel;
+    min_chunks += (t.numel + kChunkMax - 1) / kChunkMax;
+    if (min_chunks > kNoAllocMaxChunks)
+      return fail(ADAMW_EINVAL, "the tensor list needs more chunks than the static scratch "
+                                "holds (limit 65536 chunks, about 1.07e9 elements)");
   }
+  *total_out = total;
+  return ADAMW_OK;
+}
 
-  std::lock_guard<std::mutex> lock(g_mutex);
+// The device address of the array on the current device, looked up (and the
+// SM count read) on the first call made with that device current.
+static adamw_status device_state(DeviceState** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return fail_cuda(e, "cudaGetDevice");
   if (dev < 0 || dev >= kMaxDevices) return fail(ADAMW_EUNSUPPORTED, "device index out of range");
   DeviceState& ds = g_dev[dev];
   if (!ds.ready) {
-    // Once per device, with that device current: the device address of the
-    // static array (the host-side symbol is only a stand-in, never an address).
+    // The host-side symbol is only a stand-in, never an address.
     e = cudaGetSymbolAddress(reinterpret_cast<void**>(&ds.scratch), g_noalloc_scratch);
     if (e != cudaSuccess) return fail_cuda(e, "cudaGetSymbolAddress");
     e = cudaDeviceGetAttribute(&ds.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceGetAttribute");
     ds.ready = true;
   }
+  *out = &ds;
+  return ADAMW_OK;
+}
+
+extern "C" adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t n_tensors,
+                                           adamw_mode mode, adamw_dtype grad_dtype,
+                                           const float* lr_dev, int32_t* step_dev, float beta1,
+                                           float beta2, float eps, const float* grad_scale_dev,
+                                           const float* found_inf_dev, void* stream) {
+  int64_t total = 0;
+  adamw_status st = check_noalloc_args(tensors, n_tensors, mode, grad_dtype, lr_dev, step_dev,
+                                       beta1, beta2, eps, grad_scale_dev, found_inf_dev, &total);
+  if (st != ADAMW_OK) return st;
+
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* dsp = nullptr;
+  if ((st = device_state(&dsp)) != ADAMW_OK) return st;
+  DeviceState& ds = *dsp;
   // The plan path's bulk-staged kernel, one CTA per SM; its shared-memory
   // size is raised once per device, mode and grad dtype (no allocation).
   int& bps = ds.blocks_per_sm[mode][grad_dtype];
+  cudaError_t e;
   if (bps == 0) {
     e = prepare_step_bulk(mode, grad_dtype, kAlgoAdamW);
     if (e != cudaSuccess) return fail_cuda(e, "cudaFuncSetAttribute(bulk step)");
@@ -158,42 +190,55 @@ extern "C" adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t 
     }
   }
 
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
   TensorDesc* d_tensors = reinterpret_cast<TensorDesc*>(ds.scratch);
   Chunk* d_chunks = reinterpret_cast<Chunk*>(ds.scratch + kTensorBytes);
   StepScratch* d_step = reinterpret_cast<StepScratch*>(ds.scratch + kTicketOffset);
   // The array keeps whatever the previous call left: refresh both tables and
-  // zero the step scratch (the ticket must start at 0; a zero memo is empty).
+  // zero the step ticket, which must start at 0 (a launch that gave up may
+  // have left it raised).  The bias-correction memo is keyed by step index
+  // and betas, so a value left by another call is still right; the fault
+  // word is kept for adamw_step_noalloc_status.
   if (n_tensors > 0 &&
       (e = cudaMemcpyAsync(d_tensors, g_host_tensors, sizeof(TensorDesc) * n_tensors,
-                           cudaMemcpyHostToDevice, st)) != cudaSuccess)
+                           cudaMemcpyHostToDevice, strm)) != cudaSuccess)
     return fail_cuda(e, "upload tensor table");
   if (n_chunks > 0 &&
       (e = cudaMemcpyAsync(d_chunks, g_host_chunks, sizeof(Chunk) * n_chunks,
-                           cudaMemcpyHostToDevice, st)) != cudaSuccess)
+                           cudaMemcpyHostToDevice, strm)) != cudaSuccess)
     return fail_cuda(e, "upload chunk table");
-  if ((e = cudaMemsetAsync(d_step, 0, sizeof(StepScratch), st)) != cudaSuccess)
-    return fail_cuda(e, "clear step scratch");
+  if ((e = cudaMemsetAsync(&d_step->ticket, 0, sizeof(d_step->ticket), strm)) != cudaSuccess)
+    return fail_cuda(e, "clear step ticket");
 
-  StepArgs a;
-  a.tensors = d_tensors;
-  a.chunks = d_chunks;
-  a.n_chunks = n_chunks;
-  a.lr = lr_dev;
-  a.step = step_dev;
-  a.grad_scale = grad_scale_dev;
-  a.found_inf = found_inf_dev;
-  a.beta1 = beta1;
-  a.beta2 = beta2;
-  a.eps = eps;
-  a.beta3 = 0.0f;
-  a.alpha = 0.0f;
-  a.scratch = d_step;
-  a.qt = nullptr;
-  a.refine = 1;
+  const StepArgs a = base_step_args(d_tensors, d_chunks, n_chunks, d_step, lr_dev, step_dev,
+                                    grad_scale_dev, found_inf_dev, beta1, beta2, eps);
   const int64_t resident = static_cast<int64_t>(bps) * ds.sms;
   const int grid = static_cast<int>(n_chunks < 1 ? 1 : (n_chunks < resident ? n_chunks : resident));
-  e = launch_step_bulk(mode, grad_dtype, a, grid, st, kAlgoAdamW);
+  e = launch_step_bulk(mode, grad_dtype, a, grid, strm, kAlgoAdamW);
   if (e != cudaSuccess) return fail_cuda(e, "launch adamw step");
+  return ADAMW_OK;
+}
+
+extern "C" adamw_status adamw_step_noalloc_status(uint32_t* fault_bits) {
+  std::lock_guard<std::mutex> lock(g_mutex);
+  DeviceState* ds = nullptr;
+  adamw_status st = device_state(&ds);
+  if (st != ADAMW_OK) return st;
+  StepScratch* d_step = reinterpret_cast<StepScratch*>(ds->scratch + kTicketOffset);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail_cuda(e, "cudaDeviceSynchronize");
+  uint32_t bits = 0;
+  if ((e = cudaMemcpy(&bits, &d_step->fault, sizeof(bits), cudaMemcpyDeviceToHost)) != cudaSuccess)
+    return fail_cuda(e, "read fault word");
+  if (bits != 0 && (e = cudaMemset(&d_step->fault, 0, sizeof(bits))) != cudaSuccess)
+    return fail_cuda(e, "clear fault word");
+  if (fault_bits) *fault_bits = bits;
+  if (bits != 0) {
+    char buf[160];
+    std::snprintf(buf, sizeof buf, "adamw_step_noalloc: a bounded wait in an earlier call gave "
+                                   "up (fault bits 0x%x)", bits);
+    set_last_error(buf);
+    return ADAMW_ETIMEOUT;
+  }
   return ADAMW_OK;
 }

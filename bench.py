@@ -2,24 +2,27 @@
 """Throughput of the fused AdamW step on GB300 (params/s and achieved HBM GB/s).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload gpt2_small|single|amp|amp_fused|q8|q4|llama3_8b|bf16rem|
+                    [--workload llama3_8b|gpt2_small|single|amp|amp_fused|q8|q4|bf16rem|
                                 ademamix_gpt2|lion_gpt2|momentum_gpt2|rmsprop_gpt2|adagrad_gpt2|
                                 adam_mini_llama3]
 
 One "step" is one optimizer update of every tensor of the workload (one launch
 of the library's step kernel; plus the non-finite check in the AMP workload).
-The default is AdamW; the *_gpt2 variants step the same list with AdEMAMix,
-Lion or the coupled-L2 rules, q8 / q4 keep 8-bit / 4-bit moments.
-The default workload is the GPT-2-small fp32 parameter list (148 tensors,
-124,439,808 elements) with a device learning rate on a cosine schedule.  Its
-inputs (3.48 GB moved per step) are larger than L2, so no flush is needed
-between steps; the L2-resident single-tensor workloads flush L2 between timed
+The default workload is the largest one that fits one GPU: the Llama-3-8B
+parameter list (291 tensors, 8,030,261,248 elements) as bf16 params with int16
+remainders, bf16 grads, fp32 m and v, lr from a device tensor (209 GB moved per
+step, far larger than L2).  The GPT-2-small fp32 list, the single-tensor and
+AMP cases, the 8-bit and 4-bit states and the other update rules are the
+other workloads; the L2-resident single-tensor ones flush L2 between timed
 launches.  Inputs are synthetic and seeded (``synth``), resident in HBM before
 timing.  Under torchrun every rank runs its own copy of the workload on its own
 GPU (weak scaling; the update is element-wise and needs no exchange).
 
-``--impl reference`` times the CPU oracle (numpy, float64 definition) on a
-bounded sample of the same workload on the host cores instead.
+The end-to-end arm (``e2e``) runs the same step through the C ABI with the
+grads copied in from pinned host memory and the updated params copied back,
+every step, inside the timed region.  ``cpu_baseline`` times the CPU oracle on
+every host core (one process per core).  ``--impl reference`` times the CPU
+oracle alone on a bounded sample of the same workload, on every host core.
 One JSON line is printed by rank 0.
 """
 
@@ -50,10 +53,10 @@ L2_FLUSH_BYTES = 512 << 20
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gpt2_small",
+    ap.add_argument("--workload", default="llama3_8b",
                     choices=["gpt2_small", "single", "amp", "amp_fused", "q8", "llama3_8b", "bf16rem",
                              "ademamix_gpt2", "lion_gpt2", "momentum_gpt2", "rmsprop_gpt2",
                              "adagrad_gpt2", "q4", "adam_mini_llama3"])
@@ -375,13 +378,41 @@ def cpu_sample_coupled(n, rule):
     return run, f"{n} elements per step, float64 {rule} oracle (oracle.coupled.step_fp64)"
 
 
-# The strict-fp32 oracle, timed beside the float64 one for the fp32-state AdamW workloads.
-CPU_SAMPLES_STRICT = {
-    "gpt2_small": lambda n: cpu_sample_fp32_strict(n),
-    "single": lambda n: cpu_sample_fp32_strict(n, lr=0.1),
-    "amp": lambda n: cpu_sample_fp32_strict(n, amp=True, lr=0.1),
-    "amp_fused": lambda n: cpu_sample_fp32_strict(n, amp=True, lr=0.1),
+def cpu_sample_bf16rem_fp64(n):
+    """The float64 definition on the bf16+remainder layout: join to the float32
+    master, one float64 step, round to float32 and split again."""
+    import numpy as np
+    from oracle import adamw as OA, remainder as OR
+    rng = np.random.default_rng(0)
+    hi = (rng.normal(0, 0.02, n).astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    rem = rng.integers(0, 1 << 15, n).astype(np.int16)
+    g = rng.normal(0, 1e-4, n)
+    m, v = np.zeros(n), np.zeros(n)
+    state = {"t": 0, "hi": hi, "rem": rem}
+
+    def run():
+        state["t"] += 1
+        x = OA.Tensor(p=OR.join(state["hi"], state["rem"]).astype(np.float64), g=g, m=m, v=v, wd=0.1)
+        OA.step_fp64([x], lr=3e-4, beta1=0.9, beta2=0.999, eps=1e-8, t=state["t"])
+        state["hi"], state["rem"] = OR.split(x.p.astype(np.float32))
+    return run, (f"{n} elements per step, float64 definition (oracle.adamw.step_fp64) on the "
+                 "joined master, rounded to float32 and split")
+
+
+# A second oracle timed beside the first: strict fp32 beside the float64
+# definition (fp32-state AdamW workloads), the float64 definition beside the
+# strict-fp32 remainder oracle (bf16+remainder workloads).
+CPU_SAMPLES_SECOND = {
+    "gpt2_small": ("strict_fp32", lambda n: cpu_sample_fp32_strict(n)),
+    "single": ("strict_fp32", lambda n: cpu_sample_fp32_strict(n, lr=0.1)),
+    "amp": ("strict_fp32", lambda n: cpu_sample_fp32_strict(n, amp=True, lr=0.1)),
+    "amp_fused": ("strict_fp32", lambda n: cpu_sample_fp32_strict(n, amp=True, lr=0.1)),
+    "llama3_8b": ("fp64", cpu_sample_bf16rem_fp64),
+    "bf16rem": ("fp64", cpu_sample_bf16rem_fp64),
 }
+
+# The arithmetic type of each workload's first CPU oracle (the reference arm).
+REFERENCE_DTYPE = {"q8": "f32", "q4": "f32", "llama3_8b": "f32", "bf16rem": "f32"}
 
 CPU_SAMPLES = {
     "gpt2_small": lambda n: cpu_sample_fp32(n),
@@ -434,22 +465,44 @@ class PipelinedE2E:
     pinned host memory and its updated params go back.  The elements are cut
     into groups with one plan (and step counter) each, so that the
     host-to-device copy of one group, the step of the previous one and the
-    device-to-host copy of the one before overlap on three streams."""
+    device-to-host copy of the one before overlap on three streams.
 
-    def _pipeline(self, g_dev, p_dev, groups):
-        """groups: (lo, hi, plan) over the flat element ranges of g_dev / p_dev."""
+    Without a ring the host holds a full pinned copy of every buffer.  With
+    ``ring`` = R the host holds R group-sized slots per buffer and group k
+    goes through slot k mod R (its grads come from that slot, its results
+    land in it): a bounded host footprint for lists whose buffers do not fit
+    in pinned host memory.  Each copy of a group is one contiguous range of a
+    flat device buffer."""
+
+    def _pipeline(self, ins, outs, groups, ring=None):
+        """ins / outs: flat device buffers copied in / out every step;
+        groups: (lo, hi, plan) over their element ranges."""
         import torch
-        self._g_dev, self._p_dev = g_dev, p_dev
-        self._host_g = torch.empty_like(g_dev, device="cpu").pin_memory()
-        self._host_g.copy_(g_dev)
-        self._host_p = torch.empty_like(p_dev, device="cpu").pin_memory()
+        self._ins, self._outs = list(ins), list(outs)
         self._groups = [(lo, hi, opt, torch.zeros(1, dtype=torch.int32, device="cuda"))
                         for lo, hi, opt in groups]
+        self._ring = ring
+        if ring is None:
+            self._host_in = [torch.empty_like(b, device="cpu").pin_memory() for b in self._ins]
+            for h, b in zip(self._host_in, self._ins):
+                h.copy_(b)
+            self._host_out = [torch.empty_like(b, device="cpu").pin_memory() for b in self._outs]
+        else:
+            width = max(hi - lo for lo, hi, _ in groups)
+            self._host_in = [torch.empty((ring, width), dtype=b.dtype).pin_memory() for b in self._ins]
+            self._host_out = [torch.empty((ring, width), dtype=b.dtype).pin_memory() for b in self._outs]
+            for j, (lo, hi, _) in enumerate(groups[:ring]):      # slot j starts as group j's grads
+                for h, b in zip(self._host_in, self._ins):
+                    h[j, :hi - lo].copy_(b[lo:hi])
         self._s = [torch.cuda.Stream() for _ in range(3)]          # in, step, out
         n = len(self._groups)
         self._ev = [[torch.cuda.Event() for _ in range(n)] for _ in range(3)]
-        return (self._host_g.numel() * self._host_g.element_size(),
-                self._host_p.numel() * self._host_p.element_size())
+        span = sum(hi - lo for lo, hi, _ in groups)
+        return (sum(span * b.element_size() for b in self._ins),
+                sum(span * b.element_size() for b in self._outs))
+
+    def _host_range(self, h, k, lo, hi):
+        return h[lo:hi] if self._ring is None else h[k % self._ring, :hi - lo]
 
     def e2e_begin(self, stream):
         for s in self._s:
@@ -466,7 +519,8 @@ class PipelinedE2E:
         for k, (lo, hi, opt, step_dev) in enumerate(self._groups):
             s_in.wait_event(ev_cmp[k])            # the previous step has consumed these grads
             with torch.cuda.stream(s_in):
-                self._g_dev[lo:hi].copy_(self._host_g[lo:hi], non_blocking=True)
+                for h, b in zip(self._host_in, self._ins):
+                    b[lo:hi].copy_(self._host_range(h, k, lo, hi), non_blocking=True)
             ev_in[k].record(s_in)
             s_cmp.wait_event(ev_in[k])
             s_cmp.wait_event(ev_out[k])           # the previous copy-out has read these params
@@ -474,7 +528,8 @@ class PipelinedE2E:
             ev_cmp[k].record(s_cmp)
             s_out.wait_event(ev_cmp[k])
             with torch.cuda.stream(s_out):
-                self._host_p[lo:hi].copy_(self._p_dev[lo:hi], non_blocking=True)
+                for h, b in zip(self._host_out, self._outs):
+                    self._host_range(h, k, lo, hi).copy_(b[lo:hi], non_blocking=True)
             ev_out[k].record(s_out)
 
 
@@ -554,7 +609,7 @@ class Gpt2Small(PipelinedE2E, Workload):
                 idx = list(range(start, k + 1))
                 runs.append((offs[start], offs[k] + self.ps[k].numel(), self._group_plan(idx)))
                 start = k + 1
-        return self._pipeline(self.g_buf, self.p_buf, runs)
+        return self._pipeline([self.g_buf], [self.p_buf], runs)
 
     def _group_plan(self, idx):
         from adamw_optimizer_step_tensor_gb300 import FusedAdamW
@@ -789,7 +844,7 @@ class Q8(PipelinedE2E, Workload):
                              [0.01], mode=self.mode, absmax_m=[self.am[a0:a1]],
                              absmax_v=[self.av[a0:a1]])
             runs.append((lo, hi, opt))
-        return self._pipeline(self.g, self.p, runs)
+        return self._pipeline([self.g], [self.p], runs)
 
     def _group_step(self, opt, i, step_dev, stream):
         self.C.adamw_step(opt.plan, self.lr.data_ptr(), step_dev.data_ptr(), 0.9, 0.999, 1e-8,
@@ -833,9 +888,14 @@ class Q4(Q8):
                 "l2": "no flush: 13.0 GB moved per step"}
 
 
-class Llama3(Workload):
+class Llama3(PipelinedE2E, Workload):
     name = "llama3_8b_bf16_rem"
     bytes_per_param = 26.0
+    e2e_steps = 8
+    e2e_what = ("pinned-host bf16 grads -> device, adamw_step, updated bf16 params and int16 "
+                "remainders -> pinned host; the flat list in 2^27-element groups (one plan "
+                "each) through a 3-slot pinned host ring, so copies in, steps and copies out "
+                "overlap on 3 streams")
 
     def __init__(self, seed=5):
         import torch
@@ -845,11 +905,11 @@ class Llama3(Workload):
         self.C = _capi
         self.specs = synth.llama3_8b()
         self.n_params = synth.total_numel(self.specs)
-        _, hs = _flat_views(self.specs, torch.bfloat16, dev)
-        _, rs = _flat_views(self.specs, torch.int16, dev)
-        _, gs = _flat_views(self.specs, torch.bfloat16, dev)
-        _, ms = _flat_views(self.specs, torch.float32, dev)
-        _, vs = _flat_views(self.specs, torch.float32, dev)
+        self.h_buf, hs = _flat_views(self.specs, torch.bfloat16, dev)
+        self.r_buf, rs = _flat_views(self.specs, torch.int16, dev)
+        self.g_buf, gs = _flat_views(self.specs, torch.bfloat16, dev)
+        self.m_buf, ms = _flat_views(self.specs, torch.float32, dev)
+        self.v_buf, vs = _flat_views(self.specs, torch.float32, dev)
         for i, (h, r, g, s) in enumerate(zip(hs, rs, gs, self.specs)):
             if "norm" in s.name:
                 h.fill_(1.0)
@@ -872,17 +932,46 @@ class Llama3(Workload):
     def describe(cls, seed=5):
         import synth
         specs = synth.llama3_8b()
-        return {"workload": "Llama-3-8B param list, bf16 params + int16 remainders",
+        return {"workload": "Llama-3-8B param list, bf16 params + int16 remainders, bf16 grads, "
+                            "fp32 m and v, lr 3e-4 from a device tensor, wd 0.1",
                 "tensors": len(specs), "numel": synth.total_numel(specs),
-                "bytes_per_param": Llama3.bytes_per_param, "l2": "no flush: 209 GB moved per step"}
+                "bytes_per_param": Llama3.bytes_per_param, "grad_dtype": "bf16",
+                "state_dtype": "f32", "param_dtype": "bf16 + int16 remainder",
+                "l2": "no flush: 209 GB moved per step, larger than the 126 MB L2"}
 
     def step(self, i):
         self.C.adamw_step(self.opt.plan, self.lr.data_ptr(), self.step_dev.data_ptr(), 0.9, 0.999,
                           1e-8, None, None, self.stream)
 
-    def e2e_setup(self):
-        return None
+    def e2e_setup(self, group=1 << 27, ring=3):
+        """Groups of `group` consecutive elements of the flat buffers (the padding
+        between tensors included in the copies), each stepped by a plan over the
+        slices of the tensors it covers (PipelinedE2E with a ring)."""
+        from adamw_optimizer_step_tensor_gb300 import FusedAdamW
+        hs, rs, gs, ms, vs = self._views
+        base = self.h_buf.data_ptr()
+        spans = [((h.data_ptr() - base) // 2, h.numel()) for h in hs]
+        total = self.h_buf.numel()
+        groups = []
+        for lo in range(0, total, group):
+            hi = min(total, lo + group)
+            sel = [[], [], [], [], [], []]
+            for j, (o, n) in enumerate(spans):
+                a, b = max(lo, o), min(hi, o + n)
+                if a >= b:
+                    continue
+                for lst, t in zip(sel, (hs[j], rs[j], gs[j], ms[j], vs[j])):
+                    lst.append(t[a - o:b - o])
+                sel[5].append(self.specs[j].wd)
+            if sel[0]:
+                opt = FusedAdamW(sel[0], sel[2], sel[3], sel[4], sel[5], mode="bf16_rem",
+                                 param_rems=sel[1])
+                groups.append((lo, hi, opt))
+        return self._pipeline([self.g_buf], [self.h_buf, self.r_buf], groups, ring=ring)
 
+    def _group_step(self, opt, i, step_dev, stream):
+        self.C.adamw_step(opt.plan, self.lr.data_ptr(), step_dev.data_ptr(), 0.9, 0.999, 1e-8,
+                          None, None, stream)
 
 
 class MiniLlama3(Workload):
@@ -1049,17 +1138,6 @@ def graph_replay_us(w, flush, k=100):
 
 
 # ----------------------------------------------------------------------------- CPU timing
-def time_cpu(run, n, budget_s, min_calls=1):
-    run()  # warm the caches / allocator
-    t0 = time.perf_counter()
-    calls = 0
-    while calls < min_calls or time.perf_counter() - t0 < budget_s:
-        run()
-        calls += 1
-    dt = time.perf_counter() - t0
-    return n * calls / dt, calls, dt
-
-
 def cpu_threads():
     try:
         return len(os.sched_getaffinity(0))
@@ -1067,34 +1145,86 @@ def cpu_threads():
         return os.cpu_count() or 1
 
 
+def _sample_table(kind):
+    if kind == "second":
+        return {k: v[1] for k, v in CPU_SAMPLES_SECOND.items()}
+    return CPU_SAMPLES
+
+
+def _cpu_worker(kind, workload, n, seconds, steps, warmup, barrier, out):
+    """One host core: builds its own sample of n elements (its own seeded
+    inputs, disjoint from every other worker's), warms up, waits for every
+    worker at the barrier, then runs the oracle step either for `seconds` or
+    for `steps` calls, and reports (elements stepped, seconds, description)."""
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    try:
+        run, desc = _sample_table(kind)[workload](n)
+        for _ in range(max(1, warmup)):
+            run()
+        barrier.wait()
+        t0 = time.perf_counter()
+        calls = 0
+        while (calls < steps) if steps else (calls < 1 or time.perf_counter() - t0 < seconds):
+            run()
+            calls += 1
+        out.put((n * calls, time.perf_counter() - t0, calls, desc, None))
+    except Exception as e:  # reported to the parent, which raises
+        barrier.abort()
+        out.put((0, 0.0, 0, "", repr(e)))
+
+
+def time_cpu_all_cores(workload, n, seconds=0.0, steps=0, warmup=1, kind="first"):
+    """The oracle on every host core at once: one spawned process per core
+    (spawn, so that no CUDA state is inherited), each on its own n-element
+    sample; the workers start together after their warm-up.  Returns
+    (elements per second over the slowest worker's time, cores, calls per
+    worker, seconds, description)."""
+    import multiprocessing as mp
+    cores = cpu_threads()
+    ctx = mp.get_context("spawn")
+    barrier, out = ctx.Barrier(cores), ctx.Queue()
+    procs = [ctx.Process(target=_cpu_worker,
+                         args=(kind, workload, n, seconds, steps, warmup, barrier, out))
+             for _ in range(cores)]
+    for p in procs:
+        p.start()
+    res = [out.get() for _ in procs]
+    for p in procs:
+        p.join()
+    errs = [r[4] for r in res if r[4]]
+    if errs:
+        raise RuntimeError(f"CPU oracle worker failed: {errs[0]}")
+    elems = sum(r[0] for r in res)
+    dt = max(r[1] for r in res)
+    return elems / dt, cores, min(r[2] for r in res), dt, res[0][3]
+
+
 # ----------------------------------------------------------------------------- main
 def run_reference(args, rank, world):
-    """The oracle as it stands, on the host cores, on a bounded sample of the workload."""
+    """The oracle as it stands, on every host core, on a bounded sample of the
+    workload: each step is one oracle step per core on that core's own sample."""
     if rank != 0:
         return 0
     make = CPU_SAMPLES[args.workload]
-    run, _ = make(1 << 16)                     # calibrate: seconds per element
+    run, _ = make(1 << 16)                     # calibrate: seconds per element on one core
     t0 = time.perf_counter()
     run()
     per_elem = (time.perf_counter() - t0) / (1 << 16)
-    budget = 120.0                             # whole --steps/--warmup run within ~2 minutes
+    budget = 90.0                              # whole --steps/--warmup run within ~2 minutes
     n = int(budget / max(1, args.steps + args.warmup) / max(per_elem, 1e-12))
-    n = max(4096, min(1 << 24, n // 256 * 256))
-    run, desc = make(n)
-    for _ in range(args.warmup):
-        run()
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        run()
-    dt = time.perf_counter() - t0
-    value = n * args.steps / dt
-    sample = f"{desc}; numpy, single-threaded ({cpu_threads()} host cores present)"
+    n = max(4096, min(1 << 23, n // 256 * 256))
+    value, cores, calls, dt, desc = time_cpu_all_cores(args.workload, n, steps=max(1, args.steps),
+                                                       warmup=args.warmup)
+    steps = max(1, args.steps)
+    sample = (f"{desc}, on each of {cores} host cores (one process per core, disjoint samples: "
+              f"{n * cores} elements per step); numpy")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic",
+            "steps": steps, "warmup": args.warmup, "ms_per_step": dt / steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": REFERENCE_DTYPE.get(args.workload, "f64"), "data": "synthetic",
             "config": dict(describe_workload(args.workload, args.numel), parallelism="1 GPU"),
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -1170,14 +1300,15 @@ def main():
 
     # ---- end to end through the C ABI with pinned host buffers
     e2e = None
-    setup = w.e2e_setup() if hasattr(w, "e2e_setup") else None
-    if setup is not None and args.e2e_steps > 0:
+    n_e2e = min(args.e2e_steps, getattr(w, "e2e_steps", args.e2e_steps))
+    setup = w.e2e_setup() if hasattr(w, "e2e_setup") and n_e2e > 0 else None
+    if setup is not None:
         h2d, d2h = setup
         begin = getattr(w, "e2e_begin", None)
         end = getattr(w, "e2e_end", None)
         if begin:
             begin(stream)
-        for i in range(3):
+        for i in range(getattr(w, "e2e_warmup", 3)):
             w.e2e_step(i)
         if end:
             end(stream)
@@ -1188,36 +1319,37 @@ def main():
         e0.record(stream)
         if begin:
             begin(stream)
-        for i in range(args.e2e_steps):
+        for i in range(n_e2e):
             w.e2e_step(i)
         if end:
             end(stream)
         e1.record(stream)
         torch.cuda.synchronize()
-        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / args.e2e_steps, world)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1) / n_e2e, world)
         e2e = {"value": w.n_params * world / (e2e_ms * 1e-3), "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-               "ms_per_step": e2e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n_e2e,
+               "ms_per_step": e2e_ms, "copies_declared": True,
                "what": getattr(w, "e2e_what",
                                "pinned-host grads -> device, adamw_step, updated params -> pinned host")}
     else:
         e2e = {"value": None, "unit": UNIT, "h2d_bytes_per_step": None, "d2h_bytes_per_step": None,
-               "note": "this workload has no host-offload arm (its buffers leave no room for a "
-                       "pinned-host copy, or --e2e-steps 0)"}
+               "note": "this workload has no host-offload arm, or --e2e-steps 0"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n = 1 << 22
-        run, desc = CPU_SAMPLES[args.workload](n)
-        v, calls, dt = time_cpu(run, n, args.cpu_seconds)
-        cpu = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": f"{desc}; {calls} steps in {dt:.1f} s, numpy single-threaded "
-                         f"({cpu_threads()} host cores present)"}
-        if args.workload in CPU_SAMPLES_STRICT:
-            run, desc = CPU_SAMPLES_STRICT[args.workload](n)
-            v, calls, dt = time_cpu(run, n, args.cpu_seconds / 2)
-            cpu["strict_fp32"] = {"value": v, "unit": UNIT, "cores": 1,
-                                  "sample": f"{desc}; {calls} steps in {dt:.1f} s"}
+        n = 1 << 21
+        v, cores, calls, dt, desc = time_cpu_all_cores(args.workload, n, seconds=args.cpu_seconds)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{desc}, on each of {cores} host cores (one process per core, disjoint "
+                         f"samples); {calls}+ steps per core in {dt:.1f} s; numpy"}
+        if args.workload in CPU_SAMPLES_SECOND:
+            label = CPU_SAMPLES_SECOND[args.workload][0]
+            v, cores, calls, dt, desc = time_cpu_all_cores(args.workload, n,
+                                                           seconds=args.cpu_seconds / 2,
+                                                           kind="second")
+            cpu[label] = {"value": v, "unit": UNIT, "cores": cores,
+                          "sample": f"{desc}, on each of {cores} host cores; {calls}+ steps per "
+                                    f"core in {dt:.1f} s"}
 
     if rank == 0:
         line = {

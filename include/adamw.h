@@ -84,8 +84,11 @@ typedef enum {
    * block of each tensor (the 8-bit blockwise 2-state step named in the
    * bitsandbytes PR above).  Per block: dequantise, update with the
    * unquantised m', v', then absmax = max|m'| and code = nearest map entry
-   * to m'/absmax (exact tie -> lower code; all-zero block -> absmax 0 and
-   * the code of 0.0). */
+   * to m' * fl(1/absmax) -- one reciprocal per block, a reading taken for
+   * speed; it moves a code by one from the nearest entry to the correctly
+   * rounded fl(m'/absmax) only where that ratio lies within 2.5 ulp of the
+   * midpoint between two entries (exact tie -> lower code; all-zero block ->
+   * absmax 0 and the code of 0.0). */
   ADAMW_MODE_Q8 = 2,
   /* The Q8 step with 4-bit codes and 128-element blocks (the 4-bit AdamW of
    * torchao named in "4 bit Adam should support non constant lr"; format of
@@ -209,23 +212,26 @@ adamw_status adamw_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev
  * Arguments are those of adamw_plan_create followed by those of adamw_step,
  * with the same meaning, validation and arithmetic; the result of a call is
  * bit-identical to adamw_plan_create + adamw_step on the same inputs.  Modes
- * ADAMW_MODE_FP32 and ADAMW_MODE_BF16_REM only (EUNSUPPORTED otherwise).
+ * ADAMW_MODE_FP32 and ADAMW_MODE_BF16_REM only (EUNSUPPORTED for the 8-bit
+ * and 4-bit modes, EDTYPE for an unknown mode or grad dtype).
  *
  * Instead of plan memory the call uses one static device array built into the
  * library (about 1.1 MB on every GPU that loads it, held until the process
  * exits).  Limits: at most 1024 tensors and 65536 chunks per call (a chunk
  * holds at most 16384 elements, so about 1.07e9 elements in all); larger lists
- * are rejected
- * with ADAMW_EINVAL before anything is enqueued.  Each call copies the tensor
- * and chunk tables from a static host buffer into the array (a pageable
- * host-to-device copy, which may make the host wait for the stream) and clears
- * the array's step counter, then launches the step kernel.
+ * are rejected with ADAMW_EINVAL before anything is enqueued.  Each call
+ * copies the tensor and chunk tables from a static host buffer into the array
+ * (a pageable host-to-device copy, which may make the host wait for the
+ * stream) and clears the array's step ticket, then launches the step kernel.
  * The first call on each device looks up the array's device address with that
- * device current.  The entry point is not meant for stream capture (every call
- * uploads its tables with a pageable host-to-device copy); a captured step is
- * adamw_step on a plan.  All calls share the one array: calls whose work may
- * overlap on the GPU (different streams without ordering between them) race
- * and must not be issued.
+ * device current; make that first call before any stream capture.  All calls
+ * share the one array and it keeps what the last call left: calls whose work
+ * may overlap on the GPU (different streams without ordering between them)
+ * race and must not be issued.
+ *
+ * A bounded wait of the step kernel that gives up (2 s; a partly applied step)
+ * sets a bit in the array's fault word, which no call clears; read it with
+ * adamw_step_noalloc_status.
  */
 adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t n_tensors,
                                 adamw_mode mode, adamw_dtype grad_dtype,
@@ -233,6 +239,15 @@ adamw_status adamw_step_noalloc(const adamw_tensor* tensors, int32_t n_tensors,
                                 float beta1, float beta2, float eps,
                                 const float* grad_scale_dev, const float* found_inf_dev,
                                 void* stream);
+
+/*
+ * The fault word of adamw_step_noalloc's static array on the current device
+ * (the pages have no counterpart): synchronises the device, stores the bits
+ * in *fault_bits (if not NULL), clears them, and returns ADAMW_ETIMEOUT when
+ * any was set (a bounded wait of an earlier call gave up and that step may be
+ * partly applied), else ADAMW_OK.  Allocates nothing.
+ */
+adamw_status adamw_step_noalloc_status(uint32_t* fault_bits);
 
 /*
  * One AdEMAMix step over every tensor of the plan (plans whose tensors all

@@ -162,6 +162,7 @@ class F32Scalars:
     step_size: np.float32  # fl(lr / bc1)
     inv_sqrt_bc2: np.float32   # fl32(1 / sqrt(1 - b2**t), both in float64)
     inv_scale: np.float32 | None  # fl(1 / grad_scale), None = no unscale
+    sqrt_bc2: np.float32 = np.float32(1.0)   # fl32(sqrt(1 - b2**t)), for the division form
 
 
 def f32_scalars(*, lr, beta1, beta2, eps, t, grad_scale=None) -> F32Scalars:
@@ -174,6 +175,7 @@ def f32_scalars(*, lr, beta1, beta2, eps, t, grad_scale=None) -> F32Scalars:
         eps=F32(eps), lr=lr32, step_size=F32(lr32 / bc1_32),
         inv_sqrt_bc2=F32(1.0 / sqrt_bc2),
         inv_scale=None if grad_scale is None else F32(F32(1.0) / F32(grad_scale)),
+        sqrt_bc2=F32(sqrt_bc2),
     )
 
 
@@ -182,7 +184,8 @@ def decay_f32(lr: np.float32, wd: float) -> np.float32:
     return F32(F32(1.0) - F32(F32(lr) * F32(wd)))
 
 
-def elementwise_f32(p, g_raw, m, v, s: F32Scalars, decay: np.float32):
+def elementwise_f32(p, g_raw, m, v, s: F32Scalars, decay: np.float32, bias_rule="reciprocal",
+                    decay_after=False):
     """The strict-fp32 element update; returns ``(p', m', v')`` as float32.
 
     Operation order (each line one rounding per operator, left to right):
@@ -193,15 +196,32 @@ def elementwise_f32(p, g_raw, m, v, s: F32Scalars, decay: np.float32):
         h   = sqrt(v') * inv_sqrt_bc2 + eps
         u   = m' / h
         p'  = p*decay - step_size*u
+
+    ``bias_rule="division"`` forms h as the AdamWMini listing of "Adam-mini <>
+    DTensor" writes it, ``sqrt(v') / sqrt_bc2 + eps`` (one division per
+    element); the library multiplies by the launch's ``inv_sqrt_bc2`` instead
+    (the default here), a reading taken for speed.  The tests measure the
+    distance between the two forms; nothing else uses the division form.
+
+    ``decay_after`` is the *wrong* ordering the bitsandbytes PR removes,
+    ``p' = (p - step_size*u) * decay``, in float32; it exists only so that the
+    tests can show their GPU parity checks reject it (the PR's own mutation
+    check).  The library has no such mode.
     """
     g = np.asarray(g_raw).astype(F32)
     if s.inv_scale is not None:
         g = g * s.inv_scale
     m1 = s.b1 * m + s.omb1 * g
     v1 = s.b2 * v + s.omb2 * (g * g)
-    h = np.sqrt(v1) * s.inv_sqrt_bc2 + s.eps
+    if bias_rule == "division":
+        h = np.sqrt(v1) / s.sqrt_bc2 + s.eps
+    else:
+        h = np.sqrt(v1) * s.inv_sqrt_bc2 + s.eps
     u = m1 / h
-    p1 = p * decay - s.step_size * u
+    if decay_after:
+        p1 = (p - s.step_size * u) * decay
+    else:
+        p1 = p * decay - s.step_size * u
     return p1.astype(F32), m1.astype(F32), v1.astype(F32)
 
 

@@ -61,7 +61,7 @@ class Maps4:
 
 
 def quantize_blockwise(x: np.ndarray, table: np.ndarray, thr: np.ndarray,
-                       block: int = BLOCK) -> tuple[np.ndarray, np.ndarray]:
+                       block: int = BLOCK, rule: str = "reciprocal") -> tuple[np.ndarray, np.ndarray]:
     """float32 state -> (codes, one per element, < 16; float32 absmax per block)."""
     x = np.asarray(x, dtype=F32)
     nb = q8.n_blocks(x.size, block)
@@ -75,7 +75,7 @@ def quantize_blockwise(x: np.ndarray, table: np.ndarray, thr: np.ndarray,
         if a == 0:
             codes[b * block:(b + 1) * block] = z
         else:
-            codes[b * block:(b + 1) * block] = qm.quantize(q8.normalise(xb, a), table, thr)
+            codes[b * block:(b + 1) * block] = qm.quantize(q8.normalise(xb, a, rule), table, thr)
     return codes, amax
 
 
@@ -85,7 +85,7 @@ def dequantize(packed: np.ndarray, absmax: np.ndarray, table: np.ndarray, n: int
 
 
 def step_f32(p, g, pm, pv, am, av, *, lr, beta1, beta2, eps, wd, t, grad_scale=None,
-             maps: Maps4 | None = None) -> bool:
+             maps: Maps4 | None = None, rule: str = "reciprocal") -> bool:
     """One strict-fp32 4-bit-state AdamW step on one flat tensor, in place.
 
     ``pm``, ``pv`` packed uint8 [ceil(n/2)]; ``am``, ``av`` float32 [ceil(n/128)].
@@ -98,8 +98,8 @@ def step_f32(p, g, pm, pv, am, av, *, lr, beta1, beta2, eps, wd, t, grad_scale=N
     m = dequantize(pm, am, maps.smap, n)
     v = dequantize(pv, av, maps.umap, n)
     p1, m1, v1 = adamw.elementwise_f32(p, g, m, v, s, adamw.decay_f32(s.lr, wd))
-    cm1, am1 = quantize_blockwise(m1, maps.smap, maps.sthr)
-    cv1, av1 = quantize_blockwise(v1, maps.umap, maps.uthr)
+    cm1, am1 = quantize_blockwise(m1, maps.smap, maps.sthr, rule=rule)
+    cv1, av1 = quantize_blockwise(v1, maps.umap, maps.uthr, rule=rule)
     p[...] = p1
     pm[...] = pack(cm1)
     pv[...] = pack(cv1)

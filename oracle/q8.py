@@ -63,15 +63,23 @@ SMALL = F32(2.0 ** -64)
 SCALE = F32(2.0 ** 64)
 
 
-def normalise(xb: np.ndarray, a: np.float32) -> np.ndarray:
-    """x * fl(1/a), with x and a first scaled by 2**64 when a < 2**-64 (exact scalings)."""
+def normalise(xb: np.ndarray, a: np.float32, rule: str = "reciprocal") -> np.ndarray:
+    """x * fl(1/a), with x and a first scaled by 2**64 when a < 2**-64 (exact scalings).
+
+    ``rule="division"`` is the plain ratio fl(x / a), one correctly rounded
+    division per element (never out of range: |x| <= a).  The library uses
+    the reciprocal form, a reading taken for speed; the tests bound how far it
+    can move a code from the division form.
+    """
+    if rule == "division":
+        return (np.asarray(xb, dtype=F32) / F32(a)).astype(F32)
     s = SCALE if a < SMALL else F32(1.0)
     y = F32(1.0) / F32(a * s)
     return (np.asarray(xb, dtype=F32) * s) * y
 
 
 def quantize_blockwise(x: np.ndarray, table: np.ndarray, thr: np.ndarray,
-                       block: int = BLOCK) -> tuple[np.ndarray, np.ndarray]:
+                       block: int = BLOCK, rule: str = "reciprocal") -> tuple[np.ndarray, np.ndarray]:
     """float32 state -> (uint8 codes, float32 absmax per block)."""
     x = np.asarray(x, dtype=F32)
     nb = n_blocks(x.size, block)
@@ -85,7 +93,7 @@ def quantize_blockwise(x: np.ndarray, table: np.ndarray, thr: np.ndarray,
         if a == 0:
             codes[b * block:(b + 1) * block] = z
         else:
-            codes[b * block:(b + 1) * block] = qm.quantize(normalise(xb, a), table, thr)
+            codes[b * block:(b + 1) * block] = qm.quantize(normalise(xb, a, rule), table, thr)
     return codes, amax
 
 
@@ -100,12 +108,14 @@ class Maps:
 
 
 def step_f32(p, g, cm, cv, am, av, *, lr, beta1, beta2, eps, wd, t,
-             grad_scale=None, maps: Maps | None = None, block: int = BLOCK) -> bool:
+             grad_scale=None, maps: Maps | None = None, block: int = BLOCK,
+             rule: str = "reciprocal") -> bool:
     """One strict-fp32 8-bit-state AdamW step on one flat tensor, in place.
 
     ``p`` float32 [n]; ``g`` raw grads [n]; ``cm``, ``cv`` uint8 codes [n];
     ``am``, ``av`` float32 absmax [ceil(n/block)].  Returns False (nothing
     changed) when a grad scale is given and a raw grad is non-finite.
+    ``rule`` selects the normalisation (``normalise``).
     """
     if grad_scale is not None and adamw.any_nonfinite([g]):
         return False
@@ -115,8 +125,8 @@ def step_f32(p, g, cm, cv, am, av, *, lr, beta1, beta2, eps, wd, t,
     m = dequantize(cm, am, maps.smap, block)
     v = dequantize(cv, av, maps.umap, block)
     p1, m1, v1 = adamw.elementwise_f32(p, g, m, v, s, adamw.decay_f32(s.lr, wd))
-    cm1, am1 = quantize_blockwise(m1, maps.smap, maps.sthr, block)
-    cv1, av1 = quantize_blockwise(v1, maps.umap, maps.uthr, block)
+    cm1, am1 = quantize_blockwise(m1, maps.smap, maps.sthr, block, rule)
+    cv1, av1 = quantize_blockwise(v1, maps.umap, maps.uthr, block, rule)
     p[...] = p1
     cm[...] = cm1
     cv[...] = cv1

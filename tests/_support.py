@@ -71,3 +71,28 @@ def first_mismatch(a, b) -> str:
         return "identical"
     i = bad[0]
     return f"{bad.size} mismatches; first at {i}: gpu={a[i]!r} oracle={b[i]!r}"
+
+
+# ---------------------------------------------------------------- acceptance checks
+# The checks the GPU parity tests apply to the library's output.  They take
+# numpy arrays, so that a CPU test can feed them a planted mistake (computed by
+# the oracle) and show that they reject it.
+
+def assert_state_bitexact(got: dict, want: dict, where: str = "") -> None:
+    """Every named array of `got` bit-identical to the same name in `want`."""
+    for k in want:
+        assert bits_equal(got[k], want[k]), f"{where}{k}: {first_mismatch(got[k], want[k])}"
+
+
+def assert_single_step_rel(p_got, p_fp64, tol: float = 1e-6) -> None:
+    """One step against the float64 definition: |dp| within tol relative to the
+    size of the terms (|p| plus the step of about lr = 0.1 at the workload)."""
+    d = np.abs(np.asarray(p_got).astype(np.float64) - p_fp64)
+    worst = float(np.max(d / (np.abs(p_fp64) + 0.1)))
+    assert worst < tol, f"single step: {worst:.3e} relative to the float64 definition"
+
+
+def assert_max_abs(p_got, p_fp64, tol: float = 5e-5) -> None:
+    """Many steps against the float64 definition: max |dp| <= tol."""
+    worst = float(np.max(np.abs(np.asarray(p_got).astype(np.float64) - p_fp64)))
+    assert worst <= tol, f"max |dp| {worst:.3e} against the float64 definition"

@@ -15,7 +15,8 @@ import torch
 from adamw_optimizer_step_tensor_gb300 import FusedAdamW
 from oracle import adamw as OA
 
-from _support import bits_equal, dev, first_mismatch, grads_of, host, scalar_f32, scalar_i32
+from _support import (assert_max_abs, assert_single_step_rel, assert_state_bitexact, bits_equal,
+                      dev, first_mismatch, grads_of, host, scalar_f32, scalar_i32)
 
 pytestmark = pytest.mark.gpu
 
@@ -76,13 +77,12 @@ def test_single_tensor_ten_steps_bitexact_and_within_fp64_tolerance():
         OA.step_f32(oracle, lr=f32(0.1), beta1=B1, beta2=B2, eps=EPS, t=t)
         OA.step_fp64(ref64, lr=f32(0.1), beta1=B1, beta2=B2, eps=EPS, t=t)
         torch.cuda.synchronize()
-        _check(ps, ms, vs, oracle)
+        assert_state_bitexact({"p": host(ps[0]), "m": host(ms[0]), "v": host(vs[0])},
+                              {"p": oracle[0].p, "m": oracle[0].m, "v": oracle[0].v}, f"step {t} ")
         if t == 1:
-            # single step: 1e-6 relative to the size of the terms
-            d = np.abs(host(ps[0]).astype(np.float64) - ref64[0].p)
-            assert np.max(d / (np.abs(ref64[0].p) + 0.1)) < 1e-6
+            assert_single_step_rel(host(ps[0]), ref64[0].p)
     assert int(step.item()) == 10
-    assert np.max(np.abs(host(ps[0]).astype(np.float64) - ref64[0].p)) <= 5e-5
+    assert_max_abs(host(ps[0]), ref64[0].p)
 
 
 SIZES = [1, 3, 8, 9, 255, 256, 257, 2047, 2048, 2049, 8191, 8192, 8193, 50001, 0, 7]

@@ -88,6 +88,29 @@ def test_gpt2_small_full_size_cosine_lr_sampled():
         _cleanup()
 
 
+def _division_rule_gap(kernel_codes, x, absmax, block, table, thr):
+    """The kernel's codes (normalised as x * fl(1/A)) against the plain division
+    rule, the nearest code of fl(x / A), on the same pre-quantisation state x of
+    the sampled blocks: every code that differs is off by one and the exact
+    ratio x / A lies within 2.5 ulp of the threshold between the two codes.
+    Returns the number of differing codes."""
+    from oracle import qmap as QM
+    x = np.asarray(x, np.float32)
+    a = np.repeat(np.asarray(absmax, np.float32), block)[: x.size]
+    nz = a > 0
+    div = np.asarray(kernel_codes).astype(np.int64).copy()
+    div[nz] = QM.quantize((x[nz] / a[nz]).astype(np.float32), table, thr)
+    k = np.asarray(kernel_codes).astype(np.int64)
+    bad = np.nonzero(k != div)[0]
+    if bad.size:
+        assert np.all(np.abs(k[bad] - div[bad]) == 1)
+        t = thr[np.minimum(k[bad], div[bad])].astype(np.float64)
+        ulp = np.nextafter(np.abs(t).astype(np.float32), np.float32(np.inf)).astype(np.float64) - np.abs(t)
+        exact = x[bad].astype(np.float64) / a[bad].astype(np.float64)
+        assert np.all(np.abs(exact - t) <= 2.5 * ulp)
+    return int(bad.size)
+
+
 def test_q8_full_size_2e30_sampled_blocks():
     """One 2^30 fp32 tensor, 8-bit m and v, bf16 grads, lr 1e-3, wd 0.01, 20 steps."""
     if _free_gib() < 12:
@@ -106,13 +129,23 @@ def test_q8_full_size_2e30_sampled_blocks():
         am = w.am[bidx].cpu().numpy()
         av = w.av[bidx].cpu().numpy()
         maps = OQ.Maps()
+        gap = 0
         for s in range(20):
             w.g.copy_(synth.normal(n, 1e-3, synth.grad_seed(8, s), "cuda", torch.bfloat16))
             g = _take(w.g, idx).float().cpu().numpy()
             w.step(s)
+            sc = OA.f32_scalars(lr=OA.f32(1e-3), beta1=OA.f32(0.9), beta2=OA.f32(0.999),
+                                eps=OA.f32(1e-8), t=s + 1)
+            _, m1, v1 = OA.elementwise_f32(p, g, OQ.dequantize(cm, am, maps.smap),
+                                           OQ.dequantize(cv, av, maps.umap), sc,
+                                           OA.decay_f32(sc.lr, OA.f32(0.01)))
             OQ.step_f32(p, g, cm, cv, am, av, lr=OA.f32(1e-3), beta1=OA.f32(0.9), beta2=OA.f32(0.999),
                         eps=OA.f32(1e-8), wd=OA.f32(0.01), t=s + 1, maps=maps)
-        torch.cuda.synchronize()
+            torch.cuda.synchronize()
+            gap += _division_rule_gap(_take(w.cm, idx).cpu().numpy(), m1, am, 256, maps.smap, maps.sthr)
+            gap += _division_rule_gap(_take(w.cv, idx).cpu().numpy(), v1, av, 256, maps.umap, maps.uthr)
+        print(f"8-bit codes that differ from the division rule: {gap} of {2 * 20 * idx.size}")
+        assert gap <= 1e-4 * 2 * 20 * idx.size
         assert np.array_equal(_take(w.p, idx).cpu().numpy().view(np.uint32), p.view(np.uint32))
         assert np.array_equal(_take(w.cm, idx).cpu().numpy(), cm)
         assert np.array_equal(_take(w.cv, idx).cpu().numpy(), cv)
@@ -277,13 +310,25 @@ def test_q4_full_size_2e30_sampled_blocks():
         am = w.am[bidx].cpu().numpy()
         av = w.av[bidx].cpu().numpy()
         maps = O4.Maps4()
+        gap = 0
         for s in range(10):
             w.g.copy_(synth.normal(n, 1e-3, synth.grad_seed(10, s), "cuda", torch.bfloat16))
             g = _take(w.g, idx).float().cpu().numpy()
             w.step(s)
+            sc = OA.f32_scalars(lr=OA.f32(1e-3), beta1=OA.f32(0.9), beta2=OA.f32(0.999),
+                                eps=OA.f32(1e-8), t=s + 1)
+            _, m1, v1 = OA.elementwise_f32(p, g, O4.dequantize(pm, am, maps.smap, idx.size),
+                                           O4.dequantize(pv, av, maps.umap, idx.size), sc,
+                                           OA.decay_f32(sc.lr, OA.f32(0.01)))
             O4.step_f32(p, g, pm, pv, am, av, lr=OA.f32(1e-3), beta1=OA.f32(0.9), beta2=OA.f32(0.999),
                         eps=OA.f32(1e-8), wd=OA.f32(0.01), t=s + 1, maps=maps)
-        torch.cuda.synchronize()
+            torch.cuda.synchronize()
+            kcm = O4.unpack(_take(w.cm, byte_idx).cpu().numpy(), idx.size)
+            kcv = O4.unpack(_take(w.cv, byte_idx).cpu().numpy(), idx.size)
+            gap += _division_rule_gap(kcm, m1, am, 128, maps.smap, maps.sthr)
+            gap += _division_rule_gap(kcv, v1, av, 128, maps.umap, maps.uthr)
+        print(f"4-bit codes that differ from the division rule: {gap} of {2 * 10 * idx.size}")
+        assert gap <= 1e-3 * 2 * 10 * idx.size
         assert np.array_equal(_take(w.p, idx).cpu().numpy().view(np.uint32), p.view(np.uint32))
         assert np.array_equal(_take(w.cm, byte_idx).cpu().numpy(), pm)
         assert np.array_equal(_take(w.cv, byte_idx).cpu().numpy(), pv)
