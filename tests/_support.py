@@ -14,8 +14,79 @@ import torch
 F32 = np.float32
 
 
-def dev(a: np.ndarray) -> torch.Tensor:
-    return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+# ---------------------------------------------------------------- guard bands
+# Every device array a GPU parity test hands to the library sits inside a
+# buffer with GUARD bytes of a fixed pseudo-random pattern before and after
+# it (the payload itself starts as that pattern too, until the test fills
+# it).  A store outside an array's bounds -- past a ragged tail, a lone 4-bit
+# nibble, a partial 8-bit block, a misaligned view's first element -- lands in
+# a band; ``assert_guards_intact`` reads every band back after a step, and a
+# fixture in conftest.py checks them again at the end of every GPU test.
+GUARD = 256
+_PATTERN = np.random.default_rng(0x5EED_BA5D).integers(0, 256, 1 << 16, dtype=np.uint8)
+_GUARDED: list = []      # (buffer, payload start byte, payload end byte)
+DEVICE = "cuda"          # where guarded arrays live (the CPU test of the bands uses "cpu")
+
+
+def _pattern(nbytes: int) -> np.ndarray:
+    return np.resize(_PATTERN, nbytes)
+
+
+def guarded_empty(n: int, dtype, shift: int = 0) -> torch.Tensor:
+    """n elements of dtype on the device, between two guard bands; the array
+    starts `shift` elements past a 256-byte boundary (shift > 0: a view off the
+    16-byte grid)."""
+    el = torch.empty(0, dtype=dtype).element_size()
+    start = GUARD + shift * el
+    end = start + n * el
+    total = end + GUARD
+    buf = torch.from_numpy(_pattern(total)).to(DEVICE)
+    _GUARDED.append((buf, start, end))
+    return buf[start:end].view(dtype)
+
+
+def guards_reset() -> None:
+    _GUARDED.clear()
+
+
+def assert_guards_intact() -> None:
+    """Every guard band of every array made since the last reset still holds its pattern."""
+    if not _GUARDED:
+        return
+    bands = torch.cat([torch.cat([b[:s], b[e:]]) for b, s, e in _GUARDED]).cpu().numpy()
+    want = np.concatenate([np.concatenate([_pattern(b.numel())[:s], _pattern(b.numel())[e:]])
+                           for b, s, e in _GUARDED])
+    if not np.array_equal(bands, want):
+        off = 0
+        for k, (b, s, e) in enumerate(_GUARDED):
+            n = s + b.numel() - e
+            if not np.array_equal(bands[off:off + n], want[off:off + n]):
+                bad = np.nonzero(bands[off:off + n] != want[off:off + n])[0]
+                where = [f"{int(i) - s} before the start" if i < s else f"{int(i) - s} past the end"
+                         for i in bad[:4]]
+                raise AssertionError(f"guard band of array {k} ({e - s} bytes) overwritten: "
+                                     f"bytes {where}")
+            off += n
+
+
+def dev(a: np.ndarray, shift: int = 0) -> torch.Tensor:
+    """A guarded device copy of a host array (see guarded_empty)."""
+    a = np.ascontiguousarray(a)
+    t = guarded_empty(a.size, torch.from_numpy(a[:0].copy()).dtype, shift)
+    if a.size:
+        t.copy_(torch.from_numpy(a.reshape(-1)))
+    return t.view(a.shape) if a.ndim > 1 else t
+
+
+def empty(n: int, dtype=torch.float32, shift: int = 0) -> torch.Tensor:
+    """A guarded device array whose contents are the pattern until written."""
+    return guarded_empty(n, dtype, shift)
+
+
+def zeros(n: int, dtype=torch.float32, shift: int = 0) -> torch.Tensor:
+    t = guarded_empty(n, dtype, shift)
+    t.zero_()
+    return t
 
 
 def host(t: torch.Tensor) -> np.ndarray:
@@ -45,12 +116,24 @@ def grads_of(x32: np.ndarray, dtype) -> tuple[torch.Tensor, np.ndarray]:
     return t.cuda(), widen_bf16(bits)
 
 
+def to_dev(t: torch.Tensor) -> torch.Tensor:
+    """A guarded device copy of a host torch tensor."""
+    out = guarded_empty(t.numel(), t.dtype)
+    if t.numel():
+        out.copy_(t.reshape(-1))
+    return out
+
+
 def scalar_f32(x: float) -> torch.Tensor:
-    return torch.tensor([x], dtype=torch.float32, device="cuda")
+    t = guarded_empty(1, torch.float32)
+    t.fill_(x)
+    return t
 
 
 def scalar_i32(x: int) -> torch.Tensor:
-    return torch.tensor([x], dtype=torch.int32, device="cuda")
+    t = guarded_empty(1, torch.int32)
+    t.fill_(x)
+    return t
 
 
 def bits_equal(a, b) -> bool:

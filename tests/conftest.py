@@ -19,3 +19,17 @@ def cuda_dev():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     return torch.device("cuda:0")
+
+
+@pytest.fixture(autouse=True)
+def _guard_bands(request):
+    """GPU tests: the guard bands around every array made through tests/_support
+    must be intact when the test ends."""
+    if request.node.get_closest_marker("gpu") is None:
+        yield
+        return
+    import _support
+    _support.guards_reset()
+    yield
+    _support.assert_guards_intact()
+    _support.guards_reset()

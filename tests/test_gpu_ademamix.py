@@ -16,7 +16,9 @@ from oracle import ademamix as X
 from oracle import adamw as A
 from oracle import remainder as R
 
-from _support import dev, grads_of, host
+from _support import (assert_guards_intact, assert_max_abs, assert_single_step_rel,
+                      assert_state_bitexact, bits_equal, dev, empty, first_mismatch, grads_of, host,
+                      scalar_f32, scalar_i32, to_dev, zeros)
 
 pytestmark = pytest.mark.gpu
 f32 = A.f32
@@ -27,8 +29,7 @@ SIZES = [1, 9, 2047, 2048, 2049, 8193, 30001, 0, 777]
 def _view(a, misalign):
     if not misalign:
         return dev(a)
-    buf = dev(np.concatenate([np.zeros(1, a.dtype), a]))
-    return buf[1:]
+    return dev(a, shift=1)   # one element off the 16-byte grid, guard bands on both sides
 
 
 def _make(mode, gdtype, seed, misalign=False):
@@ -49,7 +50,7 @@ def _make(mode, gdtype, seed, misalign=False):
             d = dict(p=_view(hi.view(np.int16), misalign).view(torch.bfloat16), r=_view(rem, misalign))
             master = R.join(hi, rem)
         d.update(m=_view(m1, misalign), m2=_view(m2, misalign), v=_view(v, misalign),
-                 g=torch.empty(n, dtype=gdtype, device="cuda"))
+                 g=empty(n, gdtype))
         dev_t.append(d)
         orc.append(X.Tensor(p=master, g=None, m1=m1.copy(), m2=m2.copy(), v=v.copy(), wd=wd))
     opt = FusedAdamW([d["p"] for d in dev_t], [d["g"] for d in dev_t], [d["m"] for d in dev_t],
@@ -60,6 +61,7 @@ def _make(mode, gdtype, seed, misalign=False):
 
 
 def _check(mode, dev_t, orc, tag):
+    assert_guards_intact()
     for i, (d, o) in enumerate(zip(dev_t, orc)):
         if mode == "fp32":
             assert np.array_equal(host(d["p"]).view(np.uint32), o.p.view(np.uint32)), (tag, i, "p")
@@ -75,7 +77,7 @@ def _check(mode, dev_t, orc, tag):
 @pytest.mark.parametrize("gdtype", [torch.float32, torch.float16, torch.bfloat16])
 def test_ademamix_bitexact(mode, gdtype):
     opt, dev_t, orc, rng = _make(mode, gdtype, seed=41)
-    lr, step = torch.tensor([f32(3e-3)], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+    lr, step = torch.tensor([f32(3e-3)], device="cuda"), zeros(1, torch.int32)
     for t in range(1, 5):
         for d, o in zip(dev_t, orc):
             x, wide = grads_of(rng.normal(0, 1e-3, d["g"].numel()).astype(np.float32), gdtype)
@@ -91,7 +93,7 @@ def test_ademamix_bitexact(mode, gdtype):
 
 def test_ademamix_scalar_path_on_misaligned_tensors():
     opt, dev_t, orc, rng = _make("fp32", torch.float32, seed=42, misalign=True)
-    lr, step = torch.tensor([f32(1e-3)], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+    lr, step = torch.tensor([f32(1e-3)], device="cuda"), zeros(1, torch.int32)
     for t in (1, 2):
         for d, o in zip(dev_t, orc):
             x = rng.normal(0, 1e-3, d["g"].numel()).astype(np.float32)
@@ -111,10 +113,10 @@ def test_ademamix_first_step_closed_form_and_skip():
     g0 = rng.normal(0, 1e-3, n).astype(np.float32)
     p = dev(p0)
     g = dev(g0 * 64)
-    z = [torch.zeros(n, device="cuda") for _ in range(3)]
+    z = [zeros(n) for _ in range(3)]
     opt = FusedAdamW([p], [g], [z[0]], [z[1]], [f32(0.1)], exp_avg_slows=[z[2]])
-    lr, step = torch.tensor([f32(0.1)], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
-    scale, found = torch.tensor([64.0], device="cuda"), torch.zeros(1, device="cuda")
+    lr, step = torch.tensor([f32(0.1)], device="cuda"), zeros(1, torch.int32)
+    scale, found = torch.tensor([64.0], device="cuda"), zeros(1)
     # a skipped step first: nothing moves
     g[11] = float("inf")
     opt.check_nonfinite(found)

@@ -14,7 +14,9 @@ from adamw_optimizer_step_tensor_gb300 import FusedAdamW, adamw_bf16rem_join, ad
 from oracle import adamw as OA
 from oracle import remainder as OR
 
-from _support import bits_equal, dev, first_mismatch, grads_of, host, scalar_f32, scalar_i32
+from _support import (assert_guards_intact, assert_max_abs, assert_single_step_rel,
+                      assert_state_bitexact, bits_equal, dev, empty, first_mismatch, grads_of, host,
+                      scalar_f32, scalar_i32, to_dev, zeros)
 
 pytestmark = pytest.mark.gpu
 f32 = OA.f32
@@ -34,11 +36,11 @@ def test_split_join_bitexact(n):
     sp = _special_bits()
     bits[: min(n, sp.size)] = sp[: min(n, sp.size)]
     master = dev(bits.view(np.float32))
-    hi = torch.empty(n, dtype=torch.int16, device="cuda")
-    rem = torch.empty(n, dtype=torch.int16, device="cuda")
+    hi = empty(n, torch.int16)
+    rem = empty(n, torch.int16)
     s = torch.cuda.current_stream().cuda_stream
     adamw_bf16rem_split(master.data_ptr(), hi.data_ptr(), rem.data_ptr(), n, s)
-    back = torch.empty(n, dtype=torch.float32, device="cuda")
+    back = empty(n, torch.float32)
     adamw_bf16rem_join(hi.data_ptr(), rem.data_ptr(), back.data_ptr(), n, s)
     torch.cuda.synchronize()
     ohi, orem = OR.split(bits)
@@ -60,13 +62,13 @@ def test_bf16rem_step_bitexact(gdtype):
                                                         n_zeros=min(n, 64) if i == len(SIZES) - 1 else 0)
         hi_bits = hi_t.view(torch.int16).numpy().view(np.uint16).copy()
         rem_np = rem_t.numpy().copy()
-        his.append(hi_t.cuda())
-        rems.append(rem_t.cuda())
+        his.append(to_dev(hi_t))
+        rems.append(to_dev(rem_t))
         m = rng.normal(0, 1e-4, n).astype(np.float32)
         v = (rng.normal(0, 1e-4, n) ** 2).astype(np.float32)
         ms.append(dev(m))
         vs.append(dev(v))
-        gs.append(torch.empty(n, dtype=gdtype, device="cuda"))
+        gs.append(empty(n, gdtype))
         oracle.append(OA.Tensor(p=OR.join(hi_bits, rem_np), g=None, m=m.copy(), v=v.copy(),
                                 wd=f32(0.1)))
     opt = FusedAdamW(his, gs, ms, vs, [f32(0.1)] * len(SIZES), mode="bf16_rem", param_rems=rems)

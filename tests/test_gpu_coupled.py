@@ -17,7 +17,9 @@ from oracle import adamw as A
 from oracle import coupled as C
 from oracle import remainder as R
 
-from _support import dev, grads_of, host
+from _support import (assert_guards_intact, assert_max_abs, assert_single_step_rel,
+                      assert_state_bitexact, bits_equal, dev, empty, first_mismatch, grads_of, host,
+                      scalar_f32, scalar_i32, to_dev, zeros)
 
 pytestmark = pytest.mark.gpu
 f32 = A.f32
@@ -31,8 +33,7 @@ HP = {"momentum": dict(beta=f32(0.9), eps=0.0),
 def _view(a, misalign):
     if not misalign:
         return dev(a)
-    buf = dev(np.concatenate([np.zeros(1, a.dtype), a]))
-    return buf[1:]
+    return dev(a, shift=1)   # one element off the 16-byte grid, guard bands on both sides
 
 
 def _make(rule, mode, gdtype, seed, misalign=False):
@@ -52,7 +53,7 @@ def _make(rule, mode, gdtype, seed, misalign=False):
             rem = rng.integers(0, 1 << 15, n).astype(np.int16)
             d = dict(p=_view(hi.view(np.int16), misalign).view(torch.bfloat16), r=_view(rem, misalign))
             master = R.join(hi, rem)
-        d.update(s=_view(s, misalign), g=torch.empty(n, dtype=gdtype, device="cuda"))
+        d.update(s=_view(s, misalign), g=empty(n, gdtype))
         dev_t.append(d)
         orc.append(C.Tensor(p=master, g=None, s=s.copy(), wd=wd))
     opt = FusedAdamW([d["p"] for d in dev_t], [d["g"] for d in dev_t], [d["s"] for d in dev_t],
@@ -62,6 +63,7 @@ def _make(rule, mode, gdtype, seed, misalign=False):
 
 
 def _check(mode, dev_t, orc, tag):
+    assert_guards_intact()
     for i, (d, o) in enumerate(zip(dev_t, orc)):
         if mode == "fp32":
             assert np.array_equal(host(d["p"]).view(np.uint32), o.p.view(np.uint32)), (tag, i, "p")
@@ -77,7 +79,7 @@ def _check(mode, dev_t, orc, tag):
 @pytest.mark.parametrize("gdtype", [torch.float32, torch.float16, torch.bfloat16])
 def test_coupled_bitexact(rule, mode, gdtype):
     opt, dev_t, orc, rng = _make(rule, mode, gdtype, seed=61)
-    lr, step = torch.tensor([f32(1e-2)], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+    lr, step = torch.tensor([f32(1e-2)], device="cuda"), zeros(1, torch.int32)
     for _ in range(4):
         for d, o in zip(dev_t, orc):
             x, wide = grads_of(rng.normal(0, 1e-3, d["g"].numel()).astype(np.float32), gdtype)
@@ -93,7 +95,7 @@ def test_coupled_bitexact(rule, mode, gdtype):
 @pytest.mark.parametrize("rule", C.RULES)
 def test_coupled_scalar_path_on_misaligned_tensors(rule):
     opt, dev_t, orc, rng = _make(rule, "fp32", torch.float32, seed=62, misalign=True)
-    lr, step = torch.tensor([f32(1e-2)], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+    lr, step = torch.tensor([f32(1e-2)], device="cuda"), zeros(1, torch.int32)
     for _ in range(2):
         for d, o in zip(dev_t, orc):
             x = rng.normal(0, 1e-3, d["g"].numel()).astype(np.float32)
@@ -114,8 +116,8 @@ def test_coupled_skip_and_unscale(rule):
     g0 = rng.normal(0, 1e-3, n).astype(np.float32)
     p, s, g = dev(p0), dev(s0), dev(g0 * 1000)
     opt = FusedAdamW([p], [g], [s], None, [f32(0.1)])
-    lr, step = torch.tensor([f32(1e-2)], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
-    scale, found = torch.tensor([1000.0], device="cuda"), torch.zeros(1, device="cuda")
+    lr, step = torch.tensor([f32(1e-2)], device="cuda"), zeros(1, torch.int32)
+    scale, found = torch.tensor([1000.0], device="cuda"), zeros(1)
     g[3] = float("-inf")
     opt.check_nonfinite(found)
     opt.step_coupled(rule, lr, step, grad_scale=scale, found_inf=found, **HP[rule])
@@ -138,7 +140,7 @@ def test_coupled_on_a_two_state_plan_leaves_v_alone_and_rejects_bad_rules():
     p0, s0, v0, g0 = (np.abs(rng.normal(0, 1e-2, n)).astype(np.float32) for _ in range(4))
     p, s, v, g = dev(p0), dev(s0), dev(v0), dev(g0)
     opt = FusedAdamW([p], [g], [s], [v], [f32(0.1)])
-    lr, step = torch.tensor([f32(1e-2)], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+    lr, step = torch.tensor([f32(1e-2)], device="cuda"), zeros(1, torch.int32)
     opt.step_coupled("rmsprop", lr, step, **HP["rmsprop"])
     ref = C.Tensor(p=p0.copy(), g=g0, s=s0.copy(), wd=f32(0.1))
     C.step_f32([ref], rule="rmsprop", lr=f32(1e-2), **HP["rmsprop"])

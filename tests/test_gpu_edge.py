@@ -7,6 +7,10 @@ import torch
 
 from adamw_optimizer_step_tensor_gb300 import FusedAdamW
 
+from _support import (assert_guards_intact, assert_max_abs, assert_single_step_rel,
+                      assert_state_bitexact, bits_equal, dev, empty, first_mismatch, grads_of, host,
+                      scalar_f32, scalar_i32, to_dev, zeros)
+
 pytestmark = pytest.mark.gpu
 
 
@@ -34,7 +38,7 @@ def _plans(n):
         "q4": (FusedAdamW(z, z, u8, u8, [0.1] * n, mode="q4", absmax_m=z, absmax_v=z),
                lambda o, lr, st: o.step(lr, st)),
         "amp": (FusedAdamW(z, z, z, z, [0.1] * n),
-                lambda o, lr, st: o.step_amp(lr, st, torch.zeros(1, device="cuda"))),
+                lambda o, lr, st: o.step_amp(lr, st, zeros(1))),
     }
 
 
@@ -42,7 +46,7 @@ def _plans(n):
 def test_degenerate_plans_count_steps(n):
     lr = torch.tensor([1e-3], device="cuda")
     for name, (opt, run) in _plans(n).items():
-        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        st = zeros(1, torch.int32)
         for _ in range(3):
             run(opt, lr, st)
         torch.cuda.synchronize()
@@ -58,17 +62,17 @@ def test_plan_info_reports_the_launch_shape():
     4-bit kernel (256 threads); the grid never exceeds the SM count times the
     CTAs that fit on one SM."""
     n = 1 << 22
-    f = lambda dt=torch.float32: torch.zeros(n, dtype=dt, device="cuda")
+    f = lambda dt=torch.float32: zeros(n, dt)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     blocks = n // 256
-    absq8 = torch.zeros(blocks, device="cuda")
-    absq4 = torch.zeros(2 * blocks, device="cuda")
+    absq8 = zeros(blocks)
+    absq4 = zeros(2 * blocks)
     cases = {
         "fp32": (FusedAdamW([f()], [f()], [f()], [f()], [0.1]), 544, 1),
         "q8": (FusedAdamW([f()], [f(torch.bfloat16)], [f(torch.uint8)], [f(torch.uint8)], [0.1],
                           mode="q8", absmax_m=[absq8], absmax_v=[absq8.clone()]), 1024, 1),
-        "q4": (FusedAdamW([f()], [f(torch.bfloat16)], [torch.zeros(n // 2, dtype=torch.uint8, device="cuda")],
-                          [torch.zeros(n // 2, dtype=torch.uint8, device="cuda")], [0.1], mode="q4",
+        "q4": (FusedAdamW([f()], [f(torch.bfloat16)], [zeros(n // 2, torch.uint8)],
+                          [zeros(n // 2, torch.uint8)], [0.1], mode="q4",
                           absmax_m=[absq4], absmax_v=[absq4.clone()]), 256, 4),
     }
     for name, (opt, threads, per_sm) in cases.items():

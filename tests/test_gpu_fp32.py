@@ -15,8 +15,9 @@ import torch
 from adamw_optimizer_step_tensor_gb300 import FusedAdamW
 from oracle import adamw as OA
 
-from _support import (assert_max_abs, assert_single_step_rel, assert_state_bitexact, bits_equal,
-                      dev, first_mismatch, grads_of, host, scalar_f32, scalar_i32)
+from _support import (assert_guards_intact, assert_max_abs, assert_single_step_rel,
+                      assert_state_bitexact, bits_equal, dev, empty, first_mismatch, grads_of, host,
+                      scalar_f32, scalar_i32, to_dev, zeros)
 
 pytestmark = pytest.mark.gpu
 
@@ -34,14 +35,13 @@ def _make(sizes, wds, gdtype, seed, misalign=False, zero_state=True):
     if misalign:
         # views one element into a larger buffer: only 4-byte aligned -> scalar path
         def view(a):
-            buf = dev(np.concatenate([np.zeros(1, a.dtype), a]))
-            return buf[1:]
+            return dev(a, shift=1)
         ps = [view(a) for a in host_p]
         ms = [view(a) for a in host_m]
         vs = [view(a) for a in host_v]
     else:
         ps, ms, vs = [dev(a) for a in host_p], [dev(a) for a in host_m], [dev(a) for a in host_v]
-    gs = [torch.empty(n, dtype=gdtype, device="cuda") for n in sizes]
+    gs = [empty(n, gdtype) for n in sizes]
     opt = FusedAdamW(ps, gs, ms, vs, wds)
     oracle = [OA.Tensor(p=a.copy(), g=None, m=b.copy(), v=c.copy(), wd=w)
               for a, b, c, w in zip(host_p, host_m, host_v, wds)]
@@ -57,6 +57,7 @@ def _new_grads(gs, oracle, rng, std=1e-3, scale=1.0):
 
 
 def _check(ps, ms, vs, oracle):
+    assert_guards_intact()
     for i, (p, m, v, o) in enumerate(zip(ps, ms, vs, oracle)):
         assert bits_equal(host(p), o.p), f"tensor {i} p: {first_mismatch(host(p), o.p)}"
         assert bits_equal(host(m), o.m), f"tensor {i} m: {first_mismatch(host(m), o.m)}"

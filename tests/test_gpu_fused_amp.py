@@ -16,6 +16,10 @@ import torch
 from adamw_optimizer_step_tensor_gb300 import FusedAdamW
 from oracle import adamw as OA
 
+from _support import (assert_guards_intact, assert_max_abs, assert_single_step_rel,
+                      assert_state_bitexact, bits_equal, dev, empty, first_mismatch, grads_of, host,
+                      scalar_f32, scalar_i32, to_dev, zeros)
+
 pytestmark = pytest.mark.gpu
 f32 = OA.f32
 B1, B2, EPS = f32(0.9), f32(0.999), f32(1e-8)
@@ -26,14 +30,14 @@ def test_fused_amp_matches_oracle_and_skips():
     n = 1 << 20
     rng = np.random.default_rng(31)
     p0 = rng.normal(0, 0.02, n).astype(np.float32)
-    p = torch.from_numpy(p0.copy()).cuda()
-    g = torch.zeros(n, dtype=torch.float16, device="cuda")
-    m, v = torch.zeros(n, device="cuda"), torch.zeros(n, device="cuda")
+    p = dev(p0)
+    g = zeros(n, torch.float16)
+    m, v = zeros(n), zeros(n)
     opt = FusedAdamW([p], [g], [m], [v], [f32(0.1)])
     ref = OA.Tensor(p=p0.copy(), g=None, m=np.zeros(n, np.float32), v=np.zeros(n, np.float32),
                     wd=f32(0.1))
     inject = synth.amp_injection(100, n, seed=31)
-    lr, step = torch.tensor([f32(0.1)], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+    lr, step = torch.tensor([f32(0.1)], device="cuda"), zeros(1, torch.int32)
     scale, found = torch.tensor([65536.0], device="cuda"), torch.full((1,), 7.0, device="cuda")
     t = 0
     for s in range(100):
@@ -68,18 +72,18 @@ def test_fused_amp_equals_two_launch_path(mode, big):
         st = []
         for n in sizes:
             if mode == "fp32":
-                pp = torch.from_numpy(rng_side.normal(0, 0.02, n).astype(np.float32)).cuda()
+                pp = dev(rng_side.normal(0, 0.02, n).astype(np.float32))
                 rr = None
             else:
-                pp = torch.from_numpy(rng_side.normal(0, 0.02, n).astype(np.float32)).to(torch.bfloat16).cuda()
-                rr = torch.from_numpy(rng_side.integers(0, 1 << 15, n).astype(np.int16)).cuda()
-            st.append(dict(p=pp, r=rr, g=torch.zeros(n, dtype=torch.bfloat16, device="cuda"),
-                           m=torch.zeros(n, device="cuda"), v=torch.zeros(n, device="cuda")))
+                pp = to_dev(torch.from_numpy(rng_side.normal(0, 0.02, n).astype(np.float32)).to(torch.bfloat16))
+                rr = dev(rng_side.integers(0, 1 << 15, n).astype(np.int16))
+            st.append(dict(p=pp, r=rr, g=zeros(n, torch.bfloat16),
+                           m=zeros(n), v=zeros(n)))
         opt = FusedAdamW([d["p"] for d in st], [d["g"] for d in st], [d["m"] for d in st],
                          [d["v"] for d in st], [0.1, 0.0, 0.1, 0.0, 0.1], mode=mode,
                          param_rems=[d["r"] for d in st] if mode == "bf16_rem" else None)
-        sides.append((st, opt, torch.zeros(1, dtype=torch.int32, device="cuda"),
-                      torch.zeros(1, device="cuda")))
+        sides.append((st, opt, zeros(1, torch.int32),
+                      zeros(1)))
     lr, scale = torch.tensor([1e-3], device="cuda"), torch.tensor([256.0], device="cuda")
     for it in range(6):
         xs = [torch.from_numpy((rng.normal(0, 1e-3, n) * 256).astype(np.float32)).to(torch.bfloat16)

@@ -19,7 +19,9 @@ from oracle import adamw as A
 from oracle import lion as L
 from oracle import remainder as R
 
-from _support import dev, grads_of, host
+from _support import (assert_guards_intact, assert_max_abs, assert_single_step_rel,
+                      assert_state_bitexact, bits_equal, dev, empty, first_mismatch, grads_of, host,
+                      scalar_f32, scalar_i32, to_dev, zeros)
 
 pytestmark = pytest.mark.gpu
 f32 = A.f32
@@ -30,8 +32,7 @@ SIZES = [1, 9, 2047, 2048, 2049, 8193, 30001, 0, 777]
 def _view(a, misalign):
     if not misalign:
         return dev(a)
-    buf = dev(np.concatenate([np.zeros(1, a.dtype), a]))
-    return buf[1:]
+    return dev(a, shift=1)   # one element off the 16-byte grid, guard bands on both sides
 
 
 def _make(mode, gdtype, seed, misalign=False):
@@ -49,7 +50,7 @@ def _make(mode, gdtype, seed, misalign=False):
             rem = rng.integers(0, 1 << 15, n).astype(np.int16)
             d = dict(p=_view(hi.view(np.int16), misalign).view(torch.bfloat16), r=_view(rem, misalign))
             master = R.join(hi, rem)
-        d.update(m=_view(m, misalign), g=torch.empty(n, dtype=gdtype, device="cuda"))
+        d.update(m=_view(m, misalign), g=empty(n, gdtype))
         dev_t.append(d)
         orc.append(L.Tensor(p=master, g=None, m=m.copy(), wd=wd))
     opt = FusedAdamW([d["p"] for d in dev_t], [d["g"] for d in dev_t], [d["m"] for d in dev_t],
@@ -65,6 +66,7 @@ def _master(mode, d):
 
 
 def _check(mode, dev_t, orc, tag):
+    assert_guards_intact()
     for i, (d, o) in enumerate(zip(dev_t, orc)):
         if mode == "fp32":
             assert np.array_equal(host(d["p"]).view(np.uint32), o.p.view(np.uint32)), (tag, i, "p")
@@ -79,7 +81,7 @@ def _check(mode, dev_t, orc, tag):
 @pytest.mark.parametrize("gdtype", [torch.float32, torch.float16, torch.bfloat16])
 def test_lion_bitexact(mode, gdtype):
     opt, dev_t, orc, rng = _make(mode, gdtype, seed=51)
-    lr, step = torch.tensor([f32(3e-4)], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+    lr, step = torch.tensor([f32(3e-4)], device="cuda"), zeros(1, torch.int32)
     for t in range(1, 5):
         for d, o in zip(dev_t, orc):
             x, wide = grads_of(rng.normal(0, 1e-3, d["g"].numel()).astype(np.float32), gdtype)
@@ -94,7 +96,7 @@ def test_lion_bitexact(mode, gdtype):
 
 def test_lion_scalar_path_on_misaligned_tensors():
     opt, dev_t, orc, rng = _make("fp32", torch.float32, seed=52, misalign=True)
-    lr, step = torch.tensor([f32(1e-3)], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+    lr, step = torch.tensor([f32(1e-3)], device="cuda"), zeros(1, torch.int32)
     for _ in range(2):
         for d, o in zip(dev_t, orc):
             x = rng.normal(0, 1e-3, d["g"].numel()).astype(np.float32)
@@ -113,7 +115,7 @@ def test_lion_moves_each_element_by_exactly_lr(mode):
     # the rounding of that subtraction (half an ulp of the result)
     opt, dev_t, orc, rng = _make(mode, torch.float32, seed=53)
     lrv = f32(1e-3)
-    lr, step = torch.tensor([lrv], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+    lr, step = torch.tensor([lrv], device="cuda"), zeros(1, torch.int32)
     # exact zeros: m = g = 0 on a stretch of one tensor gives c = 0, so no move
     d6 = dev_t[6]
     d6["m"][100:200] = 0
@@ -152,8 +154,8 @@ def test_lion_skip_and_unscale():
     g0 = rng.normal(0, 1e-3, n).astype(np.float32)
     p, m, g = dev(p0), dev(m0), dev(g0 * 128)
     opt = FusedAdamW([p], [g], [m], None, [f32(0.1)])
-    lr, step = torch.tensor([f32(1e-3)], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
-    scale, found = torch.tensor([128.0], device="cuda"), torch.zeros(1, device="cuda")
+    lr, step = torch.tensor([f32(1e-3)], device="cuda"), zeros(1, torch.int32)
+    scale, found = torch.tensor([128.0], device="cuda"), zeros(1)
     g[7] = float("nan")
     opt.check_nonfinite(found)
     opt.step_lion(lr, step, betas=(B1, B2), grad_scale=scale, found_inf=found)
@@ -176,7 +178,7 @@ def test_lion_leaves_second_and_slow_states_alone():
     p0, m0, v0, s0, g0 = (rng.normal(0, 1e-2, n).astype(np.float32) for _ in range(5))
     p, m, v, s, g = dev(p0), dev(m0), dev(np.abs(v0)), dev(s0), dev(g0)
     opt = FusedAdamW([p], [g], [m], [v], [0.0], exp_avg_slows=[s])
-    lr, step = torch.tensor([f32(1e-3)], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+    lr, step = torch.tensor([f32(1e-3)], device="cuda"), zeros(1, torch.int32)
     opt.step_lion(lr, step, betas=(B1, B2))
     ref = L.Tensor(p=p0.copy(), g=g0, m=m0.copy(), wd=0.0)
     L.step_f32([ref], lr=f32(1e-3), beta1=B1, beta2=B2)
@@ -187,12 +189,12 @@ def test_lion_leaves_second_and_slow_states_alone():
 
 def test_one_state_plan_refuses_two_state_steps():
     n = 4096
-    p, m, g = (torch.zeros(n, device="cuda") for _ in range(3))
+    p, m, g = (zeros(n) for _ in range(3))
     opt = FusedAdamW([p], [g], [m], None, [0.0])
-    lr, step = torch.tensor([f32(1e-3)], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+    lr, step = torch.tensor([f32(1e-3)], device="cuda"), zeros(1, torch.int32)
     with pytest.raises(AdamWError):
         opt.step(lr, step)
-    found = torch.zeros(1, device="cuda")
+    found = zeros(1)
     with pytest.raises(AdamWError):
         opt.step_amp(lr, step, found)
     torch.cuda.synchronize()

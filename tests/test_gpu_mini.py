@@ -22,7 +22,9 @@ from oracle import adamw as A
 from oracle import mini as M
 from oracle import remainder as R
 
-from _support import dev, grads_of, host
+from _support import (assert_guards_intact, assert_max_abs, assert_single_step_rel,
+                      assert_state_bitexact, bits_equal, dev, empty, first_mismatch, grads_of, host,
+                      scalar_f32, scalar_i32, to_dev, zeros)
 
 pytestmark = pytest.mark.gpu
 f32 = A.f32
@@ -49,7 +51,7 @@ def _make(mode, gdtype, seed):
             rem = rng.integers(0, 1 << 15, n).astype(np.int16)
             d = dict(p=dev(hi.view(np.int16)).view(torch.bfloat16), r=dev(rem))
             master = R.join(hi, rem)
-        d.update(m=dev(m), v=dev(v), g=torch.empty(n, dtype=gdtype, device="cuda"))
+        d.update(m=dev(m), v=dev(v), g=empty(n, gdtype))
         dev_t.append(d)
         orc.append(M.Tensor(p=master, g=None, m=m.copy(), v=v.copy(), wd=wd, block=b))
     opt = FusedAdamW([d["p"] for d in dev_t], [d["g"] for d in dev_t], [d["m"] for d in dev_t],
@@ -72,6 +74,7 @@ def _ulps(a, b):
 
 
 def _check(mode, dev_t, orc, lr, steps_done, tag):
+    assert_guards_intact()
     exact_v = total_v = 0
     for i, (d, o) in enumerate(zip(dev_t, orc)):
         if o.p.size == 0:
@@ -98,7 +101,7 @@ def _check(mode, dev_t, orc, lr, steps_done, tag):
 def test_mini_matches_oracle(mode, gdtype):
     opt, dev_t, orc, rng = _make(mode, gdtype, seed=71)
     lr_v = f32(1e-3)
-    lr, step = torch.tensor([lr_v], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+    lr, step = torch.tensor([lr_v], device="cuda"), zeros(1, torch.int32)
     for t in range(1, 4):
         for d, o in zip(dev_t, orc):
             x, wide = grads_of(rng.normal(0, 1e-3, d["g"].numel()).astype(np.float32), gdtype)
@@ -117,10 +120,10 @@ def test_mini_first_step_closed_form():
     p0 = rng.normal(0, 0.02, n).astype(np.float32)
     g0 = (rng.normal(0, 1e-3, n) * np.repeat(rng.uniform(0.1, 10, n // block), block)).astype(np.float32)
     p, g = dev(p0), dev(g0)
-    m, v = torch.zeros(n, device="cuda"), torch.zeros(n // block, device="cuda")
+    m, v = zeros(n), zeros(n // block)
     opt = FusedAdamW([p], [g], [m], [v], [f32(0.1)], v_blocks=[block])
     lr = f32(0.1)
-    opt.step_mini(torch.tensor([lr], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda"),
+    opt.step_mini(torch.tensor([lr], device="cuda"), zeros(1, torch.int32),
                   betas=(HP["beta1"], HP["beta2"]), eps=HP["eps"])
     torch.cuda.synchronize()
     gd = g0.astype(np.float64)
@@ -136,7 +139,7 @@ def test_mini_skip_and_plan_rules():
         d["g"].copy_(dev((rng.normal(0, 1e-3, d["g"].numel()) * 1024).astype(np.float16)))
     dev_t[4]["g"][17] = float("inf")
     before = [{k: host(x) for k, x in d.items() if x is not None and k != "g"} for d in dev_t]
-    found, step = torch.zeros(1, device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+    found, step = zeros(1), zeros(1, torch.int32)
     scale = torch.tensor([1024.0], device="cuda")
     opt.check_nonfinite(found)
     opt.step_mini(torch.tensor([f32(1e-3)], device="cuda"), step, grad_scale=scale, found_inf=found)
@@ -159,14 +162,14 @@ def test_mini_llama_sized_blocks():
     for n, b in layout:
         p = rng.normal(0, 0.02, n).astype(np.float32)
         g = rng.normal(0, 1e-4, n).astype(np.float32)
-        ds.append(dict(p=dev(p), g=dev(g), m=torch.zeros(n, device="cuda"),
-                       v=torch.zeros(n // b, device="cuda")))
+        ds.append(dict(p=dev(p), g=dev(g), m=zeros(n),
+                       v=zeros(n // b)))
         orc.append(M.Tensor(p=p, g=g, m=np.zeros(n, np.float32), v=np.zeros(n // b, np.float32),
                             wd=f32(0.1), block=b))
     opt = FusedAdamW([d["p"] for d in ds], [d["g"] for d in ds], [d["m"] for d in ds],
                      [d["v"] for d in ds], [f32(0.1)] * 3, v_blocks=[b for _, b in layout])
     lr = f32(3e-4)
-    opt.step_mini(torch.tensor([lr], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda"),
+    opt.step_mini(torch.tensor([lr], device="cuda"), zeros(1, torch.int32),
                   betas=(HP["beta1"], HP["beta2"]), eps=HP["eps"])
     M.step_f32(orc, lr=lr, t=1, **HP)
     torch.cuda.synchronize()

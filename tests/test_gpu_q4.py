@@ -18,7 +18,9 @@ from oracle import adamw as OA
 from oracle import q4 as O4
 from oracle import q8 as OQ
 
-from _support import bits_equal, dev, first_mismatch, grads_of, host, scalar_f32, scalar_i32
+from _support import (assert_guards_intact, assert_max_abs, assert_single_step_rel,
+                      assert_state_bitexact, bits_equal, dev, empty, first_mismatch, grads_of, host,
+                      scalar_f32, scalar_i32, to_dev, zeros)
 
 pytestmark = pytest.mark.gpu
 f32 = OA.f32
@@ -29,7 +31,7 @@ SIZES = [1, 7, 127, 128, 129, 255, 256, 257, 2048 + 100, 8192 + 301, 70001, 0]
 def _view(a, misalign):
     if not misalign:
         return dev(a)
-    return dev(np.concatenate([np.zeros(1, a.dtype), a]))[1:]   # 4 bytes off the 16-byte grid
+    return dev(a, shift=1)   # one element off the 16-byte grid, guard bands on both sides
 
 
 def _build(sizes, gdtype, seed, zero_state, misalign=False):
@@ -44,7 +46,7 @@ def _build(sizes, gdtype, seed, zero_state, misalign=False):
         av = np.zeros(nb, np.float32) if zero_state else rng.uniform(0, 1e-6, nb).astype(np.float32)
         st.append(dict(p=p, cm=pm, cv=pv, am=am, av=av))
     d = [{k: (_view(v, misalign) if k == "p" else dev(v)) for k, v in s.items()} for s in st]
-    gs = [torch.empty(n, dtype=gdtype, device="cuda") for n in sizes]
+    gs = [empty(n, gdtype) for n in sizes]
     opt = FusedAdamW([x["p"] for x in d], gs, [x["cm"] for x in d], [x["cv"] for x in d],
                      [f32(0.01) if i % 2 else 0.0 for i in range(len(sizes))], mode="q4",
                      absmax_m=[x["am"] for x in d], absmax_v=[x["av"] for x in d])
@@ -65,6 +67,7 @@ def _steps(opt, st, d, gs, rng, gdtype, n_steps, lr=1e-3):
             O4.step_f32(s["p"], w, s["cm"], s["cv"], s["am"], s["av"], lr=f32(lr), beta1=B1,
                         beta2=B2, eps=EPS, wd=f32(0.01) if i % 2 else 0.0, t=t, maps=maps)
         torch.cuda.synchronize()
+        assert_guards_intact()
         for i, (s, x) in enumerate(zip(st, d)):
             assert bits_equal(host(x["p"]), s["p"]), f"t{t} tensor {i} p: {first_mismatch(host(x['p']), s['p'])}"
             assert np.array_equal(host(x["cm"]), s["cm"]), f"t{t} tensor {i} m codes"
@@ -135,10 +138,10 @@ def test_q4_export_import_match_oracle():
     for which, table, thr in ((0, maps.smap, maps.sthr), (1, maps.umap, maps.uthr)):
         xs = x if which == 0 else np.abs(x)
         xd = dev(xs)
-        codes = torch.empty((n + 1) // 2, dtype=torch.uint8, device="cuda")
-        am = torch.empty(nb, dtype=torch.float32, device="cuda")
+        codes = empty((n + 1) // 2, torch.uint8)
+        am = empty(nb, torch.float32)
         C.adamw_q4_quant(opt.plan, which, xd.data_ptr(), codes.data_ptr(), am.data_ptr(), n, sh)
-        out = torch.empty(n, dtype=torch.float32, device="cuda")
+        out = empty(n, torch.float32)
         C.adamw_q4_dequant(opt.plan, which, codes.data_ptr(), am.data_ptr(), out.data_ptr(), n, sh)
         torch.cuda.synchronize()
         oc, oa = O4.quantize_blockwise(xs, table, thr)
@@ -147,10 +150,10 @@ def test_q4_export_import_match_oracle():
         assert np.array_equal(host(out), OQ.dequantize(oc, oa, table, O4.BLOCK), equal_nan=True), which
     assert qmap.empty_block_code(maps.umap) == 0
     with pytest.raises(C.AdamWError):   # an 8-bit plan refuses the 4-bit calls
-        opt8 = FusedAdamW([d[0]["p"]], [gs[0]], [torch.zeros(n, dtype=torch.uint8, device="cuda")],
-                          [torch.zeros(n, dtype=torch.uint8, device="cuda")], [0.0], mode="q8",
-                          absmax_m=[torch.zeros(OQ.n_blocks(n), device="cuda")],
-                          absmax_v=[torch.zeros(OQ.n_blocks(n), device="cuda")])
+        opt8 = FusedAdamW([d[0]["p"]], [gs[0]], [zeros(n, torch.uint8)],
+                          [zeros(n, torch.uint8)], [0.0], mode="q8",
+                          absmax_m=[zeros(OQ.n_blocks(n))],
+                          absmax_v=[zeros(OQ.n_blocks(n))])
         C.adamw_q4_dequant(opt8.plan, 0, codes.data_ptr(), am.data_ptr(), out.data_ptr(), n, sh)
 
 

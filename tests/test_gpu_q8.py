@@ -16,7 +16,9 @@ from adamw_optimizer_step_tensor_gb300 import FusedAdamW, _capi as C
 from oracle import adamw as OA
 from oracle import q8 as OQ
 
-from _support import bits_equal, dev, first_mismatch, grads_of, host, scalar_f32, scalar_i32
+from _support import (assert_guards_intact, assert_max_abs, assert_single_step_rel,
+                      assert_state_bitexact, bits_equal, dev, empty, first_mismatch, grads_of, host,
+                      scalar_f32, scalar_i32, to_dev, zeros)
 
 pytestmark = pytest.mark.gpu
 f32 = OA.f32
@@ -27,7 +29,7 @@ SIZES = [1, 255, 256, 257, 2048 + 100, 8192 + 300, 70001, 0]
 def _view(a, misalign):
     if not misalign:
         return dev(a)
-    return dev(np.concatenate([np.zeros(1, a.dtype), a]))[1:]   # 4 bytes off the 16-byte grid
+    return dev(a, shift=1)   # one element off the 16-byte grid, guard bands on both sides
 
 
 def _build(sizes, gdtype, seed, zero_state, misalign=False):
@@ -42,7 +44,7 @@ def _build(sizes, gdtype, seed, zero_state, misalign=False):
         av = np.zeros(nb, np.float32) if zero_state else rng.uniform(0, 1e-6, nb).astype(np.float32)
         st.append(dict(p=p, cm=cm, cv=cv, am=am, av=av))
     d = [{k: (_view(v, misalign) if k == "p" else dev(v)) for k, v in s.items()} for s in st]
-    gs = [torch.empty(n, dtype=gdtype, device="cuda") for n in sizes]
+    gs = [empty(n, gdtype) for n in sizes]
     opt = FusedAdamW([x["p"] for x in d], gs, [x["cm"] for x in d], [x["cv"] for x in d],
                      [f32(0.01)] * len(sizes), mode="q8", absmax_m=[x["am"] for x in d],
                      absmax_v=[x["av"] for x in d])
@@ -65,6 +67,7 @@ def test_q8_steps_bitexact(gdtype):
             OQ.step_f32(s["p"], w, s["cm"], s["cv"], s["am"], s["av"], lr=f32(1e-3), beta1=B1,
                         beta2=B2, eps=EPS, wd=f32(0.01), t=t, maps=maps)
         torch.cuda.synchronize()
+        assert_guards_intact()
         for i, (s, x) in enumerate(zip(st, d)):
             assert bits_equal(host(x["p"]), s["p"]), f"t{t} tensor {i} p: {first_mismatch(host(x['p']), s['p'])}"
             assert np.array_equal(host(x["cm"]), s["cm"]), f"t{t} tensor {i} m codes"
@@ -92,6 +95,7 @@ def test_q8_element_path_on_misaligned_params():
             OQ.step_f32(s["p"], w, s["cm"], s["cv"], s["am"], s["av"], lr=f32(1e-3), beta1=B1,
                         beta2=B2, eps=EPS, wd=f32(0.01), t=t, maps=maps)
         torch.cuda.synchronize()
+        assert_guards_intact()
         for i, (s, x) in enumerate(zip(st, d)):
             assert bits_equal(host(x["p"]), s["p"]), f"t{t} tensor {i} p"
             assert np.array_equal(host(x["cm"]), s["cm"]), f"t{t} tensor {i} m codes"
@@ -125,11 +129,11 @@ def test_q8_export_import_match_oracle():
     for which, table, thr in ((0, maps.smap, maps.sthr), (1, maps.umap, maps.uthr)):
         xs = x if which == 0 else np.abs(x)
         xd.copy_(dev(xs))
-        codes = torch.empty(n, dtype=torch.uint8, device="cuda")
-        am = torch.empty(nb, dtype=torch.float32, device="cuda")
+        codes = empty(n, torch.uint8)
+        am = empty(nb, torch.float32)
         sh = torch.cuda.current_stream().cuda_stream
         C.adamw_q8_quant(opt.plan, which, xd.data_ptr(), codes.data_ptr(), am.data_ptr(), n, sh)
-        out = torch.empty(n, dtype=torch.float32, device="cuda")
+        out = empty(n, torch.float32)
         C.adamw_q8_dequant(opt.plan, which, codes.data_ptr(), am.data_ptr(), out.data_ptr(), n, sh)
         torch.cuda.synchronize()
         oc, oa = OQ.quantize_blockwise(xs, table, thr)
