@@ -19,9 +19,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT, "libadamw.so")
-SOURCES = ["capi.cpp", "qmap.cpp", "step_kernels.cu", "bulk_kernels.cu", "aux_kernels.cu", "noalloc.cu",
-           "mini_kernels.cu",
-           "q4_kernels.cu"]
+SOURCES = ["capi.cpp", "qmap.cpp", "step_kernels.cu", "bulk_kernels.cu", "small_kernels.cu",
+           "aux_kernels.cu", "noalloc.cu", "mini_kernels.cu", "q4_kernels.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -19,6 +19,7 @@
 
 #include "internal.h"
 #include "step_common.cuh"
+#include "async_copy.cuh"
 
 namespace adamw {
 namespace {
@@ -26,55 +27,6 @@ namespace {
 constexpr int kConsumers = kBulkConsumers;     // consumer threads (16 warps)
 constexpr int kTile = kConsumers * 4;           // elements per stage: 4 per consumer thread
 static_assert(kTile % kVec == 0, "bulk copies move whole 8-element groups");
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-      " selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ uint64_t global_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-// Bounded wait: false if the phase did not complete within limit_ns.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          uint64_t limit_ns = kWaitLimitNs) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (global_ns() - t0 > limit_ns) return false;
-  return true;
-}
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
-                                         uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
-
 // Byte layout of one stage: p, rem (bf16 mode), g, m, v (not Lion), m2
 // (AdEMAMix) -- each kTile elements.
 template <adamw_mode MODE, typename GT, int ALGO>
@@ -164,17 +116,6 @@ __device__ void produce(const StepArgs& a, unsigned char* ring, uint64_t* full, 
   }
 }
 
-template <typename GT>
-__device__ __forceinline__ float grad_from_smem(const unsigned char* base, int idx) {
-  if constexpr (sizeof(GT) == 4) {
-    return reinterpret_cast<const float*>(base)[idx];
-  } else {
-    const uint32_t h = reinterpret_cast<const uint16_t*>(base)[idx];
-    if constexpr (std::is_same<GT, __half>::value) return f16_to_f32(h);
-    return bf16_to_f32(h);
-  }
-}
-
 // Four consecutive elements [j, j+4) of a tile from shared memory.
 template <adamw_mode MODE, typename GT, int ALGO>
 __device__ __forceinline__ void load4_smem(const unsigned char* st, int j, float (&p)[4],
@@ -237,8 +178,8 @@ __global__ void __launch_bounds__(kBulkThreads, AlgoTune<ALGO>::ctas) step_bulk_
       mbar_init(&full[s], 1);                     // the producer's arrive.expect_tx
       mbar_init(&empty[s], kConsumers / 32);      // one arrive per consumer warp
     }
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    fence_mbar_init();
+    fence_proxy_async_smem();
   }
   __syncthreads();
 
@@ -394,7 +335,7 @@ __global__ void wait_selftest_kernel(uint64_t limit_ns) {
   __shared__ uint64_t bar;
   if (threadIdx.x != 0) return;
   mbar_init(&bar, 1);
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  fence_mbar_init();
   const uint64_t t0 = global_ns();
   const bool done = mbar_wait(&bar, 0u, limit_ns);   // phase 0 never completes
   g_selftest_ns = global_ns() - t0;

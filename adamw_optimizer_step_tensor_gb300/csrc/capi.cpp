@@ -52,6 +52,14 @@ struct adamw_plan {
   bool mini = false;
   int64_t n_blocks = 0, n_red = 0;
   int grid_red = 1;
+  // plans small enough to sit in shared memory whole (small_kernels.cu): the
+  // tensor table as kernel parameters, one piece of one tensor per CTA
+  bool small = false;
+  bool small_fused = false;    // adamw_step_amp takes the fused small path too
+  SmallArgs small_args{};
+  int small_grid = 0;
+  int small_smem = 0;
+  int small_smem_fused = 0;
   MiniBlock* d_blocks = nullptr;
   int32_t* d_chunk_blk = nullptr;
   int64_t* d_red_chunks = nullptr;
@@ -133,6 +141,23 @@ StepArgs step_args(const adamw_plan* plan, const float* lr_dev, int32_t* step_de
                    float beta2, float eps) {
   return base_step_args(plan->d_tensors, plan->d_chunks, plan->n_chunks, plan->d_scratch, lr_dev,
                         step_dev, grad_scale_dev, found_inf_dev, beta1, beta2, eps);
+}
+
+// The kernel parameters of a small plan's step: its tensor table and this
+// call's run-time scalars.
+SmallArgs small_args(const adamw_plan* plan, const float* lr_dev, int32_t* step_dev,
+                     const float* grad_scale_dev, const float* found_inf_dev, float beta1,
+                     float beta2, float eps) {
+  SmallArgs a = plan->small_args;
+  a.lr = lr_dev;
+  a.step = step_dev;
+  a.grad_scale = grad_scale_dev;
+  a.found_inf = found_inf_dev;
+  a.scratch = plan->d_scratch;
+  a.beta1 = beta1;
+  a.beta2 = beta2;
+  a.eps = eps;
+  return a;
 }
 
 // n = 256 (8-bit maps, both must contain 0.0) or 16 (the 4-bit maps; the v
@@ -304,7 +329,7 @@ static adamw_status create_plan(const adamw_tensor* tensors, int32_t n_tensors, 
   e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device);
   if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
   int bps = 0, smem = 0, bps_sd = 1;
-  const bool bulk = kUseBulk && !quantized(mode);
+  const bool bulk = !quantized(mode);
   if (bulk) {
     e = cudaSuccess;
     for (int algo : {kAlgoLion, kAlgoMomentum, kAlgoRmsprop, kAlgoAdagrad})
@@ -446,6 +471,59 @@ static adamw_status create_plan(const adamw_tensor* tensors, int32_t n_tensors, 
     if (fb && (e = cudaMemcpy(p->d_chunks_fused, fchunks.data(), fb, cudaMemcpyHostToDevice)) != cudaSuccess)
       return cuda_fail(e, "upload fused chunk table");
   }
+  if (!quantized(mode) && !v_block && with_v && sized > 0 && sized <= kSmallMaxTensors) {
+    // the small-plan path: every tensor in pieces of `piece` elements (a
+    // multiple of 8, at least 256), one per CTA, at most one CTA per SM, and
+    // each piece staged whole in shared memory
+    const size_t per_elem = psz + (mode == ADAMW_MODE_BF16_REM ? 2 : 0) + gsz + 8;
+    int64_t piece = ((total + sms - 1) / sms + 7) / 8 * 8;
+    if (piece < 256) piece = 256;
+    int64_t items = 0;
+    for (int guard = 0; guard < 64; ++guard) {
+      items = 0;
+      for (int32_t i = 0; i < n_tensors; ++i) items += (td[i].numel + piece - 1) / piece;
+      if (items <= sms) break;
+      piece = ((piece * items + sms - 1) / sms + 7) / 8 * 8;
+    }
+    const int64_t slice = ((piece / 8 * 8) + kSmallThreads / 32 * 8 - 1) / (kSmallThreads / 32 * 8) * 8;
+    const int64_t smem_b = slice * (kSmallThreads / 32) * static_cast<int64_t>(per_elem);
+    // the fused variant also stages its results (p [+ remainder], m, v)
+    const int64_t smem_f =
+        slice * (kSmallThreads / 32) *
+        static_cast<int64_t>(per_elem + psz + (mode == ADAMW_MODE_BF16_REM ? 2 : 0) + 8);
+    bool all_vec = true;
+    for (int32_t i = 0; i < n_tensors; ++i)
+      if (td[i].numel > 0 && !td[i].vec_ok) all_vec = false;
+    if (items <= sms && smem_b <= kSmallSmemMax && piece <= INT32_MAX) {
+      SmallArgs& sa = p->small_args;
+      int32_t item = 0, k = 0;
+      for (int32_t i = 0; i < n_tensors; ++i) {
+        if (td[i].numel == 0) continue;
+        SmallTensor& st = sa.t[k++];
+        st.p = td[i].p;
+        st.rem = td[i].rem;
+        st.g = td[i].g;
+        st.m = static_cast<float*>(td[i].m);
+        st.v = static_cast<float*>(td[i].v);
+        st.numel = td[i].numel;
+        st.wd = td[i].wd;
+        st.first_item = item;
+        st.piece = static_cast<int32_t>(piece);
+        st.vec_ok = td[i].vec_ok;
+        item += static_cast<int32_t>((td[i].numel + piece - 1) / piece);
+      }
+      sa.n_tensors = k;
+      p->small_grid = item;
+      p->small_smem = static_cast<int>(smem_b < 16 ? 16 : smem_b);
+      // the fused variant keeps one saved element per thread for the ragged
+      // tails, so it takes plans whose tensors are all 16-byte aligned
+      p->small_fused = all_vec && smem_f <= kSmallSmemMax;
+      p->small_smem_fused = p->small_fused ? static_cast<int>(smem_f < 16 ? 16 : smem_f) : 0;
+      if ((e = prepare_step_small(mode, grad_dtype, p->small_smem, p->small_smem_fused)) != cudaSuccess)
+        return cuda_fail(e, "cudaFuncSetAttribute(small-plan step)");
+      p->small = true;
+    }
+  }
   if (quantized(mode)) {
     std::unique_ptr<QTables> qt(new QTables);
     float smap[256], umap[256];
@@ -488,8 +566,9 @@ adamw_status adamw_plan_info(const adamw_plan* plan, int64_t* total_numel, int64
   if (!plan) return fail(ADAMW_EINVAL, "plan is NULL");
   if (total_numel) *total_numel = plan->total_numel;
   if (n_chunks) *n_chunks = plan->n_chunks;
-  if (grid_blocks) *grid_blocks = plan->grid;
-  if (block_threads) *block_threads = plan->block_threads;
+  // the launch shape of adamw_step's kernel
+  if (grid_blocks) *grid_blocks = plan->small ? plan->small_grid : plan->grid;
+  if (block_threads) *block_threads = plan->small ? kSmallThreads : plan->block_threads;
   return ADAMW_OK;
 }
 
@@ -544,10 +623,18 @@ adamw_status adamw_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev
   if (!plan->has_v) return fail(ADAMW_EINVAL, "the plan's tensors carry no exp_avg_sq");
   if (plan->mini) return fail(ADAMW_EINVAL, "an Adam-mini plan steps with adamw_mini_step");
   if ((st = check_device(plan)) != ADAMW_OK) return st;
+  cudaStream_t st_ = static_cast<cudaStream_t>(stream);
+  if (plan->small) {
+    const SmallArgs sa = small_args(plan, lr_dev, step_dev, grad_scale_dev, found_inf_dev, beta1,
+                                    beta2, eps);
+    cudaError_t e = launch_step_small(plan->mode, plan->gdt, sa, plan->small_grid, plan->small_smem,
+                                      false, nullptr, st_);
+    if (e != cudaSuccess) return cuda_fail(e, "launch small-plan adamw step");
+    return ADAMW_OK;
+  }
   StepArgs a = step_args(plan, lr_dev, step_dev, grad_scale_dev, found_inf_dev, beta1, beta2, eps);
   a.qt = plan->d_qt;
   a.refine = plan->refine;
-  cudaStream_t st_ = static_cast<cudaStream_t>(stream);
   cudaError_t e = plan->bulk ? launch_step_bulk(plan->mode, plan->gdt, a, plan->grid, st_, kAlgoAdamW)
                   : plan->mode == ADAMW_MODE_Q4 ? launch_step_q4(plan->gdt, a, plan->grid, st_)
                                                 : launch_step(plan->mode, plan->gdt, a, plan->grid, st_);
@@ -668,6 +755,17 @@ adamw_status adamw_step_amp(adamw_plan* plan, const float* lr_dev, int32_t* step
   if (!plan->has_v) return fail(ADAMW_EINVAL, "the plan's tensors carry no exp_avg_sq");
   if (plan->mini) return fail(ADAMW_EINVAL, "an Adam-mini plan steps with adamw_mini_step");
   if ((st = check_device(plan)) != ADAMW_OK) return st;
+  if (plan->small_fused) {
+    // the whole plan in shared memory: grads read once, check and step in one
+    // cooperative launch (every CTA resident: at most one per SM)
+    const SmallArgs sa = small_args(plan, lr_dev, step_dev, grad_scale_dev, nullptr, beta1, beta2,
+                                    eps);
+    cudaError_t e = launch_step_small(plan->mode, plan->gdt, sa, plan->small_grid,
+                                      plan->small_smem_fused, true, found_inf_dev,
+                                      static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cooperative launch of the small-plan fused step");
+    return ADAMW_OK;
+  }
   // Past a few million elements the grads no longer stay in L2 between the
   // scan and the update, and the bulk-staged step outruns the cooperative one
   // (fp16 grads on GB300: fused 33.5 us vs 35.9 us at 4 Mi elements, 57.3 vs

@@ -16,18 +16,18 @@ constexpr int kVec = 8;
 constexpr int kPass = kThreads * kVec;       // 2048 elements per CTA pass
 // Passes whose loads a thread issues together, and the resident CTAs per SM
 // the register budget targets, of the register-load fp32 / bf16+remainder
-// kernel (the A/B baseline of the bulk-staged one, see kUseBulk).  Measured on
-// GB300: 2 x 2 -> 92% of copy bandwidth vs 88% for 1 x 3.
+// path of the fused check + step (measured on GB300 for the plain step when it
+// used this path: 2 x 2 -> 92% of copy bandwidth vs 88% for 1 x 3).
 template <int MODE> struct Tune { static constexpr int unroll = 1, min_blocks = 3; };
 template <> struct Tune<ADAMW_MODE_FP32> { static constexpr int unroll = 2, min_blocks = 2; };
 constexpr int kChunkMax = 8 * kPass;         // chunks hold up to 16384 elements (chosen per plan)
 // fp32 and bf16+remainder steps stage tiles through shared memory with bulk
-// async copies (bulk_kernels.cu) instead of 128-bit register loads.  The
-// 8-bit and 4-bit steps load into registers: they are bound by instruction
-// issue and load latency, and staging would spend shared-memory bandwidth
-// that their code-table lookups need (a bulk-staged 8-bit step measured 5%
-// slower, per-warp cp.async staging 24-38% slower).
-constexpr bool kUseBulk = true;
+// async copies (bulk_kernels.cu; 92% -> 98% of the copy bandwidth against
+// 128-bit register loads).  The 8-bit and 4-bit steps load into registers:
+// they are bound by instruction issue and load latency, and staging would
+// spend shared-memory bandwidth that their code-table lookups need (a
+// bulk-staged 8-bit step measured 5% slower, per-warp cp.async staging 24-38%
+// slower).
 // The bulk-staged step: 16 consumer warps and one producer warp per CTA.
 constexpr int kBulkConsumers = 2 * kThreads;
 constexpr int kBulkThreads = kBulkConsumers + 32;
@@ -138,6 +138,37 @@ struct StepArgs {
   const float* blk_r = nullptr;         // Adam-mini: fl(1/bc1) / h of each block, this step
 };
 
+// Plans small enough to sit in shared memory whole (small_kernels.cu): every
+// CTA takes one piece of one tensor and stages all of it at once.  The tensor
+// table travels in the kernel parameters (no dependent global loads before the
+// first copy); tensor t's pieces are CTAs first_item .. first_item + its piece
+// count - 1, each `piece` elements but the tensor's last.
+constexpr int kSmallMaxTensors = 16;
+constexpr int kSmallThreads = 1024;                 // 32 warps, each its own slice
+constexpr int kSmallSmemMax = 216 * 1024;           // staged bytes per CTA, at most
+struct SmallTensor {
+  void* p;
+  int16_t* rem;
+  const void* g;
+  float* m;
+  float* v;
+  int64_t numel;
+  float wd;
+  int32_t first_item;  // first CTA of this tensor
+  int32_t piece;       // elements per CTA, a multiple of 8
+  int32_t vec_ok;      // all pointers 16-byte aligned
+};
+struct SmallArgs {
+  const float* lr;
+  int32_t* step;
+  const float* grad_scale;   // may be null
+  const float* found_inf;    // may be null (the fused kernel decides the skip itself)
+  StepScratch* scratch;
+  float beta1, beta2, eps;
+  int32_t n_tensors;
+  SmallTensor t[kSmallMaxTensors];
+};
+
 // Adam-mini: one block of `len` contiguous elements sharing one v value
 // (exp_avg_sq[v_index] of its tensor); its chunks are contiguous in the
 // chunk table.
@@ -204,6 +235,15 @@ cudaError_t launch_split(const float* master, uint16_t* hi, int16_t* rem, int64_
 cudaError_t fused_occupancy(adamw_mode mode, adamw_dtype gdt, int* blocks_per_sm);
 cudaError_t launch_step_fused_amp(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int grid,
                                   float* found_inf_out, cudaStream_t s);
+// Shared-memory-resident step of small plans (small_kernels.cu).  `fused`:
+// the non-finite check and the step in one cooperative launch (found_inf_out
+// written by CTA 0); otherwise a plain launch that honours a.found_inf.  The
+// fused variant stages the results beside the originals (smem_fused_bytes;
+// 0: the plan has no fused small path).
+cudaError_t prepare_step_small(adamw_mode mode, adamw_dtype gdt, int smem_bytes,
+                               int smem_fused_bytes);
+cudaError_t launch_step_small(adamw_mode mode, adamw_dtype gdt, const SmallArgs& a, int grid,
+                              int smem_bytes, bool fused, float* found_inf_out, cudaStream_t s);
 cudaError_t launch_lr_from_table(const float* table, int32_t n, const int32_t* step, float* lr,
                                  cudaStream_t s);
 cudaError_t launch_join(const uint16_t* hi, const int16_t* rem, float* master, int64_t n,

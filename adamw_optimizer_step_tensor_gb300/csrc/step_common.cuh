@@ -43,16 +43,32 @@ __device__ BiasCorr bias_corrections(float beta1, float beta2, int t) {
   return r;
 }
 
-// Thread 0 of every CTA, before the CTA's barrier: read the run-time scalars
-// (all loads issued together) and decide skip.  The float64 bias corrections
-// are taken from the plan's memo when the previous launch left them for this
-// step index and these betas, otherwise computed here.
-__device__ bool prologue(const StepArgs& a, Scal& s, int& t_out) {
-  const float found = a.found_inf != nullptr ? *a.found_inf : 0.0f;
-  const int step = *a.step;
-  const float lr = *a.lr;
-  const float gscale = a.grad_scale != nullptr ? *a.grad_scale : 1.0f;
-  const StepScratch memo = *a.scratch;
+// The run-time scalars as loaded, before any arithmetic: a kernel can issue
+// these loads, then other memory work, and finish the scalars afterwards.
+struct RawScalars {
+  float found, lr, gscale;
+  int step;
+  StepScratch memo;
+};
+
+__device__ __forceinline__ RawScalars load_scalars(const StepArgs& a) {
+  RawScalars r;
+  r.found = a.found_inf != nullptr ? *a.found_inf : 0.0f;
+  r.step = *a.step;
+  r.lr = *a.lr;
+  r.gscale = a.grad_scale != nullptr ? *a.grad_scale : 1.0f;
+  r.memo = *a.scratch;
+  return r;
+}
+
+// Decide skip and compute the launch's float32 scalars from the loaded raw
+// values.  The float64 bias corrections are taken from the plan's memo when
+// the previous launch left them for this step index and these betas,
+// otherwise computed here.
+__device__ bool finish_scalars(const StepArgs& a, const RawScalars& r, Scal& s, int& t_out) {
+  const float found = r.found, lr = r.lr, gscale = r.gscale;
+  const int step = r.step;
+  const StepScratch& memo = r.memo;
   if (found != 0.0f) return true;
   const int t = step + 1;
   const BiasCorr bc = (memo.memo_t == t && memo.memo_b1 == __float_as_uint(a.beta1) &&
@@ -77,10 +93,34 @@ __device__ bool prologue(const StepArgs& a, Scal& s, int& t_out) {
   return false;
 }
 
+// Thread 0 of every CTA, before the CTA's barrier: read the run-time scalars
+// (all loads issued together) and decide skip.
+__device__ bool prologue(const StepArgs& a, Scal& s, int& t_out) {
+  return finish_scalars(a, load_scalars(a), s, t_out);
+}
+
 // Thread 0 of every CTA that runs the step, after the barrier: take a ticket.
 // Every CTA read *step (and the memo) before its ticket -- the fence orders
 // it -- so the last CTA to take one can store t and the memo for step t + 1
 // without any CTA of this launch seeing either.  Nothing waits on anything.
+// take_ticket_with: the same with the next step's bias corrections already
+// computed (a kernel that takes its ticket late computes them early, so the
+// last CTA's epilogue is a few stores).
+__device__ void take_ticket_with(const StepArgs& a, int t, const BiasCorr& nx) {
+  __threadfence();
+  const unsigned tk = atomicAdd(&a.scratch->ticket, 1u);
+  if (tk == gridDim.x - 1) {
+    *a.step = t;
+    StepScratch* m = a.scratch;
+    m->memo_bc1 = nx.bc1;
+    m->memo_inv_sqrt_bc2 = nx.inv_sqrt_bc2;
+    m->memo_b1 = __float_as_uint(a.beta1);
+    m->memo_b2 = __float_as_uint(a.beta2);
+    m->memo_t = t + 1;
+    atomicExch(&m->ticket, 0u);
+  }
+}
+
 __device__ void take_ticket(const StepArgs& a, int t) {
   __threadfence();
   const unsigned tk = atomicAdd(&a.scratch->ticket, 1u);
@@ -95,6 +135,62 @@ __device__ void take_ticket(const StepArgs& a, int t) {
     m->memo_t = t + 1;
     atomicExch(&m->ticket, 0u);
   }
+}
+
+// The grid-wide vote of a fused check + step (one cooperative launch, all
+// CTAs resident), in three parts so that a kernel can work between them.
+// amp_enter: thread 0 of every CTA takes the launch index (it needs nothing
+// but the launch itself, so it can be taken early).  amp_arrive: the same
+// thread announces whether its CTA saw a non-finite grad (the flag is made
+// visible before the arrival by the release reduction, which waits for no
+// reply).  amp_await: it waits, bounded by 2 s, until every CTA of the
+// launch has arrived.  The plan's three counters only ever grow, so nothing
+// is reset between launches (a plan's fused launches all have the same
+// grid).  CTA 0 writes the found-inf flag.  amp_await returns 0 (step), 1
+// (skip) or 2 (the wait gave up: fault bit 8 set, the CTA must not store).
+__device__ unsigned long long amp_enter(StepScratch* sc) {
+  return atomicAdd(&sc->amp_enter, 1ull) / gridDim.x;
+}
+
+__device__ void amp_arrive(StepScratch* sc, unsigned long long launch, bool bad) {
+  if (bad) atomicMax(&sc->amp_inf, launch + 1);
+  asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(&sc->amp_arrive) : "memory");
+}
+
+__device__ unsigned long long amp_publish(StepScratch* sc, bool bad) {
+  const unsigned long long launch = amp_enter(sc);
+  amp_arrive(sc, launch, bad);
+  return launch;
+}
+
+__device__ int amp_await(StepScratch* sc, unsigned long long launch, float* found_inf_out) {
+  const unsigned long long target = (launch + 1) * gridDim.x;
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t0));
+  // poll with acquire loads: atomics on the counter would queue behind (and
+  // delay) the other CTAs' publishing atomics on the same L2 line
+  auto arrived = [&]() {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(&sc->amp_arrive) : "memory");
+    return v;
+  };
+  while (arrived() < target) {
+    __nanosleep(32);
+    uint64_t t1;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t1));
+    if (t1 - t0 > 2000000000ull) {
+      atomicOr(&sc->fault, 8u);
+      return 2;
+    }
+  }
+  __threadfence();
+  const bool skip = atomicAdd(&sc->amp_inf, 0ull) == launch + 1;
+  if (blockIdx.x == 0) *found_inf_out = skip ? 1.0f : 0.0f;
+  return skip ? 1 : 0;
+}
+
+__device__ int amp_grid_vote(StepScratch* sc, bool bad, float* found_inf_out) {
+  return amp_await(sc, amp_publish(sc, bad), found_inf_out);
 }
 
 __device__ __forceinline__ void update(float& p, float g, float& m, float& v, const Scal& s,
@@ -221,6 +317,18 @@ template <> struct Grad<__nv_bfloat16> {
     return bf16_to_f32(static_cast<const uint16_t*>(g)[e]);
   }
 };
+
+// One raw grad of a shared-memory stage, widened exactly to float32.
+template <typename GT>
+__device__ __forceinline__ float grad_from_smem(const unsigned char* base, int idx) {
+  if constexpr (sizeof(GT) == 4) {
+    return reinterpret_cast<const float*>(base)[idx];
+  } else {
+    const uint32_t h = reinterpret_cast<const uint16_t*>(base)[idx];
+    if constexpr (std::is_same<GT, __half>::value) return f16_to_f32(h);
+    return bf16_to_f32(h);
+  }
+}
 
 // Remainder join / split on one element (integer only; see adamw.h).
 __device__ __forceinline__ float rem_join(uint32_t hi, uint32_t rem16) {

@@ -1,14 +1,14 @@
 // step_kernels.cu -- the register-load step kernels for sm_103a: the 8-bit
-// step, the fused non-finite check + step of adamw_step_amp, and the fp32 /
-// bf16+remainder step that the bulk-staged kernel (bulk_kernels.cu) replaced,
-// kept behind kUseBulk as its A/B baseline.
+// step and the fused non-finite check + step of adamw_step_amp for plans
+// between the shared-memory-resident size and a few million elements.
 //
 // One persistent launch covers every tensor of a plan: CTAs stride over the
 // plan's chunk table (up to 16384 contiguous elements of one tensor per chunk,
 // a multiple of 256 but at a tensor's end), and each thread moves 8
-// consecutive elements per pass with 128-bit streaming loads and stores.  The step is a pure HBM stream (28 B per element in fp32
-// mode, 26 in bf16+remainder mode, 14.06 in 8-bit mode), so there is no
-// tensor-core work; the kernel's job is to keep enough bytes in flight.
+// consecutive elements per pass with 128-bit streaming loads and stores.  The
+// step is a pure HBM stream (28 B per element in fp32 mode, 26 in
+// bf16+remainder mode, 14.06 in 8-bit mode), so there is no tensor-core work;
+// the kernel's job is to keep enough bytes in flight.
 //
 // The element update is the decoupled-decay AdamW of "Fix decoupled weight
 // decay ordering in the CUDA Adam/AdEMAMix kernels" (bitsandbytes PR #2040):
@@ -104,63 +104,11 @@ __device__ __forceinline__ void load_trip(const TensorDesc& td, const Cursor& k,
   }
 }
 
-template <adamw_mode MODE, typename GT>
-__global__ void __launch_bounds__(kThreads, Tune<MODE>::min_blocks) step_kernel(const StepArgs a) {
-  constexpr int kUnroll = Tune<MODE>::unroll;
-  __shared__ Scal s_sc;
-  __shared__ int s_skip;
-  // The first trip's loads are issued before the run-time scalars are known,
-  // so thread 0's float64 bias corrections overlap their DRAM latency.  Loads
-  // are harmless if the step turns out to be skipped: nothing is stored.
-  Cursor k{static_cast<int64_t>(blockIdx.x), static_cast<int>(threadIdx.x) * kVec, Chunk{}};
-  bool have = seek(a, k);
-  TensorDesc td{};
-  Group x[kUnroll];
-  if (have) {
-    td = a.tensors[k.ch.tensor];
-    load_trip<MODE, GT, kUnroll>(td, k, td.vec_ok != 0, x);
-  }
-  int t = 0;
-  if (threadIdx.x == 0) s_skip = prologue(a, s_sc, t);
-  __syncthreads();
-  if (s_skip) return;
-  const Scal s = s_sc;
-  if (threadIdx.x == 0) take_ticket(a, t);
-
-  while (have) {
-    const float decay = __fsub_rn(1.0f, __fmul_rn(s.lr, td.wd));
-    const bool vec = td.vec_ok != 0;
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const int off = k.base + u * kPass;
-      if (vec && off + kVec <= k.ch.len)
-        update_store_group<MODE>(td, k.ch.start + off, x[u], s, decay);
-      else if (off < k.ch.len)
-        update_scalar<MODE, GT>(td, k.ch.start + off, min(kVec, k.ch.len - off), s, decay);
-    }
-    k.base += kPass * kUnroll;
-    if (k.base >= k.ch.len) {
-      const int32_t prev = k.ch.tensor;
-      k.c += gridDim.x;
-      k.base = threadIdx.x * kVec;
-      have = seek(a, k);
-      if (have && k.ch.tensor != prev) td = a.tensors[k.ch.tensor];
-    }
-    if (have) load_trip<MODE, GT, kUnroll>(td, k, td.vec_ok != 0, x);
-  }
-}
-
 // ---------------------------------------------------------------- fused AMP step
 // Non-finite check and update in one cooperative launch: every CTA scans the
 // grads of the chunks it will update, publishes whether it saw +-inf or NaN,
 // and waits (bounded, 2 s) at a grid barrier; then all CTAs skip or update
 // together.  For plans whose grads stay in L2 between the two passes.
-__device__ __forceinline__ uint64_t fused_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
-  return t;
-}
-
 template <typename GT>
 __device__ __forceinline__ bool nonfinite1(const void* g, int64_t k) {
   if (sizeof(GT) == 4)
@@ -204,32 +152,11 @@ step_fused_amp_kernel(const StepArgs a, float* found_inf_out) {
   bad = __syncthreads_or(bad);
 
   // 2. grid barrier: publish, then wait until every CTA of this launch has
-  if (threadIdx.x == 0) {
-    const unsigned long long g = gridDim.x;
-    const unsigned long long launch = atomicAdd(&sc->amp_enter, 1ull) / g;
-    if (bad) atomicMax(&sc->amp_inf, launch + 1);
-    __threadfence();
-    atomicAdd(&sc->amp_arrive, 1ull);
-    const unsigned long long target = (launch + 1) * g;
-    const uint64_t t0 = fused_ns();
-    int ok = 1;
-    while (atomicAdd(&sc->amp_arrive, 0ull) < target) {
-      __nanosleep(32);
-      if (fused_ns() - t0 > 2000000000ull) {
-        atomicOr(&sc->fault, 8u);
-        ok = 0;
-        break;
-      }
-    }
-    __threadfence();
-    const bool skip = atomicAdd(&sc->amp_inf, 0ull) == launch + 1;
-    if (blockIdx.x == 0 && ok) *found_inf_out = skip ? 1.0f : 0.0f;
-    s_skip = ok ? (skip ? 1 : 0) : 2;
-  }
+  if (threadIdx.x == 0) s_skip = amp_grid_vote(sc, bad, found_inf_out);
   __syncthreads();
   if (s_skip) return;
 
-  // 3. the step itself (the register-load path of step_kernel)
+  // 3. the step itself, loads into registers
   int t = 0;
   if (threadIdx.x == 0) s_skip = prologue(a, s_sc, t);
   __syncthreads();
@@ -393,20 +320,9 @@ __global__ void __launch_bounds__(kQ8Threads, 1) step_q8_kernel(const StepArgs a
   }
 }
 
-template <typename K>
-cudaError_t occ(K kernel, int smem, int* bps) {
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, kernel, kThreads, smem);
-}
-
 template <typename GT>
 cudaError_t launch_mode(adamw_mode mode, const StepArgs& a, int grid, cudaStream_t st) {
   switch (mode) {
-    case ADAMW_MODE_FP32:
-      step_kernel<ADAMW_MODE_FP32, GT><<<grid, kThreads, 0, st>>>(a);
-      break;
-    case ADAMW_MODE_BF16_REM:
-      step_kernel<ADAMW_MODE_BF16_REM, GT><<<grid, kThreads, 0, st>>>(a);
-      break;
     case ADAMW_MODE_Q8:
       if (a.refine <= 1)
         step_q8_kernel<GT, 1><<<grid, kQ8Threads, kQ8Smem, st>>>(a);
@@ -424,12 +340,6 @@ cudaError_t launch_mode(adamw_mode mode, const StepArgs& a, int grid, cudaStream
 template <typename GT>
 cudaError_t occupancy_mode(adamw_mode mode, int* bps, int* smem) {
   switch (mode) {
-    case ADAMW_MODE_FP32:
-      *smem = 0;
-      return occ(step_kernel<ADAMW_MODE_FP32, GT>, 0, bps);
-    case ADAMW_MODE_BF16_REM:
-      *smem = 0;
-      return occ(step_kernel<ADAMW_MODE_BF16_REM, GT>, 0, bps);
     case ADAMW_MODE_Q8: {
       // the lane-private tables exceed the 48 KB default: raise the limit of
       // each refine variant (before any launch), then ask for the occupancy

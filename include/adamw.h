@@ -134,6 +134,12 @@ typedef struct adamw_plan adamw_plan;
  * whose pointers are all 16-byte aligned take the 128-bit vector path, the
  * rest a scalar path.  Synchronous (allocates device memory and copies).
  * On success *out owns the device tables until adamw_plan_destroy.
+ * An fp32 or bf16+remainder plan with exp_avg_sq, at most 16 non-empty
+ * tensors and few enough elements that one piece per SM (every tensor cut
+ * into pieces of equal length, a multiple of 8) fits in 216 KB of shared
+ * memory -- about two million elements -- is a small plan: adamw_step and
+ * adamw_step_amp then stage each piece whole in one CTA's shared memory, with
+ * the tensor table passed as kernel parameters.  Same results either way.
  */
 adamw_status adamw_plan_create(const adamw_tensor* tensors, int32_t n_tensors,
                                adamw_mode mode, adamw_dtype grad_dtype,
@@ -374,11 +380,14 @@ adamw_status adamw_coupled_step(adamw_plan* plan, adamw_coupled_rule rule, const
  * at 2 s and reported through adamw_plan_status), and then either all skip --
  * params, states and *step_dev untouched -- or all update, exactly as
  * adamw_check_nonfinite + adamw_step would.  *found_inf_dev (output) receives
- * 1.0f or 0.0f for the caller's loss-scale logic.  Meant for plans whose grads
- * stay in L2 between the scan and the update (the scan then costs one read of
- * the grads): plans of more than 6 Mi (6,291,456) elements run
- * adamw_check_nonfinite + adamw_step instead, with the same results and the
- * same *found_inf_dev, because past that size the two launches are faster.
+ * 1.0f or 0.0f for the caller's loss-scale logic.  On a small plan (see
+ * adamw_plan_create) each CTA scans the grads it has staged in shared memory,
+ * so they are read from HBM once, and computes its update in place before the
+ * vote; only the stores wait for it.  On larger plans the scan reads the grads
+ * and the update reads them again (from L2): plans of more than 6 Mi
+ * (6,291,456) elements run adamw_check_nonfinite + adamw_step instead, with
+ * the same results and the same *found_inf_dev, because past that size the
+ * two launches are faster.
  * Other arguments as adamw_step.  fp32 and bf16+remainder modes.
  */
 adamw_status adamw_step_amp(adamw_plan* plan, const float* lr_dev, int32_t* step_dev,

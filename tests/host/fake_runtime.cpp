@@ -59,6 +59,9 @@ cudaError_t record(const char* kind, int mode, int gdt, int grid, int algo,
   return cudaSuccess;
 }
 
+adamw::SmallArgs g_small{};     // kernel parameters of the last small-plan launch
+int g_small_smem = 0;
+
 // back = 0: the last launch, 1: the one before, ...
 const Launch& at(int back) { return g_hist[(g_count - 1 - back + 64 * kHist) % kHist]; }
 }  // namespace
@@ -122,6 +125,8 @@ const void* probe_blocks(int back) { return at(back).ma.blocks; }
 const void* probe_red_chunks(int back) { return at(back).ma.red_chunks; }
 int64_t probe_n_red(int back) { return at(back).ma.n_red; }
 int probe_refine(int back) { return at(back).a.refine; }
+const void* probe_small_args(void) { return &g_small; }
+int probe_small_smem(void) { return g_small_smem; }
 }
 
 // ---------------------------------------------------------------- launchers
@@ -181,6 +186,13 @@ cudaError_t fused_occupancy(adamw_mode, adamw_dtype, int* bps) {
 cudaError_t launch_step_fused_amp(adamw_mode mode, adamw_dtype gdt, const StepArgs& a, int grid,
                                   float*, cudaStream_t) {
   return record("fused_amp", mode, gdt, grid, -1, &a, nullptr, 0);
+}
+cudaError_t prepare_step_small(adamw_mode, adamw_dtype, int, int) { return cudaSuccess; }
+cudaError_t launch_step_small(adamw_mode mode, adamw_dtype gdt, const SmallArgs& a, int grid,
+                              int smem, bool fused, float*, cudaStream_t) {
+  g_small = a;
+  g_small_smem = smem;
+  return record(fused ? "small_fused" : "small", mode, gdt, grid, -1, nullptr, nullptr, 0);
 }
 cudaError_t launch_lr_from_table(const float*, int32_t n, const int32_t*, float*, cudaStream_t) {
   return record("lr_table", -1, -1, 1, -1, nullptr, nullptr, n);

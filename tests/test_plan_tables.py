@@ -88,6 +88,8 @@ def lib(tmp_path_factory):
         "probe_red_chunks": (_vp, [ctypes.c_int]),
         "probe_n_red": (ctypes.c_int64, [ctypes.c_int]),
         "probe_set_sms": (None, [ctypes.c_int]),
+        "probe_small_args": (_vp, []),
+        "probe_small_smem": (ctypes.c_int, []),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -209,7 +211,9 @@ def test_chunk_size_limits(lib):
         plan = _create(lib, _records(sizes, C.MODE_FP32, fake), C.MODE_FP32, C.F32)
         try:
             lr, step = _scalars(fake)
-            assert lib.adamw_step(plan, lr, step, 0.9, 0.999, 1e-8, None, None, None) == C.OK
+            # momentum walks the plan's chunk table whatever the plan's size
+            assert lib.adamw_coupled_step(plan, C.RULES["momentum"], lr, step, 0.9, 1e-8, None,
+                                          None, None) == C.OK
             chunks = _read(lib.probe_chunks(0), CHUNK, lib.probe_n_chunks(0))
             assert chunks[0]["len"] == min(want, sizes[0]), sizes
             _check_cover(chunks, sizes, want)
@@ -279,7 +283,7 @@ def test_adam_mini_chunks_stay_inside_blocks(lib):
 
 def test_fused_amp_table_and_threshold(lib):
     fake = Fake()
-    for sizes, fused in (([1 << 20, 4097], True), ([7 << 20], False)):
+    for sizes, fused in (([3 << 20, 4097], True), ([7 << 20], False)):
         plan = _create(lib, _records(sizes, C.MODE_FP32, fake), C.MODE_FP32, C.F16)
         try:
             lr, step = _scalars(fake)
@@ -350,8 +354,9 @@ def test_rule_launches_and_empty_plans(lib):
         assert lib.probe_kind(0).decode() == "bulk" and lib.probe_algo(0) == 1
         tds = _read(lib.probe_tensors(0), TDESC, 2)
         assert [int(t["m2"]) for t in tds] == [r.exp_avg_slow for r in recs]
+        # the same plan's AdamW step: a small plan, staged whole in shared memory
         assert lib.adamw_step(plan, lr, step, 0.9, 0.999, 1e-8, None, None, None) == C.OK
-        assert lib.probe_algo(0) == 0
+        assert lib.probe_kind(0).decode() == "small"
     finally:
         lib.adamw_plan_destroy(plan)
     # Lion on a 1-state plan: rule 2, one CTA per SM
@@ -370,5 +375,83 @@ def test_rule_launches_and_empty_plans(lib):
         try:
             assert lib.adamw_step(plan, lr, step, 0.9, 0.999, 1e-8, None, None, None) == C.OK
             assert lib.probe_n_chunks(0) == 0 and lib.probe_grid(0) == 1, mode
+        finally:
+            lib.adamw_plan_destroy(plan)
+
+
+SMALLT = np.dtype([("p", "<u8"), ("rem", "<u8"), ("g", "<u8"), ("m", "<u8"), ("v", "<u8"),
+                   ("numel", "<i8"), ("wd", "<f4"), ("first_item", "<i4"), ("piece", "<i4"),
+                   ("vec_ok", "<i4")], align=True)
+
+
+def _small_args(lib):
+    raw = _read(lib.probe_small_args(), np.dtype("u1"), 56 + 16 * SMALLT.itemsize).tobytes()
+    n_tensors = int(np.frombuffer(raw[52:56], "<i4")[0])
+    return n_tensors, np.frombuffer(raw[56:], SMALLT)[:n_tensors]
+
+
+@pytest.mark.parametrize("mode,gdt,sizes", [
+    (C.MODE_FP32, C.F32, [1 << 20]),
+    (C.MODE_FP32, C.F16, [1 << 20, 4097]),
+    (C.MODE_BF16_REM, C.BF16, [1000]),
+    (C.MODE_FP32, C.BF16, [1, 3, 8, 9, 255, 256, 257, 2047, 2048, 2049, 8191, 8192, 8193, 50001, 0, 7]),
+    (C.MODE_FP32, C.F32, [152 * 1000]),
+])
+def test_small_plans_stage_whole_pieces(lib, mode, gdt, sizes):
+    """A small plan: every non-empty tensor in pieces of one length (a multiple of 8,
+    at least 256), pieces numbered tensor by tensor, one CTA each, at most one per SM,
+    and each CTA's 32 warp slices of one piece within 216 KB of shared memory; both
+    adamw_step launches it, and adamw_step_amp its fused variant when every tensor is
+    16-byte aligned."""
+    fake = Fake()
+    recs = _records(sizes, mode, fake, misalign=(1,) if len(sizes) > 2 else ())
+    plan = _create(lib, recs, mode, gdt)
+    try:
+        lr, step = _scalars(fake)
+        assert lib.adamw_step(plan, lr, step, 0.9, 0.999, 1e-8, None, None, None) == C.OK
+        assert lib.probe_kind(0).decode() == "small"
+        grid = lib.probe_grid(0)
+        n, t = _small_args(lib)
+        live = [(i, r) for i, r in enumerate(recs) if r.numel > 0]
+        assert n == len(live)
+        piece = int(t[0]["piece"])
+        assert piece % 8 == 0 and piece >= 256 and all(int(x["piece"]) == piece for x in t)
+        first = 0
+        for (i, r), x in zip(live, t):
+            assert x["numel"] == r.numel and x["p"] == r.param and x["g"] == r.grad, i
+            assert x["m"] == r.exp_avg and x["v"] == r.exp_avg_sq and x["rem"] == (r.param_rem or 0), i
+            assert x["wd"] == np.float32(r.weight_decay) and x["first_item"] == first, i
+            assert x["vec_ok"] == (0 if (len(sizes) > 2 and i == 1) else 1), i
+            first += -(-r.numel // piece)
+        assert grid == first <= SMS
+        per_elem = (4 if mode == C.MODE_FP32 else 4) + (2 if gdt != C.F32 else 4) + 8
+        slice_ = -(-(piece // 8 * 8) // (32 * 8)) * 8          # 32 warps, slices of 8k elements
+        assert lib.probe_small_smem() == max(16, 32 * slice_ * per_elem) <= 216 * 1024
+        b = ctypes.c_int32()
+        g = ctypes.c_int32()
+        assert lib.adamw_plan_info(plan, None, None, ctypes.byref(g), ctypes.byref(b)) == C.OK
+        assert (g.value, b.value) == (grid, 1024)
+        found = fake(4)
+        assert lib.adamw_step_amp(plan, lr, step, 0.9, 0.999, 1e-8, fake(4), found, None) == C.OK
+        if len(sizes) > 2:
+            # a tensor off the 16-byte grid: the fused check + step takes the chunked path
+            assert lib.probe_kind(0).decode() == "fused_amp"
+        else:
+            # the fused variant stages its results beside the originals
+            assert lib.probe_kind(0).decode() == "small_fused" and lib.probe_grid(0) == grid
+            extra = (4 if mode == C.MODE_FP32 else 4) + 8
+            assert lib.probe_small_smem() == max(16, 32 * slice_ * (per_elem + extra)) <= 216 * 1024
+    finally:
+        lib.adamw_plan_destroy(plan)
+
+
+def test_plans_beyond_the_shared_memory_size_stay_on_the_bulk_path(lib):
+    fake = Fake()
+    for sizes, mode, gdt in (([3 << 20], C.MODE_FP32, C.F32), ([1 << 20] * 17, C.MODE_FP32, C.F32)):
+        plan = _create(lib, _records(sizes, mode, fake), mode, gdt)
+        try:
+            lr, step = _scalars(fake)
+            assert lib.adamw_step(plan, lr, step, 0.9, 0.999, 1e-8, None, None, None) == C.OK
+            assert lib.probe_kind(0).decode() == "bulk", sizes
         finally:
             lib.adamw_plan_destroy(plan)
