@@ -72,8 +72,9 @@ __device__ __forceinline__ uint32_t pack_nibbles(const uint32_t (&q)[8]) {
   return w;
 }
 
-template <typename GT, int R>
+template <typename GT, int R, bool SCALED>
 __global__ void __launch_bounds__(kThreads, kQ4MinBlocks) step_q4_kernel(const StepArgs a) {
+  constexpr int kSc = SCALED ? 1 : 0;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   QTables& qt = *reinterpret_cast<QTables*>(smem_raw);
   __shared__ Scal s_sc;
@@ -125,9 +126,11 @@ __global__ void __launch_bounds__(kThreads, kQ4MinBlocks) step_q4_kernel(const S
         for (int i = 0; i < 8; ++i) {
           m[i] = __fmul_rn(qt.map[0].value[(wm >> (4 * i)) & 0xFu], am);
           v[i] = __fmul_rn(qt.map[1].value[(wv >> (4 * i)) & 0xFu], av);
-          update(p[i], gr[i], m[i], v[i], s, decay);
+          update<kSc>(p[i], gr[i], m[i], v[i], s, decay);
           mx_m = max(mx_m, __float_as_uint(m[i]) & 0x7FFFFFFFu);
-          mx_v = max(mx_v, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+          // v' is never negative and never -0 (its NaN is the canonical,
+          // positive one): its bits need no sign mask
+          mx_v = max(mx_v, __float_as_uint(v[i]));
         }
         st8f(pf + e, p);
         const BlockNorm nm = block_norm(half_warp_max(mx_m));
@@ -156,7 +159,7 @@ __global__ void __launch_bounds__(kThreads, kQ4MinBlocks) step_q4_kernel(const S
             float pi = pf[e + i];
             m[i] = __fmul_rn(qt.map[0].value[(codes(tdp->m)[(e + i) / 2] >> sh) & 0xFu], am);
             v[i] = __fmul_rn(qt.map[1].value[(codes(tdp->v)[(e + i) / 2] >> sh) & 0xFu], av);
-            update(pi, Grad<GT>::load1(td.g, e + i), m[i], v[i], s, decay);
+            update<kSc>(pi, Grad<GT>::load1(td.g, e + i), m[i], v[i], s, decay);
             pf[e + i] = pi;
             mx_m = max(mx_m, __float_as_uint(m[i]) & 0x7FFFFFFFu);
             mx_v = max(mx_v, __float_as_uint(v[i]) & 0x7FFFFFFFu);
@@ -183,15 +186,21 @@ __global__ void __launch_bounds__(kThreads, kQ4MinBlocks) step_q4_kernel(const S
   }
 }
 
+template <typename GT, bool SCALED>
+cudaError_t launch_q4_scaled(const StepArgs& a, int grid, cudaStream_t st) {
+  if (a.refine <= 1)
+    step_q4_kernel<GT, 1, SCALED><<<grid, kThreads, sizeof(QTables), st>>>(a);
+  else if (a.refine <= 2)
+    step_q4_kernel<GT, 2, SCALED><<<grid, kThreads, sizeof(QTables), st>>>(a);
+  else
+    step_q4_kernel<GT, kMaxRefine, SCALED><<<grid, kThreads, sizeof(QTables), st>>>(a);
+  return cudaGetLastError();
+}
+
 template <typename GT>
 cudaError_t launch_q4(const StepArgs& a, int grid, cudaStream_t st) {
-  if (a.refine <= 1)
-    step_q4_kernel<GT, 1><<<grid, kThreads, sizeof(QTables), st>>>(a);
-  else if (a.refine <= 2)
-    step_q4_kernel<GT, 2><<<grid, kThreads, sizeof(QTables), st>>>(a);
-  else
-    step_q4_kernel<GT, kMaxRefine><<<grid, kThreads, sizeof(QTables), st>>>(a);
-  return cudaGetLastError();
+  return a.grad_scale != nullptr ? launch_q4_scaled<GT, true>(a, grid, st)
+                                 : launch_q4_scaled<GT, false>(a, grid, st);
 }
 
 }  // namespace
@@ -209,14 +218,14 @@ cudaError_t q4_occupancy(adamw_dtype gdt, int* bps, int* smem) {
   *smem = static_cast<int>(sizeof(QTables));
   switch (gdt) {
     case ADAMW_F32:
-      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, step_q4_kernel<float, kMaxRefine>,
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, step_q4_kernel<float, kMaxRefine, false>,
                                                            kThreads, *smem);
     case ADAMW_F16:
-      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, step_q4_kernel<__half, kMaxRefine>,
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, step_q4_kernel<__half, kMaxRefine, false>,
                                                            kThreads, *smem);
     case ADAMW_BF16:
       return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-          bps, step_q4_kernel<__nv_bfloat16, kMaxRefine>, kThreads, *smem);
+          bps, step_q4_kernel<__nv_bfloat16, kMaxRefine, false>, kThreads, *smem);
   }
   return cudaErrorInvalidValue;
 }

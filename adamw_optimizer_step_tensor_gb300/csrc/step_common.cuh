@@ -193,9 +193,12 @@ __device__ int amp_grid_vote(StepScratch* sc, bool bad, float* found_inf_out) {
   return amp_await(sc, amp_publish(sc, bad), found_inf_out);
 }
 
+// SC: 1 when the grads carry a loss scale, 0 when they do not, -1 to ask
+// s.scaled at run time.
+template <int SC = -1>
 __device__ __forceinline__ void update(float& p, float g, float& m, float& v, const Scal& s,
                                        float decay) {
-  if (s.scaled) g = __fmul_rn(g, s.inv_scale);
+  if (SC == 1 || (SC < 0 && s.scaled)) g = __fmul_rn(g, s.inv_scale);
   m = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
   v = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, __fmul_rn(g, g)));
   const float h = __fadd_rn(__fmul_rn(__fsqrt_rn(v), s.inv_sqrt_bc2), s.eps);

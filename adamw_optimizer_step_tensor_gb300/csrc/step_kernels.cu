@@ -216,8 +216,9 @@ __device__ __forceinline__ uint8_t* codes_v(const TensorDesc* td) {
   return static_cast<uint8_t*>(td->v);
 }
 
-template <typename GT, int R>
+template <typename GT, int R, bool SCALED>
 __global__ void __launch_bounds__(kQ8Threads, 1) step_q8_kernel(const StepArgs a) {
+  constexpr int kSc = SCALED ? 1 : 0;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   LaneTables<256>& lt = *reinterpret_cast<LaneTables<256>*>(smem_raw);
   __shared__ Scal s_sc;
@@ -265,9 +266,11 @@ __global__ void __launch_bounds__(kQ8Threads, 1) step_q8_kernel(const StepArgs a
           const int sh = (i & 3) * 8;
           m[i] = __fmul_rn(lt.value[0][(wm >> sh) & 0xFFu][lane], am);
           v[i] = __fmul_rn(lt.value[1][(wv >> sh) & 0xFFu][lane], av);
-          update(p[i], gr[i], m[i], v[i], s, decay);
+          update<kSc>(p[i], gr[i], m[i], v[i], s, decay);
           mx_m = max(mx_m, __float_as_uint(m[i]) & 0x7FFFFFFFu);
-          mx_v = max(mx_v, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+          // v' = b2*v + (1-b2)*g*g is never negative and never -0 (its NaN
+          // is the canonical, positive one): its bits need no sign mask
+          mx_v = max(mx_v, __float_as_uint(v[i]));
         }
         // store each result as soon as it is final: short live ranges keep the
         // kernel within its 64 registers
@@ -294,7 +297,7 @@ __global__ void __launch_bounds__(kQ8Threads, 1) step_q8_kernel(const StepArgs a
             gr[i] = Grad<GT>::load1(td.g, e + i);
             m[i] = __fmul_rn(lt.value[0][codes_m(tdp)[e + i]][lane], am);
             v[i] = __fmul_rn(lt.value[1][codes_v(tdp)[e + i]][lane], av);
-            update(p[i], gr[i], m[i], v[i], s, decay);
+            update<kSc>(p[i], gr[i], m[i], v[i], s, decay);
             mx_m = max(mx_m, __float_as_uint(m[i]) & 0x7FFFFFFFu);
             mx_v = max(mx_v, __float_as_uint(v[i]) & 0x7FFFFFFFu);
           }
@@ -320,17 +323,36 @@ __global__ void __launch_bounds__(kQ8Threads, 1) step_q8_kernel(const StepArgs a
   }
 }
 
+template <typename GT, bool SCALED>
+cudaError_t launch_q8(const StepArgs& a, int grid, cudaStream_t st) {
+  if (a.refine <= 1)
+    step_q8_kernel<GT, 1, SCALED><<<grid, kQ8Threads, kQ8Smem, st>>>(a);
+  else if (a.refine <= 2)
+    step_q8_kernel<GT, 2, SCALED><<<grid, kQ8Threads, kQ8Smem, st>>>(a);
+  else
+    step_q8_kernel<GT, kMaxRefine, SCALED><<<grid, kQ8Threads, kQ8Smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename GT, bool SCALED>
+cudaError_t q8_smem_limits() {
+  cudaError_t e = cudaFuncSetAttribute(step_q8_kernel<GT, 1, SCALED>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kQ8Smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(step_q8_kernel<GT, 2, SCALED>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kQ8Smem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(step_q8_kernel<GT, kMaxRefine, SCALED>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, kQ8Smem);
+  return e;
+}
+
 template <typename GT>
 cudaError_t launch_mode(adamw_mode mode, const StepArgs& a, int grid, cudaStream_t st) {
   switch (mode) {
     case ADAMW_MODE_Q8:
-      if (a.refine <= 1)
-        step_q8_kernel<GT, 1><<<grid, kQ8Threads, kQ8Smem, st>>>(a);
-      else if (a.refine <= 2)
-        step_q8_kernel<GT, 2><<<grid, kQ8Threads, kQ8Smem, st>>>(a);
-      else
-        step_q8_kernel<GT, kMaxRefine><<<grid, kQ8Threads, kQ8Smem, st>>>(a);
-      break;
+      if (a.grad_scale != nullptr) return launch_q8<GT, true>(a, grid, st);
+      return launch_q8<GT, false>(a, grid, st);
     default:
       return cudaErrorInvalidValue;
   }
@@ -342,19 +364,13 @@ cudaError_t occupancy_mode(adamw_mode mode, int* bps, int* smem) {
   switch (mode) {
     case ADAMW_MODE_Q8: {
       // the lane-private tables exceed the 48 KB default: raise the limit of
-      // each refine variant (before any launch), then ask for the occupancy
+      // each variant (before any launch), then ask for the occupancy
       *smem = kQ8Smem;
-      cudaError_t e = cudaFuncSetAttribute(step_q8_kernel<GT, 1>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, kQ8Smem);
-      if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(step_q8_kernel<GT, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kQ8Smem);
-      if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(step_q8_kernel<GT, kMaxRefine>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kQ8Smem);
+      cudaError_t e = q8_smem_limits<GT, false>();
+      if (e == cudaSuccess) e = q8_smem_limits<GT, true>();
       if (e != cudaSuccess) return e;
-      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(bps, step_q8_kernel<GT, kMaxRefine>,
-                                                           kQ8Threads, kQ8Smem);
+      return cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+          bps, step_q8_kernel<GT, kMaxRefine, false>, kQ8Threads, kQ8Smem);
     }
     default:
       return cudaErrorInvalidValue;
