@@ -88,3 +88,42 @@ def test_bf16rem_step_bitexact(gdtype):
             assert bits_equal(host(m), o.m), f"tensor {i} m: {first_mismatch(host(m), o.m)}"
             assert bits_equal(host(v), o.v), f"tensor {i} v: {first_mismatch(host(v), o.v)}"
     assert int(step.item()) == 5
+
+
+def test_bf16rem_bulk_path_with_twenty_tensors():
+    """20 tensors (more than a small plan takes): the bulk-staged kernel, bit-exact."""
+    import synth
+    rng = np.random.default_rng(17)
+    sizes = SIZES + [16385, 3, 40000, 1 << 15, 255, 8200, 1, 999, 4096, 12345]
+    his, rems, ms, vs, gs, oracle = [], [], [], [], [], []
+    for i, n in enumerate(sizes):
+        hi_t, rem_t = synth.bf16_params_with_remainders(n, 0.02, seed=200 + i, device="cpu")
+        hi_bits = hi_t.view(torch.int16).numpy().view(np.uint16).copy()
+        rem_np = rem_t.numpy().copy()
+        his.append(to_dev(hi_t))
+        rems.append(to_dev(rem_t))
+        m = rng.normal(0, 1e-4, n).astype(np.float32)
+        v = (rng.normal(0, 1e-4, n) ** 2).astype(np.float32)
+        ms.append(dev(m))
+        vs.append(dev(v))
+        gs.append(empty(n, torch.bfloat16))
+        oracle.append(OA.Tensor(p=OR.join(hi_bits, rem_np), g=None, m=m.copy(), v=v.copy(),
+                                wd=f32(0.1)))
+    opt = FusedAdamW(his, gs, ms, vs, [f32(0.1)] * len(sizes), mode="bf16_rem", param_rems=rems)
+    assert opt.info()["block_threads"] == 544
+    lr, step = scalar_f32(f32(3e-4)), scalar_i32(0)
+    for t in range(1, 4):
+        for g, o in zip(gs, oracle):
+            tg, wide = grads_of(rng.normal(0, 1e-4, g.numel()).astype(np.float32), torch.bfloat16)
+            g.copy_(tg)
+            o.g = wide
+        opt.step(lr, step, betas=(B1, B2), eps=EPS)
+        OA.step_f32(oracle, lr=f32(3e-4), beta1=B1, beta2=B2, eps=EPS, t=t)
+        torch.cuda.synchronize()
+        assert_guards_intact()
+        for i, (h, r, m, v, o) in enumerate(zip(his, rems, ms, vs, oracle)):
+            ohi, orem = OR.split(o.p)
+            assert np.array_equal(host(h).view(np.uint16), ohi), f"tensor {i} bf16 step {t}"
+            assert np.array_equal(host(r), orem), f"tensor {i} rem step {t}"
+            assert bits_equal(host(m), o.m), f"tensor {i} m"
+            assert bits_equal(host(v), o.v), f"tensor {i} v"

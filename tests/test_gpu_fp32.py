@@ -218,3 +218,44 @@ def test_nonfinite_check_flags_each_kind():
             opt.check_nonfinite(found)
             torch.cuda.synchronize()
             assert found.item() == 1.0
+
+
+# More tensors than a small plan takes (16): the bulk-staged kernel, with
+# ragged tails, partial tiles and tensors off the 16-byte grid.
+BULK_SIZES = [1, 3, 8, 9, 255, 256, 257, 2047, 2048, 2049, 8191, 8192, 8193, 50001, 0, 7,
+              16383, 16385, 40000, 1 << 16]
+
+
+@pytest.mark.parametrize("gdtype", [torch.float32, torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("misalign", [False, True])
+def test_bulk_path_ragged_list_all_grad_dtypes(gdtype, misalign):
+    wds = [f32(0.1) if i % 3 else 0.0 for i in range(len(BULK_SIZES))]
+    opt, ps, gs, ms, vs, oracle, rng = _make(BULK_SIZES, wds, gdtype, seed=8, misalign=misalign,
+                                            zero_state=False)
+    info = opt.info()
+    assert info["block_threads"] == 544          # the bulk kernel: 16 consumer warps + 1 producer
+    lr, step = scalar_f32(f32(0.02)), scalar_i32(0)
+    for t in range(1, 4):
+        _new_grads(gs, oracle, rng)
+        opt.step(lr, step, betas=(B1, B2), eps=EPS)
+        OA.step_f32(oracle, lr=f32(0.02), beta1=B1, beta2=B2, eps=EPS, t=t)
+        torch.cuda.synchronize()
+        _check(ps, ms, vs, oracle)
+    assert int(step.item()) == 3
+
+
+def test_small_path_is_taken_and_bitexact_at_the_size_limit():
+    """A plan just inside the small path's size (one piece per SM within its shared
+    memory) and one just outside it give the oracle's bits either way."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for n, threads in ((sms * 12_000, 1024), (sms * 15_000, 544)):
+        opt, ps, gs, ms, vs, oracle, rng = _make([n, 77], [f32(0.1), 0.0], torch.float32, seed=9,
+                                                zero_state=False)
+        assert opt.info()["block_threads"] == threads, n
+        lr, step = scalar_f32(f32(0.01)), scalar_i32(0)
+        for t in range(1, 3):
+            _new_grads(gs, oracle, rng)
+            opt.step(lr, step, betas=(B1, B2), eps=EPS)
+            OA.step_f32(oracle, lr=f32(0.01), beta1=B1, beta2=B2, eps=EPS, t=t)
+        torch.cuda.synchronize()
+        _check(ps, ms, vs, oracle)
