@@ -424,8 +424,12 @@ static adamw_status create_plan(const adamw_tensor* tensors, int32_t n_tensors, 
     p->mini = true;
     p->n_blocks = static_cast<int64_t>(blocks.size());
     p->n_red = static_cast<int64_t>(red_chunks.size());
-    const int64_t red_res = 32LL * sms;   // several waves: the grid-stride tail balances
-    p->grid_red = static_cast<int>(p->n_red < 1 ? 1 : (p->n_red < red_res ? p->n_red : red_res));
+    // one reduction chunk per warp, the CTAs left to the hardware scheduler
+    // (it balances the tail better than a resident grid walking the chunks:
+    // 25.8 against 26.7 ms on the Llama-3-8B Adam-mini step)
+    const int64_t red_ctas = (p->n_red + kRedWarps - 1) / kRedWarps;
+    const int64_t red_max = 0x7FFFFFFF;   // beyond it the kernel's warps stride
+    p->grid_red = static_cast<int>(red_ctas < 1 ? 1 : (red_ctas < red_max ? red_ctas : red_max));
     if ((e = prepare_step_bulk(mode, grad_dtype, kAlgoMini)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(Adam-mini step)");
     const size_t nb = blocks.size(), nc = chunks.size(), nr = red_chunks.size();

@@ -33,6 +33,8 @@ constexpr int kBulkConsumers = 2 * kThreads;
 constexpr int kBulkThreads = kBulkConsumers + 32;
 // The 8-bit step runs one CTA of kQ8Threads per SM (64 registers a thread):
 // its lane-private code tables (lane_tables.cuh, 141.7 KB) fit once per SM.
+// The Adam-mini reduction: one chunk per warp, kRedWarps warps per CTA.
+constexpr int kRedWarps = 8;
 constexpr int kQ8Threads = 1024;
 constexpr int kQ8Pass = kQ8Threads * kVec;   // 8192 elements per CTA pass
 constexpr int kQBlock = ADAMW_Q8_BLOCK;      // 256

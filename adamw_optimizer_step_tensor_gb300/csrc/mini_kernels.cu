@@ -8,24 +8,28 @@
 // element update is the bulk-staged step kernel (kAlgoMini), launched next on
 // the same stream.
 //
-// Chunks never straddle blocks.  Each CTA sums g*g over one chunk: every
-// thread keeps its sum as an unevaluated pair of float32 (s, c) -- each square
-// split exactly into x*x = p + e with one fma, each addition into s made
-// error-free with TwoSum, the errors gathered in c (Ogita, Rump and Oishi,
-// "Accurate sum and dot product", 2005: relative error about (n*2^-24)^2 for
-// the n = 64 squares of a thread, with no float64 operation per element,
-// which GB300 runs at a small fraction of its float32 rate) -- the pairs are added in float64 in a fixed
-// tree, and the chunk's sum is stored.  A block of one chunk is
-// finalised by that CTA; otherwise the CTA that completes the block's arrival
-// count adds the block's chunk sums (float64, each thread a fixed stride of
-// them, then the fixed tree) and finalises it, then clears the count for the
-// next step.  Nothing waits on another CTA.
+// Chunks never straddle blocks.  Each warp sums g*g over one chunk on its
+// own -- no CTA barrier inside the walk, so a warp whose loads are back never
+// waits for the others -- with kRedLoads loads of 8 grads per lane in flight.
+// Every lane keeps its sum as an unevaluated pair of float32 (s, c): each
+// square split exactly into x*x = p + e with one fma, each addition into s
+// made error-free with TwoSum, the errors gathered in c (Ogita, Rump and
+// Oishi, "Accurate sum and dot product", 2005: relative error about
+// (n*2^-24)^2 for the n <= 512 squares of a lane, with no float64 operation
+// per element, which GB300 runs at a small fraction of its float32 rate).
+// The lanes' pairs meet in a fixed xor tree of error-free pair additions and
+// the chunk's sum is s + c in float64.  A block of one chunk is finalised by
+// that warp; otherwise the warp whose arrival completes the block's count adds
+// the block's chunk sums (float64, each lane a fixed stride of them, then a
+// fixed xor tree), finalises the block and clears the count for the next
+// step.  Nothing waits on another warp.
 #include "step_common.cuh"
 
 namespace adamw {
 namespace {
 
-constexpr int kRedThreads = 256;
+constexpr int kRedThreads = kRedWarps * 32;
+constexpr int kRedLoads = 4;   // 8-grad loads in flight per lane
 
 // (s, c) += x*x: TwoProduct of the square by fma, TwoSum of the addition.
 __device__ __forceinline__ void add_square(float& s, float& c, float x) {
@@ -39,7 +43,9 @@ __device__ __forceinline__ void add_square(float& s, float& c, float x) {
 }
 
 // (s, c) += (s2, c2) for two error-free pairs: TwoSum of the leading parts,
-// the rounding error joins the trailing parts.
+// the rounding error joins the trailing parts.  The result does not depend on
+// the order of the operands, so every lane of an xor tree ends with the same
+// pair.
 __device__ __forceinline__ void add_pair(float& s, float& c, float s2, float c2) {
   const float t = __fadd_rn(s, s2);
   const float bp = __fsub_rn(t, s);
@@ -48,41 +54,57 @@ __device__ __forceinline__ void add_pair(float& s, float& c, float s2, float c2)
   c = __fadd_rn(__fadd_rn(c, c2), err);
 }
 
-// The sum over the CTA of one pair per thread, in a fixed order (xor tree of
-// pairs in each warp, then the warps' pairs in float64 in order).  The result
-// is valid in thread 0.  Float64 work stays at 16 additions per CTA: GB300
-// issues float64 at a small fraction of its float32 rate.
-__device__ __forceinline__ double cta_pair_sum(float s, float c, float2* s_pair) {
+// 8 consecutive raw grads of one lane, kept as loaded (16-bit grads stay
+// packed until they are squared).
+template <typename GT>
+struct RawGrads {
+  uint4 w[sizeof(GT) == 4 ? 2 : 1];
+};
+
+template <typename GT>
+__device__ __forceinline__ void load_raw(const void* g, int64_t e, int n, bool vec,
+                                         RawGrads<GT>& r) {
+  if (vec && n == kVec) {
+    const uint4* q = reinterpret_cast<const uint4*>(static_cast<const unsigned char*>(g) +
+                                                    e * static_cast<int64_t>(sizeof(GT)));
+    r.w[0] = __ldcs(q);
+    if constexpr (sizeof(GT) == 4) r.w[1] = __ldcs(q + 1);
+  } else {
+    uint32_t b[8];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1)
-    add_pair(s, c, __shfl_xor_sync(0xFFFFFFFFu, s, o), __shfl_xor_sync(0xFFFFFFFFu, c, o));
-  if ((threadIdx.x & 31) == 0) s_pair[threadIdx.x >> 5] = make_float2(s, c);
-  __syncthreads();
-  double total = 0.0;
-  if (threadIdx.x == 0) {
-#pragma unroll
-    for (int w = 0; w < kRedThreads / 32; ++w) {
-      total += static_cast<double>(s_pair[w].x);
-      total += static_cast<double>(s_pair[w].y);
+    for (int q = 0; q < 8; ++q) {
+      b[q] = 0u;   // +0 in every grad type: its square adds nothing
+      if (q < n) {
+        if constexpr (sizeof(GT) == 4)
+          b[q] = static_cast<const uint32_t*>(g)[e + q];
+        else
+          b[q] = static_cast<const uint16_t*>(g)[e + q];
+      }
+    }
+    if constexpr (sizeof(GT) == 4) {
+      r.w[0] = make_uint4(b[0], b[1], b[2], b[3]);
+      r.w[1] = make_uint4(b[4], b[5], b[6], b[7]);
+    } else {
+      r.w[0] = make_uint4(b[0] | b[1] << 16, b[2] | b[3] << 16, b[4] | b[5] << 16,
+                          b[6] | b[7] << 16);
     }
   }
-  __syncthreads();
-  return total;
 }
 
-// The float64 sum of one value per thread, in a fixed order; valid in thread 0.
-__device__ __forceinline__ double cta_sum(double x, double* s_warp) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
-  if ((threadIdx.x & 31) == 0) s_warp[threadIdx.x >> 5] = x;
-  __syncthreads();
-  double total = 0.0;
-  if (threadIdx.x == 0) {
-#pragma unroll
-    for (int w = 0; w < kRedThreads / 32; ++w) total += s_warp[w];
+// Grad q (0..7) of a group, widened exactly to float32.
+template <typename GT>
+__device__ __forceinline__ float raw_grad(const RawGrads<GT>& r, int q) {
+  if constexpr (sizeof(GT) == 4) {
+    const uint4 w = r.w[q >> 2];
+    const uint32_t x = (q & 3) == 0 ? w.x : (q & 3) == 1 ? w.y : (q & 3) == 2 ? w.z : w.w;
+    return __uint_as_float(x);
+  } else {
+    const uint4 w = r.w[0];
+    const uint32_t x = (q >> 1) == 0 ? w.x : (q >> 1) == 1 ? w.y : (q >> 1) == 2 ? w.z : w.w;
+    const uint32_t h = (q & 1) ? x >> 16 : x & 0xFFFFu;
+    if constexpr (std::is_same<GT, __half>::value) return f16_to_f32(h);
+    return bf16_to_f32(h);
   }
-  __syncthreads();
-  return total;
 }
 
 // v, h and r of one block from the float64 sum of g*g over it.
@@ -102,64 +124,72 @@ __global__ void __launch_bounds__(kRedThreads) mini_reduce_kernel(const StepArgs
                                                                   const MiniArgs ma) {
   __shared__ Scal s_sc;
   __shared__ int s_skip;
-  __shared__ double s_warp[kRedThreads / 32];
-  __shared__ float2 s_pair[kRedThreads / 32];
-  __shared__ int s_last;
   int t = 0;
   if (threadIdx.x == 0) s_skip = prologue(a, s_sc, t);
   __syncthreads();
   if (s_skip) return;
   const Scal s = s_sc;
+  const int lane = threadIdx.x & 31;
+  constexpr int kStride = 32 * kVec;   // elements between one lane's groups
+  const int64_t n_warps = static_cast<int64_t>(gridDim.x) * kRedWarps;
 
-  for (int64_t i = blockIdx.x; i < ma.n_red; i += gridDim.x) {
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kRedWarps + (threadIdx.x >> 5); i < ma.n_red;
+       i += n_warps) {
     const int64_t c = ma.red_chunks[i];
     const Chunk ch = a.chunks[c];
-    const TensorDesc td = a.tensors[ch.tensor];
+    const TensorDesc* const tdp = a.tensors + ch.tensor;
+    const void* const g = tdp->g;
+    const bool vec = tdp->vec_ok != 0;
     float sum = 0.0f, comp = 0.0f;
-    for (int off = threadIdx.x * kVec; off < ch.len; off += kRedThreads * kVec) {
-      const int64_t e = ch.start + off;
-      float g[8];
-      const int n = min(kVec, ch.len - off);
-      if (td.vec_ok && n == kVec) {
-        Grad<GT>::load8(td.g, e, g);
-      } else {
+    // lane l takes the groups of 8 at l*8, l*8 + 256, ...: each load of the
+    // warp covers 256 consecutive grads; the squares go in in element order
+    for (int off0 = lane * kVec; off0 < ch.len; off0 += kRedLoads * kStride) {
+      RawGrads<GT> r[kRedLoads];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) g[q] = q < n ? Grad<GT>::load1(td.g, e + q) : 0.0f;
+      for (int u = 0; u < kRedLoads; ++u) {
+        const int off = off0 + u * kStride;
+        load_raw<GT>(g, ch.start + off, max(0, min(kVec, ch.len - off)), vec, r[u]);
       }
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float x = s.scaled ? __fmul_rn(g[q], s.inv_scale) : g[q];
-        add_square(sum, comp, x);
-      }
-    }
-    const double d = cta_pair_sum(sum, comp, s_pair);
-    const int32_t b = a.chunk_blk[c];
-    const MiniBlock blk = ma.blocks[b];
-    if (blk.n_chunks == 1) {
-      if (threadIdx.x == 0) finalise(a, ma, b, d, s);
-    } else {
-      if (threadIdx.x == 0) {
-        ma.partial[c] = d;
-        __threadfence();
-        const uint32_t prev = atomicAdd(&ma.arrived[b], 1u);
-        s_last = prev == static_cast<uint32_t>(blk.n_chunks - 1);
-      }
-      __syncthreads();
-      if (s_last) {
-        // this CTA completed the block: add its chunk sums, each thread a
-        // fixed stride of them, then the fixed tree
-        __threadfence();
-        double part = 0.0;
-        for (int64_t k = threadIdx.x; k < blk.n_chunks; k += kRedThreads)
-          part += __ldcg(&ma.partial[blk.first_chunk + k]);
-        const double total = cta_sum(part, s_warp);
-        if (threadIdx.x == 0) {
-          finalise(a, ma, b, total, s);
-          ma.arrived[b] = 0u;
+      for (int u = 0; u < kRedLoads; ++u) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float x = raw_grad<GT>(r[u], q);
+          add_square(sum, comp, s.scaled ? __fmul_rn(x, s.inv_scale) : x);
         }
       }
     }
-    __syncthreads();
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      add_pair(sum, comp, __shfl_xor_sync(0xFFFFFFFFu, sum, o),
+               __shfl_xor_sync(0xFFFFFFFFu, comp, o));
+    const double d = static_cast<double>(sum) + static_cast<double>(comp);
+    const int32_t b = a.chunk_blk[c];
+    const MiniBlock blk = ma.blocks[b];
+    if (blk.n_chunks == 1) {
+      if (lane == 0) finalise(a, ma, b, d, s);
+      continue;
+    }
+    uint32_t last = 0u;
+    if (lane == 0) {
+      ma.partial[c] = d;
+      __threadfence();
+      last = atomicAdd(&ma.arrived[b], 1u) == static_cast<uint32_t>(blk.n_chunks - 1) ? 1u : 0u;
+    }
+    if (__shfl_sync(0xFFFFFFFFu, last, 0)) {
+      // this warp completed the block: add its chunk sums, each lane a fixed
+      // stride of them, then the fixed xor tree
+      __threadfence();
+      double part = 0.0;
+      for (int64_t k = lane; k < blk.n_chunks; k += 32)
+        part += __ldcg(&ma.partial[blk.first_chunk + k]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xFFFFFFFFu, part, o);
+      if (lane == 0) {
+        finalise(a, ma, b, part, s);
+        ma.arrived[b] = 0u;
+      }
+    }
   }
 }
 
