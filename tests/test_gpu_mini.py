@@ -3,7 +3,7 @@
 Against the strict-fp32 Adam-mini oracle on ragged lists mixing block
 lengths 1 (the AdamW branch), heads (several per tensor) and whole tensors,
 with blocks that fit one chunk and blocks spread over many chunks (summed by
-the last CTA to arrive), in the fp32 and bf16 + remainder modes, for
+the last warp to arrive), in the fp32 and bf16 + remainder modes, for
 fp32/fp16/bf16 grads.  The block means come from a float64 sum of exact
 squares in the oracle and from error-free float32 pairs on the GPU: they agree
 bit for bit except, rarely, by one ulp next to a rounding boundary, so v is
@@ -112,6 +112,28 @@ def test_mini_matches_oracle(mode, gdtype):
         torch.cuda.synchronize()
         _check(mode, dev_t, orc, lr_v, t, t)
     assert int(step.item()) == 3 and opt.status() == 0
+
+
+def test_mini_reduction_is_deterministic():
+    """Two copies of the same state and grads, stepped by two plans, agree bit
+    for bit over three steps: the block sums are added in a fixed order, not in
+    the order the warps of the reduction happen to arrive."""
+    runs = []
+    for _ in range(2):
+        opt, dev_t, orc, rng = _make("fp32", torch.bfloat16, seed=75)
+        lr, step = torch.tensor([f32(1e-3)], device="cuda"), zeros(1, torch.int32)
+        for _t in range(3):
+            for d in dev_t:
+                x, _ = grads_of(rng.normal(0, 1e-3, d["g"].numel()).astype(np.float32),
+                                torch.bfloat16)
+                d["g"].copy_(x)
+            opt.step_mini(lr, step, betas=(HP["beta1"], HP["beta2"]), eps=HP["eps"])
+        torch.cuda.synchronize()
+        runs.append([{k: host(d[k]) for k in ("p", "m", "v")} for d in dev_t])
+        del opt, dev_t
+    for i, (a, b) in enumerate(zip(*runs)):
+        for k in ("p", "m", "v"):
+            assert bits_equal(a[k], b[k]), (i, k)
 
 
 def test_mini_first_step_closed_form():
