@@ -227,6 +227,103 @@ def test_single_tensor_beyond_2e31_elements():
         _cleanup()
 
 
+def _blocks_beyond_2e31(n, block, rng):
+    """Whole blocks sampled at both ends of an n-element tensor, across element
+    2^31 and at random, sorted; the partial last block's index comes last."""
+    full = n // block
+    pivot = (1 << 31) // block
+    blocks = np.unique(np.concatenate([np.arange(0, 4), np.arange(pivot - 4, pivot + 4),
+                                       np.arange(full - 4, full), rng.integers(0, full, 16)]))
+    idx = np.concatenate([(blocks[:, None] * block + np.arange(block)[None, :]).ravel(),
+                          np.arange(full * block, n)]).astype(np.int64)
+    return np.concatenate([blocks, [full]]).astype(np.int64), idx
+
+
+def test_q8_tensor_beyond_2e31_elements():
+    """One fp32 tensor of 2^31 + 4097 elements with 8-bit m and v (bf16 grads): whole
+    blocks across element 2^31, at both ends and at random, plus the 1-element last
+    block, bit-exact over 3 steps."""
+    n = (1 << 31) + 4097
+    if _free_gib() < 30:
+        pytest.skip("needs ~25 GiB of free device memory")
+    from adamw_optimizer_step_tensor_gb300 import FusedAdamW
+    try:
+        rng = np.random.default_rng(63)
+        nb = (n + 255) // 256
+        w_p = synth.normal(n, 0.02, 64, "cuda")
+        w_g = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+        cm = torch.zeros(n, dtype=torch.uint8, device="cuda")
+        cv = torch.zeros(n, dtype=torch.uint8, device="cuda")
+        am, av = torch.zeros(nb, device="cuda"), torch.zeros(nb, device="cuda")
+        opt = FusedAdamW([w_p], [w_g], [cm], [cv], [OA.f32(0.01)], mode="q8",
+                         absmax_m=[am], absmax_v=[av])
+        bidx, idx = _blocks_beyond_2e31(n, 256, rng)
+        tb = torch.from_numpy(bidx).cuda()
+        p, ocm, ocv = _take(w_p, idx).cpu().numpy(), _take(cm, idx).cpu().numpy(), _take(cv, idx).cpu().numpy()
+        oam, oav = am[tb].cpu().numpy(), av[tb].cpu().numpy()
+        maps = OQ.Maps()
+        lr, step = torch.tensor([OA.f32(1e-3)], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+        for s in range(3):
+            w_g.copy_(synth.normal(n, 1e-3, 65 + s, "cuda", torch.bfloat16))
+            g = _take(w_g, idx).float().cpu().numpy()
+            opt.step(lr, step)
+            OQ.step_f32(p, g, ocm, ocv, oam, oav, lr=OA.f32(1e-3), beta1=OA.f32(0.9),
+                        beta2=OA.f32(0.999), eps=OA.f32(1e-8), wd=OA.f32(0.01), t=s + 1, maps=maps)
+        torch.cuda.synchronize()
+        assert np.array_equal(_take(w_p, idx).cpu().numpy().view(np.uint32), p.view(np.uint32))
+        assert np.array_equal(_take(cm, idx).cpu().numpy(), ocm)
+        assert np.array_equal(_take(cv, idx).cpu().numpy(), ocv)
+        assert np.array_equal(am[tb].cpu().numpy().view(np.uint32), oam.view(np.uint32))
+        assert np.array_equal(av[tb].cpu().numpy().view(np.uint32), oav.view(np.uint32))
+        assert int(step.item()) == 3 and opt.status() == 0
+    finally:
+        _cleanup()
+
+
+def test_q4_tensor_beyond_2e31_elements():
+    """One fp32 tensor of 2^31 + 4097 elements with 4-bit m and v (bf16 grads): whole
+    128-element blocks across element 2^31, at both ends and at random, plus the
+    1-element last block (a lone low nibble), bit-exact over 3 steps."""
+    from oracle import q4 as O4
+    n = (1 << 31) + 4097
+    if _free_gib() < 25:
+        pytest.skip("needs ~20 GiB of free device memory")
+    from adamw_optimizer_step_tensor_gb300 import FusedAdamW
+    try:
+        rng = np.random.default_rng(66)
+        nb = (n + 127) // 128
+        w_p = synth.normal(n, 0.02, 67, "cuda")
+        w_g = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+        cm = torch.zeros((n + 1) // 2, dtype=torch.uint8, device="cuda")
+        cv = torch.zeros((n + 1) // 2, dtype=torch.uint8, device="cuda")
+        am, av = torch.zeros(nb, device="cuda"), torch.zeros(nb, device="cuda")
+        opt = FusedAdamW([w_p], [w_g], [cm], [cv], [OA.f32(0.01)], mode="q4",
+                         absmax_m=[am], absmax_v=[av])
+        bidx, idx = _blocks_beyond_2e31(n, 128, rng)
+        tb = torch.from_numpy(bidx).cuda()
+        byte_idx = np.unique(idx // 2)   # whole blocks are 64 bytes; the last byte holds one code
+        p = _take(w_p, idx).cpu().numpy()
+        pm, pv = _take(cm, byte_idx).cpu().numpy(), _take(cv, byte_idx).cpu().numpy()
+        oam, oav = am[tb].cpu().numpy(), av[tb].cpu().numpy()
+        maps = O4.Maps4()
+        lr, step = torch.tensor([OA.f32(1e-3)], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+        for s in range(3):
+            w_g.copy_(synth.normal(n, 1e-3, 68 + s, "cuda", torch.bfloat16))
+            g = _take(w_g, idx).float().cpu().numpy()
+            opt.step(lr, step)
+            O4.step_f32(p, g, pm, pv, oam, oav, lr=OA.f32(1e-3), beta1=OA.f32(0.9),
+                        beta2=OA.f32(0.999), eps=OA.f32(1e-8), wd=OA.f32(0.01), t=s + 1, maps=maps)
+        torch.cuda.synchronize()
+        assert np.array_equal(_take(w_p, idx).cpu().numpy().view(np.uint32), p.view(np.uint32))
+        assert np.array_equal(_take(cm, byte_idx).cpu().numpy(), pm)
+        assert np.array_equal(_take(cv, byte_idx).cpu().numpy(), pv)
+        assert np.array_equal(am[tb].cpu().numpy().view(np.uint32), oam.view(np.uint32))
+        assert np.array_equal(av[tb].cpu().numpy().view(np.uint32), oav.view(np.uint32))
+        assert int(step.item()) == 3 and opt.status() == 0
+    finally:
+        _cleanup()
+
+
 def _elementwise_full_size(w, step_fn, make_orc, check, n_steps, seed):
     """Shared driver for the GPT-2-list variants: sampled windows of every tensor."""
     rng = np.random.default_rng(seed)
