@@ -227,6 +227,43 @@ def test_single_tensor_beyond_2e31_elements():
         _cleanup()
 
 
+def test_bf16rem_tensor_beyond_2e31_elements():
+    """One bf16 + int16-remainder tensor of 2^31 + 4097 elements (bf16 grads): windows
+    at both ends and across element 2^31, bit-exact over 3 steps."""
+    n = (1 << 31) + 4097
+    if _free_gib() < 45:
+        pytest.skip("needs ~40 GiB of free device memory")
+    from adamw_optimizer_step_tensor_gb300 import FusedAdamW
+    try:
+        hi, rem = synth.bf16_params_with_remainders(n, 0.02, 69, "cuda", n_zeros=64)
+        g = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+        m = torch.zeros(n, device="cuda")
+        v = torch.zeros(n, device="cuda")
+        opt = FusedAdamW([hi], [g], [m], [v], [OA.f32(0.1)], mode="bf16_rem", param_rems=[rem])
+        idx = np.concatenate([np.arange(0, 4096), np.arange((1 << 31) - 2048, (1 << 31) + 2048),
+                              np.arange(n - 4096, n)]).astype(np.int64)
+        orc = OA.Tensor(p=OR.join(_take(hi.view(torch.int16), idx).cpu().numpy().view(np.uint16),
+                                  _take(rem, idx).cpu().numpy()),
+                        g=None, m=np.zeros(idx.size, np.float32), v=np.zeros(idx.size, np.float32),
+                        wd=OA.f32(0.1))
+        lr, step = torch.tensor([OA.f32(3e-4)], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+        for s in range(3):
+            g.copy_(synth.normal(n, 1e-4, 70 + s, "cuda", torch.bfloat16))
+            orc.g = _take(g, idx).float().cpu().numpy()
+            opt.step(lr, step)
+            OA.step_f32([orc], lr=OA.f32(3e-4), beta1=OA.f32(0.9), beta2=OA.f32(0.999),
+                        eps=OA.f32(1e-8), t=s + 1)
+        torch.cuda.synchronize()
+        ohi, orem = OR.split(orc.p)
+        assert np.array_equal(_take(hi.view(torch.int16), idx).cpu().numpy().view(np.uint16), ohi)
+        assert np.array_equal(_take(rem, idx).cpu().numpy(), orem)
+        assert np.array_equal(_take(m, idx).cpu().numpy().view(np.uint32), orc.m.view(np.uint32))
+        assert np.array_equal(_take(v, idx).cpu().numpy().view(np.uint32), orc.v.view(np.uint32))
+        assert int(step.item()) == 3 and opt.status() == 0
+    finally:
+        _cleanup()
+
+
 def _blocks_beyond_2e31(n, block, rng):
     """Whole blocks sampled at both ends of an n-element tensor, across element
     2^31 and at random, sorted; the partial last block's index comes last."""
