@@ -99,26 +99,49 @@ def block_mean_sq(g32: np.ndarray, block: int) -> np.ndarray:
     return (np.sum(gb * gb, axis=1) / F64(block)).astype(F32)
 
 
+def block_sum_sq(g32: np.ndarray) -> np.float64:
+    """The float64 sum of the exact squares of some float32 values.  The order
+    of a block's sum is free, so a block too large to hold at once is summed
+    piece by piece: S_b = the float64 sum of its pieces' block_sum_sq."""
+    x = np.asarray(g32, dtype=F32).astype(F64)
+    return F64(np.sum(x * x))
+
+
+def mean_from_sum(s_b: np.float64, length: int) -> np.float32:
+    """mean_b = fl32(S_b / block length)."""
+    return F32(F64(s_b) / F64(length))
+
+
 def step_f32(tensors: list[Tensor], *, lr, beta1, beta2, eps, t: int,
-             grad_scale=None) -> bool:
-    """One strict-fp32 Adam-mini step, in place (float32 p, m, v)."""
+             grad_scale=None, means: list | None = None) -> bool:
+    """One strict-fp32 Adam-mini step, in place (float32 p, m, v).
+
+    ``means`` (optional, per tensor: None or float32 block means from
+    ``mean_from_sum``) stands in for the block means of ``x.g``: it lets a
+    caller follow a sample of one huge block, whose mean it summed piece by
+    piece, with ``x.p``, ``x.g``, ``x.m`` holding only the sampled elements
+    (``x.block`` = the sample's length).  Without a grad scale only."""
     if grad_scale is not None and A.any_nonfinite([x.g for x in tensors]):
         return False
     s = A.f32_scalars(lr=lr, beta1=beta1, beta2=beta2, eps=eps, t=t, grad_scale=grad_scale)
     bc1, _ = A.bias_corrections(float(F32(beta1)), float(F32(beta2)), t)
     rbc1 = F32(F32(1.0) / F32(bc1))
-    for x in tensors:
+    for i, x in enumerate(tensors):
         if x.p.size == 0:
             continue
         decay = A.decay_f32(s.lr, x.wd) if x.wd > 0 else F32(1.0)
-        if x.block == 1:
+        given = None if means is None else means[i]
+        if x.block == 1 and given is None:
             p1, m1, v1 = A.elementwise_f32(x.p, x.g, x.m, x.v, s, decay)
             x.p[...], x.m[...], x.v[...] = p1, m1, v1
             continue
         g = np.asarray(x.g).astype(F32)
         if s.inv_scale is not None:
             g = g * s.inv_scale
-        v1 = s.b2 * x.v + s.omb2 * block_mean_sq(g, x.block)
+        if given is not None and s.inv_scale is not None:
+            raise ValueError("precomputed block means are for unscaled grads")
+        mean = block_mean_sq(g, x.block) if given is None else np.asarray(given, dtype=F32)
+        v1 = s.b2 * x.v + s.omb2 * mean
         h = np.sqrt(v1) * s.inv_sqrt_bc2 + s.eps
         r = rbc1 / h
         m1 = s.b1 * x.m + s.omb1 * g

@@ -264,6 +264,50 @@ def test_bf16rem_tensor_beyond_2e31_elements():
         _cleanup()
 
 
+def test_adam_mini_block_beyond_2e31_elements():
+    """One Adam-mini block (v shared by the whole tensor) of 2^31 + 4097 elements,
+    bf16 grads, 2 steps: the reduction over the block's 131,073 chunks and the update
+    across element 2^31.  The oracle's block sum is taken piece by piece in float64
+    on the host (its order is free); v must match to one ulp per step, m bit for bit,
+    and the sampled params to the error one v ulp can cause."""
+    from oracle import mini as M
+    n = (1 << 31) + 4097
+    if _free_gib() < 35:
+        pytest.skip("needs ~30 GiB of free device memory")
+    from adamw_optimizer_step_tensor_gb300 import FusedAdamW
+    try:
+        p = synth.normal(n, 0.02, 76, "cuda")
+        g = torch.empty(n, dtype=torch.bfloat16, device="cuda")
+        m = torch.zeros(n, device="cuda")
+        v = torch.zeros(1, device="cuda")
+        opt = FusedAdamW([p], [g], [m], [v], [OA.f32(0.1)], v_blocks=[n])
+        idx = np.concatenate([np.arange(0, 4096), np.arange((1 << 31) - 2048, (1 << 31) + 2048),
+                              np.arange(n - 4096, n)]).astype(np.int64)
+        orc = M.Tensor(p=_take(p, idx).cpu().numpy(), g=None, m=np.zeros(idx.size, np.float32),
+                       v=np.zeros(1, np.float32), wd=OA.f32(0.1), block=idx.size)
+        lr = OA.f32(3e-4)
+        lr_dev, step = torch.tensor([lr], device="cuda"), torch.zeros(1, dtype=torch.int32, device="cuda")
+        piece = 1 << 27
+        for s in range(2):
+            g.copy_(synth.normal(n, 1e-3, 77 + s, "cuda", torch.bfloat16))
+            total = sum(M.block_sum_sq(g[a:a + piece].float().cpu().numpy()) for a in range(0, n, piece))
+            orc.g = _take(g, idx).float().cpu().numpy()
+            opt.step_mini(lr_dev, step, betas=(OA.f32(0.9), OA.f32(0.999)), eps=OA.f32(1e-8))
+            M.step_f32([orc], lr=lr, beta1=OA.f32(0.9), beta2=OA.f32(0.999), eps=OA.f32(1e-8),
+                       t=s + 1, means=[np.array([M.mean_from_sum(total, n)])])
+        torch.cuda.synchronize()
+        vd = v.cpu().numpy()
+        assert abs(int(vd.view(np.int32)[0]) - int(orc.v.view(np.int32)[0])) <= 2, (vd, orc.v)
+        assert np.array_equal(_take(m, idx).cpu().numpy().view(np.uint32), orc.m.view(np.uint32))
+        pd = _take(p, idx).cpu().numpy().astype(np.float64)
+        r_scale = np.abs(orc.m).astype(np.float64) / np.sqrt(float(orc.v[0]))
+        tol = 2.0 ** -22 * (np.abs(orc.p) + lr * r_scale * 4) * 2
+        assert np.all(np.abs(pd - orc.p) <= tol)
+        assert int(step.item()) == 2 and opt.status() == 0
+    finally:
+        _cleanup()
+
+
 def _blocks_beyond_2e31(n, block, rng):
     """Whole blocks sampled at both ends of an n-element tensor, across element
     2^31 and at random, sorted; the partial last block's index comes last."""

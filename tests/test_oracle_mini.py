@@ -160,3 +160,40 @@ def test_f32_tracks_fp64():
     for a, b in zip(xs64, xs32):
         assert np.max(np.abs(b.p - a.p) / (np.abs(a.p) + hp["lr"])) < 16 * 2.0 ** -24
         assert np.max(np.abs(b.v - a.v) / a.v) < 16 * 2.0 ** -24
+
+
+def test_block_sum_in_pieces_equals_the_whole_block_mean():
+    """Values on a 2^-12 grid below 4: every square and every partial sum is
+    exact in float64, so any order of the block's sum gives the same S_b, and
+    the mean summed over uneven pieces must equal block_mean_sq of the block."""
+    rng = np.random.default_rng(41)
+    n = 100_003
+    g = (rng.integers(-4 * 4096, 4 * 4096, n) / 4096.0).astype(np.float32)
+    cuts = [0, 17, 4096, 50_000, 50_001, 99_999, n]
+    s = sum(M.block_sum_sq(g[a:b]) for a, b in zip(cuts[:-1], cuts[1:]))
+    assert s == np.sum(g.astype(np.float64) ** 2)
+    assert M.mean_from_sum(s, n) == M.block_mean_sq(g, n)[0]
+
+
+def test_given_mean_follows_a_sample_of_the_block():
+    """step_f32 on a sample of one block, with the block's mean given, equals the
+    full step restricted to the sample, bit for bit (p, m, v)."""
+    rng = np.random.default_rng(42)
+    n = 40_000
+    p = rng.normal(0, 0.02, n).astype(np.float32)
+    g = rng.normal(0, 1e-3, n).astype(np.float32)
+    m = rng.normal(0, 1e-3, n).astype(np.float32)
+    v = np.array([1e-6], dtype=np.float32)
+    idx = np.sort(rng.choice(n, 1000, replace=False))
+    full = M.Tensor(p=p.copy(), g=g, m=m.copy(), v=v.copy(), wd=A.f32(0.1), block=n)
+    part = M.Tensor(p=p[idx].copy(), g=g[idx], m=m[idx].copy(), v=v.copy(), wd=A.f32(0.1),
+                    block=idx.size)
+    hp = dict(lr=A.f32(1e-3), beta1=A.f32(0.9), beta2=A.f32(0.999), eps=A.f32(1e-8), t=3)
+    M.step_f32([full], **hp)
+    mean = M.mean_from_sum(M.block_sum_sq(g), n)
+    M.step_f32([part], means=[np.array([mean])], **hp)
+    assert np.array_equal(part.p.view(np.uint32), full.p[idx].view(np.uint32))
+    assert np.array_equal(part.m.view(np.uint32), full.m[idx].view(np.uint32))
+    assert np.array_equal(part.v.view(np.uint32), full.v.view(np.uint32))
+    with pytest.raises(ValueError):
+        M.step_f32([part], means=[np.array([mean])], grad_scale=A.f32(2.0), **hp)
