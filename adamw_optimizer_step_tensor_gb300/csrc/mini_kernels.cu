@@ -11,18 +11,17 @@
 // Chunks never straddle blocks.  Each warp sums g*g over one chunk on its
 // own -- no CTA barrier inside the walk, so a warp whose loads are back never
 // waits for the others -- with kRedLoads loads of 8 grads per lane in flight.
-// Every lane keeps its sum as an unevaluated pair of float32 (s, c): each
-// square split exactly into x*x = p + e with one fma, each addition into s
-// made error-free with TwoSum, the errors gathered in c (Ogita, Rump and
-// Oishi, "Accurate sum and dot product", 2005: relative error about
-// (n*2^-24)^2 for the n <= 512 squares of a lane, with no float64 operation
-// per element, which GB300 runs at a small fraction of its float32 rate).
-// The lanes' pairs meet in a fixed xor tree of error-free pair additions and
-// the chunk's sum is s + c in float64.  A block of one chunk is finalised by
-// that warp; otherwise the warp whose arrival completes the block's count adds
-// the block's chunk sums (float64, each lane a fixed stride of them, then a
-// fixed xor tree), finalises the block and clears the count for the next
-// step.  Nothing waits on another warp.
+// Each lane sums the 32 squares of one round of loads as an unevaluated pair
+// of float32 (s, c): each square split exactly into x*x = p + e with one fma,
+// each addition into s made error-free with TwoSum, the errors gathered in c
+// (Ogita, Rump and Oishi, "Accurate sum and dot product", 2005: relative error
+// about (32*2^-24)^2, with no float64 operation per element, which GB300 runs
+// at a small fraction of its float32 rate), and adds s + c to its float64
+// total.  The lanes' totals meet in a fixed float64 xor tree.  A block of one
+// chunk is finalised by that warp; otherwise the warp whose arrival completes
+// the block's count adds the block's chunk sums (float64, each lane a fixed
+// stride of them, then a fixed xor tree), finalises the block and clears the
+// count for the next step.  Nothing waits on another warp.
 #include "step_common.cuh"
 
 namespace adamw {
@@ -40,18 +39,6 @@ __device__ __forceinline__ void add_square(float& s, float& c, float x) {
   const float err = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(p, bp));
   s = t;
   c = __fadd_rn(c, __fadd_rn(err, e));
-}
-
-// (s, c) += (s2, c2) for two error-free pairs: TwoSum of the leading parts,
-// the rounding error joins the trailing parts.  The result does not depend on
-// the order of the operands, so every lane of an xor tree ends with the same
-// pair.
-__device__ __forceinline__ void add_pair(float& s, float& c, float s2, float c2) {
-  const float t = __fadd_rn(s, s2);
-  const float bp = __fsub_rn(t, s);
-  const float err = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(s2, bp));
-  s = t;
-  c = __fadd_rn(__fadd_rn(c, c2), err);
 }
 
 // 8 consecutive raw grads of one lane, kept as loaded (16-bit grads stay
@@ -140,9 +127,11 @@ __global__ void __launch_bounds__(kRedThreads) mini_reduce_kernel(const StepArgs
     const TensorDesc* const tdp = a.tensors + ch.tensor;
     const void* const g = tdp->g;
     const bool vec = tdp->vec_ok != 0;
-    float sum = 0.0f, comp = 0.0f;
     // lane l takes the groups of 8 at l*8, l*8 + 256, ...: each load of the
-    // warp covers 256 consecutive grads; the squares go in in element order
+    // warp covers 256 consecutive grads; the squares go in in element order,
+    // 8 * kRedLoads into one float32 pair, which then joins the lane's float64
+    // total (so no pair takes more than 32 squares)
+    double lane_sum = 0.0;
     for (int off0 = lane * kVec; off0 < ch.len; off0 += kRedLoads * kStride) {
       RawGrads<GT> r[kRedLoads];
 #pragma unroll
@@ -150,6 +139,7 @@ __global__ void __launch_bounds__(kRedThreads) mini_reduce_kernel(const StepArgs
         const int off = off0 + u * kStride;
         load_raw<GT>(g, ch.start + off, max(0, min(kVec, ch.len - off)), vec, r[u]);
       }
+      float sum = 0.0f, comp = 0.0f;
 #pragma unroll
       for (int u = 0; u < kRedLoads; ++u) {
 #pragma unroll
@@ -158,12 +148,13 @@ __global__ void __launch_bounds__(kRedThreads) mini_reduce_kernel(const StepArgs
           add_square(sum, comp, s.scaled ? __fmul_rn(x, s.inv_scale) : x);
         }
       }
+      lane_sum += static_cast<double>(sum) + static_cast<double>(comp);
     }
+    // the lanes' totals in a fixed xor tree (float64 addition commutes: every
+    // lane ends with the same chunk sum)
+    double d = lane_sum;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-      add_pair(sum, comp, __shfl_xor_sync(0xFFFFFFFFu, sum, o),
-               __shfl_xor_sync(0xFFFFFFFFu, comp, o));
-    const double d = static_cast<double>(sum) + static_cast<double>(comp);
+    for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xFFFFFFFFu, d, o);
     const int32_t b = a.chunk_blk[c];
     const MiniBlock blk = ma.blocks[b];
     if (blk.n_chunks == 1) {

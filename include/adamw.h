@@ -318,10 +318,10 @@ adamw_status adamw_mini_plan_create(const adamw_tensor* tensors, const int64_t* 
 
 /*
  * One Adam-mini step: two launches on `stream`.  The first sums g*g over
- * every block longer than one element (per thread an error-free pair of
- * float32 -- exact squares by fma, TwoSum additions, after Ogita, Rump and
- * Oishi -- combined in float64 in a fixed order, the block's chunks in chunk
- * order), then per block, one rounding per operation:
+ * every block longer than one element (each 32 squares as an error-free pair
+ * of float32 -- exact squares by fma, TwoSum additions, after Ogita, Rump and
+ * Oishi -- the pairs added in float64 in a fixed order, the block's chunks in
+ * chunk order), then per block, one rounding per operation:
  *     mean = fl32(sum / len);  v' = b2*v + fl(1-b2)*mean
  *     h = sqrt(v')*fl32(1/sqrt(1-b2^t)) + eps;  r = fl(1/fl32(1-b1^t)) / h
  * The second updates every element:
@@ -330,7 +330,7 @@ adamw_status adamw_mini_plan_create(const adamw_tensor* tensors, const int64_t* 
  *                 p' = p*decay - lr*(m'*r)
  * with decay = fl(1 - fl(lr*wd)) when wd > 0 and no decay otherwise (the
  * listing decays only for wd > 0).  The sum's relative error stays below
- * about 2^-35 (64 squares per thread and chunk), so the mean is the correctly
+ * about 2^-37 (32 squares per float32 pair), so the mean is the correctly
  * rounded mean of the squares except within that distance of a float32
  * rounding boundary (one ulp off then), or when a square leaves the float32
  * range.  lr_dev, step_dev, grad_scale_dev, found_inf_dev, skip

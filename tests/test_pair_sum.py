@@ -1,14 +1,14 @@
 """The accuracy of the Adam-mini block reduction's summation method (CPU only).
 
 The GPU reduction sums g*g over a block without a float64 operation per
-element: every thread keeps an unevaluated pair of float32 (s, c) -- each
-square split exactly into x*x = p + e (one fma), each addition into s made
-error-free by TwoSum, the errors gathered in c (Ogita, Rump and Oishi,
-"Accurate sum and dot product", 2005) -- and the pairs are added in float64.
-This file emulates that method in numpy float32 arithmetic (every operation
-rounded once, as on the GPU; the fma's error term is exact in float64) over
-chains of 64 squares, the length one thread sums in a 16384-element chunk,
-and checks it against the exactly rounded sum (``math.fsum``): the relative
+element: every lane sums the 32 squares of one round of its loads as an
+unevaluated pair of float32 (s, c) -- each square split exactly into
+x*x = p + e (one fma), each addition into s made error-free by TwoSum, the
+errors gathered in c (Ogita, Rump and Oishi, "Accurate sum and dot product",
+2005) -- and the pairs are added in float64.  This file emulates that method
+in numpy float32 arithmetic (every operation rounded once, as on the GPU; the
+fma's error term is exact in float64) over chains of 32 squares, and checks it
+against the exactly rounded sum (``math.fsum``): the relative
 error stays below 2^-40 on wide-range and on cancellation-free data alike,
 far inside the one float32 ulp (2^-24) at which the block mean is stored.
 A plain float32 running sum, for contrast, is off by about 2^-20 already.
@@ -34,7 +34,7 @@ def two_sum(a, b):
     return t, err
 
 
-def pair_sum(x: np.ndarray, chain: int = 64) -> float:
+def pair_sum(x: np.ndarray, chain: int = 32) -> float:
     """Sum of x*x: chains of `chain` squares in float32 pairs, chains added in float64."""
     x = np.asarray(x, dtype=F32).reshape(-1, chain)
     s = np.zeros(x.shape[0], F32)
