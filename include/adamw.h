@@ -24,8 +24,10 @@
  * Results are therefore reproducible bit for bit by any IEEE float32
  * implementation of the same sequence.  The other rules (AdEMAMix, Lion, the
  * coupled-L2 rules, Adam-mini) and the 8-bit and 4-bit modes state their own
- * sequences below in the same terms; the one fused multiply-add in the library
- * is the exact split of a square in the Adam-mini block reduction.
+ * sequences below in the same terms.  The library's two fused multiply-adds
+ * change no result: the exact split of a square in the Adam-mini block
+ * reduction, and 16x - 1.5 in the 4-bit v code search, where 16x is exact so
+ * the fused and the unfused forms round the same value once.
  *
  * Conventions shared by all entry points
  *   - Every tensor, scalar and stream is owned by the caller.  Pointers named
@@ -292,7 +294,7 @@ adamw_status adamw_ademamix_step(adamw_plan* plan, const float* lr_dev, int32_t*
  * 20 bytes per element with fp32 params and grads.
  * lr_dev, step_dev, grad_scale_dev, found_inf_dev, skip and step counting as
  * adamw_step (*step_dev advances although Lion has no bias correction).
- * EINVAL for betas outside [0, 1); EUNSUPPORTED for Q8 plans.
+ * EINVAL for betas outside [0, 1); EUNSUPPORTED for 8-bit and 4-bit plans.
  */
 adamw_status adamw_lion_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev,
                              float beta1, float beta2, const float* grad_scale_dev,
@@ -365,7 +367,7 @@ typedef enum {
  * Adagrad); eps finite and >= 0 (unused by momentum).  20 bytes per element
  * with fp32 params and grads.  lr_dev, step_dev, grad_scale_dev,
  * found_inf_dev, skip and step counting as adamw_step.  EINVAL for an unknown
- * rule, EUNSUPPORTED for Q8 plans.
+ * rule, EUNSUPPORTED for 8-bit and 4-bit plans.
  */
 adamw_status adamw_coupled_step(adamw_plan* plan, adamw_coupled_rule rule, const float* lr_dev,
                                 int32_t* step_dev, float beta, float eps,
