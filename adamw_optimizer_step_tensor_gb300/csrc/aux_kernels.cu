@@ -1,6 +1,7 @@
 // aux_kernels.cu -- the non-finite grad check, the remainder split/join and
 // the Q8 state export/import kernels.
 #include "internal.h"
+#include "step_common.cuh"
 
 namespace adamw {
 namespace {
@@ -64,10 +65,10 @@ __global__ void split_kernel(const float* __restrict__ master, uint16_t* __restr
                              int16_t* __restrict__ rem, int64_t n) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const uint32_t b = __float_as_uint(master[i]);
-    const uint32_t lo = b & 0xFFFFu;
-    hi[i] = static_cast<uint16_t>(((b >> 16) + (lo >> 15)) & 0xFFFFu);
-    rem[i] = static_cast<int16_t>(static_cast<uint16_t>(lo));
+    uint32_t h, r;
+    rem_split(master[i], h, r);
+    hi[i] = static_cast<uint16_t>(h);
+    rem[i] = static_cast<int16_t>(static_cast<uint16_t>(r));
   }
 }
 
@@ -75,9 +76,7 @@ __global__ void join_kernel(const uint16_t* __restrict__ hi, const int16_t* __re
                             float* __restrict__ master, int64_t n) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
-    const uint32_t r = static_cast<uint16_t>(rem[i]);
-    const uint32_t top = (static_cast<uint32_t>(hi[i]) - (r >> 15)) & 0xFFFFu;
-    master[i] = __uint_as_float((top << 16) | r);
+    master[i] = rem_join(hi[i], static_cast<uint16_t>(rem[i]));
   }
 }
 

@@ -339,7 +339,11 @@ __device__ __forceinline__ float rem_join(uint32_t hi, uint32_t rem16) {
   return __uint_as_float((top << 16) | (rem16 & 0xFFFFu));
 }
 __device__ __forceinline__ void rem_split(float x, uint32_t& hi, uint32_t& rem16) {
-  const uint32_t b = __float_as_uint(x);
+  uint32_t b = __float_as_uint(x);
+  // a NaN master is stored as the quiet NaN 0x7FC00000: bf16 half 0x7FC0 (a
+  // NaN), remainder 0 -- the increment would carry the all-ones NaNs (the
+  // GPU's own 0x7FFFFFFF among them) out of the half, to -0.0 / +0.0
+  if ((b & 0x7FFFFFFFu) > 0x7F800000u) b = 0x7FC00000u;
   const uint32_t lo = b & 0xFFFFu;
   hi = ((b >> 16) + (lo >> 15)) & 0xFFFFu;
   rem16 = lo;

@@ -77,7 +77,8 @@ typedef enum {
   ADAMW_MODE_FP32 = 0,
   /* bf16 model param plus an int16 remainder per element that together hold
    * the fp32 master exactly ("Support store_param_remainders feature from
-   * Apex in TE Fused Adam #1408", Description); fp32 m and v.  The pair is
+   * Apex in TE Fused Adam #1408", Description; a NaN master as the quiet NaN,
+   * see adamw_bf16rem_split); fp32 m and v.  The pair is
    * joined to the fp32 master, updated, and split again in registers; the
    * split is adamw_bf16rem_split's. */
   ADAMW_MODE_BF16_REM = 1,
@@ -410,10 +411,15 @@ adamw_status adamw_lr_from_table(const float* table, int32_t n, const int32_t* s
 
 /*
  * Remainder split / join (the rule used by ADAMW_MODE_BF16_REM).
- *   split: lo = bits & 0xFFFF; bf16 = (bits >> 16) + (lo >= 0x8000) (mod 2^16);
- *          rem = (int16)lo.  bf16 is the nearest bf16, ties away from zero.
+ *   split: a NaN master is first replaced by the quiet NaN 0x7FC00000; then
+ *          lo = bits & 0xFFFF; bf16 = (bits >> 16) + (lo >= 0x8000) (mod 2^16);
+ *          rem = (int16)lo.  bf16 is the nearest bf16, ties away from zero,
+ *          and a NaN for a NaN master (bf16 0x7FC0, remainder 0).
  *   join:  bits = ((bf16 - (rem < 0)) mod 2^16) << 16 | (uint16)rem.
- * join(split(x)) == x for all 2^32 bit patterns.  n >= 0 elements; device
+ * join(split(x)) == x for every bit pattern but a NaN, and a NaN for a NaN.
+ * Without the replacement the all-ones NaNs (0x7FFF8000..0x7FFFFFFF, the
+ * GPU's 0x7FFFFFFF among them, and their negatives) would carry out of the
+ * 16-bit half and read as bf16 -0.0 / +0.0.  n >= 0 elements; device
  * pointers, each aligned to its element size.
  */
 adamw_status adamw_bf16rem_split(const float* master, uint16_t* bf16, int16_t* rem,

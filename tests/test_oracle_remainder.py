@@ -29,8 +29,13 @@ def _grid(tops, los):
 
 
 def _roundtrip_ok(bits):
+    """join(split(x)) is x for every master but a NaN; a NaN master is stored as
+    the quiet NaN (bf16 half 0x7FC0, a NaN; remainder 0) and comes back as it."""
     hi, rem = R.split(bits)
-    return np.array_equal(R.join(hi, rem).view(np.uint32), bits)
+    back = R.join(hi, rem).view(np.uint32)
+    nan = (bits & np.uint32(0x7FFFFFFF)) > np.uint32(0x7F800000)
+    return (np.array_equal(back[~nan], bits[~nan]) and np.all(back[nan] == 0x7FC00000)
+            and np.all(hi[nan] == 0x7FC0) and np.all(rem[nan] == 0))
 
 
 def test_roundtrip_all_top_halves():
@@ -107,6 +112,22 @@ def test_special_values_round_trip_and_bf16_view():
     assert bf[5] == 1.0 and bf[6] == -1.0
     # FLT_MAX is past the last bf16 tie: rounds to inf, the remainder still rebuilds it
     assert bf[8] == np.inf and back[8] == np.finfo(np.float32).max
+
+
+def test_every_nan_master_is_a_nan_in_the_bf16_half():
+    """The all-ones NaNs -- 0x7FFFFFFF is the NaN a GPU's arithmetic returns --
+    would carry out of the 16-bit half under the plain increment and read as
+    -0.0 / +0.0; every NaN master must give a NaN bf16 model parameter."""
+    tops = np.array([0x7F80, 0x7F81, 0x7FBF, 0x7FC0, 0x7FFE, 0x7FFF,
+                     0xFF80, 0xFF81, 0xFFC0, 0xFFFE, 0xFFFF], dtype=np.uint32)
+    bits = _grid(tops, np.arange(1 << 16, dtype=np.uint32))
+    bits = bits[(bits & 0x7FFFFFFF) > 0x7F800000]          # NaNs only (drops the infinities)
+    hi, rem = R.split(bits)
+    assert np.all(np.isnan(R.bf16_bits_to_f32(hi)))
+    assert np.all(hi == 0x7FC0) and np.all(rem == 0)
+    assert np.all(R.join(hi, rem).view(np.uint32) == 0x7FC00000)
+    gpu_nan = np.array([0x7FFFFFFF], dtype=np.uint32)
+    assert np.isnan(R.bf16_bits_to_f32(R.split(gpu_nan)[0]))[0]
 
 
 def test_remainder_sign_says_rounded_up():
