@@ -17,7 +17,8 @@
 // (Ogita, Rump and Oishi, "Accurate sum and dot product", 2005: relative error
 // about (32*2^-24)^2, with no float64 operation per element, which GB300 runs
 // at a small fraction of its float32 rate), and adds s + c to its float64
-// total.  The lanes' totals meet in a fixed float64 xor tree.  A block of one
+// total; a round whose pair is not finite is summed again with float64
+// squares.  The lanes' totals meet in a fixed float64 xor tree.  A block of one
 // chunk is finalised by that warp; otherwise the warp whose arrival completes
 // the block's count adds the block's chunk sums (float64, each lane a fixed
 // stride of them, then a fixed xor tree), finalises the block and clears the
@@ -28,6 +29,7 @@ namespace adamw {
 namespace {
 
 constexpr int kRedThreads = kRedWarps * 32;
+constexpr float kF32Max = 3.40282347e38f;   // the largest finite float32
 constexpr int kRedLoads = 4;   // 8-grad loads in flight per lane
 
 // (s, c) += x*x: TwoProduct of the square by fma, TwoSum of the addition.
@@ -107,7 +109,7 @@ __device__ void finalise(const StepArgs& a, const MiniArgs& ma, int32_t b, doubl
 }
 
 template <typename GT>
-__global__ void __launch_bounds__(kRedThreads) mini_reduce_kernel(const StepArgs a,
+__global__ void __launch_bounds__(kRedThreads, sizeof(GT) == 4 ? 4 : 5) mini_reduce_kernel(const StepArgs a,
                                                                   const MiniArgs ma) {
   __shared__ Scal s_sc;
   __shared__ int s_skip;
@@ -148,7 +150,31 @@ __global__ void __launch_bounds__(kRedThreads) mini_reduce_kernel(const StepArgs
           add_square(sum, comp, s.scaled ? __fmul_rn(x, s.inv_scale) : x);
         }
       }
-      lane_sum += static_cast<double>(sum) + static_cast<double>(comp);
+      if (fabsf(sum) <= kF32Max) {
+        lane_sum += static_cast<double>(sum) + static_cast<double>(comp);
+      } else {
+        // a NaN or infinite grad, or a square or partial sum past the float32
+        // range, where the split of a square is not exact (inf - inf): this
+        // round again with float64 squares, exact for every float32 -- inf
+        // and NaN as the definition gives them, and a finite mean where the
+        // float64 sum of squares allows one
+        // (the grads are loaded again: this rare path keeps no registers
+        // live through the common one)
+        double acc = 0.0;
+#pragma unroll
+        for (int u = 0; u < kRedLoads; ++u) {
+          const int off = off0 + u * kStride;
+          RawGrads<GT> again;
+          load_raw<GT>(g, ch.start + off, max(0, min(kVec, ch.len - off)), vec, again);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const float x = raw_grad<GT>(again, q);
+            const double xd = static_cast<double>(s.scaled ? __fmul_rn(x, s.inv_scale) : x);
+            acc += xd * xd;
+          }
+        }
+        lane_sum += acc;
+      }
     }
     // the lanes' totals in a fixed xor tree (float64 addition commutes: every
     // lane ends with the same chunk sum)

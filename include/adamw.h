@@ -335,8 +335,12 @@ adamw_status adamw_mini_plan_create(const adamw_tensor* tensors, const int64_t* 
  * listing decays only for wd > 0).  The sum's relative error stays below
  * about 2^-37 (32 squares per float32 pair), so the mean is the correctly
  * rounded mean of the squares except within that distance of a float32
- * rounding boundary (one ulp off then), or when a square leaves the float32
- * range.  lr_dev, step_dev, grad_scale_dev, found_inf_dev, skip
+ * rounding boundary (one ulp off then).  A round of 32 squares whose float32
+ * pair is not finite (a NaN or infinite grad, a square or a partial sum past
+ * the float32 range) is summed again with float64 squares, so such blocks get
+ * the float64 definition's inf, NaN or finite mean; squares below about
+ * 2^-100, where the float32 split of a square stops being exact, may each
+ * lose up to 2^-149.  lr_dev, step_dev, grad_scale_dev, found_inf_dev, skip
  * (both launches) and step counting (the second launch) as adamw_step.
  */
 adamw_status adamw_mini_step(adamw_plan* plan, const float* lr_dev, int32_t* step_dev,

@@ -198,3 +198,37 @@ def test_mini_llama_sized_blocks():
     _check("fp32", ds, orc, lr, 1, "llama-sized")
     del ds
     torch.cuda.empty_cache()
+
+
+def test_mini_block_sums_past_the_float32_range():
+    """Blocks of 256 whose squares or partial sums leave float32: one grad of
+    1.9e19 (its square overflows, the block mean 1.4e36 does not), one +inf,
+    one NaN, one -3e38 (the mean overflows too), and every grad 1e19 (the float32
+    running sum overflows, the mean 1e38 does not) -- v as the float64 definition
+    gives it: finite where the mean is, inf and NaN where they belong."""
+    rng = np.random.default_rng(76)
+    block = 256
+    g0 = rng.normal(0, 1e-3, 6 * block).astype(np.float32)
+    g0[3] = 1.9e19
+    g0[block + 7] = np.inf
+    g0[2 * block + 9] = np.nan
+    g0[3 * block + 11] = -3e38
+    g0[4 * block:5 * block] = 1e19
+    n = g0.size
+    p0 = rng.normal(0, 0.02, n).astype(np.float32)
+    p, g, m, v = dev(p0), dev(g0), zeros(n), zeros(n // block)
+    opt = FusedAdamW([p], [g], [m], [v], [f32(0.1)], v_blocks=[block])
+    opt.step_mini(torch.tensor([f32(1e-3)], device="cuda"), zeros(1, torch.int32),
+                  betas=(HP["beta1"], HP["beta2"]), eps=HP["eps"])
+    o = M.Tensor(p=p0.copy(), g=g0, m=np.zeros(n, np.float32), v=np.zeros(n // block, np.float32),
+                 wd=f32(0.1), block=block)
+    with np.errstate(invalid="ignore", over="ignore"):
+        M.step_f32([o], lr=f32(1e-3), t=1, **HP)
+    torch.cuda.synchronize()
+    vd = host(v)
+    assert np.isfinite(o.v[0]) and np.isfinite(o.v[4])        # the float64 means that stay finite
+    assert np.isinf(o.v[1]) and np.isnan(o.v[2]) and np.isinf(o.v[3])
+    assert np.array_equal(np.isnan(vd), np.isnan(o.v)) and np.array_equal(np.isinf(vd), np.isinf(o.v))
+    fin = np.isfinite(o.v)
+    assert np.all(_ulps(vd[fin], o.v[fin]) <= 1), (vd, o.v)
+    assert opt.status() == 0
