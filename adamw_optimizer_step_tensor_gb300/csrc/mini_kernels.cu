@@ -33,14 +33,22 @@ constexpr float kF32Max = 3.40282347e38f;   // the largest finite float32
 constexpr int kRedLoads = 4;   // 8-grad loads in flight per lane
 
 // (s, c) += x*x: TwoProduct of the square by fma, TwoSum of the addition.
+// EXACT_SQUARE: x has at most 12 significant bits (an unscaled 16-bit grad),
+// so x*x is exact in float32 wherever it is a normal number and the product's
+// error term is 0: it is not computed.
+template <bool EXACT_SQUARE>
 __device__ __forceinline__ void add_square(float& s, float& c, float x) {
   const float p = __fmul_rn(x, x);
-  const float e = __fmaf_rn(x, x, -p);
   const float t = __fadd_rn(s, p);
   const float bp = __fsub_rn(t, s);
   const float err = __fadd_rn(__fsub_rn(s, __fsub_rn(t, bp)), __fsub_rn(p, bp));
   s = t;
-  c = __fadd_rn(c, __fadd_rn(err, e));
+  if constexpr (EXACT_SQUARE) {
+    c = __fadd_rn(c, err);
+  } else {
+    const float e = __fmaf_rn(x, x, -p);
+    c = __fadd_rn(c, __fadd_rn(err, e));
+  }
 }
 
 // 8 consecutive raw grads of one lane, kept as loaded (16-bit grads stay
@@ -108,7 +116,10 @@ __device__ void finalise(const StepArgs& a, const MiniArgs& ma, int32_t b, doubl
   ma.blk_r[b] = __fdiv_rn(s.rbc1, h);
 }
 
-template <typename GT>
+// SCALED: the launch has a loss scale (the unscale is then applied to every
+// grad; x * 1 is exact, so a scale of 1 changes nothing) -- a template
+// parameter, so the unscaled step spends no instruction per element on it.
+template <typename GT, bool SCALED>
 __global__ void __launch_bounds__(kRedThreads, sizeof(GT) == 4 ? 4 : 5) mini_reduce_kernel(const StepArgs a,
                                                                   const MiniArgs ma) {
   __shared__ Scal s_sc;
@@ -121,6 +132,8 @@ __global__ void __launch_bounds__(kRedThreads, sizeof(GT) == 4 ? 4 : 5) mini_red
   const int lane = threadIdx.x & 31;
   constexpr int kStride = 32 * kVec;   // elements between one lane's groups
   const int64_t n_warps = static_cast<int64_t>(gridDim.x) * kRedWarps;
+  // bf16 (8 significant bits) and fp16 (11) squares are exact in float32
+  constexpr bool kExactSquare = !SCALED && sizeof(GT) == 2;
 
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * kRedWarps + (threadIdx.x >> 5); i < ma.n_red;
        i += n_warps) {
@@ -147,7 +160,7 @@ __global__ void __launch_bounds__(kRedThreads, sizeof(GT) == 4 ? 4 : 5) mini_red
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const float x = raw_grad<GT>(r[u], q);
-          add_square(sum, comp, s.scaled ? __fmul_rn(x, s.inv_scale) : x);
+          add_square<kExactSquare>(sum, comp, SCALED ? __fmul_rn(x, s.inv_scale) : x);
         }
       }
       if (fabsf(sum) <= kF32Max) {
@@ -169,7 +182,7 @@ __global__ void __launch_bounds__(kRedThreads, sizeof(GT) == 4 ? 4 : 5) mini_red
 #pragma unroll
           for (int q = 0; q < 8; ++q) {
             const float x = raw_grad<GT>(again, q);
-            const double xd = static_cast<double>(s.scaled ? __fmul_rn(x, s.inv_scale) : x);
+            const double xd = static_cast<double>(SCALED ? __fmul_rn(x, s.inv_scale) : x);
             acc += xd * xd;
           }
         }
@@ -210,17 +223,25 @@ __global__ void __launch_bounds__(kRedThreads, sizeof(GT) == 4 ? 4 : 5) mini_red
   }
 }
 
+template <typename GT>
+cudaError_t launch_reduce(const StepArgs& a, const MiniArgs& ma, int grid, cudaStream_t s) {
+  if (a.grad_scale != nullptr)
+    mini_reduce_kernel<GT, true><<<grid, kRedThreads, 0, s>>>(a, ma);
+  else
+    mini_reduce_kernel<GT, false><<<grid, kRedThreads, 0, s>>>(a, ma);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_mini_reduce(adamw_dtype gdt, const StepArgs& a, const MiniArgs& ma, int grid,
                                cudaStream_t s) {
   switch (gdt) {
-    case ADAMW_F32: mini_reduce_kernel<float><<<grid, kRedThreads, 0, s>>>(a, ma); break;
-    case ADAMW_F16: mini_reduce_kernel<__half><<<grid, kRedThreads, 0, s>>>(a, ma); break;
-    case ADAMW_BF16: mini_reduce_kernel<__nv_bfloat16><<<grid, kRedThreads, 0, s>>>(a, ma); break;
-    default: return cudaErrorInvalidValue;
+    case ADAMW_F32: return launch_reduce<float>(a, ma, grid, s);
+    case ADAMW_F16: return launch_reduce<__half>(a, ma, grid, s);
+    case ADAMW_BF16: return launch_reduce<__nv_bfloat16>(a, ma, grid, s);
   }
-  return cudaGetLastError();
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace adamw

@@ -322,9 +322,10 @@ adamw_status adamw_mini_plan_create(const adamw_tensor* tensors, const int64_t* 
 /*
  * One Adam-mini step: two launches on `stream`.  The first sums g*g over
  * every block longer than one element (each 32 squares as an error-free pair
- * of float32 -- exact squares by fma, TwoSum additions, after Ogita, Rump and
- * Oishi -- the pairs added in float64 in a fixed order, the block's chunks in
- * chunk order), then per block, one rounding per operation:
+ * of float32 -- exact squares by fma, or exact as they are for unscaled
+ * 16-bit grads, TwoSum additions, after Ogita, Rump and Oishi -- the pairs
+ * added in float64 in a fixed order, the block's chunks in chunk order), then
+ * per block, one rounding per operation:
  *     mean = fl32(sum / len);  v' = b2*v + fl(1-b2)*mean
  *     h = sqrt(v')*fl32(1/sqrt(1-b2^t)) + eps;  r = fl(1/fl32(1-b1^t)) / h
  * The second updates every element:
