@@ -74,3 +74,22 @@ def test_pair_sum_of_equal_values():
     x = np.full(16384, F32(3e-3))       # a float32 running sum drifts most on equal terms
     ref = exact_sum_of_squares(x)
     assert abs(pair_sum(x) - ref) / ref < 2.0 ** -40
+
+
+def test_unscaled_16bit_squares_are_exact_in_float32():
+    """The reduction skips the product's error term for unscaled bf16 and fp16
+    grads: every one of their 65,536 patterns squares exactly in float32
+    wherever the square is a normal float32 (8 or 11 significant bits squared
+    fit in 24); a square below that range or past it is where the header's
+    bound and the float64 fallback take over."""
+    bf = (np.arange(1 << 16, dtype=np.uint32) << np.uint32(16)).view(np.float32)
+    hf = np.arange(1 << 16, dtype=np.uint16).view(np.float16).astype(F32)
+    tiny, big = np.finfo(F32).tiny, np.finfo(F32).max
+    for x in (bf, hf):
+        x = x[np.isfinite(x)]
+        exact = x.astype(np.float64) ** 2
+        normal = (exact >= tiny) & (exact <= big)
+        with np.errstate(over="ignore", under="ignore"):
+            sq = (x * x).astype(F32)
+        assert np.array_equal(sq[normal].astype(np.float64), exact[normal])
+        assert normal.sum() > 20000
