@@ -136,6 +136,28 @@ def test_mini_reduction_is_deterministic():
             assert bits_equal(a[k], b[k]), (i, k)
 
 
+@pytest.mark.parametrize("gdtype", [torch.float16, torch.bfloat16, torch.float32])
+def test_mini_with_a_loss_scale(gdtype):
+    """The loss-scaled reduction and update (the scaled kernel instantiations):
+    grads scaled by 3000 (not a power of two, so the unscale rounds), three
+    steps, no non-finite grad -- against the oracle with the same scale."""
+    opt, dev_t, orc, rng = _make("fp32", gdtype, seed=77)
+    scale_v = 3000.0
+    lr_v = f32(1e-3)
+    lr, step = torch.tensor([lr_v], device="cuda"), zeros(1, torch.int32)
+    scale = torch.tensor([scale_v], device="cuda")
+    for t in range(1, 4):
+        for d, o in zip(dev_t, orc):
+            x, wide = grads_of((rng.normal(0, 1e-3, d["g"].numel()) * scale_v).astype(np.float32), gdtype)
+            d["g"].copy_(x)
+            o.g = wide
+        opt.step_mini(lr, step, betas=(HP["beta1"], HP["beta2"]), eps=HP["eps"], grad_scale=scale)
+        assert M.step_f32(orc, lr=lr_v, t=t, grad_scale=f32(scale_v), **HP)
+        torch.cuda.synchronize()
+        _check("fp32", dev_t, orc, lr_v, t, t)
+    assert int(step.item()) == 3 and opt.status() == 0
+
+
 def test_mini_first_step_closed_form():
     rng = np.random.default_rng(72)
     n, block = 8 * 40_000, 40_000
