@@ -53,19 +53,24 @@ def _build(sizes, gdtype, seed, zero_state, misalign=False):
     return opt, st, d, gs, rng
 
 
-def _steps(opt, st, d, gs, rng, gdtype, n_steps, lr=1e-3):
+def _steps(opt, st, d, gs, rng, gdtype, n_steps, lr=1e-3, scale=None):
+    """n_steps against the oracle; ``scale``: grads scaled by it and the loss
+    scale passed to both sides (the scaled kernel instantiation)."""
     maps = O4.Maps4()
     lr_d, step = scalar_f32(f32(lr)), scalar_i32(0)
+    scale_d = None if scale is None else scalar_f32(f32(scale))
     for t in range(1, n_steps + 1):
         wide = []
         for g in gs:
-            tg, w = grads_of(rng.normal(0, 1e-3, g.numel()).astype(np.float32), gdtype)
+            x = rng.normal(0, 1e-3, g.numel()) * (1.0 if scale is None else scale)
+            tg, w = grads_of(x.astype(np.float32), gdtype)
             g.copy_(tg)
             wide.append(w)
-        opt.step(lr_d, step, betas=(B1, B2), eps=EPS)
+        opt.step(lr_d, step, betas=(B1, B2), eps=EPS, grad_scale=scale_d)
         for i, (s, w) in enumerate(zip(st, wide)):
             O4.step_f32(s["p"], w, s["cm"], s["cv"], s["am"], s["av"], lr=f32(lr), beta1=B1,
-                        beta2=B2, eps=EPS, wd=f32(0.01) if i % 2 else 0.0, t=t, maps=maps)
+                        beta2=B2, eps=EPS, wd=f32(0.01) if i % 2 else 0.0, t=t, maps=maps,
+                        grad_scale=None if scale is None else f32(scale))
         torch.cuda.synchronize()
         assert_guards_intact()
         for i, (s, x) in enumerate(zip(st, d)):
@@ -81,6 +86,14 @@ def _steps(opt, st, d, gs, rng, gdtype, n_steps, lr=1e-3):
 def test_q4_steps_bitexact(gdtype):
     opt, st, d, gs, rng = _build(SIZES, gdtype, seed=31, zero_state=False)
     _steps(opt, st, d, gs, rng, gdtype, 4)
+
+
+@pytest.mark.parametrize("gdtype", [torch.float16, torch.bfloat16, torch.float32])
+def test_q4_steps_bitexact_with_a_loss_scale(gdtype):
+    """A loss scale of 3000 (its reciprocal rounds) on every step: the scaled
+    kernel instantiation, bit-exact."""
+    opt, st, d, gs, rng = _build(SIZES, gdtype, seed=37, zero_state=False)
+    _steps(opt, st, d, gs, rng, gdtype, 3, scale=3000.0)
 
 
 def test_q4_from_zero_state_bitexact():

@@ -76,6 +76,34 @@ def test_q8_steps_bitexact(gdtype):
             assert bits_equal(host(x["av"]), s["av"]), f"t{t} tensor {i} absmax v"
 
 
+@pytest.mark.parametrize("gdtype", [torch.float16, torch.bfloat16, torch.float32])
+def test_q8_steps_bitexact_with_a_loss_scale(gdtype):
+    """A loss scale of 3000 (its reciprocal rounds) on every step: the scaled
+    kernel instantiation, bit-exact on the ragged list."""
+    opt, st, d, gs, rng = _build(SIZES, gdtype, seed=17, zero_state=False)
+    maps = OQ.Maps()
+    lr, step, scale = scalar_f32(f32(1e-3)), scalar_i32(0), scalar_f32(f32(3000.0))
+    for t in range(1, 4):
+        wide = []
+        for g in gs:
+            tg, w = grads_of((rng.normal(0, 1e-3, g.numel()) * 3000.0).astype(np.float32), gdtype)
+            g.copy_(tg)
+            wide.append(w)
+        opt.step(lr, step, betas=(B1, B2), eps=EPS, grad_scale=scale)
+        for s, w in zip(st, wide):
+            OQ.step_f32(s["p"], w, s["cm"], s["cv"], s["am"], s["av"], lr=f32(1e-3), beta1=B1,
+                        beta2=B2, eps=EPS, wd=f32(0.01), t=t, maps=maps, grad_scale=f32(3000.0))
+        torch.cuda.synchronize()
+        assert_guards_intact()
+        for i, (s, x) in enumerate(zip(st, d)):
+            assert bits_equal(host(x["p"]), s["p"]), f"t{t} tensor {i} p: {first_mismatch(host(x['p']), s['p'])}"
+            assert np.array_equal(host(x["cm"]), s["cm"]), f"t{t} tensor {i} m codes"
+            assert np.array_equal(host(x["cv"]), s["cv"]), f"t{t} tensor {i} v codes"
+            assert bits_equal(host(x["am"]), s["am"]), f"t{t} tensor {i} absmax m"
+            assert bits_equal(host(x["av"]), s["av"]), f"t{t} tensor {i} absmax v"
+    assert int(step.item()) == 3
+
+
 def test_q8_element_path_on_misaligned_params():
     """Params 4 bytes off the 16-byte grid: every block of those tensors takes
     the element path (scalar loads, per-element predicates), several warps of
