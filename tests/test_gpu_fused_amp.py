@@ -4,7 +4,9 @@ Same AMP workload as the two-launch test (fp16 grads N(0,1e-3)*65536, loss scale
 65536, one non-finite grad per 20-step window, 100 steps): bit-exact against the
 strict-fp32 oracle, skipped steps leave everything untouched, the found-inf
 output reports every skip, and results equal adamw_check_nonfinite +
-adamw_step on the same plan type.
+adamw_step on the same plan type -- on all three routes adamw_step_amp takes
+(the small kernel's fused variant, the cooperative fused kernel of mid-size or
+misaligned plans, and the two launches past 6 Mi elements).
 """
 
 import math
@@ -60,25 +62,35 @@ def test_fused_amp_matches_oracle_and_skips():
     assert t == 95 and opt.status() == 0
 
 
+# the plan sizes adamw_step_amp routes three ways: the small kernel's fused
+# variant (70,000 elements), the cooperative fused kernel of mid-size plans
+# (3,000,000; and a small plan with a tensor off the 16-byte grid), and the
+# two launches past 6 Mi elements (7,000,000)
+CASES = {"small": (70_000, False), "mid": (3_000_000, False), "misaligned": (70_000, True),
+         "big": (7_000_000, False)}
+
+
 @pytest.mark.parametrize("mode", ["fp32", "bf16_rem"])
-@pytest.mark.parametrize("big", [False, True])
-def test_fused_amp_equals_two_launch_path(mode, big):
-    # big: more than 6 Mi elements, where adamw_step_amp itself runs the two launches
-    sizes = [1, 4099, 7_000_000 if big else 70000, 0, 257]
+@pytest.mark.parametrize("case", list(CASES))
+def test_fused_amp_equals_two_launch_path(mode, case):
+    size, misalign = CASES[case]
+    sizes = [1, 4099, size, 0, 257]
     rng = np.random.default_rng(32)
     sides = []
     for _ in range(2):
         rng_side = np.random.default_rng(33)
         st = []
-        for n in sizes:
+        for i, n in enumerate(sizes):
             if mode == "fp32":
                 pp = dev(rng_side.normal(0, 0.02, n).astype(np.float32))
                 rr = None
             else:
                 pp = to_dev(torch.from_numpy(rng_side.normal(0, 0.02, n).astype(np.float32)).to(torch.bfloat16))
                 rr = dev(rng_side.integers(0, 1 << 15, n).astype(np.int16))
+            # misaligned: tensor 1's m starts one float off the 16-byte grid
+            mm = dev(np.zeros(n, np.float32), shift=1) if (misalign and i == 1) else zeros(n)
             st.append(dict(p=pp, r=rr, g=zeros(n, torch.bfloat16),
-                           m=zeros(n), v=zeros(n)))
+                           m=mm, v=zeros(n)))
         opt = FusedAdamW([d["p"] for d in st], [d["g"] for d in st], [d["m"] for d in st],
                          [d["v"] for d in st], [0.1, 0.0, 0.1, 0.0, 0.1], mode=mode,
                          param_rems=[d["r"] for d in st] if mode == "bf16_rem" else None)
