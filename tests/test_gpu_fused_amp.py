@@ -70,9 +70,11 @@ CASES = {"small": (70_000, False), "mid": (3_000_000, False), "misaligned": (70_
          "big": (7_000_000, False)}
 
 
+@pytest.mark.parametrize("gdtype", [torch.bfloat16, torch.float16, torch.float32],
+                         ids=["bf16", "f16", "f32"])
 @pytest.mark.parametrize("mode", ["fp32", "bf16_rem"])
 @pytest.mark.parametrize("case", list(CASES))
-def test_fused_amp_equals_two_launch_path(mode, case):
+def test_fused_amp_equals_two_launch_path(mode, case, gdtype):
     size, misalign = CASES[case]
     sizes = [1, 4099, size, 0, 257]
     rng = np.random.default_rng(32)
@@ -89,7 +91,7 @@ def test_fused_amp_equals_two_launch_path(mode, case):
                 rr = dev(rng_side.integers(0, 1 << 15, n).astype(np.int16))
             # misaligned: tensor 1's m starts one float off the 16-byte grid
             mm = dev(np.zeros(n, np.float32), shift=1) if (misalign and i == 1) else zeros(n)
-            st.append(dict(p=pp, r=rr, g=zeros(n, torch.bfloat16),
+            st.append(dict(p=pp, r=rr, g=zeros(n, gdtype),
                            m=mm, v=zeros(n)))
         opt = FusedAdamW([d["p"] for d in st], [d["g"] for d in st], [d["m"] for d in st],
                          [d["v"] for d in st], [0.1, 0.0, 0.1, 0.0, 0.1], mode=mode,
@@ -98,7 +100,7 @@ def test_fused_amp_equals_two_launch_path(mode, case):
                       zeros(1)))
     lr, scale = torch.tensor([1e-3], device="cuda"), torch.tensor([256.0], device="cuda")
     for it in range(6):
-        xs = [torch.from_numpy((rng.normal(0, 1e-3, n) * 256).astype(np.float32)).to(torch.bfloat16)
+        xs = [torch.from_numpy((rng.normal(0, 1e-3, n) * 256).astype(np.float32)).to(gdtype)
               for n in sizes]
         if it == 3:
             xs[2][5] = math.inf
