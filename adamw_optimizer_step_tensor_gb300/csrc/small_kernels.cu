@@ -156,7 +156,7 @@ step_small_kernel(const __grid_constant__ SmallArgs a, float* found_inf_out) {
   int t = 0;
   const bool flagged = finish_scalars(sa, raw, s, t);   // found_inf set (plain launch only)
   const float decay = __fsub_rn(1.0f, __fmul_rn(s.lr, T.wd));
-  if (warp == kNext && lane == 0 && !flagged) s_next = bias_corrections(a.beta1, a.beta2, t + 1);
+  if (warp == kNext && lane == 0 && !flagged) s_next = bias_corrections(a.beta1, a.beta2, next_step(t));
   // fused: the lead takes the launch index now, while the data streams in
   unsigned long long launch = 0;
   if (FUSED && warp == kLead && lane == 0) launch = amp_enter(a.scratch);
@@ -215,7 +215,11 @@ step_small_kernel(const __grid_constant__ SmallArgs a, float* found_inf_out) {
     __syncwarp();
   }
 
-  // update the slice in place, four elements per lane per pass
+  // update the slice in place, four elements per lane per pass.  The grads
+  // travel on their own barrier: the plain variant waits for it here (the
+  // fused one did so before its scan) -- landing first is likely, not
+  // ordered, and only the completed phase makes the copy visible
+  if (!FUSED) wait_bar(&bar_g[warp]);
   wait_bar(&bar_s[warp]);
   if (landed) {
     for (int j = lane * 4; j < wn; j += 128) {

@@ -20,14 +20,22 @@ struct Scal {
 };
 
 // b^t by float64 square-and-multiply; every product is one IEEE rounding.
+// b^t by square-and-multiply.  The exponent is taken as an unsigned 32-bit
+// count, so the loop ends after at most 32 rounds whatever the step counter
+// holds (a counter the caller set negative, or one that wrapped past
+// INT32_MAX, reads as a huge step: b^t = 0, bias corrections of 1).
 __device__ double pow_binary(double b, int t) {
   double r = 1.0, x = b;
-  while (t) {
-    if (t & 1) r = __dmul_rn(r, x);
+  for (uint32_t u = static_cast<uint32_t>(t); u != 0u; u >>= 1) {
+    if (u & 1u) r = __dmul_rn(r, x);
     x = __dmul_rn(x, x);
-    t >>= 1;
   }
   return r;
+}
+
+// t + 1 with 32-bit wrap-around (no signed overflow).
+__device__ __forceinline__ int next_step(int t) {
+  return static_cast<int>(static_cast<uint32_t>(t) + 1u);
 }
 
 struct BiasCorr {
@@ -70,7 +78,7 @@ __device__ bool finish_scalars(const StepArgs& a, const RawScalars& r, Scal& s, 
   const int step = r.step;
   const StepScratch& memo = r.memo;
   if (found != 0.0f) return true;
-  const int t = step + 1;
+  const int t = next_step(step);
   const BiasCorr bc = (memo.memo_t == t && memo.memo_b1 == __float_as_uint(a.beta1) &&
                        memo.memo_b2 == __float_as_uint(a.beta2))
                           ? BiasCorr{memo.memo_bc1, memo.memo_inv_sqrt_bc2}
@@ -116,7 +124,7 @@ __device__ void take_ticket_with(const StepArgs& a, int t, const BiasCorr& nx) {
     m->memo_inv_sqrt_bc2 = nx.inv_sqrt_bc2;
     m->memo_b1 = __float_as_uint(a.beta1);
     m->memo_b2 = __float_as_uint(a.beta2);
-    m->memo_t = t + 1;
+    m->memo_t = next_step(t);
     atomicExch(&m->ticket, 0u);
   }
 }
@@ -126,13 +134,13 @@ __device__ void take_ticket(const StepArgs& a, int t) {
   const unsigned tk = atomicAdd(&a.scratch->ticket, 1u);
   if (tk == gridDim.x - 1) {
     *a.step = t;
-    const BiasCorr nx = bias_corrections(a.beta1, a.beta2, t + 1);
+    const BiasCorr nx = bias_corrections(a.beta1, a.beta2, next_step(t));
     StepScratch* m = a.scratch;
     m->memo_bc1 = nx.bc1;
     m->memo_inv_sqrt_bc2 = nx.inv_sqrt_bc2;
     m->memo_b1 = __float_as_uint(a.beta1);
     m->memo_b2 = __float_as_uint(a.beta2);
-    m->memo_t = t + 1;
+    m->memo_t = next_step(t);
     atomicExch(&m->ticket, 0u);
   }
 }

@@ -153,7 +153,8 @@ def first_mismatch(a, b) -> str:
     if bad.size == 0:
         return "identical"
     i = bad[0]
-    return f"{bad.size} mismatches; first at {i}: gpu={a[i]!r} oracle={b[i]!r}"
+    return (f"{bad.size} mismatches; first at {i}: gpu={a[i]!r} oracle={b[i]!r}; "
+            f"at {bad[:16].tolist()}")
 
 
 # ---------------------------------------------------------------- acceptance checks
@@ -161,10 +162,24 @@ def first_mismatch(a, b) -> str:
 # numpy arrays, so that a CPU test can feed them a planted mistake (computed by
 # the oracle) and show that they reject it.
 
-def assert_state_bitexact(got: dict, want: dict, where: str = "") -> None:
-    """Every named array of `got` bit-identical to the same name in `want`."""
+def assert_state_bitexact(got: dict, want: dict, where: str = "", prev: dict | None = None) -> None:
+    """Every named array of `got` bit-identical to the same name in `want`.  On a
+    mismatch every array is reported, and with `prev` (the oracle's state one step
+    earlier) how many of the mismatching values are exactly that earlier state --
+    a step that was not applied there."""
+    report = []
     for k in want:
-        assert bits_equal(got[k], want[k]), f"{where}{k}: {first_mismatch(got[k], want[k])}"
+        if not bits_equal(got[k], want[k]):
+            msg = f"{where}{k}: {first_mismatch(got[k], want[k])}"
+            if prev is not None and k in prev:
+                g = np.asarray(got[k], dtype=F32).ravel()
+                w = np.asarray(want[k], dtype=F32).ravel()
+                bad = np.nonzero(g.view(np.uint32) != w.view(np.uint32))[0]
+                old = np.asarray(prev[k], dtype=F32).ravel()[bad]
+                same = int(np.sum(g[bad].view(np.uint32) == old.view(np.uint32)))
+                msg += f"; {same} of {bad.size} equal the previous step's oracle value"
+            report.append(msg)
+    assert not report, " | ".join(report)
 
 
 def assert_single_step_rel(p_got, p_fp64, tol: float = 1e-6) -> None:

@@ -81,3 +81,55 @@ def test_plan_info_reports_the_launch_shape():
         assert info["total_numel"] == n, name
         assert 1 <= info["grid_blocks"] <= per_sm * sms, name
         opt.close()
+
+
+@pytest.mark.parametrize("start", [2**31 - 1, -7])
+def test_step_counter_at_its_limits(start):
+    """A step counter the caller left at INT32_MAX (t wraps) or set negative: the
+    step ends (the bias corrections' power loop reads t as an unsigned 32-bit
+    count, at most 32 rounds), the counter advances with 32-bit wrap-around, and
+    the update is the oracle's at that unsigned t, where b^t = 0 and both bias
+    corrections are 1 -- on the small kernel, the bulk kernel and the 8-bit one."""
+    import numpy as np
+    from oracle import adamw as OA
+    from oracle import q8 as OQ
+    f32 = OA.f32
+    t_dev = (start + 1 + 2**31) % 2**32 - 2**31      # the counter after the step
+    t_exp = (start + 1) % 2**32                      # the exponent the kernels use
+    rng = np.random.default_rng(81)
+    lr_v = f32(1e-3)
+    hp = dict(beta1=f32(0.9), beta2=f32(0.999), eps=f32(1e-8))
+    for sizes in ([5000], [4096 + 37 * i for i in range(20)]):   # small kernel, bulk kernel
+        ps = [rng.normal(0, 0.02, n).astype(np.float32) for n in sizes]
+        gs = [rng.normal(0, 1e-3, n).astype(np.float32) for n in sizes]
+        d = [dict(p=dev(p), g=dev(g), m=zeros(p.size), v=zeros(p.size)) for p, g in zip(ps, gs)]
+        opt = FusedAdamW([x["p"] for x in d], [x["g"] for x in d], [x["m"] for x in d],
+                         [x["v"] for x in d], [f32(0.1)] * len(sizes))
+        step = scalar_i32(start)
+        opt.step(scalar_f32(lr_v), step, betas=(hp["beta1"], hp["beta2"]), eps=hp["eps"])
+        orc = [OA.Tensor(p=p.copy(), g=g, m=np.zeros(p.size, np.float32),
+                         v=np.zeros(p.size, np.float32), wd=f32(0.1)) for p, g in zip(ps, gs)]
+        OA.step_f32(orc, lr=lr_v, t=t_exp, **hp)
+        torch.cuda.synchronize()
+        assert int(step.item()) == t_dev and opt.status() == 0
+        for x, o in zip(d, orc):
+            assert bits_equal(host(x["p"]), o.p) and bits_equal(host(x["m"]), o.m)
+            assert bits_equal(host(x["v"]), o.v)
+        opt.close()
+    # the 8-bit kernel's own launch
+    n = 3000
+    p, g = rng.normal(0, 0.02, n).astype(np.float32), rng.normal(0, 1e-3, n).astype(np.float32)
+    nb = OQ.n_blocks(n)
+    cm, cv = rng.integers(0, 256, n).astype(np.uint8), rng.integers(0, 256, n).astype(np.uint8)
+    am, av = rng.uniform(0, 1e-3, nb).astype(np.float32), rng.uniform(0, 1e-6, nb).astype(np.float32)
+    x = dict(p=dev(p), g=dev(g), cm=dev(cm), cv=dev(cv), am=dev(am), av=dev(av))
+    opt = FusedAdamW([x["p"]], [x["g"]], [x["cm"]], [x["cv"]], [f32(0.01)], mode="q8",
+                     absmax_m=[x["am"]], absmax_v=[x["av"]])
+    step = scalar_i32(start)
+    opt.step(scalar_f32(lr_v), step, betas=(hp["beta1"], hp["beta2"]), eps=hp["eps"])
+    OQ.step_f32(p, g, cm, cv, am, av, lr=lr_v, wd=f32(0.01), t=t_exp, **hp)
+    torch.cuda.synchronize()
+    assert int(step.item()) == t_dev and opt.status() == 0
+    assert bits_equal(host(x["p"]), p) and np.array_equal(host(x["cm"]), cm)
+    assert np.array_equal(host(x["cv"]), cv) and bits_equal(host(x["am"]), am)
+    opt.close()

@@ -74,12 +74,14 @@ def test_single_tensor_ten_steps_bitexact_and_within_fp64_tolerance():
     for t in range(1, 11):
         _new_grads(gs, oracle, rng)
         ref64[0].g = oracle[0].g.astype(np.float64)
+        prev = {"p": oracle[0].p.copy(), "m": oracle[0].m.copy(), "v": oracle[0].v.copy()}
         opt.step(lr, step, betas=(B1, B2), eps=EPS)
         OA.step_f32(oracle, lr=f32(0.1), beta1=B1, beta2=B2, eps=EPS, t=t)
         OA.step_fp64(ref64, lr=f32(0.1), beta1=B1, beta2=B2, eps=EPS, t=t)
         torch.cuda.synchronize()
         assert_state_bitexact({"p": host(ps[0]), "m": host(ms[0]), "v": host(vs[0])},
-                              {"p": oracle[0].p, "m": oracle[0].m, "v": oracle[0].v}, f"step {t} ")
+                              {"p": oracle[0].p, "m": oracle[0].m, "v": oracle[0].v}, f"step {t} ",
+                              prev=prev)
         if t == 1:
             assert_single_step_rel(host(ps[0]), ref64[0].p)
     assert int(step.item()) == 10
