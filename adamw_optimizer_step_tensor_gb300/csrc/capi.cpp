@@ -548,6 +548,11 @@ static adamw_status create_plan(const adamw_tensor* tensors, int32_t n_tensors, 
     if ((e = cudaMemcpy(p->d_qt, qt.get(), sizeof(QTables), cudaMemcpyHostToDevice)) != cudaSuccess)
       return cuda_fail(e, "upload code maps");
   }
+  // The clears (scratch, Adam-mini counters) are queued on the legacy stream
+  // and a copy from pageable memory may return before its DMA lands: wait for
+  // them, so that a step on any stream, blocking or not, sees the whole plan.
+  if ((e = cudaStreamSynchronize(cudaStreamLegacy)) != cudaSuccess)
+    return cuda_fail(e, "finish the plan's uploads");
   *out = p.release();
   return ADAMW_OK;
 }
@@ -833,8 +838,14 @@ adamw_status adamw_q8_set_maps(adamw_plan* plan, const float signed_map[256],
   std::unique_ptr<QTables> qt(new QTables);
   adamw_status st = build_qtables(signed_map, unsigned_map, 256, qt.get());
   if (st != ADAMW_OK) return st;
-  cudaError_t e = cudaMemcpy(plan->d_qt, qt.get(), sizeof(QTables), cudaMemcpyHostToDevice);
+  // steps already queued on any stream read the old maps: let them finish
+  // first, and let the new maps land before returning
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceSynchronize");
+  e = cudaMemcpy(plan->d_qt, qt.get(), sizeof(QTables), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_fail(e, "upload code maps");
+  if ((e = cudaStreamSynchronize(cudaStreamLegacy)) != cudaSuccess)
+    return cuda_fail(e, "finish the map upload");
   plan->refine = qt->refine;
   return ADAMW_OK;
 }

@@ -465,8 +465,9 @@ adamw_status adamw_q4_quant(const adamw_plan* plan, int32_t which, const float* 
                             uint8_t* codes, float* absmax, int64_t n, void* stream);
 
 /* Replace a Q8 plan's maps (host arrays, 256 strictly ascending finite
- * floats each).  Synchronous.  EUNSUPPORTED if the maps are too dense for the
- * kernel's bucketed nearest-code search. */
+ * floats each).  Synchronous: waits for all work queued on the device (steps
+ * already queued read the old maps), then uploads the new ones.  EUNSUPPORTED
+ * if the maps are too dense for the kernel's bucketed nearest-code search. */
 adamw_status adamw_q8_set_maps(adamw_plan* plan, const float signed_map[256],
                                const float unsigned_map[256]);
 

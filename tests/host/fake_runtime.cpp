@@ -106,6 +106,7 @@ cudaError_t cudaMemsetAsync(void* p, int v, size_t n, cudaStream_t) {
   return cudaSuccess;
 }
 cudaError_t cudaDeviceSynchronize(void) { return cudaSuccess; }
+cudaError_t cudaStreamSynchronize(cudaStream_t) { return cudaSuccess; }
 const char* cudaGetErrorString(cudaError_t) { return "fake runtime error"; }
 const char* cudaGetErrorName(cudaError_t) { return "cudaErrorFake"; }
 
