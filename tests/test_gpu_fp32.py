@@ -88,6 +88,27 @@ def test_single_tensor_ten_steps_bitexact_and_within_fp64_tolerance():
     assert_max_abs(host(ps[0]), ref64[0].p)
 
 
+@pytest.mark.parametrize("gdtype", [torch.float16, torch.float32], ids=["f16", "f32"])
+def test_small_plan_soak_bitexact_every_step(gdtype):
+    """60 steps of a 3-tensor small plan (the shared-memory kernel), every step
+    compared bit for bit: a copy read before it lands shows as a wrong sector in
+    some step, which a short run can miss."""
+    sizes = [1 << 20, 70001, 4099]
+    opt, ps, gs, ms, vs, oracle, rng = _make(sizes, [f32(0.1), 0.0, f32(0.1)], gdtype, seed=91,
+                                             zero_state=False)
+    assert opt.info()["block_threads"] == 1024
+    lr, step = scalar_f32(f32(1e-3)), scalar_i32(0)
+    for t in range(1, 61):
+        _new_grads(gs, oracle, rng)
+        opt.step(lr, step, betas=(B1, B2), eps=EPS)
+        OA.step_f32(oracle, lr=f32(1e-3), beta1=B1, beta2=B2, eps=EPS, t=t)
+        torch.cuda.synchronize()
+        for i, (p, m, v, o) in enumerate(zip(ps, ms, vs, oracle)):
+            assert_state_bitexact({"p": host(p), "m": host(m), "v": host(v)},
+                                  {"p": o.p, "m": o.m, "v": o.v}, f"step {t} tensor {i} ")
+    assert int(step.item()) == 60 and opt.status() == 0
+
+
 SIZES = [1, 3, 8, 9, 255, 256, 257, 2047, 2048, 2049, 8191, 8192, 8193, 50001, 0, 7]
 
 
